@@ -1,0 +1,221 @@
+/*
+ * flare.h -- C ABI of the GB300 (sm_103a) FLARE / FLARE++ token-mixer library.
+ *
+ * The operations follow "FLARE++: Low-rank attention with dynamic attention
+ * routing", appendix on context parallelism (arXiv 2608.11519, HTML). On that
+ * page R context-parallel ranks each hold one token shard and exchange small
+ * latent results with all-reduces; on one GPU the ranks become token shards of
+ * one device buffer and the all-reduces become an in-device merge.
+ *
+ * Conventions shared by every entry point
+ *  - Layouts are row-major. Token tensors (K, V, K~, V~, Y, dK, dV) are
+ *    [B, N, H, D]: the per-token projection output with C = H*D channels.
+ *    Latent tensors (Z, Q(X), dQ, dZ) are [B, H, M, D]. Row statistics (L)
+ *    are [B, H, M]. A query Q (or FLARE++ seed tensor) is [H, M, D] shared by
+ *    every batch element when dims->q_batch_stride == 0, else [B, H, M, D]
+ *    with that many elements between batch elements.
+ *  - Q, K, V, K~, V~, Y, dK, dV have the element type dims->dtype (fp32 or
+ *    bf16). Z, L, O_r, L_r, Q(X), dZ, dQ are fp32. L values are natural-log
+ *    log-normalisers that include the score scale.
+ *  - mask is uint8 [B, N], 1 = valid token, 0 = padding (excluded from every
+ *    softmax normalisation); NULL means every token is valid.
+ *  - shard_offsets is a HOST array of R+1 int64 with offsets[0] = 0,
+ *    offsets[R] = N and offsets nondecreasing; shard r owns tokens
+ *    [offsets[r], offsets[r+1]) of every batch element. Shards may be empty.
+ *    1 <= R <= FLARE_MAX_SHARDS.
+ *  - Every other pointer is DEVICE memory owned by the caller. The library
+ *    never allocates: a call that needs scratch memory takes a caller-owned
+ *    workspace of at least flare_workspace_bytes() bytes. Workspaces and
+ *    outputs must not overlap inputs. Concurrent calls need separate
+ *    workspaces.
+ *  - stream is a cudaStream_t (NULL = legacy default stream). Calls are
+ *    stream-ordered and asynchronous: argument errors are reported
+ *    synchronously before anything is launched; launch failures are returned
+ *    as FLARE_ERR_CUDA; a kernel that abandoned a bounded wait records
+ *    FLARE_ERR_TIMEOUT on the device, reported by flare_device_status().
+ *  - On any error flare_last_error_string() describes it (thread-local).
+ */
+#ifndef FLARE_H_
+#define FLARE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FLARE_API __attribute__((visibility("default")))
+#else
+#define FLARE_API
+#endif
+
+#define FLARE_MAX_SHARDS 256
+
+typedef enum {
+    FLARE_OK = 0,
+    FLARE_ERR_INVALID_ARG = 1,  /* bad pointer, size, offsets or layout          */
+    FLARE_ERR_UNSUPPORTED = 2,  /* valid, but no kernel for this shape or dtype  */
+    FLARE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required    */
+    FLARE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed          */
+    FLARE_ERR_TIMEOUT = 5       /* a kernel gave up a bounded wait (device flag) */
+} flare_status_t;
+
+typedef enum { FLARE_F32 = 0, FLARE_BF16 = 1 } flare_dtype_t;
+
+/* Kernel family selection. AUTO picks the tensor-core (tcgen05/TMEM, TMA)
+ * kernels for bf16 shapes they support and the CUDA-core kernels otherwise;
+ * TENSOR returns FLARE_ERR_UNSUPPORTED where no tensor-core kernel applies. */
+typedef enum { FLARE_KERNEL_AUTO = 0, FLARE_KERNEL_SIMT = 1, FLARE_KERNEL_TENSOR = 2 } flare_kernel_t;
+
+typedef struct {
+    int B;                  /* batch size                                      */
+    int H;                  /* heads                                           */
+    int M;                  /* latent queries per head (1..256)                */
+    int N;                  /* tokens per batch element (all shards)           */
+    int D;                  /* head dimension (1..128)                         */
+    float scale;            /* score scale s; <= 0 selects s = D^-1/2          */
+    flare_dtype_t dtype;    /* element type of the token tensors and of Q      */
+    int64_t q_batch_stride; /* 0: Q is [H,M,D] replicated; H*M*D: [B,H,M,D]    */
+    flare_kernel_t kernel;  /* kernel family (FLARE_KERNEL_AUTO by default)    */
+} flare_dims_t;
+
+typedef enum {
+    FLARE_OP_ENCODER_FWD = 0,
+    FLARE_OP_LSE_MERGE = 1,
+    FLARE_OP_DECODE_FWD = 2,
+    FLARE_OP_FWD = 3,
+    FLARE_OP_PP_FWD = 4,
+    FLARE_OP_ENCODER_BWD = 5
+} flare_op_t;
+
+/* Workspace bytes `op` needs for these sizes and shard offsets (host array of
+ * R+1 entries, may be NULL for ops that take none). Returns 0 when the op
+ * needs no workspace, and (size_t)-1 when the arguments are invalid. */
+FLARE_API size_t flare_workspace_bytes(flare_op_t op, const flare_dims_t *dims,
+                             const int64_t *shard_offsets, int R);
+
+/*
+ * Split-KV encoder. Source: the per-shard local encoder and eq. 23 of the
+ * appendix (the local primitive returns O_r normalised over shard r and the
+ * row log-normaliser L_r; eq. 18 is the global result).
+ * For every batch b, head h, latent m and shard r:
+ *   S_mn = s <Q_m, K_n> over the valid tokens n of shard r,
+ *   L_r  = log sum_n exp(S_mn),  O_r = sum_n exp(S_mn - L_r) V_n,
+ * with L_r = -inf and O_r = 0 for a row that has no valid token on shard r.
+ * When Z and L are given the shards are merged in the same call (eq. 23, see
+ * flare_lse_merge) into the global Z [B,H,M,D] and L [B,H,M].
+ *   Q       dims->dtype, [H,M,D] or [B,H,M,D] (dims->q_batch_stride)
+ *   K, V    dims->dtype, [B,N,H,D]
+ *   O_r     fp32 [R,B,H,M,D] or NULL;   L_r fp32 [R,B,H,M] or NULL
+ *   Z       fp32 [B,H,M,D] or NULL;     L   fp32 [B,H,M] or NULL
+ * At least one of the pairs (O_r, L_r) or (Z, L) must be given, each pair
+ * complete. Scores are never stored: memory use does not grow with N*M.
+ */
+FLARE_API flare_status_t flare_encoder_fwd(const flare_dims_t *dims, const void *Q, const void *K,
+                                 const void *V, const uint8_t *mask,
+                                 const int64_t *shard_offsets, int R, float *O_r, float *L_r,
+                                 float *Z, float *L, void *workspace, size_t workspace_bytes,
+                                 void *stream);
+
+/*
+ * Exact log-sum-exp merge of R per-shard results. Source: eq. 23 and the
+ * cross-rank log-sum-exp paragraph of the appendix (the all-reduce max and the
+ * two all-reduce sums, done here in one kernel). Per row:
+ *   L_max = max_r L_r,  a = sum_r exp(L_r - L_max),
+ *   U = sum_r exp(L_r - L_max) O_r,  Z = U / a,  L = L_max + log a.
+ * Rows where every L_r is -inf return L = -inf and Z = 0 (never NaN).
+ *   O_r fp32 [R,B,H,M,D], L_r fp32 [R,B,H,M] -> Z fp32 [B,H,M,D], L fp32 [B,H,M].
+ * No workspace. Shards are folded in index order, so results are
+ * bit-reproducible run to run.
+ */
+FLARE_API flare_status_t flare_lse_merge(const float *O_r, const float *L_r, int R, int B, int H, int M,
+                               int D, float *Z, float *L, void *stream);
+
+/*
+ * Local decode. Source: the FLARE decode paragraph of the appendix (the query
+ * of each output token is local, both latent tensors replicated). Reading of
+ * the stripped formula: each token's key is its decode query against the M
+ * latent queries, with Z as values:
+ *   Y[b,n,h] = sum_m softmax_m(s <K[b,n,h], Q_m>) Z[b,h,m].
+ * Every token slot is decoded (there is no mask: the softmax runs over the M
+ * latents, never empty).
+ *   Q  dims->dtype [H,M,D] or [B,H,M,D];  Z fp32 [B,H,M,D];
+ *   K  dims->dtype [B,N,H,D];  Y dims->dtype [B,N,H,D] (written).
+ * No workspace.
+ */
+FLARE_API flare_status_t flare_decode_fwd(const flare_dims_t *dims, const void *Q, const float *Z,
+                                const void *K, void *Y, void *stream);
+
+/*
+ * FLARE mixer forward: the split-KV encoder with the fused merge, then the
+ * local decode. Source: the FLARE paragraph of the appendix (one globally
+ * communicating encoder and one local decoder).
+ *   Y dims->dtype [B,N,H,D]; Z fp32 [B,H,M,D]; L fp32 [B,H,M] (all written;
+ *   Z and L are the saved forward statistics of the backward).
+ */
+FLARE_API flare_status_t flare_fwd(const flare_dims_t *dims, const void *Q, const void *K, const void *V,
+                         const uint8_t *mask, const int64_t *shard_offsets, int R, void *Y,
+                         float *Z, float *L, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/*
+ * FLARE++ mixer forward. Source: the FLARE++ paragraph of the appendix (the
+ * same distributed encoder invoked twice, then the local decode):
+ *   Q(X), L1 = encoder(seeds Q~, K~, V~)       (dynamic routing queries)
+ *   Z, L2    = encoder(Q(X), K, V)             (physical latent values)
+ *   Y        = decode(Q(X), Z, K)
+ *   Qseed  dims->dtype, [H,M,D] or [B,H,M,D] (dims->q_batch_stride)
+ *   Kt, Vt, K, V  dims->dtype [B,N,H,D] (projected tokens, same mask/shards)
+ *   Y dims->dtype [B,N,H,D]; Qdyn fp32 [B,H,M,D]; L1, L2 fp32 [B,H,M];
+ *   Z fp32 [B,H,M,D]. Both encoders' statistics are returned because their
+ *   backward passes need their own saved outputs.
+ * On the bf16 path Q(X) is rounded to bf16 (round-to-nearest-even) where it
+ * feeds the tensor-core kernels; Qdyn itself is returned in fp32.
+ */
+FLARE_API flare_status_t flare_pp_fwd(const flare_dims_t *dims, const void *Qseed, const void *Kt,
+                            const void *Vt, const void *K, const void *V, const uint8_t *mask,
+                            const int64_t *shard_offsets, int R, void *Y, float *Qdyn,
+                            float *L1, float *Z, float *L2, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/*
+ * Encoder backward with the global forward statistics. Source: the backward
+ * paragraphs of the appendix (globally normalised local probabilities, the
+ * row scalar c, local gradients, query gradient summed over shards):
+ *   P_mn = exp(s <Q_m, K_n> - L_m)   (global L; masked tokens and rows with
+ *                                     L = -inf give P = 0)
+ *   c_m  = <dZ_m, Z_m>
+ *   dV_n = sum_m P_mn dZ_m
+ *   dS_mn = P_mn (<dZ_m, V_n> - c_m)
+ *   dK_n = s sum_m dS_mn Q_m,   dQ_m = s sum_n dS_mn K_n  (sum over all shards)
+ *   Z, L  fp32 (from the forward), dZ fp32 [B,H,M,D] (summed over every
+ *         consumer of Z by the caller)
+ *   dQ fp32 [B,H,M,D] (one slice per batch element, also when Q is
+ *         replicated: the caller sums over B); dK, dV dims->dtype [B,N,H,D].
+ * With the global L and c every token's gradient is independent of the other
+ * shards, so the shard offsets only need to be valid.
+ */
+FLARE_API flare_status_t flare_encoder_bwd(const flare_dims_t *dims, const void *Q, const void *K,
+                                 const void *V, const uint8_t *mask,
+                                 const int64_t *shard_offsets, int R, const float *Z,
+                                 const float *L, const float *dZ, float *dQ, void *dK, void *dV,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronises `stream`, then reads and clears the device status word that
+ * kernels set when they abandon a bounded wait: FLARE_OK, FLARE_ERR_TIMEOUT,
+ * or FLARE_ERR_CUDA if the synchronisation itself failed. */
+FLARE_API flare_status_t flare_device_status(void *stream);
+
+/* Text of the calling thread's most recent error (empty if none). */
+FLARE_API const char *flare_last_error_string(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+FLARE_API int flare_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLARE_H_ */

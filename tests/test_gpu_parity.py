@@ -1,0 +1,229 @@
+"""GPU parity of every entry point against the fp64 oracle at sizes the oracle
+finishes in seconds: several tiles, ragged tails, ragged/empty/padded shards,
+both kernel families, and the degenerate cases of the method."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from latent_query_split_gb300 import flare
+from parity import assert_close, assert_L_close
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = ["simt", "tensor"]
+
+
+def _call(fn, *a, **kw):
+    try:
+        return fn(*a, **kw)
+    except flare.FlareError as e:
+        if e.status == flare.FLARE_ERR_UNSUPPORTED and kw.get("kernel") == "tensor":
+            pytest.skip(f"no tensor-core kernel: {e}")
+        raise
+
+
+def _problem(seed, B, H, M, N, D, dtype, offsets, pad=0.1, q_std=0.5, replicated=True, dev="cuda"):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    Q = (torch.randn((H, M, D) if replicated else (B, H, M, D), generator=g) * q_std).to(dt)
+    K = torch.randn((B, N, H, D), generator=g).to(dt)
+    V = torch.randn((B, N, H, D), generator=g).to(dt)
+    mask = (torch.rand((B, N), generator=g) > pad).to(torch.uint8) if pad > 0 else None
+    return Q.to(dev), K.to(dev), V.to(dev), None if mask is None else mask.to(dev)
+
+
+CASES = [
+    # B, H, M, N, D, offsets, dtype
+    (2, 2, 16, 1000, 32, [0, 250, 500, 750, 1000], "f32"),
+    (2, 2, 64, 3001, 64, [0, 700, 700, 2000, 3001], "bf16"),
+    (1, 3, 128, 5000, 64, [0, 1234, 1300, 4999, 5000], "bf16"),
+    (2, 2, 256, 2600, 64, [0, 1000, 2600], "bf16"),
+    (1, 2, 64, 2100, 128, [0, 129, 2100], "bf16"),
+    (1, 2, 128, 1500, 128, [0, 1500], "f32"),
+    (2, 1, 37, 777, 40, [0, 300, 777], "f32"),
+    (1, 2, 128, 2048, 64, [0, 512, 1024, 1536, 2048], "f32"),
+]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"B{c[0]}H{c[1]}M{c[2]}N{c[3]}D{c[4]}{c[6]}")
+def test_encoder_shards_and_merge(cuda_device, kernel, case):
+    B, H, M, N, D, off, dt = case
+    Q, K, V, mask = _problem(1, B, H, M, N, D, dt, off)
+    O_r, L_r, Z, L = _call(flare.flare_encoder_fwd, Q, K, V, mask, off, shard_outputs=True,
+                           kernel=kernel)
+    flare.flare_device_status()
+    Zo, Lo = oracle.encode(Q, K, V, mask)
+    Oo, Lro = oracle.encode_shards(Q, K, V, mask, off)
+    assert_close("Z", Z, Zo, dt)
+    assert_L_close("L", L, Lo)
+    assert_close("O_r", O_r, Oo, dt)
+    assert_L_close("L_r", L_r, Lro)
+    # the standalone merge over the per-shard outputs gives the fused result
+    Zm, Lm = flare.flare_lse_merge(O_r, L_r)
+    assert_close("Z(merge)", Zm, Zo, dt)
+    assert_L_close("L(merge)", Lm, Lo)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"B{c[0]}H{c[1]}M{c[2]}N{c[3]}D{c[4]}{c[6]}")
+def test_flare_fwd_and_decode(cuda_device, kernel, case):
+    B, H, M, N, D, off, dt = case
+    Q, K, V, mask = _problem(2, B, H, M, N, D, dt, off)
+    Y, Z, L = _call(flare.flare_fwd, Q, K, V, mask, off, kernel=kernel)
+    flare.flare_device_status()
+    Zo, Lo, Yo = oracle.flare_fwd(Q, K, V, mask)
+    assert_close("Z", Z, Zo, dt)
+    assert_L_close("L", L, Lo)
+    assert_close("Y", Y, Yo, dt)
+    # decode alone, on the oracle's own Z (fp32), against the oracle decode
+    Zf = torch.from_numpy(Zo).float().to(K.device)
+    Y2 = _call(flare.flare_decode_fwd, Q, Zf, K, kernel=kernel)
+    assert_close("Y(decode)", Y2, oracle.decode(Q, Zf, K), dt)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_per_batch_query(cuda_device, kernel):
+    B, H, M, N, D = 2, 2, 128, 1800, 64
+    off = [0, 900, 1800]
+    Q, K, V, mask = _problem(3, B, H, M, N, D, "bf16", off, replicated=False)
+    Y, Z, L = _call(flare.flare_fwd, Q, K, V, mask, off, kernel=kernel)
+    Zo, Lo, Yo = oracle.flare_fwd(Q, K, V, mask)
+    assert_close("Z", Z, Zo, "bf16")
+    assert_L_close("L", L, Lo)
+    assert_close("Y", Y, Yo, "bf16")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dt,M,D", [("f32", 16, 32), ("bf16", 256, 64), ("bf16", 64, 128)])
+def test_flare_pp_fwd(cuda_device, kernel, dt, M, D):
+    B, H, N = 2, 2, 2500
+    off = [0, 600, 600, 2500]
+    g = torch.Generator().manual_seed(4)
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    Qs = (torch.randn((H, M, D), generator=g) * 0.02).to(tdt).cuda()
+    Kt, Vt, K, V = (torch.randn((B, N, H, D), generator=g).to(tdt).cuda() for _ in range(4))
+    mask = (torch.rand((B, N), generator=g) > 0.1).to(torch.uint8).cuda()
+    Y, Qd, L1, Z, L2 = _call(flare.flare_pp_fwd, Qs, Kt, Vt, K, V, mask, off, kernel=kernel)
+    flare.flare_device_status()
+    Qdo, L1o, Zo, L2o, Yo = oracle.flare_pp_fwd(Qs, Kt, Vt, K, V, mask)
+    assert_close("Q(X)", Qd, Qdo, dt)
+    assert_L_close("L1", L1, L1o)
+    assert_close("Z", Z, Zo, dt)
+    assert_L_close("L2", L2, L2o)
+    assert_close("Y", Y, Yo, dt)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dt,M,D,N", [("f32", 16, 32, 700), ("bf16", 128, 64, 3000),
+                                      ("bf16", 64, 128, 1100), ("bf16", 256, 64, 900)])
+def test_encoder_bwd(cuda_device, kernel, dt, M, D, N):
+    B, H = 2, 2
+    off = [0, 200, 200, N]
+    Q, K, V, mask = _problem(5, B, H, M, N, D, dt, off, q_std=1.0)
+    mask[1, 200:] = 0                         # batch element 1: only shard 0 is live
+    g = torch.Generator().manual_seed(6)
+    dZ = torch.randn((B, H, M, D), generator=g).cuda()
+    Zo, Lo = oracle.encode(Q, K, V, mask)
+    Zf = torch.from_numpy(Zo).float().cuda()
+    Lf = torch.from_numpy(Lo).float().cuda()
+    dQ, dK, dV = _call(flare.flare_encoder_bwd, Q, K, V, mask, off, Zf, Lf, dZ, kernel=kernel)
+    flare.flare_device_status()
+    dQo, dKo, dVo = oracle.encode_bwd(Q, K, V, mask, Zf, Lf, dZ)
+    assert_close("dQ", dQ, dQo, dt)
+    assert_close("dK", dK, dKo, dt)
+    assert_close("dV", dV, dVo, dt)
+
+
+# ---- edge cases ------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_empty_and_masked_rows(cuda_device, kernel):
+    """Rows with no valid key anywhere return L = -inf, Z = 0 (never NaN); an
+    empty shard returns L_r = -inf, O_r = 0."""
+    B, H, M, N, D = 3, 2, 64, 1000, 64
+    off = [0, 0, 400, 400, 1000]
+    Q, K, V, mask = _problem(7, B, H, M, N, D, "bf16", off)
+    mask[0] = 0                      # batch element 0: every row empty
+    mask[1, 400:] = 0                # batch element 1: shard 3 all padding
+    O_r, L_r, Z, L = _call(flare.flare_encoder_fwd, Q, K, V, mask, off, shard_outputs=True,
+                           kernel=kernel)
+    Zo, Lo = oracle.encode(Q, K, V, mask)
+    assert_close("Z", Z, Zo, "bf16")
+    assert_L_close("L", L, Lo)
+    assert torch.all(L[0] == -math.inf) and torch.all(Z[0] == 0)
+    assert torch.all(L_r[[0, 2]] == -math.inf) and torch.all(O_r[[0, 2]] == 0)
+    assert torch.all(L_r[3, 1] == -math.inf)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("N", [1, 127, 129])
+def test_tiny_token_counts(cuda_device, kernel, N):
+    Q, K, V, mask = _problem(8, 1, 2, 128, N, 64, "bf16", [0, N], pad=0)
+    Y, Z, L = _call(flare.flare_fwd, Q, K, V, None, [0, N], kernel=kernel)
+    Zo, Lo, Yo = oracle.flare_fwd(Q, K, V, None)
+    assert_close("Z", Z, Zo, "bf16")
+    assert_L_close("L", L, Lo)
+    assert_close("Y", Y, Yo, "bf16")
+
+
+def test_no_tokens(cuda_device):
+    Q, K, V, _ = _problem(9, 2, 2, 16, 0, 32, "f32", [0, 0], pad=0)
+    O_r, L_r, Z, L = flare.flare_encoder_fwd(Q, K, V, None, [0, 0, 0], shard_outputs=True)
+    assert torch.all(L == -math.inf) and torch.all(Z == 0)
+    assert torch.all(L_r == -math.inf) and torch.all(O_r == 0)
+    Y = flare.flare_decode_fwd(Q, Z, K)
+    assert Y.numel() == 0
+
+
+def test_max_shards_and_single_token_shards(cuda_device):
+    N = 300
+    off = list(range(0, 256)) + [N]              # 255 one-token shards + one long shard
+    Q, K, V, mask = _problem(10, 1, 1, 16, N, 32, "f32", off)
+    O_r, L_r, Z, L = flare.flare_encoder_fwd(Q, K, V, mask, off, shard_outputs=True)
+    Zo, Lo = oracle.encode(Q, K, V, mask)
+    assert_close("Z", Z, Zo, "f32")
+    assert_L_close("L", L, Lo)
+    Oo, Lro = oracle.encode_shards(Q, K, V, mask, off)
+    assert_close("O_r", O_r, Oo, "f32")
+    assert_L_close("L_r", L_r, Lro)
+
+
+def test_minimal_sizes(cuda_device):
+    Q, K, V, _ = _problem(11, 1, 1, 1, 5, 1, "f32", [0, 5], pad=0)
+    Y, Z, L = flare.flare_fwd(Q, K, V)
+    Zo, Lo, Yo = oracle.flare_fwd(Q, K, V)
+    assert_close("Z", Z, Zo, "f32")
+    assert_close("Y", Y, Yo, "f32")
+
+
+def test_merge_all_empty_rows_and_shard_order(cuda_device):
+    g = torch.Generator().manual_seed(12)
+    R, B, H, M, D = 5, 2, 2, 40, 24
+    O_r = torch.randn((R, B, H, M, D), generator=g)
+    L_r = torch.randn((R, B, H, M), generator=g) * 5
+    L_r[1] = -math.inf
+    O_r[1] = 0
+    L_r[:, 0, 0, :3] = -math.inf
+    O_r[:, 0, 0, :3] = 0
+    Z, L = flare.flare_lse_merge(O_r.cuda(), L_r.cuda())
+    Zo, Lo = oracle.lse_merge(O_r, L_r)
+    assert_close("Z", Z, Zo, "f32", atol=1e-5, rel=1e-5)
+    assert_L_close("L", L, Lo)
+    assert torch.all(Z[0, 0, :3] == 0) and torch.all(L[0, 0, :3] == -math.inf)
+    perm = torch.randperm(R, generator=g)
+    Zp, Lp = flare.flare_lse_merge(O_r[perm].contiguous().cuda(), L_r[perm].contiguous().cuda())
+    assert (Zp - Z).abs().max().item() <= 4 * R * 1.2e-7 * Z.abs().max().item()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_repeated_runs_are_bit_identical(cuda_device, kernel):
+    Q, K, V, mask = _problem(13, 2, 2, 128, 4000, 64, "bf16", [0, 1000, 4000])
+    off = [0, 1000, 4000]
+    a = _call(flare.flare_fwd, Q, K, V, mask, off, kernel=kernel)
+    b = _call(flare.flare_fwd, Q, K, V, mask, off, kernel=kernel)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
