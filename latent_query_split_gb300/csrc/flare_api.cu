@@ -161,28 +161,32 @@ bool use_tensor_cores(const flare_dims_t *d) {
 }
 
 struct EncoderLayout {
-    ShardPlan plan;
+    ShardPlan plan;        // CUDA-core path
     int mtiles;
     bool tc;
+    TcTilePlan tcplan;     // tensor-core path
+    TcEncLayout tclay;
     EncoderWorkspace ws;   // pointers relative to a null base until bound
 };
 
 void encoder_layout(const flare_dims_t *d, const int64_t *off, int R, bool tc, EncoderLayout &lay) {
     const int sms = planning_sms();
     lay.tc = tc;
+    const size_t bh = (size_t)d->B * d->H;
+    EncoderWorkspace &w = lay.ws;
     if (tc) {
         lay.mtiles = 1;
-        make_plan(off, R, d->N, tc_encoder_tile(), tc_encoder_min_chunk(d->M, d->D),
-                  (int64_t)d->B * d->H, (int64_t)sms * tc_encoder_ctas_per_sm(d->M, d->D) *
-                  tc_encoder_waves(), lay.plan);
-    } else {
-        lay.mtiles = (d->M + kSimtRows - 1) / kSimtRows;
-        make_plan(off, R, d->N, kSimtTile, 256, (int64_t)d->B * d->H * lay.mtiles,
-                  (int64_t)sms * 8, lay.plan);
+        tc_encoder_plan(make_problem(d), off, R, sms, lay.tcplan, lay.tclay);
+        w.tickets = (unsigned *)lay.tclay.tickets;
+        w.part_L = (float *)lay.tclay.part_L;
+        w.part_O = (float *)lay.tclay.part_O;
+        w.shard_L = (float *)lay.tclay.shard_L;
+        w.bytes = lay.tclay.bytes;
+        return;
     }
-    const size_t bh = (size_t)d->B * d->H;
+    lay.mtiles = (d->M + kSimtRows - 1) / kSimtRows;
+    make_plan(off, R, d->N, kSimtTile, 256, (int64_t)bh * lay.mtiles, (int64_t)sms * 8, lay.plan);
     size_t o = 0;
-    EncoderWorkspace &w = lay.ws;
     w.tickets = (unsigned *)o;
     o += align256(sizeof(unsigned) * bh * lay.mtiles);
     w.part_L = (float *)o;
@@ -205,13 +209,12 @@ EncoderWorkspace bind(const EncoderWorkspace &rel, void *base) {
 }
 
 size_t encoder_ws_bytes(const flare_dims_t *d, const int64_t *off, int R) {
-    EncoderLayout a;
+    static thread_local EncoderLayout a;
     encoder_layout(d, off, R, false, a);
     size_t bytes = a.ws.bytes;
     if (use_tensor_cores(d)) {
-        EncoderLayout b;
-        encoder_layout(d, off, R, true, b);
-        if (b.ws.bytes > bytes) bytes = b.ws.bytes;
+        encoder_layout(d, off, R, true, a);
+        if (a.ws.bytes > bytes) bytes = a.ws.bytes;
     }
     return bytes;
 }
@@ -251,14 +254,14 @@ flare_status_t encoder_run(const flare_dims_t *d, const void *Q, bool q_is_f32, 
     if (d->kernel == FLARE_KERNEL_TENSOR && !want_tc)
         return fail(FLARE_ERR_UNSUPPORTED, "no tensor-core encoder for dtype=%d M=%d D=%d",
                     (int)d->dtype, d->M, d->D);
-    const bool tc = want_tc && tc_pointers_ok(K, V, d->H, d->D);
+    const bool tc = want_tc && tc_pointers_ok(K, V, d->H, d->D) && (q_is_f32 || aligned(Q, 16));
     if (d->kernel == FLARE_KERNEL_TENSOR && !tc)
-        return fail(FLARE_ERR_INVALID_ARG, "tensor-core encoder needs 16-byte aligned K and V");
-    EncoderLayout lay;
+        return fail(FLARE_ERR_INVALID_ARG, "tensor-core encoder needs 16-byte aligned Q, K and V");
+    static thread_local EncoderLayout lay;     // ~7 KB: kept off the stack
     encoder_layout(d, off, R, tc, lay);
     const size_t need = encoder_ws_bytes(d, off, R);
     const int64_t bhm = (int64_t)pr.B * pr.H * pr.M;
-    if (lay.plan.total_chunks == 0) {          // N == 0: every row is empty
+    if (pr.N == 0) {                           // no token: every row is empty
         fill_empty_kernel<<<64, 256, 0, st>>>(O_r, O_r ? R * bhm * pr.D : 0, L_r, L_r ? R * bhm : 0,
                                                Z, Z ? bhm * pr.D : 0, L, L ? bhm : 0);
         cudaError_t e = cudaGetLastError();
@@ -269,14 +272,16 @@ flare_status_t encoder_run(const flare_dims_t *d, const void *Q, bool q_is_f32, 
     if (!aligned(ws, 256)) return fail(FLARE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     EncoderWorkspace w = bind(lay.ws, ws);
     EncoderOut out{O_r, L_r, Z, L};
-    cudaError_t e = cudaMemsetAsync(w.tickets, 0, sizeof(unsigned) * (size_t)pr.B * pr.H * lay.mtiles, st);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(tickets)");
+    cudaError_t e;
     if (tc) {
         DeviceInfo di;
         flare_status_t s = device_info(di);
         if (s != FLARE_OK) return s;
-        e = launch_encoder_tc(pr, lay.plan, Q, q_is_f32, K, V, mask, w, out, di.status, st);
+        e = launch_encoder_tc(pr, lay.tcplan, lay.tclay, Q, q_is_f32, K, V, mask, ws, out,
+                              di.status, st);
     } else {
+        e = cudaMemsetAsync(w.tickets, 0, sizeof(unsigned) * (size_t)pr.B * pr.H * lay.mtiles, st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(tickets)");
         e = launch_encoder_simt(pr, lay.plan, Q, q_is_f32, K, V, mask, w, out, st);
     }
     return e == cudaSuccess ? FLARE_OK : cuda_fail(e, "encoder launch");
@@ -290,7 +295,7 @@ flare_status_t decode_run(const flare_dims_t *d, const void *Q, bool q_is_f32, c
     const size_t es = elem_size(d);
     if (!aligned(Q, q_is_f32 ? 4 : es) || !aligned(K, es) || !aligned(Y, es) || !aligned(Z, 4))
         return fail(FLARE_ERR_INVALID_ARG, "tensors must be aligned to their element size");
-    const bool want_tc = use_tensor_cores(d);
+    const bool want_tc = use_tensor_cores(d) && tc_decode_available();
     if (d->kernel == FLARE_KERNEL_TENSOR && !want_tc)
         return fail(FLARE_ERR_UNSUPPORTED, "no tensor-core decode for dtype=%d M=%d D=%d",
                     (int)d->dtype, d->M, d->D);

@@ -1,27 +1,49 @@
 // tc_common.cuh -- host-side interface of the tensor-core (tcgen05 / TMEM,
-// TMA) kernels: which shapes they cover, how the encoder is tiled, and the
-// launchers.
+// TMA) kernels: which shapes they cover, how the encoder splits its work, the
+// workspace it needs, and the launchers.
 #pragma once
 
 #include "flare_internal.cuh"
 
 namespace flare {
 
-// bf16 token tensors with M in {64, 128, 256} latents and D in {64, 128}.
+// bf16 token tensors with M in {64, 128, 256} latents and D in {64, 128}
+// (M = 256 only with D = 64).
 bool tc_supported(bool bf16, int M, int D);
 // TMA needs 16-byte aligned bases and a token stride (H*D*2 bytes) that is a
 // multiple of 16.
 bool tc_pointers_ok(const void *a, const void *b, int H, int D);
 
-int tc_encoder_tile();                      // tokens per pipeline stage
-int tc_encoder_min_chunk(int M, int D);     // smallest chunk worth a partial
-int tc_encoder_ctas_per_sm(int M, int D);   // resident encoder CTAs per SM
-int tc_encoder_waves();                     // grid size target in waves
+// Split of the encoder's work. Every shard is cut into tiles of 128 tokens
+// (the last one ragged); all (b, h) share the shard layout, so tile t of the
+// flattened order (b, h)-major, then shard, then tile sits at a computable
+// place. `grid` persistent CTAs each take one contiguous, equally long span
+// of that order; a span cut into (b, h, shard) pieces gives one partial
+// (normalised output and log-normaliser) per piece, merged by the last CTA
+// that finishes a piece of the same (b, h).
+struct TcTilePlan {
+    int R;
+    int T_bh;                       // tiles per (b, h)
+    int P_max;                      // partial slots per (b, h, shard)
+    int grid;                       // persistent CTAs
+    int64_t T_total;                // tiles over every (b, h)
+    int64_t off[kMaxShards + 1];    // shard token offsets
+    int tile_start[kMaxShards + 1]; // first tile of each shard within a (b, h)
+};
 
-cudaError_t launch_encoder_tc(const Problem &pr, const ShardPlan &plan, const void *Q,
-                              bool q_is_f32, const void *K, const void *V, const uint8_t *mask,
-                              const EncoderWorkspace &ws, const EncoderOut &out,
+// Byte offsets of the encoder workspace regions.
+struct TcEncLayout {
+    size_t tickets, part_L, part_O, shard_L, q_bf16, bytes;
+};
+
+bool tc_encoder_plan(const Problem &pr, const int64_t *off, int R, int sms, TcTilePlan &plan,
+                     TcEncLayout &lay);
+
+cudaError_t launch_encoder_tc(const Problem &pr, const TcTilePlan &plan, const TcEncLayout &lay,
+                              const void *Q, bool q_is_f32, const void *K, const void *V,
+                              const uint8_t *mask, void *ws, const EncoderOut &out,
                               unsigned *status, cudaStream_t st);
+bool tc_decode_available();
 cudaError_t launch_decode_tc(const Problem &pr, const void *Q, bool q_is_f32, const float *Z,
                              const void *K, void *Y, int sms, unsigned *status, cudaStream_t st);
 

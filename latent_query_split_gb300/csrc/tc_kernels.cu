@@ -1,23 +1,168 @@
-// tc_kernels.cu -- tensor-core kernels (placeholder: no shape routed here yet).
+// tc_kernels.cu -- host side of the tensor-core kernels: shape coverage, the
+// encoder's work split and workspace, TMA tensor maps, and the launchers.
 #include "tc_common.cuh"
+#include "tc_encoder.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
 
 namespace flare {
+namespace {
 
-bool tc_supported(bool, int, int) { return false; }
-bool tc_pointers_ok(const void *, const void *, int, int) { return false; }
-int tc_encoder_tile() { return 128; }
-int tc_encoder_min_chunk(int, int) { return 1024; }
-int tc_encoder_ctas_per_sm(int, int) { return 1; }
-int tc_encoder_waves() { return 2; }
-cudaError_t launch_encoder_tc(const Problem &, const ShardPlan &, const void *, bool, const void *,
-                              const void *, const uint8_t *, const EncoderWorkspace &,
-                              const EncoderOut &, unsigned *, cudaStream_t) {
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 4-D bf16 tensor map, dims innermost first, 128-byte swizzle, box {64, b1, b2, 1}.
+bool make_map(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint64_t d3, uint32_t box1, uint32_t box2) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {d0, d1, d2, d3};
+    const cuuint64_t strides[3] = {d0 * 2, d0 * d1 * 2, d0 * d1 * d2 * 2};
+    const cuuint32_t box[4] = {64, box1, box2, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+__global__ void f32_to_bf16_kernel(const float *__restrict__ x, __nv_bfloat16 *__restrict__ y,
+                                   int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        y[i] = __float2bfloat16_rn(x[i]);
+}
+
+template <int D, int ROWG, int STAGES>
+cudaError_t launch_enc(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq,
+                       const tc::EncArgs &args, int grid, cudaStream_t st) {
+    using L = tc::EncSmem<D, ROWG, STAGES>;
+    auto k = tc::enc_fwd_tc_kernel<D, ROWG, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::ALLOC);
+    if (e != cudaSuccess) return e;
+    k<<<grid, 64 + 128 * ROWG, L::ALLOC, st>>>(mk, mv, mq, args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(bool bf16, int M, int D) {
+    if (!bf16) return false;
+    if (D == 64) return M == 64 || M == 128 || M == 256;
+    if (D == 128) return M == 64 || M == 128;
+    return false;
+}
+
+bool tc_pointers_ok(const void *a, const void *b, int H, int D) {
+    return ((uintptr_t)a % 16 == 0) && ((uintptr_t)b % 16 == 0) && ((size_t)H * D * 2) % 16 == 0;
+}
+
+bool tc_encoder_plan(const Problem &pr, const int64_t *off, int R, int sms, TcTilePlan &p,
+                     TcEncLayout &lay) {
+    std::memset(&p, 0, sizeof p);
+    p.R = R;
+    int ts = 0, max_nt = 0;
+    for (int r = 0; r < R; ++r) {
+        p.off[r] = off[r];
+        p.tile_start[r] = ts;
+        const int nt = (int)((off[r + 1] - off[r] + 127) / 128);
+        ts += nt;
+        if (nt > max_nt) max_nt = nt;
+    }
+    p.off[R] = off[R];
+    p.tile_start[R] = ts;
+    p.T_bh = ts;
+    p.T_total = (int64_t)pr.B * pr.H * ts;
+    const int64_t want = (int64_t)sms;   // one persistent CTA per SM
+    p.grid = (int)(p.T_total < want ? p.T_total : want);
+    if (p.grid < 1) p.grid = 1;
+    const int64_t span_min = p.T_total > 0 ? p.T_total / p.grid : 1;
+    p.P_max = (int)((max_nt + span_min - 1) / (span_min > 0 ? span_min : 1)) + 1;
+    const size_t bh = (size_t)pr.B * pr.H;
+    size_t o = 0;
+    lay.tickets = o;
+    o += align256(sizeof(unsigned) * bh);
+    lay.part_L = o;
+    o += align256(sizeof(float) * bh * R * p.P_max * pr.M);
+    lay.part_O = o;
+    o += align256(sizeof(float) * bh * R * p.P_max * pr.M * pr.D);
+    lay.shard_L = o;
+    o += align256(sizeof(float) * bh * R * pr.M);
+    lay.q_bf16 = o;
+    o += align256(2 * bh * pr.M * pr.D);
+    lay.bytes = o;
+    return true;
+}
+
+cudaError_t launch_encoder_tc(const Problem &pr, const TcTilePlan &plan, const TcEncLayout &lay,
+                              const void *Q, bool q_is_f32, const void *K, const void *V,
+                              const uint8_t *mask, void *ws, const EncoderOut &out,
+                              unsigned *status, cudaStream_t st) {
+    char *w = (char *)ws;
+    cudaError_t e = cudaMemsetAsync(w + lay.tickets, 0, sizeof(unsigned) * (size_t)pr.B * pr.H, st);
+    if (e != cudaSuccess) return e;
+    const void *Qbf = Q;
+    int64_t qb = pr.q_bstride == 0 ? 1 : pr.B;
+    if (q_is_f32) {
+        // the dynamic FLARE++ queries are fp32: round them to bf16 once for TMA
+        const int64_t n = qb * pr.H * pr.M * pr.D;
+        f32_to_bf16_kernel<<<(unsigned)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024), 256, 0, st>>>(
+            (const float *)Q, (__nv_bfloat16 *)(w + lay.q_bf16), n);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        Qbf = w + lay.q_bf16;
+    }
+    CUtensorMap mk, mv, mq;
+    const uint32_t qrows = pr.M < 128 ? (uint32_t)pr.M : 128u;
+    if (!make_map(&mk, K, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
+        !make_map(&mv, V, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
+        !make_map(&mq, Qbf, pr.D, pr.M, pr.H, qb, qrows, 1))
+        return cudaErrorInvalidValue;
+    tc::EncArgs a;
+    a.B = pr.B;
+    a.H = pr.H;
+    a.M = pr.M;
+    a.N = pr.N;
+    a.sl2 = pr.scale * 1.4426950408889634f;
+    a.q_per_batch = pr.q_bstride != 0;
+    a.mask = mask;
+    a.tickets = (unsigned *)(w + lay.tickets);
+    a.part_L = (float *)(w + lay.part_L);
+    a.part_O = (float *)(w + lay.part_O);
+    a.shard_L = (float *)(w + lay.shard_L);
+    a.O_r = out.O_r;
+    a.L_r = out.L_r;
+    a.Z = out.Z;
+    a.L = out.L;
+    a.status = status;
+    a.plan = plan;
+    if (pr.D == 64 && pr.M <= 128) return launch_enc<64, 1, 4>(mk, mv, mq, a, plan.grid, st);
+    if (pr.D == 64 && pr.M == 256) return launch_enc<64, 2, 3>(mk, mv, mq, a, plan.grid, st);
+    if (pr.D == 128 && pr.M <= 128) return launch_enc<128, 1, 2>(mk, mv, mq, a, plan.grid, st);
     return cudaErrorNotSupported;
 }
+
+bool tc_decode_available() { return false; }
+
 cudaError_t launch_decode_tc(const Problem &, const void *, bool, const float *, const void *,
                              void *, int, unsigned *, cudaStream_t) {
     return cudaErrorNotSupported;
 }
+
 bool tc_bwd_available() { return false; }
 size_t tc_encoder_bwd_workspace(const Problem &, int) { return 0; }
 cudaError_t launch_encoder_bwd_tc(const Problem &, const void *, const void *, const void *,
