@@ -176,7 +176,11 @@ void encoder_layout(const flare_dims_t *d, const int64_t *off, int R, bool tc, E
     EncoderWorkspace &w = lay.ws;
     if (tc) {
         lay.mtiles = 1;
-        tc_encoder_plan(make_problem(d), off, R, sms, lay.tcplan, lay.tclay);
+        if (!tc_encoder_plan(make_problem(d), off, R, sms, lay.tcplan, lay.tclay)) {
+            lay.tc = false;               // too many pieces per (b, h): CUDA-core path
+            encoder_layout(d, off, R, false, lay);
+            return;
+        }
         w.tickets = (unsigned *)lay.tclay.tickets;
         w.part_L = (float *)lay.tclay.part_L;
         w.part_O = (float *)lay.tclay.part_O;
@@ -259,6 +263,7 @@ flare_status_t encoder_run(const flare_dims_t *d, const void *Q, bool q_is_f32, 
         return fail(FLARE_ERR_INVALID_ARG, "tensor-core encoder needs 16-byte aligned Q, K and V");
     static thread_local EncoderLayout lay;     // ~7 KB: kept off the stack
     encoder_layout(d, off, R, tc, lay);
+    const bool use_tc = lay.tc;
     const size_t need = encoder_ws_bytes(d, off, R);
     const int64_t bhm = (int64_t)pr.B * pr.H * pr.M;
     if (pr.N == 0) {                           // no token: every row is empty
@@ -273,7 +278,7 @@ flare_status_t encoder_run(const flare_dims_t *d, const void *Q, bool q_is_f32, 
     EncoderWorkspace w = bind(lay.ws, ws);
     EncoderOut out{O_r, L_r, Z, L};
     cudaError_t e;
-    if (tc) {
+    if (use_tc) {
         DeviceInfo di;
         flare_status_t s = device_info(di);
         if (s != FLARE_OK) return s;

@@ -38,7 +38,7 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 __global__ void f32_to_bf16_kernel(const float *__restrict__ x, __nv_bfloat16 *__restrict__ y,
@@ -48,14 +48,14 @@ __global__ void f32_to_bf16_kernel(const float *__restrict__ x, __nv_bfloat16 *_
         y[i] = __float2bfloat16_rn(x[i]);
 }
 
-template <int D, int ROWG, int STAGES>
+template <int D, bool HALVES, int STAGES>
 cudaError_t launch_enc(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq,
                        const tc::EncArgs &args, int grid, cudaStream_t st) {
-    using L = tc::EncSmem<D, ROWG, STAGES>;
-    auto k = tc::enc_fwd_tc_kernel<D, ROWG, STAGES>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::ALLOC);
+    using C = tc::EncCfg<D, HALVES, STAGES>;
+    auto k = tc::enc_fwd_tc_kernel<D, HALVES, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
     if (e != cudaSuccess) return e;
-    k<<<grid, 64 + 128 * ROWG, L::ALLOC, st>>>(mk, mv, mq, args);
+    k<<<grid, C::THREADS, C::ALLOC, st>>>(mk, mv, mq, args);
     return cudaGetLastError();
 }
 
@@ -93,6 +93,8 @@ bool tc_encoder_plan(const Problem &pr, const int64_t *off, int R, int sms, TcTi
     if (p.grid < 1) p.grid = 1;
     const int64_t span_min = p.T_total > 0 ? p.T_total / p.grid : 1;
     p.P_max = (int)((max_nt + span_min - 1) / (span_min > 0 ? span_min : 1)) + 1;
+    // the in-kernel merge keeps the pieces of one (b, h) in a table of kMergePieces
+    if ((int64_t)R * p.P_max > tc::kMergePieces) return false;
     const size_t bh = (size_t)pr.B * pr.H;
     size_t o = 0;
     lay.tickets = o;
@@ -150,9 +152,9 @@ cudaError_t launch_encoder_tc(const Problem &pr, const TcTilePlan &plan, const T
     a.L = out.L;
     a.status = status;
     a.plan = plan;
-    if (pr.D == 64 && pr.M <= 128) return launch_enc<64, 1, 4>(mk, mv, mq, a, plan.grid, st);
-    if (pr.D == 64 && pr.M == 256) return launch_enc<64, 2, 3>(mk, mv, mq, a, plan.grid, st);
-    if (pr.D == 128 && pr.M <= 128) return launch_enc<128, 1, 2>(mk, mv, mq, a, plan.grid, st);
+    if (pr.D == 64 && pr.M <= 128) return launch_enc<64, false, 5>(mk, mv, mq, a, plan.grid, st);
+    if (pr.D == 64 && pr.M == 256) return launch_enc<64, true, 5>(mk, mv, mq, a, plan.grid, st);
+    if (pr.D == 128 && pr.M <= 128) return launch_enc<128, false, 2>(mk, mv, mq, a, plan.grid, st);
     return cudaErrorNotSupported;
 }
 
