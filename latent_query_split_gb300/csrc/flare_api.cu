@@ -304,9 +304,9 @@ flare_status_t decode_run(const flare_dims_t *d, const void *Q, bool q_is_f32, c
     if (d->kernel == FLARE_KERNEL_TENSOR && !want_tc)
         return fail(FLARE_ERR_UNSUPPORTED, "no tensor-core decode for dtype=%d M=%d D=%d",
                     (int)d->dtype, d->M, d->D);
-    const bool tc = want_tc && tc_pointers_ok(K, Y, d->H, d->D);
+    const bool tc = want_tc && tc_pointers_ok(K, Y, d->H, d->D) && aligned(Q, 16) && aligned(Z, 16);
     if (d->kernel == FLARE_KERNEL_TENSOR && !tc)
-        return fail(FLARE_ERR_INVALID_ARG, "tensor-core decode needs 16-byte aligned K and Y");
+        return fail(FLARE_ERR_INVALID_ARG, "tensor-core decode needs 16-byte aligned Q, Z, K and Y");
     cudaError_t e;
     if (tc) {
         DeviceInfo di;

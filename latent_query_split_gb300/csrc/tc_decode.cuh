@@ -1,0 +1,373 @@
+// tc_decode.cuh -- FLARE local decode on sm_103a tensor cores.
+//
+// Y[b,n,h] = sum_m softmax_m(s <K[b,n,h], Q_m>) Z[b,h,m]  ("FLARE++: Low-rank
+// attention with dynamic attention routing", appendix on context parallelism,
+// FLARE decode paragraph: each token's query is local, the latent tensors Q
+// and Z are replicated). Each token row's softmax runs over the M latents, so
+// it is exact in one tile (no running rescale).
+//
+// One persistent CTA per SM walks a contiguous span of 128-token tiles in
+// (b, h, tile) order. Warp roles:
+//   warp 0     producer: K tiles by TMA into a STAGES-deep ring; on every
+//              (b, h) change it converts Q and Z (bf16 or fp32) into swizzled
+//              bf16 operand tiles in shared memory.
+//   warp 1     TMEM allocator; lane 0 issues the MMAs:
+//                S_g = K Q^T   (A = K tile, B = Q, both shared memory)
+//                Y_g = P_g Z   (A = P from tensor memory, B = Z shared memory)
+//   warps 2-9  two groups of four warps take alternate tiles (one token row per
+//              thread = TMEM lane): row max, exp2, P (bf16) over S in tensor
+//              memory, then Y / l rounded to bf16 and stored to global memory.
+#pragma once
+
+#include "tc_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace flare {
+namespace tc {
+
+struct DecArgs {
+    int B, H, M, N;
+    float sl2;                  // score scale * log2(e)
+    int q_per_batch;            // Q has a batch dimension
+    int q_f32;                  // Q is fp32 (else bf16)
+    const void *Q;
+    const float *Z;
+    __nv_bfloat16 *Y;
+    int64_t T_bh;               // tiles per (b, h)
+    int64_t T_total;            // tiles over every (b, h)
+    int grid;
+    unsigned *status;
+};
+
+template <int M, int D, int STAGES>
+struct DecCfg {
+    static constexpr int KA = D / 64;                   // 64-element atoms along D
+    static constexpr int NG = M <= 128 ? 2 : 1;         // softmax groups (tiles in flight)
+    static constexpr int THREADS = 64 + 128 * NG;
+    static constexpr uint32_t QZ_ATOM = M * 128;        // bytes of one M-row x 64-col atom
+    static constexpr uint32_t Q_OFF = 0;
+    static constexpr uint32_t Z_OFF = Q_OFF + KA * QZ_ATOM;
+    static constexpr uint32_t STAGE_OFF = Z_OFF + KA * QZ_ATOM;
+    static constexpr uint32_t STAGE_BYTES = KA * 128 * 128;   // one K tile
+    static constexpr uint32_t BAR_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
+    static constexpr int NCH = M / 32;                   // P chunks of 32 latents
+    // full[S], empty[S], qz_full, qz_free, s_full[2], p_chunk[2][8], o_done[2]
+    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 16 + 2;
+    static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr uint32_t BYTES = MISC_OFF + 64;
+    static constexpr uint32_t ALLOC = BYTES + 1024;
+    static_assert(ALLOC <= 232448, "shared memory budget of one CTA exceeded");
+    static constexpr uint32_t TMEM_COLS = 512;           // group g: S/P at 256g, Y at 256g + M
+};
+
+// Writes rows [0, M) x D of a row-major matrix into the 128-byte-swizzled bf16
+// operand layout (64-column atoms of M rows, 16-byte chunk j of row r at chunk
+// position j ^ (r % 8)), by the 32 lanes of one warp. 16-byte loads.
+__device__ __forceinline__ uint4 load_chunk8(const __nv_bfloat16 *src) {
+    return __ldg(reinterpret_cast<const uint4 *>(src));
+}
+__device__ __forceinline__ uint4 load_chunk8(const float *src) {
+    const float4 lo = __ldg(reinterpret_cast<const float4 *>(src));
+    const float4 hi = __ldg(reinterpret_cast<const float4 *>(src) + 1);
+    return make_uint4(pack_bf16(lo.x, lo.y), pack_bf16(lo.z, lo.w), pack_bf16(hi.x, hi.y),
+                      pack_bf16(hi.z, hi.w));
+}
+template <int M, int D, typename T>
+__device__ __forceinline__ void stage_rows_bf16(uint8_t *dst, const T *src, int lane) {
+    constexpr int CHUNKS = M * D / 8;                   // 16-byte output chunks
+#pragma unroll 4
+    for (int c = lane; c < CHUNKS; c += 32) {
+        const int row = c / (D / 8), j = c % (D / 8);    // chunk j covers cols 8j..8j+7
+        const int atom = j >> 3, jj = j & 7;
+        uint8_t *p = dst + atom * (M * 128) + row * 128 + ((jj ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4 *>(p) = load_chunk8(src + (int64_t)row * D + 8 * j);
+    }
+}
+
+template <int M, int D, int STAGES>
+__global__ void __launch_bounds__(DecCfg<M, D, STAGES>::THREADS, 1)
+dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const DecArgs a) {
+    using C = DecCfg<M, D, STAGES>;
+    constexpr int KA = C::KA;
+    constexpr int NG = C::NG;
+    constexpr int NCH = C::NCH;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + C::Q_OFF, sZ = sbase + C::Z_OFF, sStage = sbase + C::STAGE_OFF;
+    const uint32_t bar0 = sbase + C::BAR_OFF;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    const uint32_t qz_full = bar0 + 8u * (2 * STAGES), qz_free = qz_full + 8;
+    auto s_full = [&](int g) { return bar0 + 8u * (2 * STAGES + 2 + g); };
+    auto p_chunk = [&](int g, int c) { return bar0 + 8u * (2 * STAGES + 4 + 8 * g + c); };
+    auto o_done = [&](int g) { return bar0 + 8u * (2 * STAGES + 20 + g); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const int64_t tb = ((int64_t)cta * a.T_total + a.grid - 1) / a.grid;
+    const int64_t te = ((int64_t)(cta + 1) * a.T_total + a.grid - 1) / a.grid;
+    const int64_t ntiles = te - tb;
+    Waiter wt{abort_flag, a.status};
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(qz_full, 1);
+        mbar_init(qz_free, 1);
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(s_full(g), 1);
+            for (int c = 0; c < 8; ++c) mbar_init(p_chunk(g, c), 128);
+            mbar_init(o_done(g), 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) prefetch_tmap(&tmK);
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // first tile and its (b, h) / token tile index, advanced without divisions
+    const int64_t bh0 = tb / a.T_bh;
+    const int64_t k0 = tb - bh0 * a.T_bh;
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        const uint64_t pol = policy_evict_first();
+        int64_t bh = bh0, kt = k0, cur_bh = -1;
+        uint32_t qz_uses = 0;
+        int64_t j = 0;
+        for (; j < ntiles && !wt.aborted(); ++j) {
+            const int b = (int)(bh / a.H), h = (int)(bh - (int64_t)b * a.H);
+            if (bh != cur_bh) {
+                // Q and Z of the new (b, h), once the MMAs on the old ones are done
+                if (qz_uses > 0 && !__all_sync(0xffffffffu, wt.wait(qz_free, (qz_uses - 1) & 1))) break;
+                const int qb = a.q_per_batch ? b : 0;
+                const int64_t qoff = ((int64_t)qb * a.H + h) * M * D;
+                if (a.q_f32)
+                    stage_rows_bf16<M, D>(smem + C::Q_OFF, reinterpret_cast<const float *>(a.Q) + qoff, lane);
+                else
+                    stage_rows_bf16<M, D>(smem + C::Q_OFF, reinterpret_cast<const __nv_bfloat16 *>(a.Q) + qoff, lane);
+                stage_rows_bf16<M, D>(smem + C::Z_OFF, a.Z + ((int64_t)b * a.H + h) * M * D, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(qz_full);
+                ++qz_uses;
+                cur_bh = bh;
+            }
+            const int s = (int)(j % STAGES);
+            if (!__all_sync(0xffffffffu, wt.wait(empty(s), ((uint32_t)(j / STAGES) & 1) ^ 1))) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full(s), C::STAGE_BYTES);
+                const uint32_t dst = sStage + s * C::STAGE_BYTES;
+                for (int ka = 0; ka < KA; ++ka)
+                    tma_load_4d_hint(dst + ka * (128 * 128), &tmK, 64 * ka, h, (int)(kt * 128), b, full(s), pol);
+            }
+            __syncwarp();
+            if (++kt == a.T_bh) {
+                kt = 0;
+                ++bh;
+            }
+        }
+        if (wt.aborted() && lane == 0) {
+            // let every issued load land before the CTA exits
+            const uint64_t t0 = globaltimer();
+            for (int64_t jj = (j > STAGES ? j - STAGES : 0); jj < j; ++jj)
+                while (!mbar_try_wait(full((int)(jj % STAGES)), (uint32_t)(jj / STAGES) & 1) &&
+                       globaltimer() - t0 < 500000000ull) {
+                }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_m128(M, 0);
+            constexpr uint32_t idPV = idesc_bf16_m128(D, 1);
+            const uint64_t dK0 = desc_sw128(sStage, 16, 1024);
+            const uint64_t dQ0 = desc_sw128(sQ, 16, 1024);
+            const uint64_t dZ0 = desc_sw128(sZ, C::QZ_ATOM, 1024);
+            constexpr uint64_t kStageDesc = C::STAGE_BYTES >> 4;
+            int64_t bhS = bh0, ktS = k0, cur_bh = -1;   // cursor of the S tiles
+            int64_t bhP = bh0, ktP = k0;                 // cursor of the PV tiles
+            uint32_t qz_uses = 0;
+            bool ok = true;
+            auto issue_s = [&](int64_t jj) -> bool {
+                const int s = (int)(jj % STAGES);
+                if (bhS != cur_bh) {
+                    if (!wt.wait(qz_full, qz_uses & 1)) return false;
+                    ++qz_uses;
+                    cur_bh = bhS;
+                }
+                if (!wt.wait(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
+                tc_fence_after();
+                const int g = NG == 2 ? (int)(jj & 1) : 0;
+                const uint64_t dK = dK0 + kStageDesc * s;
+#pragma unroll
+                for (int kb = 0; kb < D / 16; ++kb) {
+                    const uint64_t offK = (uint64_t)((kb >> 2) * (128 * 128) + (kb & 3) * 32) >> 4;
+                    const uint64_t offQ = (uint64_t)((kb >> 2) * C::QZ_ATOM + (kb & 3) * 32) >> 4;
+                    umma_bf16_ss(tmem + g * 256, dK + offK, dQ0 + offQ, idS, kb > 0 ? 1u : 0u);
+                }
+                umma_commit(s_full(g));
+                umma_commit(empty(s));            // the K tile is only read by S
+                if (++ktS == a.T_bh) {
+                    ktS = 0;
+                    ++bhS;
+                }
+                return true;
+            };
+            // S runs at most NG tiles ahead of PV; the S of a new (b, h) waits
+            // until every older tile's PV is issued (Q and Z are then replaced)
+            int64_t jS = 0, nP = 0;
+            auto pump_s = [&]() -> bool {
+                while (jS < ntiles && jS < nP + NG && (bhS == cur_bh || nP == jS))
+                    if (!issue_s(jS++)) return false;
+                return true;
+            };
+            ok = pump_s();
+            for (; nP < ntiles && ok;) {
+                const int64_t jP = nP;
+                const int g = NG == 2 ? (int)(jP & 1) : 0;
+                const int64_t kP = NG == 2 ? (jP >> 1) : jP;
+                for (int c = 0; c < NCH && ok; ++c) {
+                    ok = wt.wait(p_chunk(g, c), (uint32_t)kP & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const int kb = 2 * c + kk;       // 16 latents per MMA
+                        umma_bf16_ts(tmem + g * 256 + M, tmem + g * 256 + kb * 8, dZ0 + kb * (2048 >> 4),
+                                     idPV, kb > 0 ? 1u : 0u);
+                    }
+                }
+                if (!ok) break;
+                umma_commit(o_done(g));
+                const int64_t bh_done = bhP;
+                if (++ktP == a.T_bh) {
+                    ktP = 0;
+                    ++bhP;
+                }
+                ++nP;
+                if (nP == ntiles || bhP != bh_done) umma_commit(qz_free);
+                ok = pump_s();
+            }
+            // make every issued MMA finish before TMEM is released
+            if (ok && ntiles > 0) {
+                const int gl = NG == 2 ? (int)((ntiles - 1) & 1) : 0;
+                const int64_t kl = NG == 2 ? ((ntiles - 1) >> 1) : ntiles - 1;
+                wt.wait(o_done(gl), (uint32_t)kl & 1);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- softmax + epilogue warps ----------------
+        const int g = (warp - 2) >> 2;
+        const int quad = warp & 3;
+        const int rig = quad * 32 + lane;            // token row within the tile (TMEM lane)
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const uint32_t s_tmem = tmem + g * 256 + lane_off;
+        const uint32_t y_tmem = tmem + g * 256 + M + lane_off;
+        const uint64_t c2 = f2pack(a.sl2, a.sl2);
+        auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
+            return __all_sync(0xffffffffu, wt.wait(bar, par));
+        };
+        int64_t bh = bh0, kt = k0;
+        for (int64_t j = 0; j < ntiles; ++j) {
+            const bool mine = NG == 1 || (int)(j & 1) == g;
+            if (mine) {
+                const int64_t k = NG == 2 ? (j >> 1) : j;
+                if (!wwait(s_full(g), (uint32_t)k & 1)) break;
+                tc_fence_after();
+                // pass 1: row maximum over the M latents
+                float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                for (int c = 0; c < M / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(s_tmem + c * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        mx[i & 1] = max3(mx[i & 1], __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                }
+                const float m = fmaxf(mx[0], mx[1]) * a.sl2;
+                const uint64_t nm2 = f2pack(-m, -m);
+                // pass 2: P = exp2(s*c - m) in bf16 over S's first M/2 columns
+                uint64_t ls2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(s_tmem + c * 32, r);
+                    tmem_wait_ld();
+                    uint32_t pw[16];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float t0, t1, t2, t3;
+                        f2unpack(fma2(f2pack(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), c2, nm2), t0, t1);
+                        f2unpack(fma2(f2pack(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), c2, nm2), t2, t3);
+                        const float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
+                        ls2[0] = add2(ls2[0], f2pack(p0, p1));
+                        ls2[1] = add2(ls2[1], f2pack(p2, p3));
+                        pw[2 * i] = pack_bf16(p0, p1);
+                        pw[2 * i + 1] = pack_bf16(p2, p3);
+                    }
+                    tmem_st16(s_tmem + c * 16, pw);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(p_chunk(g, c));
+                }
+                float l;
+                {
+                    float a0, a1, a2, a3;
+                    f2unpack(ls2[0], a0, a1);
+                    f2unpack(ls2[1], a2, a3);
+                    l = (a0 + a1) + (a2 + a3);
+                }
+                // epilogue: Y row / l in bf16 (rows past N belong to no token)
+                if (!wwait(o_done(g), (uint32_t)k & 1)) break;
+                tc_fence_after();
+                const float inv = 1.f / l;
+                const int b = (int)(bh / a.H), h = (int)(bh - (int64_t)b * a.H);
+                const int64_t n = kt * 128 + rig;
+                __nv_bfloat16 *yrow = a.Y + (((int64_t)b * a.N + n) * a.H + h) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(y_tmem + c * 32, r);
+                    tmem_wait_ld();
+                    if (n < a.N) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                w[q] = pack_bf16(__uint_as_float(r[8 * v + 2 * q]) * inv,
+                                                 __uint_as_float(r[8 * v + 2 * q + 1]) * inv);
+                            reinterpret_cast<uint4 *>(yrow + c * 32)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+                tc_fence_before();
+            }
+            if (++kt == a.T_bh) {
+                kt = 0;
+                ++bh;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+}  // namespace tc
+}  // namespace flare

@@ -2,6 +2,7 @@
 // encoder's work split and workspace, TMA tensor maps, and the launchers.
 #include "tc_common.cuh"
 #include "tc_encoder.cuh"
+#include "tc_decode.cuh"
 
 #include <cudaTypedefs.h>
 
@@ -158,10 +159,45 @@ cudaError_t launch_encoder_tc(const Problem &pr, const TcTilePlan &plan, const T
     return cudaErrorNotSupported;
 }
 
-bool tc_decode_available() { return false; }
+bool tc_decode_available() { return true; }
 
-cudaError_t launch_decode_tc(const Problem &, const void *, bool, const float *, const void *,
-                             void *, int, unsigned *, cudaStream_t) {
+namespace {
+template <int M, int D, int STAGES>
+cudaError_t launch_dec(const CUtensorMap &mk, const tc::DecArgs &args, cudaStream_t st) {
+    using C = tc::DecCfg<M, D, STAGES>;
+    auto k = tc::dec_fwd_tc_kernel<M, D, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
+    if (e != cudaSuccess) return e;
+    k<<<args.grid, C::THREADS, C::ALLOC, st>>>(mk, args);
+    return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_decode_tc(const Problem &pr, const void *Q, bool q_is_f32, const float *Z,
+                             const void *K, void *Y, int sms, unsigned *status, cudaStream_t st) {
+    CUtensorMap mk;
+    if (!make_map(&mk, K, pr.D, pr.H, pr.N, pr.B, 1, 128)) return cudaErrorInvalidValue;
+    tc::DecArgs a;
+    a.B = pr.B;
+    a.H = pr.H;
+    a.M = pr.M;
+    a.N = pr.N;
+    a.sl2 = pr.scale * 1.4426950408889634f;
+    a.q_per_batch = pr.q_bstride != 0;
+    a.q_f32 = q_is_f32;
+    a.Q = Q;
+    a.Z = Z;
+    a.Y = (__nv_bfloat16 *)Y;
+    a.T_bh = (pr.N + 127) / 128;
+    a.T_total = (int64_t)pr.B * pr.H * a.T_bh;
+    a.grid = (int)(a.T_total < sms ? a.T_total : sms);
+    a.status = status;
+    if (a.T_total == 0) return cudaSuccess;
+    if (pr.M == 128 && pr.D == 64) return launch_dec<128, 64, 8>(mk, a, st);
+    if (pr.M == 64 && pr.D == 64) return launch_dec<64, 64, 8>(mk, a, st);
+    if (pr.M == 256 && pr.D == 64) return launch_dec<256, 64, 8>(mk, a, st);
+    if (pr.M == 64 && pr.D == 128) return launch_dec<64, 128, 5>(mk, a, st);
+    if (pr.M == 128 && pr.D == 128) return launch_dec<128, 128, 4>(mk, a, st);
     return cudaErrorNotSupported;
 }
 
