@@ -38,9 +38,9 @@ PROFILE_SUMMARY = {  # kernel -> committed ncu summary holding its DRAM traffic
     "encoder": os.path.join(ROOT, "profiles", "encoder_c2_bf16.md"),
     "decode": os.path.join(ROOT, "profiles", "decode_c2_bf16.md"),
 }
-KERNEL_SOURCES = {
-    "encoder": ["tc_kernels.cu", "tc_encoder.cuh", "simt_kernels.cu"],
-    "decode": ["tc_kernels.cu", "tc_decode.cuh", "simt_kernels.cu"],
+KERNEL_SOURCES = {   # files whose content the profiled traffic belongs to
+    "encoder": ["tc_encoder.cuh", "tc_ptx.cuh", "tc_kernels.cu"],
+    "decode": ["tc_decode.cuh", "tc_ptx.cuh", "tc_kernels.cu"],
 }
 
 
