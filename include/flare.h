@@ -203,6 +203,27 @@ FLARE_API flare_status_t flare_encoder_bwd(const flare_dims_t *dims, const void 
                                  const float *L, const float *dZ, float *dQ, void *dK, void *dV,
                                  void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Split-KV encoder without a workspace argument, for callers that cannot
+ * allocate device memory: plugins inside host frameworks that own all device
+ * memory and hand none to extensions, and code on paths where calling
+ * cudaMalloc is not allowed. The pages have no counterpart; the arithmetic,
+ * arguments and results are those of flare_encoder_fwd.
+ * Its scratch memory is one static device array of 32 MiB (2^25 bytes) in
+ * this library, held by every GPU that loads the library until the process
+ * exits. Problems whose flare_workspace_bytes(FLARE_OP_ENCODER_FWD, ...)
+ * exceeds it are rejected with FLARE_ERR_WORKSPACE. The first call on a
+ * device looks the array's device address up (cudaGetSymbolAddress), so make
+ * that first call before any stream capture. Every call on a device shares
+ * the array: calls that may overlap on the GPU (other streams, other host
+ * threads) race and give wrong results; serialise them. Nothing is allocated
+ * or freed; the ticket counters are cleared with cudaMemsetAsync each call.
+ */
+FLARE_API flare_status_t flare_encoder_fwd_noalloc(const flare_dims_t *dims, const void *Q,
+                                                   const void *K, const void *V, const uint8_t *mask,
+                                                   const int64_t *shard_offsets, int R, float *O_r,
+                                                   float *L_r, float *Z, float *L, void *stream);
+
 /* Synchronises `stream`, then reads and clears the device status word that
  * kernels set when they abandon a bounded wait: FLARE_OK, FLARE_ERR_TIMEOUT,
  * or FLARE_ERR_CUDA if the synchronisation itself failed. */

@@ -320,6 +320,27 @@ flare_status_t decode_run(const flare_dims_t *d, const void *Q, bool q_is_f32, c
 }
 
 }  // namespace
+
+// Entry points for the allocation-free encoder (noalloc.cu): the same
+// validation, planning and launch as flare_encoder_fwd, with the workspace
+// size and the error text exposed.
+size_t encoder_workspace_size(const flare_dims_t *dims, const int64_t *off, int R) {
+    if (check_dims(dims) != FLARE_OK || check_offsets(off, R, dims->N) != FLARE_OK) return (size_t)-1;
+    return encoder_ws_bytes(dims, off, R);
+}
+
+flare_status_t encoder_fwd_with_workspace(const flare_dims_t *dims, const void *Q, const void *K,
+                                          const void *V, const uint8_t *mask, const int64_t *off,
+                                          int R, float *O_r, float *L_r, float *Z, float *L,
+                                          void *ws, size_t ws_bytes, cudaStream_t st) {
+    flare_status_t s = check_dims(dims);
+    if (s != FLARE_OK) return s;
+    if ((s = check_offsets(off, R, dims->N)) != FLARE_OK) return s;
+    return encoder_run(dims, Q, false, K, V, mask, off, R, O_r, L_r, Z, L, ws, ws_bytes, st);
+}
+
+flare_status_t report_error(flare_status_t s, const char *msg) { return fail(s, "%s", msg); }
+
 }  // namespace flare
 
 using namespace flare;

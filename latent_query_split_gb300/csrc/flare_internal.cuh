@@ -92,6 +92,14 @@ constexpr int kSimtRows = 32;
 // Tokens one SIMT encoder tile covers.
 constexpr int kSimtTile = 32;
 
+// Shared with the allocation-free encoder entry point (noalloc.cu).
+size_t encoder_workspace_size(const flare_dims_t *dims, const int64_t *off, int R);
+flare_status_t encoder_fwd_with_workspace(const flare_dims_t *dims, const void *Q, const void *K,
+                                          const void *V, const uint8_t *mask, const int64_t *off,
+                                          int R, float *O_r, float *L_r, float *Z, float *L,
+                                          void *ws, size_t ws_bytes, cudaStream_t st);
+flare_status_t report_error(flare_status_t s, const char *msg);
+
 void reset_device_status();
 unsigned read_and_clear_device_status(cudaStream_t st, cudaError_t *err);
 

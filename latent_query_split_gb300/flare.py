@@ -28,8 +28,8 @@ FLARE_MAX_SHARDS = 256
 
 # Every symbol the header declares (checked by the test-suite).
 EXPORTS = ("flare_workspace_bytes", "flare_encoder_fwd", "flare_lse_merge", "flare_decode_fwd",
-           "flare_fwd", "flare_pp_fwd", "flare_encoder_bwd", "flare_device_status",
-           "flare_last_error_string", "flare_version")
+           "flare_fwd", "flare_pp_fwd", "flare_encoder_bwd", "flare_encoder_fwd_noalloc",
+           "flare_device_status", "flare_last_error_string", "flare_version")
 
 
 class FlareError(RuntimeError):
@@ -72,6 +72,7 @@ def load_library(build_if_missing: bool = True):
     lib.flare_fwd.argtypes = [D, P, P, P, P, P, I, P, P, P, P, Z, P]
     lib.flare_pp_fwd.argtypes = [D, P, P, P, P, P, P, P, I, P, P, P, P, P, P, Z, P]
     lib.flare_encoder_bwd.argtypes = [D, P, P, P, P, P, I, P, P, P, P, P, P, P, Z, P]
+    lib.flare_encoder_fwd_noalloc.argtypes = [D, P, P, P, P, P, I, P, P, P, P, P]
     lib.flare_device_status.argtypes = [P]
     lib.flare_last_error_string.restype = ctypes.c_char_p
     lib.flare_version.restype = I
@@ -253,6 +254,30 @@ def flare_encoder_bwd(Q, K, V, mask, shard_offsets, Z, L, dZ, *, dQ=None, dK=Non
                                  R, _ptr(Z), _ptr(L), _ptr(dZ), _ptr(dQ), _ptr(dK), _ptr(dV),
                                  _ptr(ws), nbytes, _stream(stream)))
     return dQ, dK, dV
+
+
+def flare_encoder_fwd_noalloc(Q, K, V, mask=None, shard_offsets=None, *, O_r=None, L_r=None,
+                              Z=None, L=None, shard_outputs=False, global_outputs=True,
+                              scale=None, kernel="auto", stream=None):
+    """flare_encoder_fwd without a workspace: the library's static device
+    scratch is used instead (see include/flare.h for its size and rules).
+    Returns (O_r, L_r, Z, L) with None for pairs not requested."""
+    lib = load_library()
+    dims = make_dims(Q, K, scale, kernel)
+    B, N, H, D = K.shape
+    M = Q.shape[-2]
+    shard_offsets = [0, N] if shard_offsets is None else list(shard_offsets)
+    R = len(shard_offsets) - 1
+    f32 = dict(dtype=torch.float32, device=K.device)
+    if shard_outputs and O_r is None:
+        O_r, L_r = torch.empty((R, B, H, M, D), **f32), torch.empty((R, B, H, M), **f32)
+    if global_outputs and Z is None:
+        Z, L = torch.empty((B, H, M, D), **f32), torch.empty((B, H, M), **f32)
+    arr, R = _offsets(shard_offsets)
+    _check(lib.flare_encoder_fwd_noalloc(ctypes.byref(dims), _ptr(Q), _ptr(K), _ptr(V), _ptr(mask),
+                                         arr, R, _ptr(O_r), _ptr(L_r), _ptr(Z), _ptr(L),
+                                         _stream(stream)))
+    return O_r, L_r, Z, L
 
 
 def flare_device_status(stream=None):
