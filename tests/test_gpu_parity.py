@@ -192,6 +192,24 @@ def test_max_shards_and_single_token_shards(cuda_device):
     assert_L_close("L_r", L_r, Lro)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_max_shards_bf16(cuda_device, kernel):
+    """FLARE_MAX_SHARDS ragged shards (some empty) on the bf16 path."""
+    N = 40000
+    rng = np.random.default_rng(14)
+    cuts = np.sort(rng.integers(0, N + 1, size=255))
+    off = [0] + [int(c) for c in cuts] + [N]
+    Q, K, V, mask = _problem(15, 1, 2, 128, N, 64, "bf16", off)
+    O_r, L_r, Z, L = _call(flare.flare_encoder_fwd, Q, K, V, mask, off, shard_outputs=True,
+                           kernel=kernel)
+    Zo, Lo = oracle.encode(Q, K, V, mask)
+    assert_close("Z", Z, Zo, "bf16")
+    assert_L_close("L", L, Lo)
+    Oo, Lro = oracle.encode_shards(Q, K, V, mask, off)
+    assert_close("O_r", O_r, Oo, "bf16")
+    assert_L_close("L_r", L_r, Lro)
+
+
 def test_minimal_sizes(cuda_device):
     Q, K, V, _ = _problem(11, 1, 1, 1, 5, 1, "f32", [0, 5], pad=0)
     Y, Z, L = flare.flare_fwd(Q, K, V)
