@@ -14,7 +14,7 @@ bool tc_supported(bool bf16, int M, int D);
 // multiple of 16.
 bool tc_pointers_ok(const void *a, const void *b, int H, int D);
 
-// Split of the encoder's work. Every shard is cut into tiles of 128 tokens
+// Split of the encoder's work. Every shard is cut into tiles of `tile` tokens
 // (the last one ragged); all (b, h) share the shard layout, so tile t of the
 // flattened order (b, h)-major, then shard, then tile sits at a computable
 // place. `grid` persistent CTAs each take one contiguous, equally long span
@@ -23,6 +23,7 @@ bool tc_pointers_ok(const void *a, const void *b, int H, int D);
 // that finishes a piece of the same (b, h).
 struct TcTilePlan {
     int R;
+    int tile;                       // tokens per tile
     int T_bh;                       // tiles per (b, h)
     int P_max;                      // partial slots per (b, h, shard)
     int grid;                       // persistent CTAs

@@ -49,11 +49,9 @@ __global__ void f32_to_bf16_kernel(const float *__restrict__ x, __nv_bfloat16 *_
         y[i] = __float2bfloat16_rn(x[i]);
 }
 
-template <int D, bool HALVES, int STAGES>
-cudaError_t launch_enc(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq,
+template <class C, class Kernel>
+cudaError_t launch_enc(Kernel k, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq,
                        const tc::EncArgs &args, int grid, cudaStream_t st) {
-    using C = tc::EncCfg<D, HALVES, STAGES>;
-    auto k = tc::enc_fwd_tc_kernel<D, HALVES, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
     if (e != cudaSuccess) return e;
     k<<<grid, C::THREADS, C::ALLOC, st>>>(mk, mv, mq, args);
@@ -77,11 +75,12 @@ bool tc_encoder_plan(const Problem &pr, const int64_t *off, int R, int sms, TcTi
                      TcEncLayout &lay) {
     std::memset(&p, 0, sizeof p);
     p.R = R;
+    p.tile = pr.D == 128 ? 64 : 128;          // one K/V stage is 32 KB either way
     int ts = 0, max_nt = 0;
     for (int r = 0; r < R; ++r) {
         p.off[r] = off[r];
         p.tile_start[r] = ts;
-        const int nt = (int)((off[r + 1] - off[r] + 127) / 128);
+        const int nt = (int)((off[r + 1] - off[r] + p.tile - 1) / p.tile);
         ts += nt;
         if (nt > max_nt) max_nt = nt;
     }
@@ -131,8 +130,8 @@ cudaError_t launch_encoder_tc(const Problem &pr, const TcTilePlan &plan, const T
     }
     CUtensorMap mk, mv, mq;
     const uint32_t qrows = pr.M < 128 ? (uint32_t)pr.M : 128u;
-    if (!make_map(&mk, K, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
-        !make_map(&mv, V, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
+    if (!make_map(&mk, K, pr.D, pr.H, pr.N, pr.B, 1, (uint32_t)plan.tile) ||
+        !make_map(&mv, V, pr.D, pr.H, pr.N, pr.B, 1, (uint32_t)plan.tile) ||
         !make_map(&mq, Qbf, pr.D, pr.M, pr.H, qb, qrows, 1))
         return cudaErrorInvalidValue;
     tc::EncArgs a;
@@ -153,9 +152,12 @@ cudaError_t launch_encoder_tc(const Problem &pr, const TcTilePlan &plan, const T
     a.L = out.L;
     a.status = status;
     a.plan = plan;
-    if (pr.D == 64 && pr.M <= 128) return launch_enc<64, false, 5>(mk, mv, mq, a, plan.grid, st);
-    if (pr.D == 64 && pr.M == 256) return launch_enc<64, true, 5>(mk, mv, mq, a, plan.grid, st);
-    if (pr.D == 128 && pr.M <= 128) return launch_enc<128, false, 2>(mk, mv, mq, a, plan.grid, st);
+    if (pr.D == 64 && pr.M <= 128)
+        return launch_enc<tc::CsCfg<64, 5>>(tc::enc_cs_kernel<64, 5>, mk, mv, mq, a, plan.grid, st);
+    if (pr.D == 128 && pr.M <= 128)
+        return launch_enc<tc::CsCfg<128, 4>>(tc::enc_cs_kernel<128, 4>, mk, mv, mq, a, plan.grid, st);
+    if (pr.D == 64 && pr.M == 256)
+        return launch_enc<tc::HalvesCfg<5>>(tc::enc_halves_kernel<5>, mk, mv, mq, a, plan.grid, st);
     return cudaErrorNotSupported;
 }
 

@@ -82,6 +82,25 @@ struct Waiter {
         if (mbar_try_wait(bar, parity)) return true;
         return wait_slow(bar, parity);
     }
+    // Spin with test_wait (no suspension): for a thread whose reaction time
+    // is on the critical path and whose warp has nothing else to do.
+    __device__ __forceinline__ bool spin(uint32_t bar, uint32_t parity) const {
+        if (mbar_test(bar, parity)) return true;
+        return spin_slow(bar, parity);
+    }
+    __device__ __noinline__ bool spin_slow(uint32_t bar, uint32_t parity) const {
+        const uint64_t t0 = globaltimer();
+        while (true) {
+            for (int i = 0; i < 64; ++i)
+                if (mbar_test(bar, parity)) return true;
+            if (*abort) return false;
+            if (globaltimer() - t0 > kWaitNs) {
+                *abort = 1;
+                atomicExch(status, 1u);
+                return false;
+            }
+        }
+    }
     __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity) const {
         const uint64_t t0 = globaltimer();
         while (true) {
@@ -168,6 +187,37 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Warp-collective forms of the two MMAs and the commit: the whole (converged)
+// warp executes them and elect.sync picks the issuing lane. Issued this way an
+// MMA costs about half the scheduler time of one issued from a single lane
+// inside a divergent branch.
+__device__ __forceinline__ void umma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit_elect(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -242,6 +292,18 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uin
     return d;
 }
 
+// UMMA shared-memory descriptor, no swizzle, K-major: 8-row x 16-byte core
+// matrices; LBO = distance between the two core matrices along K (a K = 16
+// bf16 block has two), SBO = distance between 8-row groups along M/N.
+__device__ __forceinline__ uint64_t desc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
 // A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), M = 128, N = n.
 __host__ __device__ constexpr uint32_t idesc_bf16_m128(uint32_t n, uint32_t b_mn) {
@@ -282,9 +344,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
-}
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 }  // namespace tc
