@@ -181,10 +181,10 @@ void encoder_layout(const flare_dims_t *d, const int64_t *off, int R, bool tc, E
             encoder_layout(d, off, R, false, lay);
             return;
         }
-        w.tickets = (unsigned *)lay.tclay.tickets;
+        w.tickets = nullptr;              // the tensor-core path merges in a separate kernel
         w.part_L = (float *)lay.tclay.part_L;
         w.part_O = (float *)lay.tclay.part_O;
-        w.shard_L = (float *)lay.tclay.shard_L;
+        w.shard_L = nullptr;
         w.bytes = lay.tclay.bytes;
         return;
     }

@@ -19,8 +19,8 @@ bool tc_pointers_ok(const void *a, const void *b, int H, int D);
 // flattened order (b, h)-major, then shard, then tile sits at a computable
 // place. `grid` persistent CTAs each take one contiguous, equally long span
 // of that order; a span cut into (b, h, shard) pieces gives one partial
-// (normalised output and log-normaliser) per piece, merged by the last CTA
-// that finishes a piece of the same (b, h).
+// (normalised output and log-normaliser) per piece, merged afterwards by a
+// separate kernel.
 struct TcTilePlan {
     int R;
     int tile;                       // tokens per tile
@@ -32,9 +32,10 @@ struct TcTilePlan {
     int tile_start[kMaxShards + 1]; // first tile of each shard within a (b, h)
 };
 
-// Byte offsets of the encoder workspace regions.
+// Byte offsets of the encoder workspace regions: per-piece partials (L, O)
+// and a bf16 copy of an fp32 query.
 struct TcEncLayout {
-    size_t tickets, part_L, part_O, shard_L, q_bf16, bytes;
+    size_t part_L, part_O, q_bf16, bytes;
 };
 
 bool tc_encoder_plan(const Problem &pr, const int64_t *off, int R, int sms, TcTilePlan &plan,

@@ -35,9 +35,9 @@
 // more than kTau), P = exp2(S - m) in bf16 written back into tensor memory
 // for the PV MMA (A operand from tensor memory).
 // At the end of each (b, h, shard) piece of its span a CTA writes a partial
-// (normalised output, log-normaliser); the CTA that completes the last piece
-// of a (b, h) (atomic ticket, nobody waits) merges them: pieces into shards
-// (O_r, L_r), shards into (Z, L), in fixed order.
+// (normalised output, log-normaliser). enc_merge_kernel, launched right after,
+// merges them in fixed order: pieces into shards (O_r, L_r), shards into
+// (Z, L), by the one log-sum-exp rule.
 #pragma once
 
 #include "tc_common.cuh"
@@ -47,9 +47,7 @@ namespace flare {
 namespace tc {
 
 constexpr float kTau = 8.0f;           // lazy-rescale threshold (log2 units)
-constexpr int kMergePieces = 512;      // pieces of one (b, h) the fast merge handles
-constexpr int kMergeRB = 4;            // shards per block of the row reduction
-constexpr int kMergePB = 4;            // pieces per block of the output sum
+constexpr int kMergePieces = 512;      // pieces of one (b, h) the merge handles
 constexpr uint32_t kAtom = 128 * 128;  // bytes of one 128-row x 128-byte swizzle column
 
 struct EncArgs {
@@ -57,8 +55,7 @@ struct EncArgs {
     float sl2;                 // score scale * log2(e)
     int q_per_batch;           // Q has a batch dimension
     const uint8_t *mask;
-    unsigned *tickets;
-    float *part_L, *part_O, *shard_L;
+    float *part_L, *part_O;    // per-piece partials (workspace)
     float *O_r, *L_r, *Z, *L;
     unsigned *status;
     TcTilePlan plan;
@@ -129,32 +126,6 @@ struct TileCursor {
 };
 
 // ---- shared-memory pieces common to both kernels ------------------------------
-// Merge scratch: row max/sum [2][256], piece prefix [kMaxShards+2], piece
-// (shard, index) [kMergePieces], shard block [kMergeRB][256], piece weights
-// [kMergePB][256]; the two groups' (m, l) [2][128] at a piece end share the
-// shard-block area (never live at the same time).
-constexpr uint32_t kMergeBytes = 2 * 256 * 4 + (kMaxShards + 2) * 4 + kMergePieces * 4 +
-                                 kMergeRB * 256 * 4 + kMergePB * 256 * 4;
-static_assert(kMergeRB * 256 * 4 >= 2 * 128 * 8, "group states must fit the shard-block area");
-
-struct MergeScratch {
-    float *lmax, *asum;       // [256] each
-    int *pstart;              // [R + 1] piece prefix
-    uint32_t *piece;          // [P] shard << 16 | index
-    float *blk;               // [kMergeRB][M]
-    float *w;                 // [kMergePB][M]
-    float2 *stat;             // [2 groups][128 rows] (m, l), aliases blk
-    __device__ __forceinline__ void carve(uint8_t *p) {
-        lmax = reinterpret_cast<float *>(p);
-        asum = lmax + 256;
-        pstart = reinterpret_cast<int *>(asum + 256);
-        piece = reinterpret_cast<uint32_t *>(pstart + kMaxShards + 2);
-        blk = reinterpret_cast<float *>(piece + kMergePieces);
-        w = blk + kMergeRB * 256;
-        stat = reinterpret_cast<float2 *>(blk);
-    }
-};
-
 // Mask bias rows of one stage: TILE rows of 16 bytes (bf16 bias, then 7
 // zeros): the first K-core-matrix of a K = 16 block, no swizzle. The constant
 // A block of the bias MMA ("ones"): 128 rows [1, 0 x 7], then 128 rows of
@@ -235,185 +206,6 @@ __device__ __forceinline__ void produce_kv(const CUtensorMap *tmK, const CUtenso
     }
 }
 
-// ---- end of a piece: ticket, and the merge of every piece of a (b, h) -----------
-// Called by all NSOFT softmax threads after the piece's partial is written.
-// The last CTA to finish a piece of the (b, h) merges all pieces; `sync` is a
-// bounded barrier of the NSOFT threads returning false on abort.
-template <int D, int NSOFT, int MMAX, class Sync>
-__device__ bool finish_piece(const EncArgs &a, int bhh, int stid, const MergeScratch &ms,
-                             volatile int *last_flag, Sync &&sync) {
-    const TcTilePlan &pl = a.plan;
-    tc_fence_before();
-    __threadfence();
-    if (!sync()) return false;
-    if (stid == 0) {
-        int expected = 0;
-        for (int r = 0; r < pl.R; ++r) {
-            const int nt = pl.tile_start[r + 1] - pl.tile_start[r];
-            if (nt == 0) continue;
-            const int64_t u0 = (int64_t)bhh * pl.T_bh + pl.tile_start[r];
-            expected += cta_of(pl, u0 + nt - 1) - cta_of(pl, u0) + 1;
-        }
-        const unsigned prev = atomicAdd(&a.tickets[bhh], 1u);
-        *last_flag = (prev == (unsigned)expected - 1u) ? 1 : 0;
-    }
-    if (!sync()) return false;
-    if (!*last_flag) return true;
-    __threadfence();
-    // ---- merge every piece of (b, h): eq. 23 over shards, pieces inside shards ----
-    // L_r = log sum_p exp(L_p) over the pieces of shard r; then per row
-    // L = L_max + log a with a = sum_r exp(L_r - L_max) (an online max/sum
-    // over shard blocks), and Z = sum_r exp(L_r - L_max)/a * O_r
-    //   = sum_pieces exp(L_p - L_max)/a * O_p  (the same sum, distributed).
-    const int M = a.M;
-    const int64_t BH = (int64_t)a.B * a.H;
-    auto piece_slot = [&](uint32_t e) -> int64_t {   // workspace slot of a piece
-        return ((int64_t)bhh * pl.R + (e >> 16)) * pl.P_max + (e & 0xffffu);
-    };
-    for (int r = stid; r < pl.R; r += NSOFT) {
-        const int nt = pl.tile_start[r + 1] - pl.tile_start[r];
-        int np = 0;
-        if (nt > 0) {
-            const int64_t u0 = (int64_t)bhh * pl.T_bh + pl.tile_start[r];
-            np = cta_of(pl, u0 + nt - 1) - cta_of(pl, u0) + 1;
-        }
-        ms.pstart[r + 1] = np;
-    }
-    if (!sync()) return false;
-    if (stid == 0) {
-        ms.pstart[0] = 0;
-        int q = 0;
-        for (int r = 0; r < pl.R; ++r) {
-            const int np = ms.pstart[r + 1];
-            for (int p = 0; p < np; ++p, ++q)
-                if (q < kMergePieces) ms.piece[q] = ((uint32_t)r << 16) | (uint32_t)p;
-            ms.pstart[r + 1] = q;
-        }
-    }
-    if (!sync()) return false;
-    const int P = ms.pstart[pl.R];
-    if (P > kMergePieces) {                  // plans keep P within the table
-        if (stid == 0) atomicExch(a.status, 2u);
-        return false;
-    }
-    // 1. shard log-normalisers, in blocks of kMergeRB shards; online row max/sum
-    float rm = -INFINITY, ra = 0.f;
-    for (int rb0 = 0; rb0 < pl.R; rb0 += kMergeRB) {
-        const int nb = min(kMergeRB, pl.R - rb0);
-        for (int it = stid; it < nb * M; it += NSOFT) {
-            const int rr = it / M, i = it - rr * M, r = rb0 + rr;
-            const int q0 = ms.pstart[r], q1 = ms.pstart[r + 1];
-            float cm = -INFINITY;
-            for (int q = q0; q < q1; ++q) cm = fmaxf(cm, __ldcg(a.part_L + piece_slot(ms.piece[q]) * M + i));
-            float Lr = -INFINITY;
-            if (cm != -INFINITY) {
-                float sum = 0.f;
-                for (int q = q0; q < q1; ++q) {
-                    const float lp = __ldcg(a.part_L + piece_slot(ms.piece[q]) * M + i);
-                    if (lp != -INFINITY) sum += expf(lp - cm);
-                }
-                Lr = cm + logf(sum);
-            }
-            if (a.L_r) a.L_r[((int64_t)r * BH + bhh) * M + i] = Lr;
-            ms.blk[rr * M + i] = Lr;
-        }
-        if (!sync()) return false;
-        if (stid < M) {
-            for (int rr = 0; rr < nb; ++rr) {
-                const float Lr = ms.blk[rr * M + stid];
-                if (Lr == -INFINITY) continue;
-                if (rm == -INFINITY) {
-                    rm = Lr;
-                    ra = 1.f;
-                } else {
-                    const float mn = fmaxf(rm, Lr);
-                    ra = ra * expf(rm - mn) + expf(Lr - mn);
-                    rm = mn;
-                }
-            }
-        }
-        if (!sync()) return false;
-    }
-    if (stid < M) {
-        ms.lmax[stid] = rm;
-        ms.asum[stid] = ra;
-        if (a.L) a.L[(int64_t)bhh * M + stid] = rm == -INFINITY ? -INFINITY : rm + logf(ra);
-    }
-    if (!sync()) return false;
-    // 2. Z = sum over pieces of exp(L_p - L_max)/a * O_p, kMergePB pieces at a time
-    constexpr int Q4 = D / 4;
-    constexpr int QPT = MMAX * Q4 / NSOFT;   // quads per thread
-    float4 acc[QPT];
-#pragma unroll
-    for (int u = 0; u < QPT; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int qb0 = 0; qb0 < P; qb0 += kMergePB) {
-        const int nb = min(kMergePB, P - qb0);
-        for (int it = stid; it < nb * M; it += NSOFT) {
-            const int qq = it / M, i = it - qq * M;
-            const float lp = __ldcg(a.part_L + piece_slot(ms.piece[qb0 + qq]) * M + i);
-            const float lm = ms.lmax[i];
-            ms.w[qq * M + i] = (lp == -INFINITY || lm == -INFINITY) ? 0.f : expf(lp - lm) / ms.asum[i];
-        }
-        if (!sync()) return false;
-#pragma unroll
-        for (int u = 0; u < QPT; ++u) {
-            const int qd = stid + u * NSOFT;
-            if (qd >= M * Q4) break;
-            const int i = qd / Q4, d4 = qd - i * Q4;
-            float4 v[kMergePB];
-            float w[kMergePB];
-#pragma unroll
-            for (int qq = 0; qq < kMergePB; ++qq) {
-                w[qq] = qq < nb ? ms.w[qq * M + i] : 0.f;
-                v[qq] = w[qq] != 0.f
-                            ? __ldcg(reinterpret_cast<const float4 *>(a.part_O + (piece_slot(ms.piece[qb0 + qq]) * M + i) * D) + d4)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int qq = 0; qq < kMergePB; ++qq) {
-                acc[u].x = fmaf(w[qq], v[qq].x, acc[u].x);
-                acc[u].y = fmaf(w[qq], v[qq].y, acc[u].y);
-                acc[u].z = fmaf(w[qq], v[qq].z, acc[u].z);
-                acc[u].w = fmaf(w[qq], v[qq].w, acc[u].w);
-            }
-        }
-        if (!sync()) return false;
-    }
-    if (a.Z) {
-#pragma unroll
-        for (int u = 0; u < QPT; ++u) {
-            const int qd = stid + u * NSOFT;
-            if (qd >= M * Q4) break;
-            const int i = qd / Q4, d4 = qd - i * Q4;
-            reinterpret_cast<float4 *>(a.Z + ((int64_t)bhh * M + i) * D)[d4] = acc[u];
-        }
-    }
-    // 3. per-shard outputs O_r = sum_p exp(L_p - L_r) O_p (when requested)
-    if (a.O_r) {
-        for (int qd = stid; qd < M * Q4; qd += NSOFT) {
-            const int i = qd / Q4, d4 = qd - i * Q4;
-            for (int r = 0; r < pl.R; ++r) {
-                const float Lr = __ldcg(a.L_r + ((int64_t)r * BH + bhh) * M + i);
-                float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (Lr != -INFINITY)
-                    for (int q = ms.pstart[r]; q < ms.pstart[r + 1]; ++q) {
-                        const float lp = __ldcg(a.part_L + piece_slot(ms.piece[q]) * M + i);
-                        if (lp == -INFINITY) continue;
-                        const float wgt = expf(lp - Lr);
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-                                                    a.part_O + (piece_slot(ms.piece[q]) * M + i) * D) + d4);
-                        o.x = fmaf(wgt, v.x, o.x);
-                        o.y = fmaf(wgt, v.y, o.y);
-                        o.z = fmaf(wgt, v.z, o.z);
-                        o.w = fmaf(wgt, v.w, o.w);
-                    }
-                reinterpret_cast<float4 *>(a.O_r + (((int64_t)r * BH + bhh) * M + i) * D)[d4] = o;
-            }
-        }
-    }
-    return sync();
-}
-
 // Slot of the partial of the piece that tile `ti` ends (this CTA's piece of
 // its (b, h, shard)).
 __device__ __forceinline__ int64_t piece_slot_of(const TcTilePlan &pl, const TileCursor &ti, int cta) {
@@ -450,8 +242,10 @@ struct CsCfg {
     // full[S], empty[S], q_full[2], s_full[2], p_full[2], o_done[2], drain, soft
     static constexpr int NBAR = 2 * STAGES + 10;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr uint32_t MERGE_OFF = MISC_OFF + 64;
-    static constexpr uint32_t BYTES = MERGE_OFF + kMergeBytes;
+    // the two groups' (m, l) of each row at a piece end, double-buffered by
+    // piece parity: [2][2 groups][128 rows]
+    static constexpr uint32_t STAT_OFF = MISC_OFF + 64;
+    static constexpr uint32_t BYTES = STAT_OFF + 2 * 2 * 128 * 8;
     static constexpr uint32_t ALLOC = BYTES + 1024;           // room to align the base to 1 KB
     static_assert(ALLOC <= 232448, "shared memory budget of one CTA exceeded");
 };
@@ -479,9 +273,7 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     const uint32_t soft = bar0 + 8u * (2 * STAGES + 9);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
-    volatile int *last_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 8);
-    MergeScratch ms;
-    ms.carve(smem + C::MERGE_OFF);
+    float2 *stat = reinterpret_cast<float2 *>(smem + C::STAT_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const TcTilePlan &pl = a.plan;
@@ -492,7 +284,6 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        *last_flag = 0;
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
@@ -642,7 +433,6 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         const int g = (warp - 2) >> 2;            // group: tokens [g*HALF, (g+1)*HALF) of a tile
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
         const int rig = quad * 32 + lane;         // latent row (TMEM lane)
-        const int stid = threadIdx.x - 64;        // 0 .. NSOFT-1
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const uint32_t o_tmem = tmem + C::O_COL + g * D + lane_off;
         auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
@@ -655,6 +445,7 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         };
         float m_ref = -INFINITY, l = 0.f;
         bool has = false;                        // this group saw a tile of the current piece
+        uint32_t pieces = 0;                     // pieces finished (parity selects the stat buffer)
 
         // End of a (b, h, shard) piece: the two groups' states of each row are
         // combined into the piece's partial (normalised output, log-normaliser).
@@ -664,9 +455,10 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             tc_fence_after();
             const int64_t slot = piece_slot_of(pl, ti, cta);
             float *part_row = a.part_O + (slot * a.M + rig) * D;
-            ms.stat[g * 128 + rig] = make_float2(has ? m_ref : -INFINITY, has ? l : 0.f);
+            float2 *st = stat + (pieces++ & 1) * 256;
+            st[g * 128 + rig] = make_float2(has ? m_ref : -INFINITY, has ? l : 0.f);
             if (!soft_sync()) return false;
-            const float2 s0 = ms.stat[rig], s1 = ms.stat[128 + rig];
+            const float2 s0 = st[rig], s1 = st[128 + rig];
             const float m = fmaxf(s0.x, s1.x);
             const float w0 = (s0.y > 0.f) ? ex2(s0.x - m) : 0.f;
             const float w1 = (s1.y > 0.f) ? ex2(s1.x - m) : 0.f;
@@ -698,7 +490,7 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             }
             if (g == 0 && rig < a.M)
                 a.part_L[slot * a.M + rig] = lt > 0.f ? (m + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
-            return finish_piece<D, NSOFT, 128>(a, ti.bh, stid, ms, last_flag, soft_sync);
+            return true;
         };
 
         TileCursor ti;
@@ -827,11 +619,10 @@ struct HalvesCfg {
     static constexpr uint32_t BIAS_BYTES = TILE * 16;
     static constexpr uint32_t ONES_OFF = BIAS_OFF + STAGES * BIAS_BYTES;
     static constexpr uint32_t BAR_OFF = ONES_OFF + kOnesBytes;
-    // full[S], empty[S], q_full[2], s_full[2], p_full[2], o_done[2], drain[2], turn[2], soft
-    static constexpr int NBAR = 2 * STAGES + 15;
+    // full[S], empty[S], q_full[2], s_full[2], p_full[2], o_done[2], drain[2], turn[2]
+    static constexpr int NBAR = 2 * STAGES + 14;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr uint32_t MERGE_OFF = MISC_OFF + 64;
-    static constexpr uint32_t BYTES = MERGE_OFF + kMergeBytes;
+    static constexpr uint32_t BYTES = MISC_OFF + 64;
     static constexpr uint32_t ALLOC = BYTES + 1024;
     static_assert(ALLOC <= 232448, "shared memory budget of one CTA exceeded");
 };
@@ -841,7 +632,7 @@ __global__ void __launch_bounds__(HalvesCfg<STAGES>::THREADS, 1)
 enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmQ, const EncArgs a) {
     using C = HalvesCfg<STAGES>;
-    constexpr int D = C::D, KA = C::KA, TILE = C::TILE, NCH = C::NCH, NSOFT = C::NSOFT;
+    constexpr int D = C::D, KA = C::KA, TILE = C::TILE, NCH = C::NCH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -857,12 +648,8 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     auto o_done = [&](int g) { return bar0 + 8u * (2 * STAGES + 6 + g); };
     auto drain = [&](int g) { return bar0 + 8u * (2 * STAGES + 8 + g); };
     auto turn = [&](int g) { return bar0 + 8u * (2 * STAGES + 10 + g); };
-    const uint32_t soft = bar0 + 8u * (2 * STAGES + 12);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
-    volatile int *last_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 8);
-    MergeScratch ms;
-    ms.carve(smem + C::MERGE_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const TcTilePlan &pl = a.plan;
@@ -873,7 +660,6 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        *last_flag = 0;
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), 2);               // one PV commit per group on the tile
@@ -886,7 +672,6 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             mbar_init(drain(g), 1);
             mbar_init(turn(g), 4);
         }
-        mbar_init(soft, NSOFT);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -916,18 +701,12 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         const int quad = warp & 3;
         const int rig = quad * 32 + lane;
         const int row = g * 128 + rig;
-        const int stid = threadIdx.x - 64;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const uint32_t s_tmem = tmem + g * 256 + C::S_COL + lane_off;
         const uint32_t p_tmem = tmem + g * 256 + C::P_COL + lane_off;
         const uint32_t o_tmem = tmem + g * 256 + C::O_COL + lane_off;
         auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
             return __all_sync(0xffffffffu, wt.wait(bar, par));
-        };
-        uint32_t soft_phase = 0;
-        auto soft_sync = [&]() -> bool {
-            mbar_arrive(soft);
-            return wwait(soft, soft_phase++ & 1);
         };
         float m_ref = -INFINITY, l = 0.f;
         bool has = false;
@@ -1004,7 +783,7 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                                          __uint_as_float(r[4 * i + 3]) * inv);
             }
             a.part_L[slot * a.M + row] = live ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-            return finish_piece<D, NSOFT, 256>(a, ti.bh, stid, ms, last_flag, soft_sync);
+            return true;
         };
 
         TileCursor ti;
@@ -1145,6 +924,126 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ===============================================================================
+// enc_merge_kernel: the partials of every (b, h) into (Z, L) and (O_r, L_r)
+// ===============================================================================
+// eq. 23 over shards, and the same log-sum-exp rule over the pieces of one
+// shard: L_r = log sum_p exp(L_p); L = log sum_r exp(L_r);
+// Z = sum_p exp(L_p - L) O_p (= sum_r exp(L_r - L) O_r); O_r = sum_{p in r}
+// exp(L_p - L_r) O_p. Rows with no valid token anywhere get L = -inf, Z = 0.
+// One block per (b, h) and kMergeRows(D) latent rows; a thread per output quad.
+__host__ __device__ constexpr int merge_rows(int D) { return 1024 / D; }
+__host__ __device__ constexpr uint32_t merge_smem_bytes(int D) {
+    return (uint32_t)((kMergePieces + kMaxShards + 1) * merge_rows(D) * 4);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) enc_merge_kernel(const EncArgs a) {
+    constexpr int RB = merge_rows(D);          // RB * D / 4 = 256 output quads per block
+    constexpr int Q4 = D / 4;
+    const TcTilePlan &pl = a.plan;
+    const int M = a.M;
+    const int nrb = (M + RB - 1) / RB;
+    const int bh = blockIdx.x / nrb, i0 = (blockIdx.x - bh * nrb) * RB;
+    const int64_t BH = (int64_t)a.B * a.H;
+    extern __shared__ float msm[];
+    float *Lp = msm;                           // [kMergePieces][RB] piece log-normalisers
+    float *Lr = Lp + kMergePieces * RB;        // [kMaxShards][RB]   shard log-normalisers
+    float *Lrow = Lr + kMaxShards * RB;        // [RB]               row log-normalisers
+    __shared__ int pstart[kMaxShards + 1];
+    __shared__ uint32_t piece[kMergePieces];   // shard << 16 | index within the shard
+    const int tid = threadIdx.x;
+    for (int r = tid; r < pl.R; r += 256) {
+        const int nt = pl.tile_start[r + 1] - pl.tile_start[r];
+        int np = 0;
+        if (nt > 0) {
+            const int64_t u0 = (int64_t)bh * pl.T_bh + pl.tile_start[r];
+            np = cta_of(pl, u0 + nt - 1) - cta_of(pl, u0) + 1;
+        }
+        pstart[r + 1] = np;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        pstart[0] = 0;
+        for (int r = 0; r < pl.R; ++r) pstart[r + 1] += pstart[r];
+    }
+    __syncthreads();
+    const int P = pstart[pl.R];
+    if (P > kMergePieces) {                    // plans keep P within the table
+        if (tid == 0) atomicExch(a.status, 2u);
+        return;
+    }
+    for (int r = tid; r < pl.R; r += 256)
+        for (int q = pstart[r]; q < pstart[r + 1]; ++q) piece[q] = ((uint32_t)r << 16) | (uint32_t)(q - pstart[r]);
+    __syncthreads();
+    auto slot = [&](int q) -> int64_t {
+        const uint32_t e = piece[q];
+        return ((int64_t)bh * pl.R + (e >> 16)) * pl.P_max + (e & 0xffffu);
+    };
+    for (int x = tid; x < P * RB; x += 256) {
+        const int q = x / RB, i = x - q * RB;
+        Lp[x] = (i0 + i < M) ? __ldcg(a.part_L + slot(q) * M + i0 + i) : -INFINITY;
+    }
+    __syncthreads();
+    for (int x = tid; x < pl.R * RB; x += 256) {
+        const int r = x / RB, i = x - r * RB;
+        float m = -INFINITY;
+        for (int q = pstart[r]; q < pstart[r + 1]; ++q) m = fmaxf(m, Lp[q * RB + i]);
+        float Lv = -INFINITY;
+        if (m != -INFINITY) {
+            float sum = 0.f;
+            for (int q = pstart[r]; q < pstart[r + 1]; ++q) {
+                const float v = Lp[q * RB + i];
+                if (v != -INFINITY) sum += expf(v - m);
+            }
+            Lv = m + logf(sum);
+        }
+        Lr[x] = Lv;
+        if (a.L_r && i0 + i < M) a.L_r[((int64_t)r * BH + bh) * M + i0 + i] = Lv;
+    }
+    __syncthreads();
+    if (tid < RB) {
+        float m = -INFINITY;
+        for (int r = 0; r < pl.R; ++r) m = fmaxf(m, Lr[r * RB + tid]);
+        float Lv = -INFINITY;
+        if (m != -INFINITY) {
+            float sum = 0.f;
+            for (int r = 0; r < pl.R; ++r) {
+                const float v = Lr[r * RB + tid];
+                if (v != -INFINITY) sum += expf(v - m);
+            }
+            Lv = m + logf(sum);
+        }
+        Lrow[tid] = Lv;
+        if (a.L && i0 + tid < M) a.L[(int64_t)bh * M + i0 + tid] = Lv;
+    }
+    __syncthreads();
+    const int i = tid / Q4, d4 = tid - i * Q4;
+    if (i0 + i >= M) return;
+    const int64_t orow = (int64_t)(i0 + i) * D;
+    // weighted sum of the pieces [q0, q1) with weights exp(L_p - Lv)
+    auto wsum = [&](int q0, int q1, float Lv) -> float4 {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (Lv == -INFINITY) return acc;
+        for (int q = q0; q < q1; ++q) {
+            const float lp = Lp[q * RB + i];
+            if (lp == -INFINITY) continue;
+            const float w = expf(lp - Lv);
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.part_O + slot(q) * M * D + orow) + d4);
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+        }
+        return acc;
+    };
+    if (a.Z) reinterpret_cast<float4 *>(a.Z + (int64_t)bh * M * D + orow)[d4] = wsum(0, P, Lrow[i]);
+    if (a.O_r)
+        for (int r = 0; r < pl.R; ++r)
+            reinterpret_cast<float4 *>(a.O_r + ((int64_t)r * BH + bh) * M * D + orow)[d4] =
+                wsum(pstart[r], pstart[r + 1], Lr[r * RB + i]);
 }
 
 }  // namespace tc

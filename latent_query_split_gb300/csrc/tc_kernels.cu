@@ -58,6 +58,17 @@ cudaError_t launch_enc(Kernel k, const CUtensorMap &mk, const CUtensorMap &mv, c
     return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_merge(const Problem &pr, const tc::EncArgs &args, cudaStream_t st) {
+    constexpr uint32_t smem = tc::merge_smem_bytes(D);
+    auto k = tc::enc_merge_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int nrb = (pr.M + tc::merge_rows(D) - 1) / tc::merge_rows(D);
+    k<<<(unsigned)((int64_t)pr.B * pr.H * nrb), 256, smem, st>>>(args);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 bool tc_supported(bool bf16, int M, int D) {
@@ -93,18 +104,14 @@ bool tc_encoder_plan(const Problem &pr, const int64_t *off, int R, int sms, TcTi
     if (p.grid < 1) p.grid = 1;
     const int64_t span_min = p.T_total > 0 ? p.T_total / p.grid : 1;
     p.P_max = (int)((max_nt + span_min - 1) / (span_min > 0 ? span_min : 1)) + 1;
-    // the in-kernel merge keeps the pieces of one (b, h) in a table of kMergePieces
+    // the merge keeps the pieces of one (b, h) in a table of kMergePieces
     if ((int64_t)R * p.P_max > tc::kMergePieces) return false;
     const size_t bh = (size_t)pr.B * pr.H;
     size_t o = 0;
-    lay.tickets = o;
-    o += align256(sizeof(unsigned) * bh);
     lay.part_L = o;
     o += align256(sizeof(float) * bh * R * p.P_max * pr.M);
     lay.part_O = o;
     o += align256(sizeof(float) * bh * R * p.P_max * pr.M * pr.D);
-    lay.shard_L = o;
-    o += align256(sizeof(float) * bh * R * pr.M);
     lay.q_bf16 = o;
     o += align256(2 * bh * pr.M * pr.D);
     lay.bytes = o;
@@ -116,8 +123,7 @@ cudaError_t launch_encoder_tc(const Problem &pr, const TcTilePlan &plan, const T
                               const uint8_t *mask, void *ws, const EncoderOut &out,
                               unsigned *status, cudaStream_t st) {
     char *w = (char *)ws;
-    cudaError_t e = cudaMemsetAsync(w + lay.tickets, 0, sizeof(unsigned) * (size_t)pr.B * pr.H, st);
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
     const void *Qbf = Q;
     int64_t qb = pr.q_bstride == 0 ? 1 : pr.B;
     if (q_is_f32) {
@@ -142,10 +148,8 @@ cudaError_t launch_encoder_tc(const Problem &pr, const TcTilePlan &plan, const T
     a.sl2 = pr.scale * 1.4426950408889634f;
     a.q_per_batch = pr.q_bstride != 0;
     a.mask = mask;
-    a.tickets = (unsigned *)(w + lay.tickets);
     a.part_L = (float *)(w + lay.part_L);
     a.part_O = (float *)(w + lay.part_O);
-    a.shard_L = (float *)(w + lay.shard_L);
     a.O_r = out.O_r;
     a.L_r = out.L_r;
     a.Z = out.Z;
@@ -153,12 +157,15 @@ cudaError_t launch_encoder_tc(const Problem &pr, const TcTilePlan &plan, const T
     a.status = status;
     a.plan = plan;
     if (pr.D == 64 && pr.M <= 128)
-        return launch_enc<tc::CsCfg<64, 5>>(tc::enc_cs_kernel<64, 5>, mk, mv, mq, a, plan.grid, st);
-    if (pr.D == 128 && pr.M <= 128)
-        return launch_enc<tc::CsCfg<128, 4>>(tc::enc_cs_kernel<128, 4>, mk, mv, mq, a, plan.grid, st);
-    if (pr.D == 64 && pr.M == 256)
-        return launch_enc<tc::HalvesCfg<5>>(tc::enc_halves_kernel<5>, mk, mv, mq, a, plan.grid, st);
-    return cudaErrorNotSupported;
+        e = launch_enc<tc::CsCfg<64, 5>>(tc::enc_cs_kernel<64, 5>, mk, mv, mq, a, plan.grid, st);
+    else if (pr.D == 128 && pr.M <= 128)
+        e = launch_enc<tc::CsCfg<128, 4>>(tc::enc_cs_kernel<128, 4>, mk, mv, mq, a, plan.grid, st);
+    else if (pr.D == 64 && pr.M == 256)
+        e = launch_enc<tc::HalvesCfg<5>>(tc::enc_halves_kernel<5>, mk, mv, mq, a, plan.grid, st);
+    else
+        return cudaErrorNotSupported;
+    if (e != cudaSuccess) return e;
+    return pr.D == 64 ? launch_merge<64>(pr, a, st) : launch_merge<128>(pr, a, st);
 }
 
 bool tc_decode_available() { return true; }
