@@ -1,10 +1,16 @@
-"""Throughput benchmark of the FLARE mixer forward (encode + merge + decode).
+"""Throughput benchmark of the FLARE / FLARE++ token mixer on one GB300.
 
-One step = one flare_fwd call over one batch of the c2_bf16 workload (FLARE
-forward, bf16, B=4 H=8 D=64 M=128 N=65536, R=8 ragged shards, 5% padded
-tokens): the split-KV encoder with its fused log-sum-exp merge, then the
-local decode of every token. Inputs are seeded synthetic tensors resident in
-HBM; K and V (256 MiB each) exceed the 129 MB L2, so no flush is needed.
+One step = one pass of the hot path over one batch of a named workload
+(latent_query_split_gb300.workloads.CONFIGS), inputs resident in HBM:
+  c2_bf16 (default)  FLARE forward bf16, B=4 H=8 D=64 M=128 N=65536, R=8
+                     ragged shards, 5% padded tokens: the split-KV encoder with
+                     its log-sum-exp merge, then the local decode of every token
+  c1_fp32_small      the same forward on the small fp32 workload
+  c4_long_bf16       the same forward, B=1 H=8 D=128 M=64 N=4194304, R=64
+  c3_pp_bf16         FLARE++ forward (encoder twice, then the decode)
+  c5_bwd_bf16        global-normaliser encoder backward (dQ, dK, dV)
+Token tensors of c2-c5 are 256 MiB or more each (larger than the 129 MB L2),
+so no flush is needed between steps; c1 flushes L2 between steps.
 
 Prints one JSON line (rank 0). Under torchrun each rank runs an independent
 replica of the workload on its own GPU (weak scaling, no collective on the
@@ -33,14 +39,13 @@ if ROOT not in sys.path:
 
 METRIC = "FLARE encode+decode tokens/s at 1 GB300; % of roofline (HBM GB/s or tensor-pipe)"
 UNIT = "tokens/s"
-WORKLOAD = "c2_bf16"
-PROFILE_SUMMARY = {  # kernel -> committed ncu summary holding its DRAM traffic
-    "encoder": os.path.join(ROOT, "profiles", "encoder_c2_bf16.md"),
-    "decode": os.path.join(ROOT, "profiles", "decode_c2_bf16.md"),
-}
-KERNEL_SOURCES = {   # files whose content the profiled traffic belongs to
+DEFAULT_WORKLOAD = "c2_bf16"
+# library sources whose content a committed ncu traffic figure belongs to
+KERNEL_SOURCES = {
     "encoder": ["tc_encoder.cuh", "tc_ptx.cuh", "tc_kernels.cu"],
     "decode": ["tc_decode.cuh", "tc_ptx.cuh", "tc_kernels.cu"],
+    "encoder_bwd": ["tc_backward.cuh", "tc_ptx.cuh", "tc_kernels.cu", "simt_kernels.cu"],
+    "flare_pp_fwd": ["tc_encoder.cuh", "tc_decode.cuh", "tc_ptx.cuh", "tc_kernels.cu"],
 }
 
 
@@ -62,10 +67,11 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def _profiled_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it still
-    describes the current kernel source (else None)."""
-    path = PROFILE_SUMMARY[kernel]
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary
+    profiles/<kernel>_<workload>.md, if it still describes the current kernel
+    source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
     fields = {}
@@ -135,42 +141,91 @@ def _dist_env():
     return world, rank, local
 
 
-def cpu_oracle_sample(w, inputs, max_heads=None):
-    """Time the fp64 oracle on a bounded sample: encode + decode of every token
-    for the first `max_heads` (b, h) pairs. Returns (tokens/s, description, threads)."""
-    import numpy as np
-    import torch
+def describe(w) -> str:
+    what = {"flare_fwd": "FLARE fwd (encoder + merge + decode)",
+            "flare_pp_fwd": "FLARE++ fwd (encoder x2 + decode)",
+            "encoder_bwd": "encoder bwd (dQ, dK, dV)"}[w.kind]
+    extra = []
+    if w.pad_frac:
+        extra.append(f"{w.pad_frac:.0%} padded slots")
+    if w.empty_shards:
+        extra.append(f"empty shards {list(w.empty_shards)}")
+    if w.padded_shard:
+        extra.append(f"shard {w.padded_shard[1]} of batch {w.padded_shard[0]} all padding")
+    if w.key_boost_frac:
+        extra.append(f"{w.key_boost_frac:.0%} of keys x{w.key_boost:g}")
+    return (f"{w.name}: {what} {w.dtype} B{w.B} H{w.H} D{w.D} M{w.M} N{w.N} R{w.R} "
+            f"{'equal' if w.equal_shards else 'ragged'} shards" +
+            ("".join(", " + e for e in extra)))
 
+
+# ---- algorithmic work per step (each required byte counted once) --------------
+def algorithmic(w, elem):
+    """Per-phase algorithmic (bytes, flops) of one step.
+
+    A pass over one (b, h) streams 2*N*D elements (K and V read, or K read and
+    Y written) and does 4*M*N*D flops (two GEMM-shaped products); the backward
+    reads K, V and writes dK, dV (4*N*D elements) with 10*M*N*D flops."""
+    bh = w.B * w.H
+    tok = bh * w.N * w.D * elem
+    pass_flops = 4.0 * bh * w.M * w.N * w.D
+    if w.kind == "flare_fwd":
+        return {"encoder": (2 * tok, pass_flops), "decode": (2 * tok, pass_flops)}
+    if w.kind == "flare_pp_fwd":
+        return {"flare_pp_fwd": (6 * tok, 3 * pass_flops)}
+    return {"encoder_bwd": (4 * tok, 2.5 * pass_flops)}
+
+
+# ---- the fp64 oracle on a bounded sample --------------------------------------
+def cpu_oracle_sample(w, inputs, pairs=1):
+    """Time the fp64 oracle on `pairs` (batch, head) pairs of the workload (every
+    token of each). Returns (tokens/s, description, threads, seconds)."""
     import oracle
-    heads = max_heads or 2
-    K = inputs["K"][0:1, :, :heads].contiguous().cpu()
-    V = inputs["V"][0:1, :, :heads].contiguous().cpu()
-    Q = inputs["Q"][:heads].contiguous().cpu()
-    mask = None if inputs["mask"] is None else inputs["mask"][0:1].cpu()
+    b = 0
+    hs = slice(0, pairs)
+    mask = None if inputs["mask"] is None else inputs["mask"][b:b + 1].cpu()
+    tok = lambda x: x[b:b + 1, :, hs].contiguous().cpu()    # noqa: E731
     oracle.build()
-    t0 = time.perf_counter()
-    Z, L = oracle.encode(Q, K, V, mask)
-    oracle.decode(Q, Z, K)
-    dt = time.perf_counter() - t0
-    # one token slot of the workload carries H heads; the sample did `heads` of them
-    equiv_tokens = w.N * heads / w.H
-    desc = (f"encode (M={w.M} latents, all {w.N} tokens) + decode of all {w.N} tokens for "
-            f"{heads} of {w.B * w.H} (batch, head) pairs = {equiv_tokens:.0f} token-equivalents")
-    return equiv_tokens / dt, desc, oracle.num_threads(), dt
+    if w.kind == "flare_fwd":
+        Q, K, V = inputs["Q"][hs].contiguous().cpu(), tok(inputs["K"]), tok(inputs["V"])
+        t0 = time.perf_counter()
+        Z, L = oracle.encode(Q, K, V, mask)
+        oracle.decode(Q, Z, K)
+        dt = time.perf_counter() - t0
+        what = "encode + decode"
+    elif w.kind == "flare_pp_fwd":
+        Qs = inputs["Qseed"][hs].contiguous().cpu()
+        Kt, Vt, K, V = (tok(inputs[k]) for k in ("Kt", "Vt", "K", "V"))
+        t0 = time.perf_counter()
+        oracle.flare_pp_fwd(Qs, Kt, Vt, K, V, mask)
+        dt = time.perf_counter() - t0
+        what = "FLARE++ forward (two encodes + decode)"
+    else:
+        Q, K, V = inputs["Q"][hs].contiguous().cpu(), tok(inputs["K"]), tok(inputs["V"])
+        dZ = inputs["dZ"][b:b + 1, hs].contiguous().cpu()
+        Z, L = oracle.encode(Q, K, V, mask)        # forward statistics, not timed
+        t0 = time.perf_counter()
+        oracle.encode_bwd(Q, K, V, mask, Z, L, dZ)
+        dt = time.perf_counter() - t0
+        what = "encoder backward"
+    equiv = w.N * pairs / w.H       # a token slot of the workload carries H heads
+    desc = (f"{what} of all {w.N} tokens (M={w.M}) for {pairs} of {w.B * w.H} "
+            f"(batch, head) pairs = {equiv:.0f} token-equivalents")
+    return equiv / dt, desc, oracle.num_threads(), dt
 
 
 def run_reference(args, w):
-    import torch
     from latent_query_split_gb300 import workloads
     world, rank, _ = _dist_env()
     if rank != 0:
         return 0
     inputs = workloads.make_inputs(w, device="cpu")
     for _ in range(args.warmup):
-        cpu_oracle_sample(w, inputs, max_heads=1)
+        cpu_oracle_sample(w, inputs)
     vals, secs = [], 0.0
+    desc, cores = "", 0
     for _ in range(args.steps):
-        v, desc, cores, dt = cpu_oracle_sample(w, inputs, max_heads=1)
+        v, desc, cores, dt = cpu_oracle_sample(w, inputs)
         vals.append(v)
         secs += dt
     value = statistics.median(vals)
@@ -178,9 +233,8 @@ def run_reference(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)", "impl": "reference",
-            "config": {"workload": f"{w.name}: FLARE fwd bf16 inputs, B{w.B} H{w.H} D{w.D} "
-                                   f"M{w.M} N{w.N} R{w.R}, 5% padded slots; one step = a "
-                                   f"bounded sample (one batch-head pair)"},
+            "config": {"workload": describe(w) + "; one step = a bounded sample "
+                                                 "(one batch-head pair)"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -189,19 +243,86 @@ def run_reference(args, w):
     return 0
 
 
+# ---- one step of the hot path through the public API --------------------------
+class Step:
+    """Builds the phases of one step (each a call of the public API) for a
+    workload, over device tensors."""
+
+    def __init__(self, w, inp, dev, kernel, stream):
+        import torch
+        from latent_query_split_gb300 import flare
+        self.w, self.inp, self.kernel, self.stream = w, inp, kernel, stream
+        B, N, H, D, M = w.B, w.N, w.H, w.D, w.M
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.off = inp["offsets"]
+        self.Z = torch.empty((B, H, M, D), **f32)
+        self.L = torch.empty((B, H, M), **f32)
+        Qref = inp["Qseed"] if w.kind == "flare_pp_fwd" else inp["Q"]
+        dims = flare.make_dims(Qref, inp["K"], None, kernel)
+        op = {"flare_fwd": flare.FLARE_OP_FWD, "flare_pp_fwd": flare.FLARE_OP_PP_FWD,
+              "encoder_bwd": flare.FLARE_OP_ENCODER_BWD}[w.kind]
+        nbytes = flare.flare_workspace_bytes(op, dims, self.off)
+        self.ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+        if w.kind == "flare_fwd":
+            self.Y = torch.empty_like(inp["K"])
+        elif w.kind == "flare_pp_fwd":
+            self.Y = torch.empty_like(inp["K"])
+            self.Qd, self.L1 = torch.empty((B, H, M, D), **f32), torch.empty((B, H, M), **f32)
+        else:
+            self.dQ = torch.empty((B, H, M, D), **f32)
+            self.dK, self.dV = torch.empty_like(inp["K"]), torch.empty_like(inp["V"])
+            # the saved forward statistics the backward consumes (not timed)
+            flare.flare_encoder_fwd(inp["Q"], inp["K"], inp["V"], inp["mask"], self.off,
+                                    Z=self.Z, L=self.L, workspace=self.ws, kernel=kernel,
+                                    stream=stream)
+
+    def phases(self, inp=None):
+        """[(name, callable)] making one step; `inp` overrides the input tensors."""
+        from latent_query_split_gb300 import flare
+        x = inp or self.inp
+        w, k, st, off = self.w, self.kernel, self.stream, self.off
+        if w.kind == "flare_fwd":
+            return [("encoder", lambda: flare.flare_encoder_fwd(
+                        x["Q"], x["K"], x["V"], x["mask"], off, Z=self.Z, L=self.L,
+                        workspace=self.ws, kernel=k, stream=st)),
+                    ("decode", lambda: flare.flare_decode_fwd(
+                        x["Q"], self.Z, x["K"], Y=self.Y, kernel=k, stream=st))]
+        if w.kind == "flare_pp_fwd":
+            return [("flare_pp_fwd", lambda: flare.flare_pp_fwd(
+                        x["Qseed"], x["Kt"], x["Vt"], x["K"], x["V"], x["mask"], off, Y=self.Y,
+                        Qdyn=self.Qd, L1=self.L1, Z=self.Z, L2=self.L, workspace=self.ws,
+                        kernel=k, stream=st))]
+        return [("encoder_bwd", lambda: flare.flare_encoder_bwd(
+                    x["Q"], x["K"], x["V"], x["mask"], off, x.get("Zs", self.Z),
+                    x.get("Ls", self.L), x["dZ"], dQ=self.dQ, dK=self.dK, dV=self.dV,
+                    workspace=self.ws, kernel=k, stream=st))]
+
+    def inputs_for_e2e(self):
+        """Names of the device inputs a user copies in each step, and the
+        outputs read back."""
+        if self.w.kind == "flare_fwd":
+            return ["Q", "K", "V", "mask"], [self.Y]
+        if self.w.kind == "flare_pp_fwd":
+            return ["Qseed", "Kt", "Vt", "K", "V", "mask"], [self.Y]
+        return ["Q", "K", "V", "mask", "Zs", "Ls", "dZ"], [self.dQ, self.dK, self.dV]
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--kernel", choices=["auto", "simt", "tensor"], default="auto")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
 
     from latent_query_split_gb300 import workloads
-    w = workloads.CONFIGS[WORKLOAD]
+    if args.workload not in workloads.CONFIGS:
+        raise SystemExit(f"unknown workload {args.workload}: {sorted(workloads.CONFIGS)}")
+    w = workloads.CONFIGS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
     if args.warmup < 3:
@@ -217,87 +338,92 @@ def main(argv=None):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    inputs = workloads.make_inputs(w.scaled(seed=w.seed + rank), device=dev)
-    Q, K, V, mask, off = inputs["Q"], inputs["K"], inputs["V"], inputs["mask"], inputs["offsets"]
-    B, N, H, D, M = w.B, w.N, w.H, w.D, w.M
-    Y = torch.empty_like(K)
-    Z = torch.empty((B, H, M, D), dtype=torch.float32, device=dev)
-    L = torch.empty((B, H, M), dtype=torch.float32, device=dev)
-    dims = flare.make_dims(Q, K, None, args.kernel)
-    ws_bytes = flare.flare_workspace_bytes(flare.FLARE_OP_FWD, dims, off)
-    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    inp = workloads.make_inputs(w.scaled(seed=w.seed + rank), device=dev)
     stream = torch.cuda.Stream(device=dev)
+    runner = Step(w, inp, dev, args.kernel, stream)
+    phases = runner.phases()
+    # an L2 flush between steps for workloads whose tensors fit in L2
+    elem = inp["K"].element_size()
+    small = w.B * w.N * w.H * w.D * elem < (256 << 20)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if small else None
 
     def step(ev=None):
-        # encoder (+ fused merge) and decode, each bracketed by events on `stream`
         with torch.cuda.stream(stream):
+            if flush is not None:
+                flush.fill_(1)
+            for i, (_, fn) in enumerate(phases):
+                if ev is not None:
+                    ev[i].record(stream)
+                fn()
             if ev is not None:
-                ev[0].record(stream)
-            flare.flare_encoder_fwd(Q, K, V, mask, off, Z=Z, L=L, workspace=ws,
-                                    kernel=args.kernel, stream=stream)
-            if ev is not None:
-                ev[1].record(stream)
-            flare.flare_decode_fwd(Q, Z, K, Y=Y, kernel=args.kernel, stream=stream)
-            if ev is not None:
-                ev[2].record(stream)
+                ev[len(phases)].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     flare.flare_device_status(stream)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
+           for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
+    launches0 = flare.flare_launch_count()
     start.record(stream)
     for i in range(args.steps):
         step(evs[i])
     end.record(stream)
+    launches = flare.flare_launch_count() - launches0
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
     clock_info = clocks.stop()
     flare.flare_device_status(stream)
     elapsed_ms = start.elapsed_time(end)
-    enc_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    phase_ms = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+                for i, (name, _) in enumerate(phases)}
     if world > 1:
         t = torch.tensor([elapsed_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
     ms_per_step = elapsed_ms / args.steps
-    tokens_per_step = B * N * world
+    if flush is not None:       # the flush is not the mixer's work
+        ms_per_step = sum(phase_ms.values())
+    tokens_per_step = w.B * w.N * world
     value = tokens_per_step / (ms_per_step * 1e-3)
 
     # end to end through the public API with host buffers (pinned), copies timed
-    hK, hV = K.cpu().pin_memory(), V.cpu().pin_memory()
-    hQ = Q.cpu().pin_memory()
-    hmask = mask.cpu().pin_memory() if mask is not None else None
-    hY = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
-    dK, dV, dQ = torch.empty_like(K), torch.empty_like(V), torch.empty_like(Q)
-    dmask = torch.empty_like(mask) if mask is not None else None
-    h2d = sum(t.numel() * t.element_size() for t in (hK, hV, hQ) + ((hmask,) if hmask is not None else ()))
-    d2h = hY.numel() * hY.element_size()
+    e2e_in, e2e_out = runner.inputs_for_e2e()
+    host, dinp = {}, dict(inp)
+    extra = {"Zs": runner.Z, "Ls": runner.L}
+    for name in e2e_in:
+        t = extra[name] if name in extra else inp[name]
+        if t is None:
+            continue
+        host[name] = t.cpu().pin_memory()
+        dinp[name] = torch.empty_like(t)
+    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in e2e_out]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+    e2e_phases = runner.phases(dinp)
 
     def e2e_step():
         with torch.cuda.stream(stream):
-            dK.copy_(hK, non_blocking=True)
-            dV.copy_(hV, non_blocking=True)
-            dQ.copy_(hQ, non_blocking=True)
-            if dmask is not None:
-                dmask.copy_(hmask, non_blocking=True)
-            flare.flare_fwd(dQ, dK, dV, dmask, off, Y=Y, Z=Z, L=L, workspace=ws,
-                            kernel=args.kernel, stream=stream)
-            hY.copy_(Y, non_blocking=True)
+            for name, t in host.items():
+                dinp[name].copy_(t, non_blocking=True)
+            for _, fn in e2e_phases:
+                fn()
+            for h, d in zip(hout, e2e_out):
+                h.copy_(d, non_blocking=True)
 
-    for _ in range(3):
+    big = h2d > (8 << 30)
+    for _ in range(1 if big else 3):
         e2e_step()
     torch.cuda.synchronize(dev)
-    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    e2e_steps = 3 if big else max(3, min(args.steps, args.e2e_steps))
     if world > 1:
         dist.barrier()
     s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -313,39 +439,40 @@ def main(argv=None):
         e2e_ms = float(t.item())
     flare.flare_device_status(stream)
 
-    # roofline of the dominant kernel (algorithmic bytes: K,V read by the
-    # encoder; K read + Y written by the decode; each byte counted once)
-    hbm_gbs, _, peak_kind = _peaks()
-    tok_bytes = B * N * H * D * K.element_size()
-    dominant = "encoder" if enc_ms >= dec_ms else "decode"
-    kern_ms = enc_ms if dominant == "encoder" else dec_ms
-    algo_bytes = 2 * tok_bytes
-    achieved = algo_bytes / (kern_ms * 1e-3) / 1e9
+    # roofline of the dominant phase: algorithmic bytes / its event time
+    hbm_gbs, bf16_tf, peak_kind = _peaks()
+    algo = algorithmic(w, elem)
+    dominant = max(phase_ms, key=phase_ms.get)
+    per_phase = {}
+    for name, ms in phase_ms.items():
+        b, f = algo[name]
+        per_phase[name] = {"ms": ms, "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_gbs,
+                           "tensor_frac": f / (ms * 1e-3) / 1e12 / bf16_tf,
+                           "algo_bytes": b, "algo_flops": f}
+    bytes_dom = algo[dominant][0]
+    achieved = bytes_dom / (phase_ms[dominant] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                "frac": achieved / hbm_gbs, "traffic": _profiled_traffic(dominant),
-                "kernel": dominant, "peak_source": peak_kind,
-                "encoder_ms": enc_ms, "decode_ms": dec_ms,
-                "encoder_frac": algo_bytes / (enc_ms * 1e-3) / 1e9 / hbm_gbs,
-                "decode_frac": algo_bytes / (dec_ms * 1e-3) / 1e9 / hbm_gbs}
+                "frac": achieved / hbm_gbs, "traffic": profiled_traffic(dominant, w.name),
+                "kernel": dominant, "peak_source": peak_kind, "phases": per_phase}
 
+    dt_name = {"f32": "f32", "bf16": "bf16"}[w.dtype]
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dt_name,
             "data": "synthetic (seeded, on device)",
-            "config": {"workload": f"{w.name}: FLARE fwd bf16 B{B} H{H} D{D} M{M} N{N} R{w.R} "
-                                   f"ragged shards, 5% padded slots",
-                       "kernel": args.kernel, "tokens_per_step": tokens_per_step,
-                       "l2": "inputs larger than L2 (K, V 256 MiB each), no flush",
+            "config": {"workload": describe(w), "kernel": args.kernel,
+                       "tokens_per_step": tokens_per_step,
+                       "l2": ("512 MiB L2 flush between steps (not timed)" if flush is not None
+                              else "inputs larger than L2 (token tensors >= 256 MiB), no flush"),
                        "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
             "clocks": clock_info,
             "e2e": {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": launches,
             "roofline": roofline}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        hin = {"K": K, "V": V, "Q": Q, "mask": mask}
-        v, desc, cores, _ = cpu_oracle_sample(w, hin, max_heads=2)
+        v, desc, cores, _ = cpu_oracle_sample(w, inp, pairs=1 if w.N > 1 << 20 else 2)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": desc}
     if rank == 0:

@@ -235,6 +235,11 @@ FLARE_API const char *flare_last_error_string(void);
 /* Library version as major*10000 + minor*100 + patch. */
 FLARE_API int flare_version(void);
 
+/* Kernels this library has launched in this process so far (every device and
+ * host thread; one count per kernel launch, memsets not included). A
+ * diagnostic: the difference across a call is that call's launch count. */
+FLARE_API unsigned long long flare_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

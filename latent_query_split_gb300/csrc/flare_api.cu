@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -16,6 +17,9 @@ namespace flare {
 
 // Status word of every kernel that waits with a bound (see flare_device_status).
 __device__ unsigned g_device_status;
+
+std::atomic<unsigned long long> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
 
@@ -269,6 +273,7 @@ flare_status_t encoder_run(const flare_dims_t *d, const void *Q, bool q_is_f32, 
     if (pr.N == 0) {                           // no token: every row is empty
         fill_empty_kernel<<<64, 256, 0, st>>>(O_r, O_r ? R * bhm * pr.D : 0, L_r, L_r ? R * bhm : 0,
                                                Z, Z ? bhm * pr.D : 0, L, L ? bhm : 0);
+        note_launch();
         cudaError_t e = cudaGetLastError();
         return e == cudaSuccess ? FLARE_OK : cuda_fail(e, "fill_empty_kernel launch");
     }
@@ -348,6 +353,8 @@ using namespace flare;
 extern "C" {
 
 int flare_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+unsigned long long flare_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char *flare_last_error_string(void) { return t_error.c_str(); }
 

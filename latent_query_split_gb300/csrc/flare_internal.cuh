@@ -100,6 +100,9 @@ flare_status_t encoder_fwd_with_workspace(const flare_dims_t *dims, const void *
                                           void *ws, size_t ws_bytes, cudaStream_t st);
 flare_status_t report_error(flare_status_t s, const char *msg);
 
+// Counts kernel launches for flare_launch_count (call once per <<<...>>>).
+void note_launch();
+
 void reset_device_status();
 unsigned read_and_clear_device_status(cudaStream_t st, cudaError_t *err);
 

@@ -597,17 +597,20 @@ cudaError_t launch_encoder_simt(const Problem &pr, const ShardPlan &plan, const 
         if ((e = set_smem(k, smem)) != cudaSuccess) return e;
         k<<<grid, kThreads, smem, st>>>(pr, plan, (const float *)Q, (const float *)K,
                                         (const float *)V, mask, ws, out, mtiles);
+        note_launch();
     } else if (q_is_f32) {
         auto k = enc_fwd_simt_kernel<float, __nv_bfloat16>;
         if ((e = set_smem(k, smem)) != cudaSuccess) return e;
         k<<<grid, kThreads, smem, st>>>(pr, plan, (const float *)Q, (const __nv_bfloat16 *)K,
                                         (const __nv_bfloat16 *)V, mask, ws, out, mtiles);
+        note_launch();
     } else {
         auto k = enc_fwd_simt_kernel<__nv_bfloat16, __nv_bfloat16>;
         if ((e = set_smem(k, smem)) != cudaSuccess) return e;
         k<<<grid, kThreads, smem, st>>>(pr, plan, (const __nv_bfloat16 *)Q,
                                         (const __nv_bfloat16 *)K, (const __nv_bfloat16 *)V, mask,
                                         ws, out, mtiles);
+        note_launch();
     }
     return cudaGetLastError();
 }
@@ -618,6 +621,7 @@ cudaError_t launch_lse_merge(const float *O_r, const float *L_r, int R, int B, i
     const int64_t blocks = (int64_t)B * H * mtiles;
     if (blocks == 0) return cudaSuccess;
     lse_merge_kernel<<<(unsigned)blocks, kThreads, 0, st>>>(O_r, L_r, R, B, H, M, D, Z, L);
+    note_launch();
     return cudaGetLastError();
 }
 
@@ -632,16 +636,19 @@ cudaError_t launch_decode_simt(const Problem &pr, const void *Q, bool q_is_f32, 
         auto k = dec_fwd_simt_kernel<float, float>;
         if ((e = set_smem(k, smem)) != cudaSuccess) return e;
         k<<<grid, kThreads, smem, st>>>(pr, (const float *)Q, Z, (const float *)K, (float *)Y);
+        note_launch();
     } else if (q_is_f32) {
         auto k = dec_fwd_simt_kernel<float, __nv_bfloat16>;
         if ((e = set_smem(k, smem)) != cudaSuccess) return e;
         k<<<grid, kThreads, smem, st>>>(pr, (const float *)Q, Z, (const __nv_bfloat16 *)K,
                                         (__nv_bfloat16 *)Y);
+        note_launch();
     } else {
         auto k = dec_fwd_simt_kernel<__nv_bfloat16, __nv_bfloat16>;
         if ((e = set_smem(k, smem)) != cudaSuccess) return e;
         k<<<grid, kThreads, smem, st>>>(pr, (const __nv_bfloat16 *)Q, Z,
                                         (const __nv_bfloat16 *)K, (__nv_bfloat16 *)Y);
+        note_launch();
     }
     return cudaGetLastError();
 }
@@ -686,9 +693,11 @@ cudaError_t launch_encoder_bwd_simt(const Problem &pr, const void *Q, const void
         if ((e = set_smem(k2, smem_q)) != cudaSuccess) return e;                              \
         k1<<<gkv, kThreads, smem_kv, st>>>(pr, (const TQ *)Q, (const TKV *)K, (const TKV *)V, \
                                             mask, Z, L, dZ, (TKV *)dK, (TKV *)dV);            \
+        note_launch();                                                                        \
         k2<<<gq, kThreads, smem_q, st>>>(pr, (const TQ *)Q, (const TKV *)K, (const TKV *)V,   \
                                           mask, Z, L, dZ, dQ, tickets, part, kBwdChunk,       \
                                           nchunks, mtiles);                                   \
+        note_launch();                                                                        \
     }
     if (!pr.bf16) FLARE_BWD_LAUNCH(float, float)
     else FLARE_BWD_LAUNCH(__nv_bfloat16, __nv_bfloat16)

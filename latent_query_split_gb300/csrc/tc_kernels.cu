@@ -55,6 +55,7 @@ cudaError_t launch_enc(Kernel k, const CUtensorMap &mk, const CUtensorMap &mv, c
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
     if (e != cudaSuccess) return e;
     k<<<grid, C::THREADS, C::ALLOC, st>>>(mk, mv, mq, args);
+    note_launch();
     return cudaGetLastError();
 }
 
@@ -66,6 +67,7 @@ cudaError_t launch_merge(const Problem &pr, const tc::EncArgs &args, cudaStream_
     if (e != cudaSuccess) return e;
     const int nrb = (pr.M + tc::merge_rows(D) - 1) / tc::merge_rows(D);
     k<<<(unsigned)((int64_t)pr.B * pr.H * nrb), 256, smem, st>>>(args);
+    note_launch();
     return cudaGetLastError();
 }
 
@@ -131,6 +133,7 @@ cudaError_t launch_encoder_tc(const Problem &pr, const TcTilePlan &plan, const T
         const int64_t n = qb * pr.H * pr.M * pr.D;
         f32_to_bf16_kernel<<<(unsigned)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024), 256, 0, st>>>(
             (const float *)Q, (__nv_bfloat16 *)(w + lay.q_bf16), n);
+        note_launch();
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         Qbf = w + lay.q_bf16;
     }
@@ -178,6 +181,7 @@ cudaError_t launch_dec(const CUtensorMap &mk, const tc::DecArgs &args, cudaStrea
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
     if (e != cudaSuccess) return e;
     k<<<args.grid, C::THREADS, C::ALLOC, st>>>(mk, args);
+    note_launch();
     return cudaGetLastError();
 }
 }  // namespace

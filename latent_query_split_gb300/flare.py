@@ -29,7 +29,8 @@ FLARE_MAX_SHARDS = 256
 # Every symbol the header declares (checked by the test-suite).
 EXPORTS = ("flare_workspace_bytes", "flare_encoder_fwd", "flare_lse_merge", "flare_decode_fwd",
            "flare_fwd", "flare_pp_fwd", "flare_encoder_bwd", "flare_encoder_fwd_noalloc",
-           "flare_device_status", "flare_last_error_string", "flare_version")
+           "flare_device_status", "flare_last_error_string", "flare_version",
+           "flare_launch_count")
 
 
 class FlareError(RuntimeError):
@@ -76,6 +77,7 @@ def load_library(build_if_missing: bool = True):
     lib.flare_device_status.argtypes = [P]
     lib.flare_last_error_string.restype = ctypes.c_char_p
     lib.flare_version.restype = I
+    lib.flare_launch_count.restype = ctypes.c_ulonglong
     _lib = lib
     return lib
 
@@ -283,3 +285,8 @@ def flare_encoder_fwd_noalloc(Q, K, V, mask=None, shard_offsets=None, *, O_r=Non
 def flare_device_status(stream=None):
     """Synchronise the stream and raise FlareError if a kernel gave up a bounded wait."""
     _check(load_library().flare_device_status(_stream(stream)))
+
+
+def flare_launch_count() -> int:
+    """Kernels the library has launched in this process (see include/flare.h)."""
+    return int(load_library().flare_launch_count())
