@@ -371,7 +371,7 @@ size_t flare_workspace_bytes(flare_op_t op, const flare_dims_t *dims, const int6
         case FLARE_OP_ENCODER_BWD: {
             const Problem pr = make_problem(dims);
             size_t b = encoder_bwd_simt_workspace(pr);
-            if (use_tensor_cores(dims)) {
+            if (dims->kernel != FLARE_KERNEL_SIMT) {
                 const size_t t = tc_encoder_bwd_workspace(pr, planning_sms());
                 if (t > b) b = t;
             }
@@ -465,11 +465,16 @@ flare_status_t flare_encoder_bwd(const flare_dims_t *dims, const void *Q, const 
     if (!aligned(Q, es) || !aligned(K, es) || !aligned(V, es) || !aligned(dK, es) ||
         !aligned(dV, es) || !aligned(Z, 4) || !aligned(L, 4) || !aligned(dZ, 4) || !aligned(dQ, 4))
         return fail(FLARE_ERR_INVALID_ARG, "tensors must be aligned to their element size");
-    const bool want_tc = use_tensor_cores(dims);
-    if (dims->kernel == FLARE_KERNEL_TENSOR && !(want_tc && tc_bwd_available()))
-        return fail(FLARE_ERR_UNSUPPORTED, "no tensor-core backward for this shape");
-    const bool tc = want_tc && tc_bwd_available() && tc_pointers_ok(K, V, dims->H, dims->D) &&
-                    tc_pointers_ok(dK, dV, dims->H, dims->D);
+    const bool want_tc = dims->kernel != FLARE_KERNEL_SIMT && tc_bwd_supported(pr.bf16, pr.M, pr.D);
+    if (dims->kernel == FLARE_KERNEL_TENSOR && !want_tc)
+        return fail(FLARE_ERR_UNSUPPORTED, "no tensor-core backward for dtype=%d M=%d D=%d",
+                    (int)dims->dtype, dims->M, dims->D);
+    const bool tc = want_tc && tc_pointers_ok(K, V, dims->H, dims->D) &&
+                    tc_pointers_ok(dK, dV, dims->H, dims->D) && aligned(Q, 16) && aligned(Z, 16) &&
+                    aligned(dZ, 16) && aligned(dQ, 16);
+    if (dims->kernel == FLARE_KERNEL_TENSOR && !tc)
+        return fail(FLARE_ERR_INVALID_ARG,
+                    "tensor-core backward needs 16-byte aligned Q, K, V, Z, dZ, dQ, dK and dV");
     const size_t need = flare_workspace_bytes(FLARE_OP_ENCODER_BWD, dims, shard_offsets, R);
     if (pr.N > 0 && (!workspace || workspace_bytes < need))
         return fail(FLARE_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", need,

@@ -1,0 +1,570 @@
+// tc_backward.cuh -- global-normaliser FLARE encoder backward on sm_103a
+// tensor cores.
+//
+// With the forward's global statistics (Z, L) every token's gradient is
+// local ("FLARE++: Low-rank attention with dynamic attention routing",
+// appendix on context parallelism, backward paragraphs: globally normalised
+// local probabilities, the row scalar c, local key/value gradients, the query
+// gradient summed over shards):
+//   P_mn  = exp(s <Q_m, K_n> - L_m)       (0 for padding and for L_m = -inf)
+//   dS_mn = P_mn (<dZ_m, V_n> - c_m),     c_m = <dZ_m, Z_m>
+//   dV_n  = sum_m P_mn dZ_m,  dK_n = s sum_m dS_mn Q_m,  dQ_m = s sum_n dS_mn K_n.
+//
+// Three kernels:
+//  * bwd_prep_kernel: per latent row, dZ rounded to bf16 (an MMA operand),
+//    -L in log2 units (-inf for an empty row, so its P is 0) and -s c.
+//  * bwd_tc_kernel: one persistent CTA per SM over a contiguous span of
+//    128-token tiles in (b, h, tile) order (shards play no part: with the
+//    global L and c each token is independent). Per tile, with the token rows
+//    in the 128 TMEM lanes:
+//        S^T = K Q^T,  dP^T = V dZ^T                    (A, B from shared memory)
+//        P = exp2(S^T s log2e - L2), s dS = P (s dP - s c)  (softmax warps, fp32)
+//        dV = P^T dZ,  dK = (s dS)^T Q                  (A = bf16 P / dS in TMEM)
+//        dQ += (s dS) K                                 (A = dS in shared memory)
+//    dK and dV leave through shared memory by TMA stores; dQ accumulates in
+//    TMEM over the (b, h)'s tiles of the span and is written as one fp32
+//    partial per (b, h) piece of the span.
+//  * bwd_dq_reduce_kernel: dQ = sum of the pieces of each (b, h), in piece
+//    order (deterministic).
+// Warp roles of bwd_tc_kernel: warp 0 TMA producer (K, V ring; Q, dZ and the
+// row statistics on every (b, h) change), warp 1 TMEM allocator and MMA
+// issuer (lane 0), warps 2-5 softmax (one token row per thread), warps 6-9
+// epilogue (dK, dV stores and the dQ partials).
+#pragma once
+
+#include "tc_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace flare {
+namespace tc {
+
+struct BwdArgs {
+    int B, H, M, N;
+    float sl2;                  // s * log2(e)
+    float s;                    // score scale
+    int q_per_batch;            // Q has a batch dimension
+    const uint8_t *mask;        // [B, N] or null
+    const float *lc;            // [B*H][2][M]: -L log2(e) (or -inf), then -s c
+    float *part;                // [B*H][P_max][M][64] dQ partials
+    int P_max;
+    int64_t T_bh, T_total;      // 128-token tiles per (b, h), and overall
+    int grid;
+    unsigned *status;
+};
+
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t m, uint32_t n, uint32_t a_mn, uint32_t b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn << 15) | (b_mn << 16) | ((n >> 3) << 17) |
+           ((m >> 4) << 24);
+}
+
+// CTA whose span holds tile t (spans: begin(c) = ceil(c T / grid)).
+__host__ __device__ __forceinline__ int bwd_cta_of(int64_t t, int64_t T_total, int grid) {
+    return (int)((t * grid) / T_total);
+}
+
+template <int M_, int STAGES_>
+struct BwdCfg {
+    static constexpr int M = M_, D = 64, TILE = 128, STAGES = STAGES_;
+    static constexpr int THREADS = 320;
+    static constexpr uint32_t TILE_BYTES = TILE * 128;     // 128 rows x 64 bf16 (swizzled)
+    static constexpr uint32_t QZ_BYTES = M * 128;          // [M][64] bf16 (swizzled)
+    static constexpr uint32_t Q_OFF = 0;
+    static constexpr uint32_t DZ_OFF = Q_OFF + QZ_BYTES;
+    static constexpr uint32_t STAGE_OFF = DZ_OFF + QZ_BYTES;
+    static constexpr uint32_t STAGE_BYTES = 2 * TILE_BYTES; // K tile, then V tile
+    // s dS^T in bf16: token rows of 64-latent atoms (atom a at a * TILE_BYTES)
+    static constexpr uint32_t DS_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
+    static constexpr uint32_t DS_BYTES = 2 * TILE_BYTES;
+    static constexpr uint32_t OUT_OFF = DS_OFF + DS_BYTES;  // dK tile, then dV tile
+    static constexpr uint32_t OUT_BYTES = 2 * TILE_BYTES;
+    // row statistics of two (b, h) generations: [2][-L2 (128), -s c (128)]
+    static constexpr uint32_t LC_OFF = OUT_OFF + OUT_BYTES;
+    static constexpr uint32_t LC_BYTES = 2 * 2 * 128 * 4;
+    static constexpr uint32_t BAR_OFF = LC_OFF + LC_BYTES;
+    // full[S], empty[S], qd_full, qd_free, lc_full[2], s_full, p_full,
+    // ds_free, dvdk_full, dvdk_free, dq_full, dq_free, drain
+    static constexpr int NBAR = 2 * STAGES + 13;
+    static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr uint32_t BYTES = MISC_OFF + 64;
+    static constexpr uint32_t ALLOC = BYTES + 1024;
+    static_assert(ALLOC <= 232448, "shared memory budget of one CTA exceeded");
+    static_assert(QZ_BYTES % 1024 == 0, "operand tiles must stay 1 KB aligned");
+    // tensor memory columns
+    static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 320, DQ_COL = 384;
+    static constexpr uint32_t TMEM_COLS = 512;
+};
+
+// ---- TMA stores (bulk-group completion) ----------------------------------------
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t src, int x, int y, int z,
+                                             int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The shared-memory sources of every committed store have been read.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Every committed store is complete.
+__device__ __forceinline__ void bulk_wait_group0() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// ---- prologue: dZ in bf16 and the per-row constants -----------------------------
+// One warp per latent row (D = 64: two elements per lane).
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const float *__restrict__ Z,
+                                                       const float *__restrict__ L,
+                                                       const float *__restrict__ dZ,
+                                                       __nv_bfloat16 *__restrict__ dZb,
+                                                       float *__restrict__ lc, int64_t rows, int M,
+                                                       float s) {
+    const int lane = threadIdx.x & 31;
+    const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (r >= rows) return;
+    const float2 z = reinterpret_cast<const float2 *>(Z + r * 64)[lane];
+    const float2 g = reinterpret_cast<const float2 *>(dZ + r * 64)[lane];
+    float c = z.x * g.x + z.y * g.y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    reinterpret_cast<uint32_t *>(dZb + r * 64)[lane] = pack_bf16(g.x, g.y);
+    if (lane == 0) {
+        const int64_t bh = r / M;
+        const int m = (int)(r - bh * M);
+        const float Lv = L[r];
+        lc[bh * 2 * M + m] = (Lv == -INFINITY) ? -INFINITY : -Lv * 1.4426950408889634f;
+        lc[bh * 2 * M + M + m] = -s * c;
+    }
+}
+
+// ---- dQ = sum over the pieces of each (b, h) ------------------------------------
+__global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const float *__restrict__ part,
+                                                            float *__restrict__ dQ, int64_t BH, int M,
+                                                            int P_max, int64_t T_bh, int64_t T_total,
+                                                            int grid) {
+    const int64_t per_bh = (int64_t)M * 16;                 // float4s of one (b, h)
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= BH * per_bh) return;
+    const int64_t bh = i / per_bh, rem = i - bh * per_bh;
+    const int c0 = bwd_cta_of(bh * T_bh, T_total, grid);
+    const int np = bwd_cta_of(bh * T_bh + T_bh - 1, T_total, grid) - c0 + 1;
+    const float4 *src = reinterpret_cast<const float4 *>(part) + bh * P_max * per_bh + rem;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p = 0; p < np; ++p) {
+        const float4 v = __ldcg(src + p * per_bh);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+    }
+    reinterpret_cast<float4 *>(dQ)[i] = acc;
+}
+
+// ---- the tile kernel -------------------------------------------------------------
+template <int M, int STAGES>
+__global__ void __launch_bounds__(BwdCfg<M, STAGES>::THREADS, 1)
+bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+              const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdZ,
+              const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+              const BwdArgs a) {
+    using C = BwdCfg<M, STAGES>;
+    constexpr uint32_t TB = C::TILE_BYTES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + C::Q_OFF, sdZ = sbase + C::DZ_OFF, sStage = sbase + C::STAGE_OFF;
+    const uint32_t sDS = sbase + C::DS_OFF, sOut = sbase + C::OUT_OFF;
+    const uint32_t bar0 = sbase + C::BAR_OFF;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    const uint32_t qd_full = bar0 + 8u * (2 * STAGES), qd_free = qd_full + 8;
+    auto lc_full = [&](int p) { return bar0 + 8u * (2 * STAGES + 2 + p); };
+    const uint32_t s_full = bar0 + 8u * (2 * STAGES + 4), p_full = s_full + 8, ds_free = s_full + 16;
+    const uint32_t dvdk_full = s_full + 24, dvdk_free = s_full + 32;
+    const uint32_t dq_full = s_full + 40, dq_free = s_full + 48, drain = s_full + 56;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+    float *lcs = reinterpret_cast<float *>(smem + C::LC_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const int64_t tb = ((int64_t)cta * a.T_total + a.grid - 1) / a.grid;
+    const int64_t te = ((int64_t)(cta + 1) * a.T_total + a.grid - 1) / a.grid;
+    const int64_t ntiles = te - tb;
+    const int64_t bh0 = tb / a.T_bh, k0 = tb - bh0 * a.T_bh;
+    Waiter wt{abort_flag, a.status};
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(qd_full, 1);
+        mbar_init(qd_free, 1);
+        mbar_init(lc_full(0), 1);
+        mbar_init(lc_full(1), 1);
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 4);          // one arrival per softmax warp
+        mbar_init(ds_free, 1);
+        mbar_init(dvdk_full, 1);
+        mbar_init(dvdk_free, 4);       // one arrival per epilogue warp
+        mbar_init(dq_full, 1);
+        mbar_init(dq_free, 4);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmdZ);
+        prefetch_tmap(&tmdK);
+        prefetch_tmap(&tmdV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (M < 128 && warp >= 2) {
+        // latents M..127 of dS^T stay zero: the dQ MMA always spans 128 rows
+        for (int q = threadIdx.x - 64; q < (int)TB / 16; q += 256)
+            reinterpret_cast<uint4 *>(smem + C::DS_OFF + TB)[q] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        const uint64_t pol = policy_evict_first();
+        int64_t bh = bh0, kt = k0, cur = -1;
+        int u = -1;
+        int64_t j = 0;
+        for (; j < ntiles && !wt.aborted(); ++j) {
+            const int b = (int)(bh / a.H), h = (int)(bh - (int64_t)b * a.H);
+            if (bh != cur) {
+                ++u;
+                cur = bh;
+                // Q, dZ and the statistics of the previous (b, h) are no longer read
+                if (u > 0 && !__all_sync(0xffffffffu, wt.wait(qd_free, (uint32_t)(u - 1) & 1))) break;
+                float *dst = lcs + (u & 1) * 256;
+                const float *src = a.lc + bh * 2 * M;
+                for (int i = lane; i < 2 * M; i += 32) dst[(i / M) * 128 + (i % M)] = src[i];
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(lc_full(u & 1));
+                    mbar_arrive_expect_tx(qd_full, 2 * C::QZ_BYTES);
+                    tma_load_4d(sQ, &tmQ, 0, 0, h, a.q_per_batch ? b : 0, qd_full);
+                    tma_load_4d(sdZ, &tmdZ, 0, 0, h, b, qd_full);
+                }
+                __syncwarp();
+            }
+            const int s = (int)(j % STAGES);
+            if (!__all_sync(0xffffffffu, wt.wait(empty(s), ((uint32_t)(j / STAGES) & 1) ^ 1))) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full(s), C::STAGE_BYTES);
+                const uint32_t dst = sStage + s * C::STAGE_BYTES;
+                tma_load_4d_hint(dst, &tmK, 0, h, (int)(kt * 128), b, full(s), pol);
+                tma_load_4d_hint(dst + TB, &tmV, 0, h, (int)(kt * 128), b, full(s), pol);
+            }
+            __syncwarp();
+            if (++kt == a.T_bh) {
+                kt = 0;
+                ++bh;
+            }
+        }
+        if (wt.aborted() && lane == 0) {
+            // let every issued load land before the CTA exits
+            const uint64_t t0 = globaltimer();
+            for (int64_t jj = (j > STAGES ? j - STAGES : 0); jj < j; ++jj)
+                while (!mbar_try_wait(full((int)(jj % STAGES)), (uint32_t)(jj / STAGES) & 1) &&
+                       globaltimer() - t0 < 500000000ull) {
+                }
+            if (u >= 0)
+                while (!mbar_try_wait(qd_full, (uint32_t)u & 1) && globaltimer() - t0 < 500000000ull) {
+                }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (lane 0) ----------------
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16(128, M, 0, 0);
+            constexpr uint32_t idG = idesc_bf16(128, 64, 0, 1);    // dV, dK: A in TMEM, B MN-major
+            constexpr uint32_t idQ = idesc_bf16(128, 64, 1, 1);    // dQ: A, B MN-major
+            const uint64_t dQk = desc_sw128(sQ, 16, 1024);          // Q, K-major (B of S^T)
+            const uint64_t dZk = desc_sw128(sdZ, 16, 1024);         // dZ, K-major (B of dP^T)
+            const uint64_t dQm = desc_sw128(sQ, TB, 1024);          // Q, MN-major (B of dK)
+            const uint64_t dZm = desc_sw128(sdZ, TB, 1024);         // dZ, MN-major (B of dV)
+            const uint64_t dDS = desc_sw128(sDS, TB, 1024);         // s dS^T, MN-major (A of dQ)
+            int64_t bhS = bh0, ktS = k0, curS = -1;                  // cursor of the S tiles
+            int uS = -1;
+            bool ok = true;
+            auto issue_sdp = [&](int64_t jj) -> bool {
+                if (bhS != curS) {
+                    ++uS;
+                    curS = bhS;
+                    if (!wt.wait(qd_full, (uint32_t)uS & 1)) return false;
+                }
+                const int s = (int)(jj % STAGES);
+                if (!wt.wait(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
+                tc_fence_after();
+                const uint64_t dK = desc_sw128(sStage + s * C::STAGE_BYTES, 16, 1024);
+                const uint64_t dV = desc_sw128(sStage + s * C::STAGE_BYTES + TB, 16, 1024);
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb)
+                    umma_bf16_ss(tmem + C::S_COL, dK + 2 * kb, dQk + 2 * kb, idS, kb > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb)
+                    umma_bf16_ss(tmem + C::DP_COL, dV + 2 * kb, dZk + 2 * kb, idS, kb > 0 ? 1u : 0u);
+                umma_commit(s_full);
+                if (++ktS == a.T_bh) {
+                    ktS = 0;
+                    ++bhS;
+                }
+                return true;
+            };
+            int64_t bhP = bh0, ktP = k0;                             // cursor of the gradient tiles
+            int uP = 0;                                              // piece of the current tile
+            if (ntiles > 0) ok = issue_sdp(0);
+            for (int64_t j = 0; j < ntiles && ok; ++j) {
+                const bool first = (j == 0) || ktP == 0;
+                int64_t bhN = bhP, ktN = ktP + 1;
+                if (ktN == a.T_bh) {
+                    ktN = 0;
+                    ++bhN;
+                }
+                const bool last = (j + 1 == ntiles) || bhN != bhP;
+                if (!(ok = wt.wait(p_full, (uint32_t)j & 1))) break;
+                tc_fence_after();
+                if (j > 0 && !(ok = wt.wait(dvdk_free, (uint32_t)(j - 1) & 1))) break;
+                tc_fence_after();
+                // dV = P^T dZ, dK = (s dS)^T Q: K = M latents, 16 per MMA
+#pragma unroll
+                for (int kb = 0; kb < M / 16; ++kb)
+                    umma_bf16_ts(tmem + C::DV_COL, tmem + C::S_COL + 8 * kb, dZm + kb * (2048 >> 4), idG,
+                                 kb > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kb = 0; kb < M / 16; ++kb)
+                    umma_bf16_ts(tmem + C::DK_COL, tmem + C::DP_COL + 8 * kb, dQm + kb * (2048 >> 4), idG,
+                                 kb > 0 ? 1u : 0u);
+                umma_commit(dvdk_full);
+                if (last) umma_commit(qd_free);
+                // the next tile's scores overwrite P and dS in TMEM (MMAs run in issue order)
+                if (j + 1 < ntiles && !(ok = issue_sdp(j + 1))) break;
+                // dQ += (s dS) K over the tile's 128 tokens, 16 per MMA
+                if (first && uP > 0 && !(ok = wt.wait(dq_free, (uint32_t)(uP - 1) & 1))) break;
+                tc_fence_after();
+                const int s = (int)(j % STAGES);
+                const uint64_t dKm = desc_sw128(sStage + s * C::STAGE_BYTES, TB, 1024);
+#pragma unroll
+                for (int kb = 0; kb < 8; ++kb)
+                    umma_bf16_ss(tmem + C::DQ_COL, dDS + kb * (2048 >> 4), dKm + kb * (2048 >> 4), idQ,
+                                 (kb > 0 || !first) ? 1u : 0u);
+                umma_commit(ds_free);
+                umma_commit(empty(s));
+                if (last) {
+                    umma_commit(dq_full);
+                    ++uP;
+                }
+                bhP = bhN;
+                ktP = ktN;
+            }
+            if (wt.aborted()) {
+                umma_commit(drain);
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < 500000000ull) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ---------------- softmax: P and s dS of one token row per thread ----------------
+        const int quad = warp & 3;
+        const int rig = quad * 32 + lane;                     // token row within the tile
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const uint32_t s_tm = tmem + C::S_COL + lane_off, dp_tm = tmem + C::DP_COL + lane_off;
+        const uint64_t c2 = f2pack(a.sl2, a.sl2), sc2 = f2pack(a.s, a.s);
+        auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
+            return __all_sync(0xffffffffu, wt.wait(bar, par));
+        };
+        int64_t bh = bh0, kt = k0, cur = -1;
+        int u = -1;
+        for (int64_t j = 0; j < ntiles; ++j) {
+            const int b = (int)(bh / a.H);
+            if (bh != cur) {
+                ++u;
+                cur = bh;
+                if (!wwait(lc_full(u & 1), (uint32_t)(u >> 1) & 1)) break;
+            }
+            const float *nl2 = lcs + (u & 1) * 256, *ncs = nl2 + 128;
+            const int64_t n = kt * 128 + rig;
+            const bool valid = n < a.N && (a.mask == nullptr || a.mask[(int64_t)b * a.N + n] != 0);
+            if (!wwait(s_full, (uint32_t)j & 1)) break;
+            tc_fence_after();
+            bool ok = true;
+#pragma unroll
+            for (int c = 0; c < M / 32; ++c) {
+                uint32_t rs[32], rp[32];
+                tmem_ld32(s_tm + 32 * c, rs);
+                tmem_ld32(dp_tm + 32 * c, rp);
+                tmem_wait_ld();
+                uint32_t pw[16], dw[16];
+                if (valid) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int m = 32 * c + 2 * i;
+                        const uint64_t nl = *reinterpret_cast<const uint64_t *>(nl2 + m);
+                        const uint64_t nc = *reinterpret_cast<const uint64_t *>(ncs + m);
+                        float t0, t1;
+                        f2unpack(fma2(f2pack(__uint_as_float(rs[2 * i]), __uint_as_float(rs[2 * i + 1])), c2, nl),
+                                 t0, t1);
+                        const uint64_t p2 = f2pack(ex2(t0), ex2(t1));
+                        const uint64_t g2 =
+                            fma2(f2pack(__uint_as_float(rp[2 * i]), __uint_as_float(rp[2 * i + 1])), sc2, nc);
+                        float p0, p1, d0, d1;
+                        f2unpack(p2, p0, p1);
+                        f2unpack(mul2(p2, g2), d0, d1);
+                        pw[i] = pack_bf16(p0, p1);
+                        dw[i] = pack_bf16(d0, d1);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pw[i] = dw[i] = 0u;
+                }
+                tmem_st16(s_tm + 16 * c, pw);
+                tmem_st16(dp_tm + 16 * c, dw);
+                // the previous tile's dQ MMA has read the shared dS buffer
+                if (c == 0 && j > 0 && !(ok = wwait(ds_free, (uint32_t)(j - 1) & 1))) break;
+                // s dS^T row into the MN-major A operand of dQ: latents 32c..32c+31
+                uint8_t *row = smem + C::DS_OFF + (c >> 1) * TB + rig * 128;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int chunk = 4 * (c & 1) + q;
+                    *reinterpret_cast<uint4 *>(row + ((chunk ^ (rig & 7)) << 4)) =
+                        make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]);
+                }
+            }
+            if (!ok) break;
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+            if (++kt == a.T_bh) {
+                kt = 0;
+                ++bh;
+            }
+        }
+    } else {
+        // ---------------- epilogue: dK, dV tiles and the dQ partials ----------------
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;                     // token row, or latent row of dQ
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const bool e0 = warp == 6 && lane == 0;               // issues the TMA stores
+        auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
+            return __all_sync(0xffffffffu, wt.wait(bar, par));
+        };
+        int64_t bh = bh0, kt = k0;
+        int u = 0;
+        for (int64_t j = 0; j < ntiles; ++j) {
+            const int b = (int)(bh / a.H), h = (int)(bh - (int64_t)b * a.H);
+            int64_t bhN = bh, ktN = kt + 1;
+            if (ktN == a.T_bh) {
+                ktN = 0;
+                ++bhN;
+            }
+            const bool last = (j + 1 == ntiles) || bhN != bh;
+            if (!wwait(dvdk_full, (uint32_t)j & 1)) break;
+            tc_fence_after();
+            uint32_t rv[2][32], rk[2][32];
+            tmem_ld32(tmem + C::DV_COL + lane_off, rv[0]);
+            tmem_ld32(tmem + C::DV_COL + 32 + lane_off, rv[1]);
+            tmem_ld32(tmem + C::DK_COL + lane_off, rk[0]);
+            tmem_ld32(tmem + C::DK_COL + 32 + lane_off, rk[1]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dvdk_free);
+            // the staging tiles are free once the previous stores have read them
+            if (j > 0) {
+                if (e0) bulk_wait_group_read0();
+                named_bar_sync(1, 128);
+            }
+            uint8_t *kr = smem + C::OUT_OFF + row * 128, *vr = kr + TB;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int chunk = 4 * h2 + q, pos = (chunk ^ (row & 7)) << 4;
+                    const uint32_t *k8 = rk[h2] + 8 * q, *v8 = rv[h2] + 8 * q;
+                    *reinterpret_cast<uint4 *>(kr + pos) = make_uint4(
+                        pack_bf16(__uint_as_float(k8[0]), __uint_as_float(k8[1])),
+                        pack_bf16(__uint_as_float(k8[2]), __uint_as_float(k8[3])),
+                        pack_bf16(__uint_as_float(k8[4]), __uint_as_float(k8[5])),
+                        pack_bf16(__uint_as_float(k8[6]), __uint_as_float(k8[7])));
+                    *reinterpret_cast<uint4 *>(vr + pos) = make_uint4(
+                        pack_bf16(__uint_as_float(v8[0]), __uint_as_float(v8[1])),
+                        pack_bf16(__uint_as_float(v8[2]), __uint_as_float(v8[3])),
+                        pack_bf16(__uint_as_float(v8[4]), __uint_as_float(v8[5])),
+                        pack_bf16(__uint_as_float(v8[6]), __uint_as_float(v8[7])));
+                }
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (e0) {
+                // rows past N are clipped by the tensor map
+                tma_store_4d(&tmdK, sOut, 0, h, (int)(kt * 128), b);
+                tma_store_4d(&tmdV, sOut + TB, 0, h, (int)(kt * 128), b);
+                bulk_commit_group();
+            }
+            if (last) {
+                // the (b, h)'s dQ partial of this span: one latent row per thread
+                if (!wwait(dq_full, (uint32_t)u & 1)) break;
+                tc_fence_after();
+                uint32_t rq[2][32];
+                tmem_ld32(tmem + C::DQ_COL + lane_off, rq[0]);
+                tmem_ld32(tmem + C::DQ_COL + 32 + lane_off, rq[1]);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dq_free);
+                if (row < M) {
+                    const int piece = cta - bwd_cta_of(bh * a.T_bh, a.T_total, a.grid);
+                    float4 *dst = reinterpret_cast<float4 *>(a.part + ((bh * a.P_max + piece) * M + row) * 64);
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[8 * h2 + q] = make_float4(
+                                __uint_as_float(rq[h2][4 * q]), __uint_as_float(rq[h2][4 * q + 1]),
+                                __uint_as_float(rq[h2][4 * q + 2]), __uint_as_float(rq[h2][4 * q + 3]));
+                }
+                ++u;
+            }
+            bh = bhN;
+            kt = ktN;
+        }
+        if (e0) bulk_wait_group0();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+}  // namespace tc
+}  // namespace flare

@@ -49,7 +49,8 @@ bool tc_decode_available();
 cudaError_t launch_decode_tc(const Problem &pr, const void *Q, bool q_is_f32, const float *Z,
                              const void *K, void *Y, int sms, unsigned *status, cudaStream_t st);
 
-bool tc_bwd_available();
+// bf16 with D = 64 and M in {64, 128}.
+bool tc_bwd_supported(bool bf16, int M, int D);
 size_t tc_encoder_bwd_workspace(const Problem &pr, int sms);
 cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *K, const void *V,
                                   const uint8_t *mask, const float *Z, const float *L,

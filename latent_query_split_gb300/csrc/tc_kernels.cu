@@ -3,6 +3,7 @@
 #include "tc_common.cuh"
 #include "tc_encoder.cuh"
 #include "tc_decode.cuh"
+#include "tc_backward.cuh"
 
 #include <cudaTypedefs.h>
 
@@ -214,13 +215,108 @@ cudaError_t launch_decode_tc(const Problem &pr, const void *Q, bool q_is_f32, co
     return cudaErrorNotSupported;
 }
 
-bool tc_bwd_available() { return false; }
-size_t tc_encoder_bwd_workspace(const Problem &, int) { return 0; }
-cudaError_t launch_encoder_bwd_tc(const Problem &, const void *, const void *, const void *,
-                                  const uint8_t *, const float *, const float *, const float *,
-                                  float *, void *, void *, void *, size_t, int, unsigned *,
-                                  cudaStream_t) {
-    return cudaErrorNotSupported;
+bool tc_bwd_supported(bool bf16, int M, int D) { return bf16 && D == 64 && (M == 64 || M == 128); }
+
+namespace {
+// Backward workspace: dZ in bf16 [B*H*M*64], the row constants [B*H][2][M]
+// and the dQ partials [B*H][P_max][M][64].
+struct BwdLayout {
+    int64_t T_bh, T_total;
+    int grid, P_max;
+    size_t dzb, lc, part, bytes;
+};
+
+void bwd_layout(const Problem &pr, int sms, BwdLayout &l) {
+    l.T_bh = (pr.N + 127) / 128;
+    l.T_total = (int64_t)pr.B * pr.H * l.T_bh;
+    l.grid = (int)(l.T_total < sms ? l.T_total : sms);
+    if (l.grid < 1) l.grid = 1;
+    // a (b, h) spans at most ceil(T_bh / shortest span) + 1 CTAs
+    const int64_t span_min = l.T_total > 0 ? l.T_total / l.grid : 1;
+    l.P_max = l.T_bh > 0 ? (int)((l.T_bh + span_min - 1) / span_min) + 1 : 1;
+    const size_t bhm = (size_t)pr.B * pr.H * pr.M;
+    size_t o = 0;
+    l.dzb = o;
+    o += align256(2 * bhm * 64);
+    l.lc = o;
+    o += align256(4 * bhm * 2);
+    l.part = o;
+    o += align256(4 * bhm * (size_t)l.P_max * 64);
+    l.bytes = o;
+}
+
+template <int M>
+cudaError_t launch_bwd(const CUtensorMap *maps, const tc::BwdArgs &a, cudaStream_t st) {
+    using C = tc::BwdCfg<M, 3>;
+    auto k = tc::bwd_tc_kernel<M, 3>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
+    if (e != cudaSuccess) return e;
+    k<<<a.grid, C::THREADS, C::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
+    note_launch();
+    return cudaGetLastError();
+}
+}  // namespace
+
+size_t tc_encoder_bwd_workspace(const Problem &pr, int sms) {
+    if (!tc_bwd_supported(pr.bf16, pr.M, pr.D)) return 0;
+    BwdLayout l;
+    bwd_layout(pr, sms, l);
+    return l.bytes;
+}
+
+cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *K, const void *V,
+                                  const uint8_t *mask, const float *Z, const float *L,
+                                  const float *dZ, float *dQ, void *dK, void *dV, void *ws,
+                                  size_t ws_bytes, int sms, unsigned *status, cudaStream_t st) {
+    if (!tc_bwd_supported(pr.bf16, pr.M, pr.D)) return cudaErrorNotSupported;
+    BwdLayout l;
+    bwd_layout(pr, sms, l);
+    if (ws_bytes < l.bytes) return cudaErrorInvalidValue;
+    const int64_t BH = (int64_t)pr.B * pr.H;
+    if (BH == 0) return cudaSuccess;
+    if (l.T_total == 0)            // no token: dQ = 0, no dK / dV
+        return cudaMemsetAsync(dQ, 0, sizeof(float) * (size_t)BH * pr.M * pr.D, st);
+    char *w = (char *)ws;
+    __nv_bfloat16 *dzb = (__nv_bfloat16 *)(w + l.dzb);
+    float *lc = (float *)(w + l.lc), *part = (float *)(w + l.part);
+    const int64_t rows = BH * pr.M;
+    tc::bwd_prep_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(Z, L, dZ, dzb, lc, rows, pr.M,
+                                                                            pr.scale);
+    note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t qb = pr.q_bstride == 0 ? 1 : pr.B;
+    CUtensorMap maps[6];
+    if (!make_map(&maps[0], K, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
+        !make_map(&maps[1], V, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
+        !make_map(&maps[2], Q, pr.D, pr.M, pr.H, qb, (uint32_t)pr.M, 1) ||
+        !make_map(&maps[3], dzb, pr.D, pr.M, pr.H, pr.B, (uint32_t)pr.M, 1) ||
+        !make_map(&maps[4], dK, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
+        !make_map(&maps[5], dV, pr.D, pr.H, pr.N, pr.B, 1, 128))
+        return cudaErrorInvalidValue;
+    tc::BwdArgs a;
+    a.B = pr.B;
+    a.H = pr.H;
+    a.M = pr.M;
+    a.N = pr.N;
+    a.s = pr.scale;
+    a.sl2 = pr.scale * 1.4426950408889634f;
+    a.q_per_batch = pr.q_bstride != 0;
+    a.mask = mask;
+    a.lc = lc;
+    a.part = part;
+    a.P_max = l.P_max;
+    a.T_bh = l.T_bh;
+    a.T_total = l.T_total;
+    a.grid = l.grid;
+    a.status = status;
+    e = pr.M == 128 ? launch_bwd<128>(maps, a, st) : launch_bwd<64>(maps, a, st);
+    if (e != cudaSuccess) return e;
+    const int64_t n4 = BH * pr.M * 16;
+    tc::bwd_dq_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(part, dQ, BH, pr.M, l.P_max,
+                                                                          l.T_bh, l.T_total, l.grid);
+    note_launch();
+    return cudaGetLastError();
 }
 
 }  // namespace flare

@@ -138,6 +138,36 @@ def test_encoder_bwd(cuda_device, kernel, dt, M, D, N):
     assert_close("dV", dV, dVo, dt)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("M,replicated", [(128, True), (64, True), (128, False)])
+def test_encoder_bwd_multi_tile_spans(cuda_device, kernel, M, replicated):
+    """Enough 128-token tiles that each persistent CTA walks several tiles and
+    crosses (b, h) boundaries, so dQ is assembled from several partial pieces;
+    rows with a global L of -inf contribute nothing; repeated runs agree bit
+    for bit (the pieces are summed in a fixed order)."""
+    B, H, N, D = 2, 3, 20000, 64
+    off = [0, 5000, 5000, N]
+    Q, K, V, mask = _problem(16, B, H, M, N, D, "bf16", off, q_std=1.0, replicated=replicated)
+    mask[1, 12000:] = 0
+    g = torch.Generator().manual_seed(17)
+    dZ = torch.randn((B, H, M, D), generator=g).cuda()
+    Zo, Lo = oracle.encode(Q, K, V, mask)
+    Lo[0, 1, :5] = -math.inf
+    Zo[0, 1, :5] = 0.0
+    Zf = torch.from_numpy(Zo).float().cuda()
+    Lf = torch.from_numpy(Lo).float().cuda()
+    dQ, dK, dV = _call(flare.flare_encoder_bwd, Q, K, V, mask, off, Zf, Lf, dZ, kernel=kernel)
+    flare.flare_device_status()
+    dQo, dKo, dVo = oracle.encode_bwd(Q, K, V, mask, Zf, Lf, dZ)
+    assert_close("dQ", dQ, dQo, "bf16")
+    assert_close("dK", dK, dKo, "bf16")
+    assert_close("dV", dV, dVo, "bf16")
+    pad = mask == 0
+    assert dK[pad].abs().max().item() == 0.0 and dV[pad].abs().max().item() == 0.0
+    dQ2, dK2, dV2 = _call(flare.flare_encoder_bwd, Q, K, V, mask, off, Zf, Lf, dZ, kernel=kernel)
+    assert torch.equal(dQ, dQ2) and torch.equal(dK, dK2) and torch.equal(dV, dV2)
+
+
 # ---- edge cases ------------------------------------------------------------------------
 
 @pytest.mark.parametrize("kernel", KERNELS)
