@@ -52,11 +52,6 @@ struct BwdArgs {
     unsigned *status;
 };
 
-__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t m, uint32_t n, uint32_t a_mn, uint32_t b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn << 15) | (b_mn << 16) | ((n >> 3) << 17) |
-           ((m >> 4) << 24);
-}
-
 // CTA whose span holds tile t (spans: begin(c) = ceil(c T / grid)).
 __host__ __device__ __forceinline__ int bwd_cta_of(int64_t t, int64_t T_total, int grid) {
     return (int)((t * grid) / T_total);
@@ -93,35 +88,6 @@ struct BwdCfg {
     static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 320, DQ_COL = 384;
     static constexpr uint32_t TMEM_COLS = 512;
 };
-
-// ---- TMA stores (bulk-group completion) ----------------------------------------
-__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t src, int x, int y, int z,
-                                             int w) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// The shared-memory sources of every committed store have been read.
-__device__ __forceinline__ void bulk_wait_group_read0() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// Every committed store is complete.
-__device__ __forceinline__ void bulk_wait_group0() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 
 // ---- prologue: dZ in bf16 and the per-row constants -----------------------------
 // One warp per latent row (D = 64: two elements per lane).
@@ -402,18 +368,31 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
             return __all_sync(0xffffffffu, wt.wait(bar, par));
         };
+        // whether this thread's token of tile (bh, kt) takes part (loaded a tile ahead)
+        auto token_valid = [&](int64_t tbh, int64_t tkt) -> bool {
+            const int64_t n = tkt * 128 + rig;
+            if (n >= a.N) return false;
+            return a.mask == nullptr || a.mask[(tbh / a.H) * a.N + n] != 0;
+        };
         int64_t bh = bh0, kt = k0, cur = -1;
         int u = -1;
+        bool valid_next = ntiles > 0 && token_valid(bh0, k0);
         for (int64_t j = 0; j < ntiles; ++j) {
-            const int b = (int)(bh / a.H);
             if (bh != cur) {
                 ++u;
                 cur = bh;
                 if (!wwait(lc_full(u & 1), (uint32_t)(u >> 1) & 1)) break;
             }
             const float *nl2 = lcs + (u & 1) * 256, *ncs = nl2 + 128;
-            const int64_t n = kt * 128 + rig;
-            const bool valid = n < a.N && (a.mask == nullptr || a.mask[(int64_t)b * a.N + n] != 0);
+            const bool valid = valid_next;
+            {
+                int64_t bhN = bh, ktN = kt + 1;
+                if (ktN == a.T_bh) {
+                    ktN = 0;
+                    ++bhN;
+                }
+                valid_next = j + 1 < ntiles && token_valid(bhN, ktN);
+            }
             if (!wwait(s_full, (uint32_t)j & 1)) break;
             tc_fence_after();
             bool ok = true;

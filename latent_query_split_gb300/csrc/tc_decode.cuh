@@ -7,7 +7,11 @@
 // it is exact in one tile (no running rescale).
 //
 // One persistent CTA per SM walks a contiguous span of 128-token tiles in
-// (b, h, tile) order. Warp roles:
+// (h, b, tile) order. Head-major order lines the CTAs of different heads up
+// on the same token positions at the same time (with the grid a multiple of
+// H they cover the same relative tile range): a token's H head rows are
+// adjacent in memory, so DRAM pages are consumed by all heads together
+// instead of once per head at unrelated times. Warp roles:
 //   warp 0     producer: K tiles by TMA into a STAGES-deep ring; on every
 //              (b, h) change it converts Q and Z (bf16 or fp32) into swizzled
 //              bf16 operand tiles in shared memory.
@@ -16,7 +20,10 @@
 //                Y_g = P_g Z   (A = P from tensor memory, B = Z shared memory)
 //   warps 2-9  two groups of four warps take alternate tiles (one token row per
 //              thread = TMEM lane): row max, exp2, P (bf16) over S in tensor
-//              memory, then Y / l rounded to bf16 and stored to global memory.
+//              memory. The epilogue of a tile (Y / l rounded to bf16, staged
+//              in shared memory, one TMA store per warp of 32 token rows) runs
+//              in the group's next iteration, once that tile's scores have
+//              arrived, so the group never waits for its own P Z product.
 #pragma once
 
 #include "tc_common.cuh"
@@ -45,11 +52,23 @@ struct DecCfg {
     static constexpr int NG = M <= 128 ? 2 : 1;         // softmax groups (tiles in flight)
     static constexpr int THREADS = 64 + 128 * NG;
     static constexpr uint32_t QZ_ATOM = M * 128;        // bytes of one M-row x 64-col atom
+    // F16P: P and Z enter Y = P Z as fp16, and Z gets one more 16-column block
+    // holding the constant c (the power of two Z was scaled by, see
+    // stage_z_f16), so the same MMA also returns c * l, the row sum of P,
+    // next to c * Y. Needs D + 16 more tensor-memory columns per group.
+    static constexpr bool F16P = NG == 2 ? (M + D + 16 <= 256) : (M + D + 16 <= 512);
+    static constexpr int YN = F16P ? D + 16 : D;        // N of the P Z product
+    static constexpr int ZA = F16P ? KA + 1 : KA;       // atoms of the staged Z
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t Z_OFF = Q_OFF + KA * QZ_ATOM;
-    static constexpr uint32_t STAGE_OFF = Z_OFF + KA * QZ_ATOM;
+    static constexpr uint32_t STAGE_OFF = Z_OFF + ZA * QZ_ATOM;
     static constexpr uint32_t STAGE_BYTES = KA * 128 * 128;   // one K tile
-    static constexpr uint32_t BAR_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
+    // Y staging of each group for the TMA store: 128 token rows, KA atoms
+    static constexpr uint32_t OUT_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
+    static constexpr uint32_t OUT_BYTES = KA * 128 * 128;
+    static constexpr uint32_t BAR_OFF = OUT_OFF + NG * OUT_BYTES;
+    // M <= 128: a token's M scores stay in registers between the max and exp passes
+    static constexpr bool REG_S = M <= 128;
     static constexpr int NCH = M / 32;                   // P chunks of 32 latents
     // full[S], empty[S], qz_full, qz_free, s_full[2], p_chunk[2][8], o_done[2]
     static constexpr int NBAR = 2 * STAGES + 2 + 2 + 16 + 2;
@@ -84,9 +103,58 @@ __device__ __forceinline__ void stage_rows_bf16(uint8_t *dst, const T *src, int 
     }
 }
 
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+    uint32_t y;
+    asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// Z [M, D] fp32 -> the fp16 operand layout of stage_rows_bf16, multiplied by
+// c = 2^-e where 2^e <= max|Z| < 2^(e+1) (e clamped to [-14, 24], so c and
+// every scaled element stay within fp16 range), plus atom D/64 whose first
+// column is c in every row (the row-sum block). c cancels in Y = (c Y)/(c l).
+template <int M, int D>
+__device__ __forceinline__ void stage_z_f16(uint8_t *dst, const float *src, int lane) {
+    constexpr int CHUNKS = M * D / 8;
+    float mx = 0.f;
+    for (int q = lane; q < CHUNKS; q += 32) {
+        const float4 lo = __ldg(reinterpret_cast<const float4 *>(src) + 2 * q);
+        const float4 hi = __ldg(reinterpret_cast<const float4 *>(src) + 2 * q + 1);
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(lo.x), fabsf(lo.y)), fmaxf(fabsf(lo.z), fabsf(lo.w))));
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(hi.x), fabsf(hi.y)), fmaxf(fabsf(hi.z), fabsf(hi.w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    int e = mx > 0.f ? ((__float_as_int(mx) >> 23) & 0xff) - 127 : 0;   // floor(log2 max|Z|)
+    e = e < -14 ? -14 : (e > 24 ? 24 : e);
+    const float c = __int_as_float((127 - e) << 23);                  // 2^-e, exact
+#pragma unroll 4
+    for (int q = lane; q < CHUNKS; q += 32) {
+        const int row = q / (D / 8), j = q % (D / 8);
+        const int atom = j >> 3, jj = j & 7;
+        const float4 lo = __ldg(reinterpret_cast<const float4 *>(src) + 2 * q);
+        const float4 hi = __ldg(reinterpret_cast<const float4 *>(src) + 2 * q + 1);
+        *reinterpret_cast<uint4 *>(dst + atom * (M * 128) + row * 128 + ((jj ^ (row & 7)) << 4)) =
+            make_uint4(pack_f16(lo.x * c, lo.y * c), pack_f16(lo.z * c, lo.w * c),
+                       pack_f16(hi.x * c, hi.y * c), pack_f16(hi.z * c, hi.w * c));
+    }
+    // the row-sum block: columns D..D+15 = [c, 0, ..., 0] (chunks 0 and 1 of the atom)
+    uint8_t *ones = dst + (D / 64) * (M * 128);
+    for (int row = lane; row < M; row += 32) {
+        *reinterpret_cast<uint4 *>(ones + row * 128 + ((0 ^ (row & 7)) << 4)) = make_uint4(pack_f16(c, 0.f), 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(ones + row * 128 + ((1 ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
 template <int M, int D, int STAGES>
 __global__ void __launch_bounds__(DecCfg<M, D, STAGES>::THREADS, 1)
-dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const DecArgs a) {
+dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmY,
+                  const DecArgs a) {
     using C = DecCfg<M, D, STAGES>;
     constexpr int KA = C::KA;
     constexpr int NG = C::NG;
@@ -123,12 +191,15 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const DecArgs a) {
         mbar_init(qz_free, 1);
         for (int g = 0; g < 2; ++g) {
             mbar_init(s_full(g), 1);
-            for (int c = 0; c < 8; ++c) mbar_init(p_chunk(g, c), 128);
+            for (int c = 0; c < 8; ++c) mbar_init(p_chunk(g, c), 4);   // one arrival per softmax warp
             mbar_init(o_done(g), 1);
         }
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) prefetch_tmap(&tmK);
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmY);
+    }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
@@ -148,7 +219,8 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const DecArgs a) {
         uint32_t qz_uses = 0;
         int64_t j = 0;
         for (; j < ntiles && !wt.aborted(); ++j) {
-            const int b = (int)(bh / a.H), h = (int)(bh - (int64_t)b * a.H);
+            // tiles run head-major: index bh = h * B + b (see the kernel comment)
+            const int h = (int)(bh / a.B), b = (int)(bh - (int64_t)h * a.B);
             if (bh != cur_bh) {
                 // Q and Z of the new (b, h), once the MMAs on the old ones are done
                 if (qz_uses > 0 && !__all_sync(0xffffffffu, wt.wait(qz_free, (qz_uses - 1) & 1))) break;
@@ -158,7 +230,10 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const DecArgs a) {
                     stage_rows_bf16<M, D>(smem + C::Q_OFF, reinterpret_cast<const float *>(a.Q) + qoff, lane);
                 else
                     stage_rows_bf16<M, D>(smem + C::Q_OFF, reinterpret_cast<const __nv_bfloat16 *>(a.Q) + qoff, lane);
-                stage_rows_bf16<M, D>(smem + C::Z_OFF, a.Z + ((int64_t)b * a.H + h) * M * D, lane);
+                if constexpr (C::F16P)
+                    stage_z_f16<M, D>(smem + C::Z_OFF, a.Z + ((int64_t)b * a.H + h) * M * D, lane);
+                else
+                    stage_rows_bf16<M, D>(smem + C::Z_OFF, a.Z + ((int64_t)b * a.H + h) * M * D, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qz_full);
@@ -188,10 +263,17 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const DecArgs a) {
                 }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
+        // ---------------- MMA issuer (whole warp, elect.sync issues) ----------------
+        // The warp stays converged so the operands stay warp-uniform; an MMA
+        // issued from one lane of a divergent branch costs several times more
+        // issue time, which made this warp the kernel's bottleneck.
+        {
+            auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
+                return __all_sync(0xffffffffu, wt.wait(bar, par));
+            };
             constexpr uint32_t idS = idesc_bf16_m128(M, 0);
-            constexpr uint32_t idPV = idesc_bf16_m128(D, 1);
+            // P Z: bf16, or fp16 with the row-sum block (N = D + 16)
+            constexpr uint32_t idPV = C::F16P ? idesc_f16(128, C::YN, 0, 1) : idesc_bf16_m128(D, 1);
             const uint64_t dK0 = desc_sw128(sStage, 16, 1024);
             const uint64_t dQ0 = desc_sw128(sQ, 16, 1024);
             const uint64_t dZ0 = desc_sw128(sZ, C::QZ_ATOM, 1024);
@@ -203,11 +285,11 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const DecArgs a) {
             auto issue_s = [&](int64_t jj) -> bool {
                 const int s = (int)(jj % STAGES);
                 if (bhS != cur_bh) {
-                    if (!wt.wait(qz_full, qz_uses & 1)) return false;
+                    if (!wwait(qz_full, qz_uses & 1)) return false;
                     ++qz_uses;
                     cur_bh = bhS;
                 }
-                if (!wt.wait(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
+                if (!wwait(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
                 tc_fence_after();
                 const int g = NG == 2 ? (int)(jj & 1) : 0;
                 const uint64_t dK = dK0 + kStageDesc * s;
@@ -215,10 +297,10 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const DecArgs a) {
                 for (int kb = 0; kb < D / 16; ++kb) {
                     const uint64_t offK = (uint64_t)((kb >> 2) * (128 * 128) + (kb & 3) * 32) >> 4;
                     const uint64_t offQ = (uint64_t)((kb >> 2) * C::QZ_ATOM + (kb & 3) * 32) >> 4;
-                    umma_bf16_ss(tmem + g * 256, dK + offK, dQ0 + offQ, idS, kb > 0 ? 1u : 0u);
+                    umma_ss_elect(tmem + g * 256, dK + offK, dQ0 + offQ, idS, kb > 0 ? 1u : 0u);
                 }
-                umma_commit(s_full(g));
-                umma_commit(empty(s));            // the K tile is only read by S
+                umma_commit_elect(s_full(g));
+                umma_commit_elect(empty(s));            // the K tile is only read by S
                 if (++ktS == a.T_bh) {
                     ktS = 0;
                     ++bhS;
@@ -239,32 +321,35 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const DecArgs a) {
                 const int g = NG == 2 ? (int)(jP & 1) : 0;
                 const int64_t kP = NG == 2 ? (jP >> 1) : jP;
                 for (int c = 0; c < NCH && ok; ++c) {
-                    ok = wt.wait(p_chunk(g, c), (uint32_t)kP & 1);
-                    if (!ok) break;
-                    tc_fence_after();
+                    // P arrives whole (registers path) or chunk by chunk
+                    if (!C::REG_S || c == 0) {
+                        ok = wwait(p_chunk(g, C::REG_S ? 0 : c), (uint32_t)kP & 1);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
                         const int kb = 2 * c + kk;       // 16 latents per MMA
-                        umma_bf16_ts(tmem + g * 256 + M, tmem + g * 256 + kb * 8, dZ0 + kb * (2048 >> 4),
+                        umma_ts_elect(tmem + g * 256 + M, tmem + g * 256 + kb * 8, dZ0 + kb * (2048 >> 4),
                                      idPV, kb > 0 ? 1u : 0u);
                     }
                 }
                 if (!ok) break;
-                umma_commit(o_done(g));
+                umma_commit_elect(o_done(g));
                 const int64_t bh_done = bhP;
                 if (++ktP == a.T_bh) {
                     ktP = 0;
                     ++bhP;
                 }
                 ++nP;
-                if (nP == ntiles || bhP != bh_done) umma_commit(qz_free);
+                if (nP == ntiles || bhP != bh_done) umma_commit_elect(qz_free);
                 ok = pump_s();
             }
             // make every issued MMA finish before TMEM is released
             if (ok && ntiles > 0) {
                 const int gl = NG == 2 ? (int)((ntiles - 1) & 1) : 0;
                 const int64_t kl = NG == 2 ? ((ntiles - 1) >> 1) : ntiles - 1;
-                wt.wait(o_done(gl), (uint32_t)kl & 1);
+                wwait(o_done(gl), (uint32_t)kl & 1);
             }
         }
         __syncwarp();
@@ -277,91 +362,192 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const DecArgs a) {
         const uint32_t s_tmem = tmem + g * 256 + lane_off;
         const uint32_t y_tmem = tmem + g * 256 + M + lane_off;
         const uint64_t c2 = f2pack(a.sl2, a.sl2);
+        // each warp stages and stores its own 32 token rows (a 4 KB slab per atom)
+        uint8_t *stage_out = smem + C::OUT_OFF + g * C::OUT_BYTES + quad * 32 * 128;
         auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
             return __all_sync(0xffffffffu, wt.wait(bar, par));
         };
+        // the group's previous tile, whose Y is still in tensor memory
+        bool have_prev = false;
+        int prev_b = 0, prev_h = 0, prev_n0 = 0;
+        int64_t prev_k = 0;
+        float prev_l = 1.f;
+        uint32_t stores = 0;
+        auto epilogue = [&]() -> bool {
+            if (!wwait(o_done(g), (uint32_t)prev_k & 1)) return false;
+            tc_fence_after();
+            uint32_t r[D / 32][32];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(y_tmem + c * 32, r[c]);
+            uint32_t lw = 0;
+            if constexpr (C::F16P) lw = tmem_ld1(y_tmem + D);    // c * l from the row-sum block
+            tmem_wait_ld();
+            tc_fence_before();
+            // the staging slab is free once the warp's previous store has read it
+            if (stores > 0) {
+                if (lane == 0) bulk_wait_group_read0();
+                __syncwarp();
+            }
+            const float inv = 1.f / (C::F16P ? __uint_as_float(lw) : prev_l);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint8_t *row = stage_out + (c >> 1) * (128 * 128) + lane * 128;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int chunk = 4 * (c & 1) + q;
+                    const uint32_t *v = r[c] + 8 * q;
+                    *reinterpret_cast<uint4 *>(row + ((chunk ^ (rig & 7)) << 4)) = make_uint4(
+                        pack_bf16(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                        pack_bf16(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                        pack_bf16(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                        pack_bf16(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int n0 = prev_n0 + quad * 32;
+            if (lane == 0 && n0 < a.N) {
+                // token rows past N are clipped by the tensor map
+#pragma unroll
+                for (int ka = 0; ka < KA; ++ka)
+                    tma_store_4d(&tmY, smem_u32(stage_out) + ka * (128 * 128), 64 * ka, prev_h, n0, prev_b);
+                bulk_commit_group();
+            }
+            ++stores;
+            return true;
+        };
         int64_t bh = bh0, kt = k0;
-        for (int64_t j = 0; j < ntiles; ++j) {
+        bool ok = true;
+        for (int64_t j = 0; j < ntiles && ok; ++j) {
             const bool mine = NG == 1 || (int)(j & 1) == g;
             if (mine) {
                 const int64_t k = NG == 2 ? (j >> 1) : j;
                 if (!wwait(s_full(g), (uint32_t)k & 1)) break;
                 tc_fence_after();
-                // pass 1: row maximum over the M latents
-                float mx[2] = {-INFINITY, -INFINITY};
+                if (have_prev && !(ok = epilogue())) break;
+                float l;
+                if constexpr (C::REG_S) {
+                    // every score of the row in registers: one load, max, exp
+                    uint32_t r[NCH][32];
 #pragma unroll
-                for (int c = 0; c < M / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(s_tmem + c * 32, r);
+                    for (int c = 0; c < NCH; ++c) tmem_ld32(s_tmem + c * 32, r[c]);
                     tmem_wait_ld();
+                    float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        mx[i & 1] = max3(mx[i & 1], __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                }
-                const float m = fmaxf(mx[0], mx[1]) * a.sl2;
-                const uint64_t nm2 = f2pack(-m, -m);
-                // pass 2: P = exp2(s*c - m) in bf16 over S's first M/2 columns
-                uint64_t ls2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+                    for (int c = 0; c < NCH; ++c)
 #pragma unroll
-                for (int c = 0; c < NCH; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(s_tmem + c * 32, r);
-                    tmem_wait_ld();
-                    uint32_t pw[16];
+                        for (int i = 0; i < 16; ++i)
+                            mx[i & 1] = max3(mx[i & 1], __uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1]));
+                    const float m = fmaxf(mx[0], mx[1]) * a.sl2;
+                    const uint64_t nm2 = f2pack(-m, -m);
+                    if constexpr (C::F16P) {
+                        // P = exp2(t) two at a time in fp16; the row sum comes from the MMA
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        float t0, t1, t2, t3;
-                        f2unpack(fma2(f2pack(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), c2, nm2), t0, t1);
-                        f2unpack(fma2(f2pack(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), c2, nm2), t2, t3);
-                        const float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
-                        ls2[0] = add2(ls2[0], f2pack(p0, p1));
-                        ls2[1] = add2(ls2[1], f2pack(p2, p3));
-                        pw[2 * i] = pack_bf16(p0, p1);
-                        pw[2 * i + 1] = pack_bf16(p2, p3);
+                        for (int c = 0; c < NCH; ++c) {
+                            uint32_t pw[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                float t0, t1;
+                                f2unpack(fma2(f2pack(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1])), c2, nm2), t0, t1);
+                                pw[i] = ex2_f16x2(pack_f16(t0, t1));
+                            }
+                            tmem_st16(s_tmem + c * 16, pw);
+                        }
+                        l = 1.f;
+                    } else {
+                        uint64_t ls2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) {
+                            uint32_t pw[16];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                float t0, t1, t2, t3;
+                                f2unpack(fma2(f2pack(__uint_as_float(r[c][4 * i]), __uint_as_float(r[c][4 * i + 1])), c2, nm2), t0, t1);
+                                f2unpack(fma2(f2pack(__uint_as_float(r[c][4 * i + 2]), __uint_as_float(r[c][4 * i + 3])), c2, nm2), t2, t3);
+                                const float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
+                                ls2[0] = add2(ls2[0], f2pack(p0, p1));
+                                ls2[1] = add2(ls2[1], f2pack(p2, p3));
+                                pw[2 * i] = pack_bf16(p0, p1);
+                                pw[2 * i + 1] = pack_bf16(p2, p3);
+                            }
+                            tmem_st16(s_tmem + c * 16, pw);
+                        }
+                        float a0, a1, a2, a3;
+                        f2unpack(ls2[0], a0, a1);
+                        f2unpack(ls2[1], a2, a3);
+                        l = (a0 + a1) + (a2 + a3);
                     }
-                    tmem_st16(s_tmem + c * 16, pw);
                     tmem_wait_st();
                     tc_fence_before();
-                    mbar_arrive(p_chunk(g, c));
-                }
-                float l;
-                {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(p_chunk(g, 0));
+                } else {
+                    // pass 1: row maximum over the M latents
+                    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                    for (int c = 0; c < M / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(s_tmem + c * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            mx[i & 1] = max3(mx[i & 1], __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                    }
+                    const float m = fmaxf(mx[0], mx[1]) * a.sl2;
+                    const uint64_t nm2 = f2pack(-m, -m);
+                    // pass 2: P = exp2(s*c - m) (fp16 or bf16) over S's first M/2 columns
+                    uint64_t ls2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(s_tmem + c * 32, r);
+                        tmem_wait_ld();
+                        uint32_t pw[16];
+                        if constexpr (C::F16P) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                float t0, t1;
+                                f2unpack(fma2(f2pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c2, nm2), t0, t1);
+                                pw[i] = ex2_f16x2(pack_f16(t0, t1));
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                float t0, t1, t2, t3;
+                                f2unpack(fma2(f2pack(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), c2, nm2), t0, t1);
+                                f2unpack(fma2(f2pack(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), c2, nm2), t2, t3);
+                                const float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
+                                ls2[0] = add2(ls2[0], f2pack(p0, p1));
+                                ls2[1] = add2(ls2[1], f2pack(p2, p3));
+                                pw[2 * i] = pack_bf16(p0, p1);
+                                pw[2 * i + 1] = pack_bf16(p2, p3);
+                            }
+                        }
+                        tmem_st16(s_tmem + c * 16, pw);
+                        tmem_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(p_chunk(g, c));
+                    }
                     float a0, a1, a2, a3;
                     f2unpack(ls2[0], a0, a1);
                     f2unpack(ls2[1], a2, a3);
                     l = (a0 + a1) + (a2 + a3);
                 }
-                // epilogue: Y row / l in bf16 (rows past N belong to no token)
-                if (!wwait(o_done(g), (uint32_t)k & 1)) break;
-                tc_fence_after();
-                const float inv = 1.f / l;
-                const int b = (int)(bh / a.H), h = (int)(bh - (int64_t)b * a.H);
-                const int64_t n = kt * 128 + rig;
-                __nv_bfloat16 *yrow = a.Y + (((int64_t)b * a.N + n) * a.H + h) * D;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(y_tmem + c * 32, r);
-                    tmem_wait_ld();
-                    if (n < a.N) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                w[q] = pack_bf16(__uint_as_float(r[8 * v + 2 * q]) * inv,
-                                                 __uint_as_float(r[8 * v + 2 * q + 1]) * inv);
-                            reinterpret_cast<uint4 *>(yrow + c * 32)[v] = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
-                    }
-                }
-                tc_fence_before();
+                have_prev = true;
+                prev_h = (int)(bh / a.B);
+                prev_b = (int)(bh - (int64_t)prev_h * a.B);
+                prev_n0 = (int)(kt * 128);
+                prev_k = k;
+                prev_l = l;
             }
             if (++kt == a.T_bh) {
                 kt = 0;
                 ++bh;
             }
         }
+        if (ok && have_prev && !wt.aborted()) epilogue();
+        if (lane == 0) bulk_wait_group0();
     }
     tc_fence_before();
     __syncthreads();

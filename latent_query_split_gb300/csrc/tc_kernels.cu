@@ -176,12 +176,13 @@ bool tc_decode_available() { return true; }
 
 namespace {
 template <int M, int D, int STAGES>
-cudaError_t launch_dec(const CUtensorMap &mk, const tc::DecArgs &args, cudaStream_t st) {
+cudaError_t launch_dec(const CUtensorMap &mk, const CUtensorMap &my, const tc::DecArgs &args,
+                       cudaStream_t st) {
     using C = tc::DecCfg<M, D, STAGES>;
     auto k = tc::dec_fwd_tc_kernel<M, D, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
     if (e != cudaSuccess) return e;
-    k<<<args.grid, C::THREADS, C::ALLOC, st>>>(mk, args);
+    k<<<args.grid, C::THREADS, C::ALLOC, st>>>(mk, my, args);
     note_launch();
     return cudaGetLastError();
 }
@@ -189,8 +190,10 @@ cudaError_t launch_dec(const CUtensorMap &mk, const tc::DecArgs &args, cudaStrea
 
 cudaError_t launch_decode_tc(const Problem &pr, const void *Q, bool q_is_f32, const float *Z,
                              const void *K, void *Y, int sms, unsigned *status, cudaStream_t st) {
-    CUtensorMap mk;
-    if (!make_map(&mk, K, pr.D, pr.H, pr.N, pr.B, 1, 128)) return cudaErrorInvalidValue;
+    CUtensorMap mk, my;
+    if (!make_map(&mk, K, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
+        !make_map(&my, Y, pr.D, pr.H, pr.N, pr.B, 1, 32))
+        return cudaErrorInvalidValue;
     tc::DecArgs a;
     a.B = pr.B;
     a.H = pr.H;
@@ -207,11 +210,11 @@ cudaError_t launch_decode_tc(const Problem &pr, const void *Q, bool q_is_f32, co
     a.grid = (int)(a.T_total < sms ? a.T_total : sms);
     a.status = status;
     if (a.T_total == 0) return cudaSuccess;
-    if (pr.M == 128 && pr.D == 64) return launch_dec<128, 64, 8>(mk, a, st);
-    if (pr.M == 64 && pr.D == 64) return launch_dec<64, 64, 8>(mk, a, st);
-    if (pr.M == 256 && pr.D == 64) return launch_dec<256, 64, 8>(mk, a, st);
-    if (pr.M == 64 && pr.D == 128) return launch_dec<64, 128, 5>(mk, a, st);
-    if (pr.M == 128 && pr.D == 128) return launch_dec<128, 128, 4>(mk, a, st);
+    if (pr.M == 128 && pr.D == 64) return launch_dec<128, 64, 8>(mk, my, a, st);
+    if (pr.M == 64 && pr.D == 64) return launch_dec<64, 64, 8>(mk, my, a, st);
+    if (pr.M == 256 && pr.D == 64) return launch_dec<256, 64, 6>(mk, my, a, st);
+    if (pr.M == 64 && pr.D == 128) return launch_dec<64, 128, 3>(mk, my, a, st);
+    if (pr.M == 128 && pr.D == 128) return launch_dec<128, 128, 3>(mk, my, a, st);
     return cudaErrorNotSupported;
 }
 
