@@ -361,7 +361,8 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         auto issue_s = [&]() -> bool {           // S of tile js into buffer js & 1
             const int u = cs.bh - bh0;
             const bool gen_start = cs.bh != s_bh;
-            if (!wwait(q_full(u & 1), (uint32_t)(u >> 1) & 1)) return false;
+            // Q of a generation is waited for once, before its first S
+            if (gen_start && !wwait(q_full(u & 1), (uint32_t)(u >> 1) & 1)) return false;
             const int s = (int)(js % STAGES);
             if (!wwait(full(s), (uint32_t)(js / STAGES) & 1)) return false;
             tc_fence_after();
@@ -733,9 +734,13 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             ++q_loads;
             q_bh = bh;
         };
+        uint32_t q_waited = 0;                    // Q loads already waited for
         auto issue_s = [&]() -> bool {            // (warp-collective) S of tile jn
             if (cn.bh != q_bh) load_q(cn.bh);
-            if (!wwait(q_full(g), (q_loads - 1) & 1)) return false;
+            if (q_waited != q_loads) {
+                if (!wwait(q_full(g), (q_loads - 1) & 1)) return false;
+                q_waited = q_loads;
+            }
             const int s = (int)(jn % STAGES);
             if (!wwait(full(s), (uint32_t)(jn / STAGES) & 1)) return false;
             tc_fence_after();
@@ -1023,19 +1028,33 @@ __global__ void __launch_bounds__(256) enc_merge_kernel(const EncArgs a) {
     const int i = tid / Q4, d4 = tid - i * Q4;
     if (i0 + i >= M) return;
     const int64_t orow = (int64_t)(i0 + i) * D;
-    // weighted sum of the pieces [q0, q1) with weights exp(L_p - Lv)
+    // weighted sum of the pieces [q0, q1) with weights exp(L_p - Lv); the
+    // loads of eight pieces are issued together (every piece slot was written
+    // by the encoder, empty pieces with zeros, so each load is of defined data)
     auto wsum = [&](int q0, int q1, float Lv) -> float4 {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (Lv == -INFINITY) return acc;
-        for (int q = q0; q < q1; ++q) {
-            const float lp = Lp[q * RB + i];
-            if (lp == -INFINITY) continue;
-            const float w = expf(lp - Lv);
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.part_O + slot(q) * M * D + orow) + d4);
-            acc.x = fmaf(w, v.x, acc.x);
-            acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z);
-            acc.w = fmaf(w, v.w, acc.w);
+        for (int qb = q0; qb < q1; qb += 8) {
+            float4 v[8];
+            float w[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int q = qb + u;
+                w[u] = 0.f;
+                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (q < q1) {
+                    const float lp = Lp[q * RB + i];
+                    w[u] = lp == -INFINITY ? 0.f : expf(lp - Lv);
+                    v[u] = __ldcg(reinterpret_cast<const float4 *>(a.part_O + slot(q) * M * D + orow) + d4);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                acc.x = fmaf(w[u], v[u].x, acc.x);
+                acc.y = fmaf(w[u], v[u].y, acc.y);
+                acc.z = fmaf(w[u], v[u].z, acc.z);
+                acc.w = fmaf(w[u], v[u].w, acc.w);
+            }
         }
         return acc;
     };
