@@ -7,23 +7,22 @@
 // it is exact in one tile (no running rescale).
 //
 // One persistent CTA per SM walks a contiguous span of 128-token tiles in
-// (h, b, tile) order. Head-major order lines the CTAs of different heads up
-// on the same token positions at the same time (with the grid a multiple of
-// H they cover the same relative tile range): a token's H head rows are
-// adjacent in memory, so DRAM pages are consumed by all heads together
-// instead of once per head at unrelated times. Warp roles:
-//   warp 0     producer: K tiles by TMA into a STAGES-deep ring; on every
-//              (b, h) change it converts Q and Z (bf16 or fp32) into swizzled
-//              bf16 operand tiles in shared memory.
-//   warp 1     TMEM allocator; lane 0 issues the MMAs:
+// (h, b, tile) order (head-major: the CTAs of different heads cover the same
+// token positions at the same time, so the H head rows of a token, adjacent
+// in memory, are fetched together). Warp roles:
+//   warp 0     producer: K tiles by TMA into a STAGES-deep ring.
+//   warp 1     TMEM allocator and MMA issuer (converged warp, elect.sync):
 //                S_g = K Q^T   (A = K tile, B = Q, both shared memory)
 //                Y_g = P_g Z   (A = P from tensor memory, B = Z shared memory)
-//   warps 2-9  two groups of four warps take alternate tiles (one token row per
-//              thread = TMEM lane): row max, exp2, P (bf16) over S in tensor
+//   warps 2..  one or two groups of four warps take alternate tiles (one token
+//              row per thread = TMEM lane): row max, exp2, P over S in tensor
 //              memory. The epilogue of a tile (Y / l rounded to bf16, staged
 //              in shared memory, one TMA store per warp of 32 token rows) runs
 //              in the group's next iteration, once that tile's scores have
 //              arrived, so the group never waits for its own P Z product.
+//   last warp  stager: converts each (b, h)'s Q and Z into swizzled operand
+//              tiles, into one of two buffers while the other is in use, so a
+//              (b, h) change does not stall the tile stream.
 #pragma once
 
 #include "tc_common.cuh"
@@ -46,11 +45,14 @@ struct DecArgs {
     unsigned *status;
 };
 
-template <int M, int D, int STAGES>
+template <int M, int D, int STAGES_, int QZB_>
 struct DecCfg {
+    static constexpr int STAGES = STAGES_;
+    static constexpr int QZB = QZB_;                    // Q/Z buffers (1 or 2)
     static constexpr int KA = D / 64;                   // 64-element atoms along D
     static constexpr int NG = M <= 128 ? 2 : 1;         // softmax groups (tiles in flight)
-    static constexpr int THREADS = 64 + 128 * NG;
+    static constexpr int STAGER = 2 + 4 * NG;           // warp index of the stager
+    static constexpr int THREADS = 32 * (STAGER + 1);
     static constexpr uint32_t QZ_ATOM = M * 128;        // bytes of one M-row x 64-col atom
     // F16P: P and Z enter Y = P Z as fp16, and Z gets one more 16-column block
     // holding the constant c (the power of two Z was scaled by, see
@@ -59,19 +61,18 @@ struct DecCfg {
     static constexpr bool F16P = NG == 2 ? (M + D + 16 <= 256) : (M + D + 16 <= 512);
     static constexpr int YN = F16P ? D + 16 : D;        // N of the P Z product
     static constexpr int ZA = F16P ? KA + 1 : KA;       // atoms of the staged Z
-    static constexpr uint32_t Q_OFF = 0;
-    static constexpr uint32_t Z_OFF = Q_OFF + KA * QZ_ATOM;
-    static constexpr uint32_t STAGE_OFF = Z_OFF + ZA * QZ_ATOM;
-    static constexpr uint32_t STAGE_BYTES = KA * 128 * 128;   // one K tile
-    // Y staging of each group for the TMA store: 128 token rows, KA atoms
+    static constexpr uint32_t QZ_BYTES = (KA + ZA) * QZ_ATOM;   // one Q + Z buffer
+    static constexpr uint32_t STAGE_BYTES = KA * 128 * 128;     // one K tile
+    static constexpr int NCH = M / 32;                  // P chunks of 32 latents
+    // full[S], empty[S], qz_full[2], qz_free[2], s_full[2], p_chunk[2][8], o_done[2]
+    static constexpr int NBAR = 2 * STAGES + 4 + 2 + 16 + 2;
+    static constexpr uint32_t STAGE_OFF = QZB * QZ_BYTES;
+    // Y staging of each group for the TMA stores: 128 token rows, KA atoms
     static constexpr uint32_t OUT_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
     static constexpr uint32_t OUT_BYTES = KA * 128 * 128;
     static constexpr uint32_t BAR_OFF = OUT_OFF + NG * OUT_BYTES;
     // M <= 128: a token's M scores stay in registers between the max and exp passes
     static constexpr bool REG_S = M <= 128;
-    static constexpr int NCH = M / 32;                   // P chunks of 32 latents
-    // full[S], empty[S], qz_full, qz_free, s_full[2], p_chunk[2][8], o_done[2]
-    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 16 + 2;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t BYTES = MISC_OFF + 64;
     static constexpr uint32_t ALLOC = BYTES + 1024;
@@ -94,7 +95,7 @@ __device__ __forceinline__ uint4 load_chunk8(const float *src) {
 template <int M, int D, typename T>
 __device__ __forceinline__ void stage_rows_bf16(uint8_t *dst, const T *src, int lane) {
     constexpr int CHUNKS = M * D / 8;                   // 16-byte output chunks
-#pragma unroll 4
+#pragma unroll 8
     for (int c = lane; c < CHUNKS; c += 32) {
         const int row = c / (D / 8), j = c % (D / 8);    // chunk j covers cols 8j..8j+7
         const int atom = j >> 3, jj = j & 7;
@@ -122,6 +123,7 @@ template <int M, int D>
 __device__ __forceinline__ void stage_z_f16(uint8_t *dst, const float *src, int lane) {
     constexpr int CHUNKS = M * D / 8;
     float mx = 0.f;
+#pragma unroll 8
     for (int q = lane; q < CHUNKS; q += 32) {
         const float4 lo = __ldg(reinterpret_cast<const float4 *>(src) + 2 * q);
         const float4 hi = __ldg(reinterpret_cast<const float4 *>(src) + 2 * q + 1);
@@ -133,7 +135,7 @@ __device__ __forceinline__ void stage_z_f16(uint8_t *dst, const float *src, int 
     int e = mx > 0.f ? ((__float_as_int(mx) >> 23) & 0xff) - 127 : 0;   // floor(log2 max|Z|)
     e = e < -14 ? -14 : (e > 24 ? 24 : e);
     const float c = __int_as_float((127 - e) << 23);                  // 2^-e, exact
-#pragma unroll 4
+#pragma unroll 8
     for (int q = lane; q < CHUNKS; q += 32) {
         const int row = q / (D / 8), j = q % (D / 8);
         const int atom = j >> 3, jj = j & 7;
@@ -151,26 +153,25 @@ __device__ __forceinline__ void stage_z_f16(uint8_t *dst, const float *src, int 
     }
 }
 
-template <int M, int D, int STAGES>
-__global__ void __launch_bounds__(DecCfg<M, D, STAGES>::THREADS, 1)
+template <int M, int D, int STAGES, int QZB_>
+__global__ void __launch_bounds__(DecCfg<M, D, STAGES, QZB_>::THREADS, 1)
 dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmY,
                   const DecArgs a) {
-    using C = DecCfg<M, D, STAGES>;
-    constexpr int KA = C::KA;
-    constexpr int NG = C::NG;
-    constexpr int NCH = C::NCH;
+    using C = DecCfg<M, D, STAGES, QZB_>;
+    constexpr int KA = C::KA, NG = C::NG, NCH = C::NCH, QZB = C::QZB;
+    static_assert(QZB == 1 || QZB == 2, "one or two Q/Z buffers");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + C::Q_OFF, sZ = sbase + C::Z_OFF, sStage = sbase + C::STAGE_OFF;
+    const uint32_t sbase = smem_u32(smem), sStage = sbase + C::STAGE_OFF;
     const uint32_t bar0 = sbase + C::BAR_OFF;
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    const uint32_t qz_full = bar0 + 8u * (2 * STAGES), qz_free = qz_full + 8;
-    auto s_full = [&](int g) { return bar0 + 8u * (2 * STAGES + 2 + g); };
-    auto p_chunk = [&](int g, int c) { return bar0 + 8u * (2 * STAGES + 4 + 8 * g + c); };
-    auto o_done = [&](int g) { return bar0 + 8u * (2 * STAGES + 20 + g); };
+    auto qz_full = [&](int q) { return bar0 + 8u * (2 * STAGES + q); };
+    auto qz_free = [&](int q) { return bar0 + 8u * (2 * STAGES + 2 + q); };
+    auto s_full = [&](int g) { return bar0 + 8u * (2 * STAGES + 4 + g); };
+    auto p_chunk = [&](int g, int c) { return bar0 + 8u * (2 * STAGES + 6 + 8 * g + c); };
+    auto o_done = [&](int g) { return bar0 + 8u * (2 * STAGES + 22 + g); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
 
@@ -187,8 +188,10 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
         }
-        mbar_init(qz_full, 1);
-        mbar_init(qz_free, 1);
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(qz_full(q), 1);
+            mbar_init(qz_free(q), 1);
+        }
         for (int g = 0; g < 2; ++g) {
             mbar_init(s_full(g), 1);
             for (int c = 0; c < 8; ++c) mbar_init(p_chunk(g, c), 4);   // one arrival per softmax warp
@@ -208,38 +211,18 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // first tile and its (b, h) / token tile index, advanced without divisions
+    // first tile: its (b, h) index (head-major: bh = h * B + b) and token tile
     const int64_t bh0 = tb / a.T_bh;
     const int64_t k0 = tb - bh0 * a.T_bh;
+    const int64_t n_gen = ntiles > 0 ? (te - 1) / a.T_bh - bh0 + 1 : 0;   // (b, h) of the span
 
     if (warp == 0) {
-        // ---------------- producer ----------------
+        // ---------------- producer: K tiles ----------------
         const uint64_t pol = policy_evict_first();
-        int64_t bh = bh0, kt = k0, cur_bh = -1;
-        uint32_t qz_uses = 0;
+        int64_t bh = bh0, kt = k0;
         int64_t j = 0;
         for (; j < ntiles && !wt.aborted(); ++j) {
-            // tiles run head-major: index bh = h * B + b (see the kernel comment)
             const int h = (int)(bh / a.B), b = (int)(bh - (int64_t)h * a.B);
-            if (bh != cur_bh) {
-                // Q and Z of the new (b, h), once the MMAs on the old ones are done
-                if (qz_uses > 0 && !__all_sync(0xffffffffu, wt.wait(qz_free, (qz_uses - 1) & 1))) break;
-                const int qb = a.q_per_batch ? b : 0;
-                const int64_t qoff = ((int64_t)qb * a.H + h) * M * D;
-                if (a.q_f32)
-                    stage_rows_bf16<M, D>(smem + C::Q_OFF, reinterpret_cast<const float *>(a.Q) + qoff, lane);
-                else
-                    stage_rows_bf16<M, D>(smem + C::Q_OFF, reinterpret_cast<const __nv_bfloat16 *>(a.Q) + qoff, lane);
-                if constexpr (C::F16P)
-                    stage_z_f16<M, D>(smem + C::Z_OFF, a.Z + ((int64_t)b * a.H + h) * M * D, lane);
-                else
-                    stage_rows_bf16<M, D>(smem + C::Z_OFF, a.Z + ((int64_t)b * a.H + h) * M * D, lane);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(qz_full);
-                ++qz_uses;
-                cur_bh = bh;
-            }
             const int s = (int)(j % STAGES);
             if (!__all_sync(0xffffffffu, wt.wait(empty(s), ((uint32_t)(j / STAGES) & 1) ^ 1))) break;
             if (lane == 0) {
@@ -262,95 +245,115 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                        globaltimer() - t0 < 500000000ull) {
                 }
         }
+    } else if (warp == C::STAGER) {
+        // ---------------- stager: Q and Z of each (b, h) ----------------
+        for (int64_t u = 0; u < n_gen && !wt.aborted(); ++u) {
+            const int q = (int)(u % QZB);
+            // the buffer's previous (b, h) has had its last P Z issued and done
+            if (u >= QZB && !__all_sync(0xffffffffu, wt.wait(qz_free(q), (uint32_t)(u / QZB - 1) & 1))) break;
+            const int64_t bh = bh0 + u;
+            const int h = (int)(bh / a.B), b = (int)(bh - (int64_t)h * a.B);
+            uint8_t *qdst = smem + q * C::QZ_BYTES, *zdst = qdst + KA * C::QZ_ATOM;
+            const int64_t qoff = ((int64_t)(a.q_per_batch ? b : 0) * a.H + h) * M * D;
+            if (a.q_f32)
+                stage_rows_bf16<M, D>(qdst, reinterpret_cast<const float *>(a.Q) + qoff, lane);
+            else
+                stage_rows_bf16<M, D>(qdst, reinterpret_cast<const __nv_bfloat16 *>(a.Q) + qoff, lane);
+            if constexpr (C::F16P)
+                stage_z_f16<M, D>(zdst, a.Z + ((int64_t)b * a.H + h) * M * D, lane);
+            else
+                stage_rows_bf16<M, D>(zdst, a.Z + ((int64_t)b * a.H + h) * M * D, lane);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qz_full(q));
+        }
     } else if (warp == 1) {
         // ---------------- MMA issuer (whole warp, elect.sync issues) ----------------
-        // The warp stays converged so the operands stay warp-uniform; an MMA
-        // issued from one lane of a divergent branch costs several times more
-        // issue time, which made this warp the kernel's bottleneck.
-        {
-            auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
-                return __all_sync(0xffffffffu, wt.wait(bar, par));
-            };
-            constexpr uint32_t idS = idesc_bf16_m128(M, 0);
-            // P Z: bf16, or fp16 with the row-sum block (N = D + 16)
-            constexpr uint32_t idPV = C::F16P ? idesc_f16(128, C::YN, 0, 1) : idesc_bf16_m128(D, 1);
-            const uint64_t dK0 = desc_sw128(sStage, 16, 1024);
-            const uint64_t dQ0 = desc_sw128(sQ, 16, 1024);
-            const uint64_t dZ0 = desc_sw128(sZ, C::QZ_ATOM, 1024);
-            constexpr uint64_t kStageDesc = C::STAGE_BYTES >> 4;
-            int64_t bhS = bh0, ktS = k0, cur_bh = -1;   // cursor of the S tiles
-            int64_t bhP = bh0, ktP = k0;                 // cursor of the PV tiles
-            uint32_t qz_uses = 0;
-            bool ok = true;
-            auto issue_s = [&](int64_t jj) -> bool {
-                const int s = (int)(jj % STAGES);
-                if (bhS != cur_bh) {
-                    if (!wwait(qz_full, qz_uses & 1)) return false;
-                    ++qz_uses;
-                    cur_bh = bhS;
-                }
-                if (!wwait(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
-                tc_fence_after();
-                const int g = NG == 2 ? (int)(jj & 1) : 0;
-                const uint64_t dK = dK0 + kStageDesc * s;
+        // The warp stays converged so that its operands stay warp-uniform.
+        auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
+            return __all_sync(0xffffffffu, wt.wait(bar, par));
+        };
+        constexpr uint32_t idS = idesc_bf16_m128(M, 0);
+        // P Z: bf16, or fp16 with the row-sum block (N = D + 16)
+        constexpr uint32_t idPV = C::F16P ? idesc_f16(128, C::YN, 0, 1) : idesc_bf16_m128(D, 1);
+        const uint64_t dK0 = desc_sw128(sStage, 16, 1024);
+        constexpr uint64_t kStageDesc = C::STAGE_BYTES >> 4;
+        int64_t bhS = bh0, ktS = k0;                 // cursor of the S tiles
+        int64_t bhP = bh0, ktP = k0;                 // cursor of the PV tiles
+        int64_t uS = -1, uP = 0;                     // (b, h) generation of each cursor
+        bool ok = true;
+        auto issue_s = [&](int64_t jj) -> bool {
+            const int s = (int)(jj % STAGES);
+            if (bhS - bh0 != uS) {
+                uS = bhS - bh0;
+                if (!wwait(qz_full((int)(uS % QZB)), (uint32_t)(uS / QZB) & 1)) return false;
+            }
+            if (!wwait(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
+            tc_fence_after();
+            const int g = NG == 2 ? (int)(jj & 1) : 0;
+            const uint64_t dK = dK0 + kStageDesc * s;
+            const uint64_t dQ0 = desc_sw128(sbase + (uint32_t)(uS % QZB) * C::QZ_BYTES, 16, 1024);
 #pragma unroll
-                for (int kb = 0; kb < D / 16; ++kb) {
-                    const uint64_t offK = (uint64_t)((kb >> 2) * (128 * 128) + (kb & 3) * 32) >> 4;
-                    const uint64_t offQ = (uint64_t)((kb >> 2) * C::QZ_ATOM + (kb & 3) * 32) >> 4;
-                    umma_ss_elect(tmem + g * 256, dK + offK, dQ0 + offQ, idS, kb > 0 ? 1u : 0u);
+            for (int kb = 0; kb < D / 16; ++kb) {
+                const uint64_t offK = (uint64_t)((kb >> 2) * (128 * 128) + (kb & 3) * 32) >> 4;
+                const uint64_t offQ = (uint64_t)((kb >> 2) * C::QZ_ATOM + (kb & 3) * 32) >> 4;
+                umma_ss_elect(tmem + g * 256, dK + offK, dQ0 + offQ, idS, kb > 0 ? 1u : 0u);
+            }
+            umma_commit_elect(s_full(g));
+            umma_commit_elect(empty(s));            // the K tile is only read by S
+            if (++ktS == a.T_bh) {
+                ktS = 0;
+                ++bhS;
+            }
+            return true;
+        };
+        // S runs at most NG tiles ahead of PV; with a single Q/Z buffer the S of
+        // a new (b, h) also waits until every older tile's P Z is issued
+        int64_t jS = 0, nP = 0;
+        auto pump_s = [&]() -> bool {
+            while (jS < ntiles && jS < nP + NG && (QZB == 2 || bhS - bh0 == uS || nP == jS))
+                if (!issue_s(jS++)) return false;
+            return true;
+        };
+        ok = pump_s();
+        for (; nP < ntiles && ok;) {
+            const int64_t jP = nP;
+            const int g = NG == 2 ? (int)(jP & 1) : 0;
+            const int64_t kP = NG == 2 ? (jP >> 1) : jP;
+            const uint64_t dZ0 = desc_sw128(sbase + (uint32_t)(uP % QZB) * C::QZ_BYTES + KA * C::QZ_ATOM,
+                                            C::QZ_ATOM, 1024);
+            for (int c = 0; c < NCH && ok; ++c) {
+                // P arrives whole (registers path) or chunk by chunk
+                if (!C::REG_S || c == 0) {
+                    ok = wwait(p_chunk(g, C::REG_S ? 0 : c), (uint32_t)kP & 1);
+                    if (!ok) break;
+                    tc_fence_after();
                 }
-                umma_commit_elect(s_full(g));
-                umma_commit_elect(empty(s));            // the K tile is only read by S
-                if (++ktS == a.T_bh) {
-                    ktS = 0;
-                    ++bhS;
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int kb = 2 * c + kk;       // 16 latents per MMA
+                    umma_ts_elect(tmem + g * 256 + M, tmem + g * 256 + kb * 8, dZ0 + kb * (2048 >> 4), idPV,
+                                  kb > 0 ? 1u : 0u);
                 }
-                return true;
-            };
-            // S runs at most NG tiles ahead of PV; the S of a new (b, h) waits
-            // until every older tile's PV is issued (Q and Z are then replaced)
-            int64_t jS = 0, nP = 0;
-            auto pump_s = [&]() -> bool {
-                while (jS < ntiles && jS < nP + NG && (bhS == cur_bh || nP == jS))
-                    if (!issue_s(jS++)) return false;
-                return true;
-            };
+            }
+            if (!ok) break;
+            umma_commit_elect(o_done(g));
+            if (++ktP == a.T_bh) {
+                ktP = 0;
+                ++bhP;
+            }
+            ++nP;
+            if (nP == ntiles || bhP - bh0 != uP) {
+                umma_commit_elect(qz_free((int)(uP % QZB)));   // this (b, h)'s Q and Z are done
+                ++uP;
+            }
             ok = pump_s();
-            for (; nP < ntiles && ok;) {
-                const int64_t jP = nP;
-                const int g = NG == 2 ? (int)(jP & 1) : 0;
-                const int64_t kP = NG == 2 ? (jP >> 1) : jP;
-                for (int c = 0; c < NCH && ok; ++c) {
-                    // P arrives whole (registers path) or chunk by chunk
-                    if (!C::REG_S || c == 0) {
-                        ok = wwait(p_chunk(g, C::REG_S ? 0 : c), (uint32_t)kP & 1);
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const int kb = 2 * c + kk;       // 16 latents per MMA
-                        umma_ts_elect(tmem + g * 256 + M, tmem + g * 256 + kb * 8, dZ0 + kb * (2048 >> 4),
-                                     idPV, kb > 0 ? 1u : 0u);
-                    }
-                }
-                if (!ok) break;
-                umma_commit_elect(o_done(g));
-                const int64_t bh_done = bhP;
-                if (++ktP == a.T_bh) {
-                    ktP = 0;
-                    ++bhP;
-                }
-                ++nP;
-                if (nP == ntiles || bhP != bh_done) umma_commit_elect(qz_free);
-                ok = pump_s();
-            }
-            // make every issued MMA finish before TMEM is released
-            if (ok && ntiles > 0) {
-                const int gl = NG == 2 ? (int)((ntiles - 1) & 1) : 0;
-                const int64_t kl = NG == 2 ? ((ntiles - 1) >> 1) : ntiles - 1;
-                wwait(o_done(gl), (uint32_t)kl & 1);
-            }
+        }
+        // make every issued MMA finish before TMEM is released
+        if (ok && ntiles > 0) {
+            const int gl = NG == 2 ? (int)((ntiles - 1) & 1) : 0;
+            const int64_t kl = NG == 2 ? ((ntiles - 1) >> 1) : ntiles - 1;
+            wwait(o_done(gl), (uint32_t)kl & 1);
         }
         __syncwarp();
     } else {

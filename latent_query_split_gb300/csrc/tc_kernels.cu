@@ -175,11 +175,11 @@ cudaError_t launch_encoder_tc(const Problem &pr, const TcTilePlan &plan, const T
 bool tc_decode_available() { return true; }
 
 namespace {
-template <int M, int D, int STAGES>
+template <int M, int D, int STAGES, int QZB>
 cudaError_t launch_dec(const CUtensorMap &mk, const CUtensorMap &my, const tc::DecArgs &args,
                        cudaStream_t st) {
-    using C = tc::DecCfg<M, D, STAGES>;
-    auto k = tc::dec_fwd_tc_kernel<M, D, STAGES>;
+    using C = tc::DecCfg<M, D, STAGES, QZB>;
+    auto k = tc::dec_fwd_tc_kernel<M, D, STAGES, QZB>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
     if (e != cudaSuccess) return e;
     k<<<args.grid, C::THREADS, C::ALLOC, st>>>(mk, my, args);
@@ -210,11 +210,12 @@ cudaError_t launch_decode_tc(const Problem &pr, const void *Q, bool q_is_f32, co
     a.grid = (int)(a.T_total < sms ? a.T_total : sms);
     a.status = status;
     if (a.T_total == 0) return cudaSuccess;
-    if (pr.M == 128 && pr.D == 64) return launch_dec<128, 64, 8>(mk, my, a, st);
-    if (pr.M == 64 && pr.D == 64) return launch_dec<64, 64, 8>(mk, my, a, st);
-    if (pr.M == 256 && pr.D == 64) return launch_dec<256, 64, 6>(mk, my, a, st);
-    if (pr.M == 64 && pr.D == 128) return launch_dec<64, 128, 3>(mk, my, a, st);
-    if (pr.M == 128 && pr.D == 128) return launch_dec<128, 128, 3>(mk, my, a, st);
+    // <M, D, K stages, Q/Z buffers>, each within the shared-memory budget
+    if (pr.M == 128 && pr.D == 64) return launch_dec<128, 64, 6, 2>(mk, my, a, st);
+    if (pr.M == 64 && pr.D == 64) return launch_dec<64, 64, 8, 2>(mk, my, a, st);
+    if (pr.M == 256 && pr.D == 64) return launch_dec<256, 64, 6, 1>(mk, my, a, st);
+    if (pr.M == 64 && pr.D == 128) return launch_dec<64, 128, 3, 1>(mk, my, a, st);
+    if (pr.M == 128 && pr.D == 128) return launch_dec<128, 128, 3, 1>(mk, my, a, st);
     return cudaErrorNotSupported;
 }
 
