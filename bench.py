@@ -276,8 +276,21 @@ class Step:
                                     Z=self.Z, L=self.L, workspace=self.ws, kernel=kernel,
                                     stream=stream)
 
+    def full_step(self, inp=None):
+        """One step through the one-call public API of the workload."""
+        from latent_query_split_gb300 import flare
+        x = inp or self.inp
+        w, k, st, off = self.w, self.kernel, self.stream, self.off
+        if w.kind == "flare_fwd":
+            flare.flare_fwd(x["Q"], x["K"], x["V"], x["mask"], off, Y=self.Y, Z=self.Z, L=self.L,
+                            workspace=self.ws, kernel=k, stream=st)
+        else:
+            for _, fn in self.phases(inp):
+                fn()
+
     def phases(self, inp=None):
-        """[(name, callable)] making one step; `inp` overrides the input tensors."""
+        """[(name, callable)]: the step's parts as separate public calls (for
+        the per-kernel roofline); `inp` overrides the input tensors."""
         from latent_query_split_gb300 import flare
         x = inp or self.inp
         w, k, st, off = self.w, self.kernel, self.stream, self.off
@@ -347,25 +360,20 @@ def main(argv=None):
     small = w.B * w.N * w.H * w.D * elem < (256 << 20)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if small else None
 
-    def step(ev=None):
+    def step():
         with torch.cuda.stream(stream):
-            if flush is not None:
-                flush.fill_(1)
-            for i, (_, fn) in enumerate(phases):
-                if ev is not None:
-                    ev[i].record(stream)
-                fn()
-            if ev is not None:
-                ev[len(phases)].record(stream)
+            runner.full_step()
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     flare.flare_device_status(stream)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
-           for _ in range(args.steps)]
+    # the timed region: whole steps through the one-call API, events at its ends
+    # (small workloads: every step bracketed by events after an L2 flush)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)] if flush is not None else None
     clocks = ClockSampler(local)
     if world > 1:
         dist.barrier()
@@ -374,7 +382,13 @@ def main(argv=None):
     launches0 = flare.flare_launch_count()
     start.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        if step_evs is not None:
+            with torch.cuda.stream(stream):
+                flush.fill_(1)
+                step_evs[i][0].record(stream)
+        step()
+        if step_evs is not None:
+            step_evs[i][1].record(stream)
     end.record(stream)
     launches = flare.flare_launch_count() - launches0
     torch.cuda.synchronize(dev)
@@ -383,15 +397,32 @@ def main(argv=None):
     clock_info = clocks.stop()
     flare.flare_device_status(stream)
     elapsed_ms = start.elapsed_time(end)
-    phase_ms = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
-                for i, (name, _) in enumerate(phases)}
+    if step_evs is not None:    # the flush is not the mixer's work
+        elapsed_ms = sum(a.elapsed_time(b) for a, b in step_evs)
     if world > 1:
         t = torch.tensor([elapsed_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
     ms_per_step = elapsed_ms / args.steps
-    if flush is not None:       # the flush is not the mixer's work
-        ms_per_step = sum(phase_ms.values())
+
+    # per-phase times for the roofline: each phase alone, timed with events
+    phase_ms = {}
+    reps = max(3, min(args.steps, 200))
+    for name, fn in phases:
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            pe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(reps)]
+            for a, b in pe:
+                if flush is not None:
+                    flush.fill_(1)
+                a.record(stream)
+                fn()
+                b.record(stream)
+        torch.cuda.synchronize(dev)
+        phase_ms[name] = statistics.mean(a.elapsed_time(b) for a, b in pe)
+    flare.flare_device_status(stream)
     tokens_per_step = w.B * w.N * world
     value = tokens_per_step / (ms_per_step * 1e-3)
 
@@ -408,14 +439,11 @@ def main(argv=None):
     hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in e2e_out]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in hout)
-    e2e_phases = runner.phases(dinp)
-
     def e2e_step():
         with torch.cuda.stream(stream):
             for name, t in host.items():
                 dinp[name].copy_(t, non_blocking=True)
-            for _, fn in e2e_phases:
-                fn()
+            runner.full_step(dinp)
             for h, d in zip(hout, e2e_out):
                 h.copy_(d, non_blocking=True)
 
@@ -453,7 +481,9 @@ def main(argv=None):
     achieved = bytes_dom / (phase_ms[dominant] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                 "frac": achieved / hbm_gbs, "traffic": profiled_traffic(dominant, w.name),
-                "kernel": dominant, "peak_source": peak_kind, "phases": per_phase}
+                "kernel": dominant, "peak_source": peak_kind,
+                "timing": "each phase alone, CUDA events on its stream, mean of "
+                          f"{reps} calls", "phases": per_phase}
 
     dt_name = {"f32": "f32", "bf16": "bf16"}[w.dtype]
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,

@@ -298,7 +298,7 @@ flare_status_t encoder_run(const flare_dims_t *d, const void *Q, bool q_is_f32, 
 }
 
 flare_status_t decode_run(const flare_dims_t *d, const void *Q, bool q_is_f32, const float *Z,
-                          const void *K, void *Y, cudaStream_t st) {
+                          const void *K, void *Y, bool after_merge, cudaStream_t st) {
     const Problem pr = make_problem(d);
     if (pr.B == 0 || pr.N == 0) return FLARE_OK;
     if (!Q || !Z || !K || !Y) return fail(FLARE_ERR_INVALID_ARG, "NULL tensor");
@@ -317,7 +317,7 @@ flare_status_t decode_run(const flare_dims_t *d, const void *Q, bool q_is_f32, c
         DeviceInfo di;
         flare_status_t s = device_info(di);
         if (s != FLARE_OK) return s;
-        e = launch_decode_tc(pr, Q, q_is_f32, Z, K, Y, di.sms, di.status, st);
+        e = launch_decode_tc(pr, Q, q_is_f32, Z, K, Y, di.sms, di.status, after_merge, st);
     } else {
         e = launch_decode_simt(pr, Q, q_is_f32, Z, K, Y, st);
     }
@@ -410,7 +410,7 @@ flare_status_t flare_decode_fwd(const flare_dims_t *dims, const void *Q, const f
                                 const void *K, void *Y, void *stream) {
     flare_status_t s = check_dims(dims);
     if (s != FLARE_OK) return s;
-    return decode_run(dims, Q, false, Z, K, Y, (cudaStream_t)stream);
+    return decode_run(dims, Q, false, Z, K, Y, false, (cudaStream_t)stream);
 }
 
 flare_status_t flare_fwd(const flare_dims_t *dims, const void *Q, const void *K, const void *V,
@@ -425,7 +425,7 @@ flare_status_t flare_fwd(const flare_dims_t *dims, const void *Q, const void *K,
     if ((s = encoder_run(dims, Q, false, K, V, mask, shard_offsets, R, nullptr, nullptr, Z, L,
                          workspace, workspace_bytes, st)) != FLARE_OK)
         return s;
-    return decode_run(dims, Q, false, Z, K, Y, st);
+    return decode_run(dims, Q, false, Z, K, Y, true, st);
 }
 
 flare_status_t flare_pp_fwd(const flare_dims_t *dims, const void *Qseed, const void *Kt,
@@ -446,7 +446,7 @@ flare_status_t flare_pp_fwd(const flare_dims_t *dims, const void *Qseed, const v
     if ((s = encoder_run(&d2, Qdyn, true, K, V, mask, shard_offsets, R, nullptr, nullptr, Z, L2,
                          workspace, workspace_bytes, st)) != FLARE_OK)
         return s;
-    return decode_run(&d2, Qdyn, true, Z, K, Y, st);
+    return decode_run(&d2, Qdyn, true, Z, K, Y, true, st);
 }
 
 flare_status_t flare_encoder_bwd(const flare_dims_t *dims, const void *Q, const void *K,

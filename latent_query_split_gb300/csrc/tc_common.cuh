@@ -46,8 +46,13 @@ cudaError_t launch_encoder_tc(const Problem &pr, const TcTilePlan &plan, const T
                               const uint8_t *mask, void *ws, const EncoderOut &out,
                               unsigned *status, cudaStream_t st);
 bool tc_decode_available();
+// after_merge: the previous kernel in the stream is this library's encoder
+// kernel that writes Z, and Q and K were written before it (the decode then
+// overlaps that kernel's tail); callers whose previous kernel is unknown pass
+// false.
 cudaError_t launch_decode_tc(const Problem &pr, const void *Q, bool q_is_f32, const float *Z,
-                             const void *K, void *Y, int sms, unsigned *status, cudaStream_t st);
+                             const void *K, void *Y, int sms, unsigned *status, bool after_merge,
+                             cudaStream_t st);
 
 // bf16 with D = 64 and M in {64, 128}.
 bool tc_bwd_supported(bool bf16, int M, int D);

@@ -247,6 +247,10 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         }
     } else if (warp == C::STAGER) {
         // ---------------- stager: Q and Z of each (b, h) ----------------
+        // Inside the library's forward the decode is launched as a programmatic
+        // dependent of the merge that writes Z: only this warp reads Z or Q, so
+        // only it waits, and the K stream starts during the merge's tail.
+        pdl_wait();
         for (int64_t u = 0; u < n_gen && !wt.aborted(); ++u) {
             const int q = (int)(u % QZB);
             // the buffer's previous (b, h) has had its last P Z issued and done

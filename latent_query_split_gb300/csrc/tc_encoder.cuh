@@ -593,6 +593,7 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+    pdl_launch_dependents();   // the merge may be scheduled (it waits for this grid)
 }
 
 // ===============================================================================
@@ -929,6 +930,7 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+    pdl_launch_dependents();   // the merge may be scheduled (it waits for this grid)
 }
 
 // ===============================================================================
@@ -948,6 +950,10 @@ template <int D>
 __global__ void __launch_bounds__(256) enc_merge_kernel(const EncArgs a) {
     constexpr int RB = merge_rows(D);          // RB * D / 4 = 256 output quads per block
     constexpr int Q4 = D / 4;
+    // launched as a programmatic dependent of the encoder: every global access
+    // below comes after the encoder grid has completed
+    pdl_wait();
+    pdl_launch_dependents();
     const TcTilePlan &pl = a.plan;
     const int M = a.M;
     const int nrb = (M + RB - 1) / RB;

@@ -43,6 +43,25 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launch with the programmatic-stream-serialization attribute when `pdl`: the
+// kernel may start before the previous kernel in the stream has finished and
+// must wait (griddepcontrol.wait) before touching that kernel's results.
+template <typename Kernel, typename... Args>
+cudaError_t launch_ex(Kernel k, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                      Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 __global__ void f32_to_bf16_kernel(const float *__restrict__ x, __nv_bfloat16 *__restrict__ y,
                                    int64_t n) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -67,9 +86,9 @@ cudaError_t launch_merge(const Problem &pr, const tc::EncArgs &args, cudaStream_
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int nrb = (pr.M + tc::merge_rows(D) - 1) / tc::merge_rows(D);
-    k<<<(unsigned)((int64_t)pr.B * pr.H * nrb), 256, smem, st>>>(args);
+    e = launch_ex(k, dim3((unsigned)((int64_t)pr.B * pr.H * nrb)), dim3(256), smem, st, true, args);
     note_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -177,19 +196,20 @@ bool tc_decode_available() { return true; }
 namespace {
 template <int M, int D, int STAGES, int QZB>
 cudaError_t launch_dec(const CUtensorMap &mk, const CUtensorMap &my, const tc::DecArgs &args,
-                       cudaStream_t st) {
+                       bool pdl, cudaStream_t st) {
     using C = tc::DecCfg<M, D, STAGES, QZB>;
     auto k = tc::dec_fwd_tc_kernel<M, D, STAGES, QZB>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
     if (e != cudaSuccess) return e;
-    k<<<args.grid, C::THREADS, C::ALLOC, st>>>(mk, my, args);
+    e = launch_ex(k, dim3(args.grid), dim3(C::THREADS), C::ALLOC, st, pdl, mk, my, args);
     note_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 }  // namespace
 
 cudaError_t launch_decode_tc(const Problem &pr, const void *Q, bool q_is_f32, const float *Z,
-                             const void *K, void *Y, int sms, unsigned *status, cudaStream_t st) {
+                             const void *K, void *Y, int sms, unsigned *status, bool after_merge,
+                             cudaStream_t st) {
     CUtensorMap mk, my;
     if (!make_map(&mk, K, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
         !make_map(&my, Y, pr.D, pr.H, pr.N, pr.B, 1, 32))
@@ -211,11 +231,11 @@ cudaError_t launch_decode_tc(const Problem &pr, const void *Q, bool q_is_f32, co
     a.status = status;
     if (a.T_total == 0) return cudaSuccess;
     // <M, D, K stages, Q/Z buffers>, each within the shared-memory budget
-    if (pr.M == 128 && pr.D == 64) return launch_dec<128, 64, 6, 2>(mk, my, a, st);
-    if (pr.M == 64 && pr.D == 64) return launch_dec<64, 64, 8, 2>(mk, my, a, st);
-    if (pr.M == 256 && pr.D == 64) return launch_dec<256, 64, 6, 1>(mk, my, a, st);
-    if (pr.M == 64 && pr.D == 128) return launch_dec<64, 128, 3, 1>(mk, my, a, st);
-    if (pr.M == 128 && pr.D == 128) return launch_dec<128, 128, 3, 1>(mk, my, a, st);
+    if (pr.M == 128 && pr.D == 64) return launch_dec<128, 64, 6, 2>(mk, my, a, after_merge, st);
+    if (pr.M == 64 && pr.D == 64) return launch_dec<64, 64, 8, 2>(mk, my, a, after_merge, st);
+    if (pr.M == 256 && pr.D == 64) return launch_dec<256, 64, 6, 1>(mk, my, a, after_merge, st);
+    if (pr.M == 64 && pr.D == 128) return launch_dec<64, 128, 3, 1>(mk, my, a, after_merge, st);
+    if (pr.M == 128 && pr.D == 128) return launch_dec<128, 128, 3, 1>(mk, my, a, after_merge, st);
     return cudaErrorNotSupported;
 }
 
