@@ -28,8 +28,11 @@
 //    order (deterministic).
 // Warp roles of bwd_tc_kernel: warp 0 TMA producer (K, V ring; Q, dZ and the
 // row statistics on every (b, h) change), warp 1 TMEM allocator and MMA
-// issuer (lane 0), warps 2-5 softmax (one token row per thread), warps 6-9
-// epilogue (dK, dV stores and the dQ partials).
+// issuer (lane 0), warps 2-9 two halves of four warps, each half owning M/2
+// latents of every token row (one token row per thread): the half's P and
+// s dS (written as bf16 into the half's own TMEM columns), then the tile's
+// epilogue (half 0 stores dV, half 1 dK, one TMA store per warp of 32 rows)
+// and, at the end of a (b, h) piece, half of the dQ partial's columns.
 #pragma once
 
 #include "tc_common.cuh"
@@ -184,12 +187,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         mbar_init(lc_full(0), 1);
         mbar_init(lc_full(1), 1);
         mbar_init(s_full, 1);
-        mbar_init(p_full, 4);          // one arrival per softmax warp
+        mbar_init(p_full, 8);          // one arrival per softmax warp
         mbar_init(ds_free, 1);
         mbar_init(dvdk_full, 1);
-        mbar_init(dvdk_free, 4);       // one arrival per epilogue warp
+        mbar_init(dvdk_free, 8);       // one arrival per softmax/epilogue warp
         mbar_init(dq_full, 1);
-        mbar_init(dq_free, 4);
+        mbar_init(dq_free, 8);
         mbar_init(drain, 1);
         fence_mbar_init();
     }
@@ -220,10 +223,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         // ---------------- producer ----------------
         const uint64_t pol = policy_evict_first();
         int64_t bh = bh0, kt = k0, cur = -1;
+        int b = (int)(bh0 / a.H), h = (int)(bh0 - (int64_t)b * a.H);   // (b, h) of tile j
         int u = -1;
         int64_t j = 0;
         for (; j < ntiles && !wt.aborted(); ++j) {
-            const int b = (int)(bh / a.H), h = (int)(bh - (int64_t)b * a.H);
             if (bh != cur) {
                 ++u;
                 cur = bh;
@@ -253,6 +256,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             if (++kt == a.T_bh) {
                 kt = 0;
                 ++bh;
+                if (++h == a.H) {
+                    h = 0;
+                    ++b;
+                }
             }
         }
         if (wt.aborted() && lane == 0) {
@@ -319,14 +326,20 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 tc_fence_after();
                 if (j > 0 && !(ok = wt.wait(dvdk_free, (uint32_t)(j - 1) & 1))) break;
                 tc_fence_after();
-                // dV = P^T dZ, dK = (s dS)^T Q: K = M latents, 16 per MMA
+                // dV = P^T dZ, dK = (s dS)^T Q: K = M latents, 16 per MMA; half h's
+                // latents sit (bf16 pairs) from column h * M/2 of S and of dP
+                auto pcol = [](int kb) -> uint32_t {
+                    constexpr int W = M / 2;
+                    const int half = 16 * kb / W;
+                    return (uint32_t)(W * half + 8 * (kb - half * (W / 16)));
+                };
 #pragma unroll
                 for (int kb = 0; kb < M / 16; ++kb)
-                    umma_bf16_ts(tmem + C::DV_COL, tmem + C::S_COL + 8 * kb, dZm + kb * (2048 >> 4), idG,
+                    umma_bf16_ts(tmem + C::DV_COL, tmem + C::S_COL + pcol(kb), dZm + kb * (2048 >> 4), idG,
                                  kb > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kb = 0; kb < M / 16; ++kb)
-                    umma_bf16_ts(tmem + C::DK_COL, tmem + C::DP_COL + 8 * kb, dQm + kb * (2048 >> 4), idG,
+                    umma_bf16_ts(tmem + C::DK_COL, tmem + C::DP_COL + pcol(kb), dQm + kb * (2048 >> 4), idG,
                                  kb > 0 ? 1u : 0u);
                 umma_commit(dvdk_full);
                 if (last) umma_commit(qd_free);
@@ -358,55 +371,86 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             }
         }
         __syncwarp();
-    } else if (warp < 6) {
-        // ---------------- softmax: P and s dS of one token row per thread ----------------
+    } else {
+        // ---------------- softmax halves + epilogue (warps 2-9) ----------------
+        constexpr int W = M / 2;                              // latents of each half
+        const int hf = (warp - 2) >> 2;                       // latent half
         const int quad = warp & 3;
         const int rig = quad * 32 + lane;                     // token row within the tile
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        const uint32_t s_tm = tmem + C::S_COL + lane_off, dp_tm = tmem + C::DP_COL + lane_off;
+        const uint32_t s_tm = tmem + C::S_COL + W * hf + lane_off;
+        const uint32_t dp_tm = tmem + C::DP_COL + W * hf + lane_off;
         const uint64_t c2 = f2pack(a.sl2, a.sl2), sc2 = f2pack(a.s, a.s);
+        // this warp's 32-row slab of the dV (half 0) or dK (half 1) staging tile
+        uint8_t *slab = smem + C::OUT_OFF + (hf * 4 + quad) * (32 * 128);
+        const CUtensorMap *tmOut = hf ? &tmdK : &tmdV;
         auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
             return __all_sync(0xffffffffu, wt.wait(bar, par));
         };
-        // whether this thread's token of tile (bh, kt) takes part (loaded a tile ahead)
-        auto token_valid = [&](int64_t tbh, int64_t tkt) -> bool {
-            const int64_t n = tkt * 128 + rig;
-            if (n >= a.N) return false;
-            return a.mask == nullptr || a.mask[(tbh / a.H) * a.N + n] != 0;
+        // The mask byte of this thread's token is loaded two tiles ahead and
+        // only compared when its tile comes up, so the load's latency is never
+        // waited for (0 stands for padding and for tokens past N).
+        // a tile cursor: (b, h) index bh = b * H + h, token tile kt; no divisions per tile
+        struct Cursor {
+            int64_t bh, kt;
+            int b, h;
         };
-        int64_t bh = bh0, kt = k0, cur = -1;
-        int u = -1;
-        bool valid_next = ntiles > 0 && token_valid(bh0, k0);
+        auto advance = [&](Cursor &t) {
+            if (++t.kt == a.T_bh) {
+                t.kt = 0;
+                ++t.bh;
+                if (++t.h == a.H) {
+                    t.h = 0;
+                    ++t.b;
+                }
+            }
+        };
+        auto mask_byte = [&](const Cursor &t) -> uint32_t {
+            const int64_t n = t.kt * 128 + rig;
+            uint32_t v = n < a.N ? 1u : 0u;
+            if (a.mask != nullptr && n < a.N) v = __ldg(a.mask + (int64_t)t.b * a.N + n);
+            return v;
+        };
+        Cursor cu{bh0, k0, (int)(bh0 / a.H), (int)(bh0 - (bh0 / a.H) * a.H)};
+        int64_t cur = -1;
+        int u = -1, pieces = 0;
+        Cursor ca = cu;                                           // tile j + 2
+        uint32_t mb0 = 0, mb1 = 0;                                // mask bytes of tiles j, j + 1
+        if (ntiles > 0) mb0 = mask_byte(ca);
+        advance(ca);
+        if (ntiles > 1) mb1 = mask_byte(ca);
+        advance(ca);
         for (int64_t j = 0; j < ntiles; ++j) {
+            const int64_t bh = cu.bh, kt = cu.kt;
+            const int b = cu.b, h = cu.h;
             if (bh != cur) {
                 ++u;
                 cur = bh;
                 if (!wwait(lc_full(u & 1), (uint32_t)(u >> 1) & 1)) break;
             }
+            Cursor cn = cu;
+            advance(cn);
+            const bool last = (j + 1 == ntiles) || cn.bh != bh;
             const float *nl2 = lcs + (u & 1) * 256, *ncs = nl2 + 128;
-            const bool valid = valid_next;
-            {
-                int64_t bhN = bh, ktN = kt + 1;
-                if (ktN == a.T_bh) {
-                    ktN = 0;
-                    ++bhN;
-                }
-                valid_next = j + 1 < ntiles && token_valid(bhN, ktN);
-            }
+            const bool valid = mb0 != 0;
+            mb0 = mb1;
+            mb1 = j + 2 < ntiles ? mask_byte(ca) : 0u;
+            advance(ca);
             if (!wwait(s_full, (uint32_t)j & 1)) break;
             tc_fence_after();
             bool ok = true;
 #pragma unroll
-            for (int c = 0; c < M / 32; ++c) {
+            for (int c = 0; c < W / 32; ++c) {
                 uint32_t rs[32], rp[32];
                 tmem_ld32(s_tm + 32 * c, rs);
                 tmem_ld32(dp_tm + 32 * c, rp);
                 tmem_wait_ld();
                 uint32_t pw[16], dw[16];
+                const int m0 = W * hf + 32 * c;                   // first latent of the chunk
                 if (valid) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const int m = 32 * c + 2 * i;
+                        const int m = m0 + 2 * i;
                         const uint64_t nl = *reinterpret_cast<const uint64_t *>(nl2 + m);
                         const uint64_t nc = *reinterpret_cast<const uint64_t *>(ncs + m);
                         float t0, t1;
@@ -425,15 +469,16 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 #pragma unroll
                     for (int i = 0; i < 16; ++i) pw[i] = dw[i] = 0u;
                 }
+                // over this half's own, already loaded, columns
                 tmem_st16(s_tm + 16 * c, pw);
                 tmem_st16(dp_tm + 16 * c, dw);
                 // the previous tile's dQ MMA has read the shared dS buffer
                 if (c == 0 && j > 0 && !(ok = wwait(ds_free, (uint32_t)(j - 1) & 1))) break;
-                // s dS^T row into the MN-major A operand of dQ: latents 32c..32c+31
-                uint8_t *row = smem + C::DS_OFF + (c >> 1) * TB + rig * 128;
+                // s dS^T row into the MN-major A operand of dQ
+                uint8_t *row = smem + C::DS_OFF + (m0 >> 6) * TB + rig * 128;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const int chunk = 4 * (c & 1) + q;
+                    const int chunk = ((m0 & 63) >> 3) + q;
                     *reinterpret_cast<uint4 *>(row + ((chunk ^ (rig & 7)) << 4)) =
                         make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]);
                 }
@@ -444,100 +489,66 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
-            if (++kt == a.T_bh) {
-                kt = 0;
-                ++bh;
-            }
-        }
-    } else {
-        // ---------------- epilogue: dK, dV tiles and the dQ partials ----------------
-        const int quad = warp & 3;
-        const int row = quad * 32 + lane;                     // token row, or latent row of dQ
-        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        const bool e0 = warp == 6 && lane == 0;               // issues the TMA stores
-        auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
-            return __all_sync(0xffffffffu, wt.wait(bar, par));
-        };
-        int64_t bh = bh0, kt = k0;
-        int u = 0;
-        for (int64_t j = 0; j < ntiles; ++j) {
-            const int b = (int)(bh / a.H), h = (int)(bh - (int64_t)b * a.H);
-            int64_t bhN = bh, ktN = kt + 1;
-            if (ktN == a.T_bh) {
-                ktN = 0;
-                ++bhN;
-            }
-            const bool last = (j + 1 == ntiles) || bhN != bh;
+            // epilogue: half 0 takes dV, half 1 dK of the warp's 32 token rows
             if (!wwait(dvdk_full, (uint32_t)j & 1)) break;
             tc_fence_after();
-            uint32_t rv[2][32], rk[2][32];
-            tmem_ld32(tmem + C::DV_COL + lane_off, rv[0]);
-            tmem_ld32(tmem + C::DV_COL + 32 + lane_off, rv[1]);
-            tmem_ld32(tmem + C::DK_COL + lane_off, rk[0]);
-            tmem_ld32(tmem + C::DK_COL + 32 + lane_off, rk[1]);
+            uint32_t rg[2][32];
+            tmem_ld32(tmem + (hf ? C::DK_COL : C::DV_COL) + lane_off, rg[0]);
+            tmem_ld32(tmem + (hf ? C::DK_COL : C::DV_COL) + 32 + lane_off, rg[1]);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(dvdk_free);
-            // the staging tiles are free once the previous stores have read them
+            // the slab is free once the warp's previous store has read it
             if (j > 0) {
-                if (e0) bulk_wait_group_read0();
-                named_bar_sync(1, 128);
+                if (lane == 0) bulk_wait_group_read0();
+                __syncwarp();
             }
-            uint8_t *kr = smem + C::OUT_OFF + row * 128, *vr = kr + TB;
+            uint8_t *srow = slab + lane * 128;
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const int chunk = 4 * h2 + q, pos = (chunk ^ (row & 7)) << 4;
-                    const uint32_t *k8 = rk[h2] + 8 * q, *v8 = rv[h2] + 8 * q;
-                    *reinterpret_cast<uint4 *>(kr + pos) = make_uint4(
-                        pack_bf16(__uint_as_float(k8[0]), __uint_as_float(k8[1])),
-                        pack_bf16(__uint_as_float(k8[2]), __uint_as_float(k8[3])),
-                        pack_bf16(__uint_as_float(k8[4]), __uint_as_float(k8[5])),
-                        pack_bf16(__uint_as_float(k8[6]), __uint_as_float(k8[7])));
-                    *reinterpret_cast<uint4 *>(vr + pos) = make_uint4(
-                        pack_bf16(__uint_as_float(v8[0]), __uint_as_float(v8[1])),
-                        pack_bf16(__uint_as_float(v8[2]), __uint_as_float(v8[3])),
-                        pack_bf16(__uint_as_float(v8[4]), __uint_as_float(v8[5])),
-                        pack_bf16(__uint_as_float(v8[6]), __uint_as_float(v8[7])));
+                    const int chunk = 4 * h2 + q;
+                    const uint32_t *g8 = rg[h2] + 8 * q;
+                    *reinterpret_cast<uint4 *>(srow + ((chunk ^ (lane & 7)) << 4)) = make_uint4(
+                        pack_bf16(__uint_as_float(g8[0]), __uint_as_float(g8[1])),
+                        pack_bf16(__uint_as_float(g8[2]), __uint_as_float(g8[3])),
+                        pack_bf16(__uint_as_float(g8[4]), __uint_as_float(g8[5])),
+                        pack_bf16(__uint_as_float(g8[6]), __uint_as_float(g8[7])));
                 }
             fence_proxy_async_smem();
-            named_bar_sync(1, 128);
-            if (e0) {
+            __syncwarp();
+            const int n0 = (int)(kt * 128) + quad * 32;
+            if (lane == 0 && n0 < a.N) {
                 // rows past N are clipped by the tensor map
-                tma_store_4d(&tmdK, sOut, 0, h, (int)(kt * 128), b);
-                tma_store_4d(&tmdV, sOut + TB, 0, h, (int)(kt * 128), b);
+                tma_store_4d(tmOut, smem_u32(slab), 0, h, n0, b);
                 bulk_commit_group();
             }
             if (last) {
-                // the (b, h)'s dQ partial of this span: one latent row per thread
-                if (!wwait(dq_full, (uint32_t)u & 1)) break;
+                // the (b, h)'s dQ partial of this span: latent rows in the
+                // lanes, half hf takes columns [32 hf, 32 hf + 32)
+                if (!wwait(dq_full, (uint32_t)pieces & 1)) break;
                 tc_fence_after();
-                uint32_t rq[2][32];
-                tmem_ld32(tmem + C::DQ_COL + lane_off, rq[0]);
-                tmem_ld32(tmem + C::DQ_COL + 32 + lane_off, rq[1]);
+                uint32_t rq[32];
+                tmem_ld32(tmem + C::DQ_COL + 32 * hf + lane_off, rq);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(dq_free);
-                if (row < M) {
+                if (rig < M) {
                     const int piece = cta - bwd_cta_of(bh * a.T_bh, a.T_total, a.grid);
-                    float4 *dst = reinterpret_cast<float4 *>(a.part + ((bh * a.P_max + piece) * M + row) * 64);
+                    float4 *dst = reinterpret_cast<float4 *>(a.part + ((bh * a.P_max + piece) * M + rig) * 64 + 32 * hf);
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[8 * h2 + q] = make_float4(
-                                __uint_as_float(rq[h2][4 * q]), __uint_as_float(rq[h2][4 * q + 1]),
-                                __uint_as_float(rq[h2][4 * q + 2]), __uint_as_float(rq[h2][4 * q + 3]));
+                    for (int q = 0; q < 8; ++q)
+                        dst[q] = make_float4(__uint_as_float(rq[4 * q]), __uint_as_float(rq[4 * q + 1]),
+                                             __uint_as_float(rq[4 * q + 2]), __uint_as_float(rq[4 * q + 3]));
                 }
-                ++u;
+                ++pieces;
             }
-            bh = bhN;
-            kt = ktN;
+            cu = cn;
         }
-        if (e0) bulk_wait_group0();
+        if (lane == 0) bulk_wait_group0();
     }
     tc_fence_before();
     __syncthreads();

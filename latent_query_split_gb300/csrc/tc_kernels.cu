@@ -315,8 +315,8 @@ cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *
         !make_map(&maps[1], V, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
         !make_map(&maps[2], Q, pr.D, pr.M, pr.H, qb, (uint32_t)pr.M, 1) ||
         !make_map(&maps[3], dzb, pr.D, pr.M, pr.H, pr.B, (uint32_t)pr.M, 1) ||
-        !make_map(&maps[4], dK, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
-        !make_map(&maps[5], dV, pr.D, pr.H, pr.N, pr.B, 1, 128))
+        !make_map(&maps[4], dK, pr.D, pr.H, pr.N, pr.B, 1, 32) ||
+        !make_map(&maps[5], dV, pr.D, pr.H, pr.N, pr.B, 1, 32))
         return cudaErrorInvalidValue;
     tc::BwdArgs a;
     a.B = pr.B;
