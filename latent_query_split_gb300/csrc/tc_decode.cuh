@@ -219,10 +219,10 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     if (warp == 0) {
         // ---------------- producer: K tiles ----------------
         const uint64_t pol = policy_evict_first();
-        int64_t bh = bh0, kt = k0;
+        int64_t kt = k0;
+        int h = (int)(bh0 / a.B), b = (int)(bh0 - (int64_t)h * a.B);   // tile j's head and batch
         int64_t j = 0;
         for (; j < ntiles && !wt.aborted(); ++j) {
-            const int h = (int)(bh / a.B), b = (int)(bh - (int64_t)h * a.B);
             const int s = (int)(j % STAGES);
             if (!__all_sync(0xffffffffu, wt.wait(empty(s), ((uint32_t)(j / STAGES) & 1) ^ 1))) break;
             if (lane == 0) {
@@ -234,7 +234,10 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             __syncwarp();
             if (++kt == a.T_bh) {
                 kt = 0;
-                ++bh;
+                if (++b == a.B) {             // head-major: bh = h * B + b
+                    b = 0;
+                    ++h;
+                }
             }
         }
         if (wt.aborted() && lane == 0) {
@@ -424,6 +427,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             return true;
         };
         int64_t bh = bh0, kt = k0;
+        int ch = (int)(bh0 / a.B), cb = (int)(bh0 - (int64_t)ch * a.B);   // tile j's head and batch
         bool ok = true;
         for (int64_t j = 0; j < ntiles && ok; ++j) {
             const bool mine = NG == 1 || (int)(j & 1) == g;
@@ -542,8 +546,8 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                     l = (a0 + a1) + (a2 + a3);
                 }
                 have_prev = true;
-                prev_h = (int)(bh / a.B);
-                prev_b = (int)(bh - (int64_t)prev_h * a.B);
+                prev_h = ch;
+                prev_b = cb;
                 prev_n0 = (int)(kt * 128);
                 prev_k = k;
                 prev_l = l;
@@ -551,6 +555,10 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             if (++kt == a.T_bh) {
                 kt = 0;
                 ++bh;
+                if (++cb == a.B) {
+                    cb = 0;
+                    ++ch;
+                }
             }
         }
         if (ok && have_prev && !wt.aborted()) epilogue();
