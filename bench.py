@@ -141,6 +141,29 @@ def _dist_env():
     return world, rank, local
 
 
+def replica_workload(w, rank: int):
+    """The workload rank `rank` runs: the same shapes, its own seed (each rank
+    is an independent replica; no data moves between ranks)."""
+    return w.scaled(seed=w.seed + rank)
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest `value` over all ranks (the slowest rank's time); the
+    identity on one rank."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(tokens_per_replica: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every replica's tokens over the slowest rank's step time."""
+    return tokens_per_replica * world / (ms_per_step * 1e-3)
+
+
 def describe(w) -> str:
     what = {"flare_fwd": "FLARE fwd (encoder + merge + decode)",
             "flare_pp_fwd": "FLARE++ fwd (encoder x2 + decode)",
@@ -351,7 +374,7 @@ def main(argv=None):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    inp = workloads.make_inputs(w.scaled(seed=w.seed + rank), device=dev)
+    inp = workloads.make_inputs(replica_workload(w, rank), device=dev)
     stream = torch.cuda.Stream(device=dev)
     runner = Step(w, inp, dev, args.kernel, stream)
     phases = runner.phases()
@@ -399,10 +422,7 @@ def main(argv=None):
     elapsed_ms = start.elapsed_time(end)
     if step_evs is not None:    # the flush is not the mixer's work
         elapsed_ms = sum(a.elapsed_time(b) for a, b in step_evs)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     ms_per_step = elapsed_ms / args.steps
 
     # per-phase times for the roofline: each phase alone, timed with events
@@ -424,7 +444,7 @@ def main(argv=None):
         phase_ms[name] = statistics.mean(a.elapsed_time(b) for a, b in pe)
     flare.flare_device_status(stream)
     tokens_per_step = w.B * w.N * world
-    value = tokens_per_step / (ms_per_step * 1e-3)
+    value = weak_scaling_value(w.B * w.N, world, ms_per_step)
 
     # end to end through the public API with host buffers (pinned), copies timed
     e2e_in, e2e_out = runner.inputs_for_e2e()
@@ -461,10 +481,7 @@ def main(argv=None):
     e2.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = s2.elapsed_time(e2) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
     flare.flare_device_status(stream)
 
     # roofline of the dominant phase: algorithmic bytes / its event time
