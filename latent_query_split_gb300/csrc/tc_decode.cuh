@@ -51,7 +51,10 @@ struct DecCfg {
     static constexpr int QZB = QZB_;                    // Q/Z buffers (1 or 2)
     static constexpr int KA = D / 64;                   // 64-element atoms along D
     static constexpr int NG = M <= 128 ? 2 : 1;         // softmax groups (tiles in flight)
-    static constexpr int STAGER = 2 + 4 * NG;           // warp index of the stager
+    // M > 128: one group of eight warps, two per TMEM lane quadrant, each
+    // owning M/2 latents of its token rows (a row maximum is exchanged)
+    static constexpr int GW = NG == 2 ? 4 : 8;          // warps per group
+    static constexpr int STAGER = 2 + 8;                // warp index of the stager
     static constexpr int THREADS = 32 * (STAGER + 1);
     static constexpr uint32_t QZ_ATOM = M * 128;        // bytes of one M-row x 64-col atom
     // F16P: P and Z enter Y = P Z as fp16, and Z gets one more 16-column block
@@ -65,19 +68,28 @@ struct DecCfg {
     static constexpr uint32_t STAGE_BYTES = KA * 128 * 128;     // one K tile
     static constexpr int NCH = M / 32;                  // P chunks of 32 latents
     // full[S], empty[S], qz_full[2], qz_free[2], s_full[2], p_chunk[2][8], o_done[2]
-    static constexpr int NBAR = 2 * STAGES + 4 + 2 + 16 + 2;
+    // + epi_done[2] (M > 128: Y of a tile lives in its S buffer, see Y_COL)
+    static constexpr int NBAR = 2 * STAGES + 4 + 2 + 16 + 2 + 2;
     static constexpr uint32_t STAGE_OFF = QZB * QZ_BYTES;
     // Y staging of each group for the TMA stores: 128 token rows, KA atoms
     static constexpr uint32_t OUT_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
     static constexpr uint32_t OUT_BYTES = KA * 128 * 128;
-    static constexpr uint32_t BAR_OFF = OUT_OFF + NG * OUT_BYTES;
-    // M <= 128: a token's M scores stay in registers between the max and exp passes
-    static constexpr bool REG_S = M <= 128;
+    // row maxima of the two latent halves (M > 128), double-buffered by tile parity
+    static constexpr uint32_t XMAX_OFF = OUT_OFF + NG * OUT_BYTES;
+    static constexpr uint32_t XMAX_BYTES = NG == 1 ? 2 * 2 * 128 * 4 : 0;
+    static constexpr uint32_t BAR_OFF = XMAX_OFF + XMAX_BYTES;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t BYTES = MISC_OFF + 64;
     static constexpr uint32_t ALLOC = BYTES + 1024;
     static_assert(ALLOC <= 232448, "shared memory budget of one CTA exceeded");
-    static constexpr uint32_t TMEM_COLS = 512;           // group g: S/P at 256g, Y at 256g + M
+    // Two TMEM buffers b = tile parity, 256 columns each: S (and P over its
+    // first M/2 columns) at 256 b, Y at 256 b + Y_COL. For M <= 128 Y sits
+    // after S; for M > 128 it reuses the upper half of S, dead once the
+    // softmax has read every score, so the buffer is only reused for S two
+    // tiles later after that tile's Y has been read (epi_done).
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t Y_COL = NG == 2 ? M : M / 2;
+    static_assert(Y_COL + YN <= 256, "tensor-memory columns of one buffer exceeded");
 };
 
 // Writes rows [0, M) x D of a row-major matrix into the 128-byte-swizzled bf16
@@ -172,6 +184,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     auto s_full = [&](int g) { return bar0 + 8u * (2 * STAGES + 4 + g); };
     auto p_chunk = [&](int g, int c) { return bar0 + 8u * (2 * STAGES + 6 + 8 * g + c); };
     auto o_done = [&](int g) { return bar0 + 8u * (2 * STAGES + 22 + g); };
+    auto epi_done = [&](int g) { return bar0 + 8u * (2 * STAGES + 24 + g); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
 
@@ -193,8 +206,9 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             mbar_init(qz_free(q), 1);
         }
         for (int g = 0; g < 2; ++g) {
+            mbar_init(epi_done(g), C::GW);   // one arrival per softmax warp
             mbar_init(s_full(g), 1);
-            for (int c = 0; c < 8; ++c) mbar_init(p_chunk(g, c), 4);   // one arrival per softmax warp
+            for (int c = 0; c < 8; ++c) mbar_init(p_chunk(g, c), C::GW);   // one arrival per softmax warp
             mbar_init(o_done(g), 1);
         }
         fence_mbar_init();
@@ -297,7 +311,10 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             }
             if (!wwait(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
             tc_fence_after();
-            const int g = NG == 2 ? (int)(jj & 1) : 0;
+            const int g = (int)(jj & 1);               // TMEM buffer
+            // M > 128: the buffer's previous tile (jj - 2) must have had its Y read
+            if (NG == 1 && jj >= 2 && !wwait(epi_done(g), (uint32_t)((jj >> 1) - 1) & 1)) return false;
+            tc_fence_after();
             const uint64_t dK = dK0 + kStageDesc * s;
             const uint64_t dQ0 = desc_sw128(sbase + (uint32_t)(uS % QZB) * C::QZ_BYTES, 16, 1024);
 #pragma unroll
@@ -318,28 +335,28 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         // a new (b, h) also waits until every older tile's P Z is issued
         int64_t jS = 0, nP = 0;
         auto pump_s = [&]() -> bool {
-            while (jS < ntiles && jS < nP + NG && (QZB == 2 || bhS - bh0 == uS || nP == jS))
+            while (jS < ntiles && jS < nP + 2 && (QZB == 2 || bhS - bh0 == uS || nP == jS))
                 if (!issue_s(jS++)) return false;
             return true;
         };
         ok = pump_s();
         for (; nP < ntiles && ok;) {
             const int64_t jP = nP;
-            const int g = NG == 2 ? (int)(jP & 1) : 0;
-            const int64_t kP = NG == 2 ? (jP >> 1) : jP;
+            const int g = (int)(jP & 1);
+            const int64_t kP = jP >> 1;
             const uint64_t dZ0 = desc_sw128(sbase + (uint32_t)(uP % QZB) * C::QZ_BYTES + KA * C::QZ_ATOM,
                                             C::QZ_ATOM, 1024);
             for (int c = 0; c < NCH && ok; ++c) {
-                // P arrives whole (registers path) or chunk by chunk
-                if (!C::REG_S || c == 0) {
-                    ok = wwait(p_chunk(g, C::REG_S ? 0 : c), (uint32_t)kP & 1);
+                // P arrives whole, published by every softmax warp at once
+                if (c == 0) {
+                    ok = wwait(p_chunk(g, 0), (uint32_t)kP & 1);
                     if (!ok) break;
                     tc_fence_after();
                 }
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
                     const int kb = 2 * c + kk;       // 16 latents per MMA
-                    umma_ts_elect(tmem + g * 256 + M, tmem + g * 256 + kb * 8, dZ0 + kb * (2048 >> 4), idPV,
+                    umma_ts_elect(tmem + g * 256 + C::Y_COL, tmem + g * 256 + kb * 8, dZ0 + kb * (2048 >> 4), idPV,
                                   kb > 0 ? 1u : 0u);
                 }
             }
@@ -358,11 +375,129 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         }
         // make every issued MMA finish before TMEM is released
         if (ok && ntiles > 0) {
-            const int gl = NG == 2 ? (int)((ntiles - 1) & 1) : 0;
-            const int64_t kl = NG == 2 ? ((ntiles - 1) >> 1) : ntiles - 1;
+            const int gl = (int)((ntiles - 1) & 1);
+            const int64_t kl = (ntiles - 1) >> 1;
             wwait(o_done(gl), (uint32_t)kl & 1);
         }
         __syncwarp();
+    } else if (NG == 1) {
+        // ---------------- softmax halves + epilogue (M > 128) ----------------
+        // Warps w and w + 4 share a TMEM lane quadrant (32 token rows); half h
+        // owns latents [M/2 h, M/2 (h + 1)). After both have loaded their
+        // scores into registers and exchanged the row maximum, P of latent m
+        // is written at column m / 2 (fp16 pairs): every score is then in
+        // registers, so the halves can overwrite each other's columns.
+        constexpr int HM = M / 2;                     // latents of a half
+        const int half = (warp - 2) >> 2;
+        const int quad = warp & 3;
+        const int rig = quad * 32 + lane;             // token row within the tile
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const uint64_t c2 = f2pack(a.sl2, a.sl2);
+        float *xmax = reinterpret_cast<float *>(smem + C::XMAX_OFF);   // [2 parity][2 half][128 rows]
+        uint8_t *slab = smem + C::OUT_OFF + quad * 32 * 128;         // the quadrant's 32 Y rows
+        const bool storer = half == 0 && lane == 0;
+        const int pair_bar = 1 + quad;                // named barrier of the quadrant's two warps
+        auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
+            return __all_sync(0xffffffffu, wt.wait(bar, par));
+        };
+        bool have_prev = false;
+        int prev_b = 0, prev_h = 0, prev_n0 = 0;
+        int64_t prev_k = 0;
+        uint32_t stores = 0;
+        // Y / l of the previous tile: half h converts columns [32 h, 32 h + 32)
+        // of each row (D = 64), half 0's lane 0 stores the quadrant's 32 rows
+        auto epilogue = [&]() -> bool {
+            const int pb = (int)(prev_k & 1);                   // the previous tile's buffer
+            if (!wwait(o_done(pb), (uint32_t)(prev_k >> 1) & 1)) return false;
+            tc_fence_after();
+            const uint32_t y_tmem = tmem + pb * 256 + C::Y_COL + lane_off;
+            uint32_t r[32];
+            tmem_ld32(y_tmem + 32 * half, r);
+            const uint32_t lw = tmem_ld1(y_tmem + D);              // c * l from the row-sum block
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(epi_done(pb));              // the buffer may take S again
+            if (stores > 0 && storer) bulk_wait_group_read0();     // the slab's last store has read it
+            named_bar_sync(pair_bar, 64);
+            const float inv = 1.f / __uint_as_float(lw);
+            uint8_t *row = slab + lane * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int chunk = 4 * half + q;
+                const uint32_t *v = r + 8 * q;
+                *reinterpret_cast<uint4 *>(row + ((chunk ^ (lane & 7)) << 4)) = make_uint4(
+                    pack_bf16(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                    pack_bf16(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                    pack_bf16(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                    pack_bf16(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(pair_bar, 64);
+            const int n0 = prev_n0 + quad * 32;
+            if (storer && n0 < a.N) {
+                // token rows past N are clipped by the tensor map
+                tma_store_4d(&tmY, smem_u32(slab), 0, prev_h, n0, prev_b);
+                bulk_commit_group();
+            }
+            ++stores;
+            return true;
+        };
+        int64_t kt = k0;
+        int ch = (int)(bh0 / a.B), cb = (int)(bh0 - (int64_t)ch * a.B);   // tile j's head and batch
+        bool ok = true;
+        for (int64_t j = 0; j < ntiles && ok; ++j) {
+            const int bb = (int)(j & 1);                        // TMEM buffer of tile j
+            const uint32_t s_tmem = tmem + bb * 256 + HM * half + lane_off;
+            const uint32_t p_tmem = tmem + bb * 256 + (HM / 2) * half + lane_off;
+            if (!wwait(s_full(bb), (uint32_t)(j >> 1) & 1)) break;
+            tc_fence_after();
+            if (have_prev && !(ok = epilogue())) break;
+            uint32_t r[HM / 32][32];
+#pragma unroll
+            for (int c = 0; c < HM / 32; ++c) tmem_ld32(s_tmem + c * 32, r[c]);
+            tmem_wait_ld();
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < HM / 32; ++c)
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    mx[i & 1] = max3(mx[i & 1], __uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1]));
+            float *xm = xmax + (j & 1) * 256;
+            xm[half * 128 + rig] = fmaxf(mx[0], mx[1]);
+            named_bar_sync(pair_bar, 64);                 // both halves' scores are in registers
+            const float m = fmaxf(xm[rig], xm[128 + rig]) * a.sl2;
+            const uint64_t nm2 = f2pack(-m, -m);
+#pragma unroll
+            for (int c = 0; c < HM / 32; ++c) {
+                uint32_t pw[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float t0, t1;
+                    f2unpack(fma2(f2pack(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1])), c2, nm2), t0, t1);
+                    pw[i] = ex2_f16x2(pack_f16(t0, t1));
+                }
+                tmem_st16(p_tmem + c * 16, pw);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_chunk(bb, 0));
+            have_prev = true;
+            prev_h = ch;
+            prev_b = cb;
+            prev_n0 = (int)(kt * 128);
+            prev_k = j;
+            if (++kt == a.T_bh) {
+                kt = 0;
+                if (++cb == a.B) {
+                    cb = 0;
+                    ++ch;
+                }
+            }
+        }
+        if (ok && have_prev && !wt.aborted()) epilogue();
+        if (storer) bulk_wait_group0();
     } else {
         // ---------------- softmax + epilogue warps ----------------
         const int g = (warp - 2) >> 2;
@@ -370,7 +505,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         const int rig = quad * 32 + lane;            // token row within the tile (TMEM lane)
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const uint32_t s_tmem = tmem + g * 256 + lane_off;
-        const uint32_t y_tmem = tmem + g * 256 + M + lane_off;
+        const uint32_t y_tmem = tmem + g * 256 + C::Y_COL + lane_off;
         const uint64_t c2 = f2pack(a.sl2, a.sl2);
         // each warp stages and stores its own 32 token rows (a 4 KB slab per atom)
         uint8_t *stage_out = smem + C::OUT_OFF + g * C::OUT_BYTES + quad * 32 * 128;
@@ -437,7 +572,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 tc_fence_after();
                 if (have_prev && !(ok = epilogue())) break;
                 float l;
-                if constexpr (C::REG_S) {
+                {
                     // every score of the row in registers: one load, max, exp
                     uint32_t r[NCH][32];
 #pragma unroll
@@ -492,58 +627,6 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(p_chunk(g, 0));
-                } else {
-                    // pass 1: row maximum over the M latents
-                    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-                    for (int c = 0; c < M / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(s_tmem + c * 32, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            mx[i & 1] = max3(mx[i & 1], __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                    }
-                    const float m = fmaxf(mx[0], mx[1]) * a.sl2;
-                    const uint64_t nm2 = f2pack(-m, -m);
-                    // pass 2: P = exp2(s*c - m) (fp16 or bf16) over S's first M/2 columns
-                    uint64_t ls2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
-#pragma unroll
-                    for (int c = 0; c < NCH; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(s_tmem + c * 32, r);
-                        tmem_wait_ld();
-                        uint32_t pw[16];
-                        if constexpr (C::F16P) {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                float t0, t1;
-                                f2unpack(fma2(f2pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c2, nm2), t0, t1);
-                                pw[i] = ex2_f16x2(pack_f16(t0, t1));
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                float t0, t1, t2, t3;
-                                f2unpack(fma2(f2pack(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), c2, nm2), t0, t1);
-                                f2unpack(fma2(f2pack(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), c2, nm2), t2, t3);
-                                const float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
-                                ls2[0] = add2(ls2[0], f2pack(p0, p1));
-                                ls2[1] = add2(ls2[1], f2pack(p2, p3));
-                                pw[2 * i] = pack_bf16(p0, p1);
-                                pw[2 * i + 1] = pack_bf16(p2, p3);
-                            }
-                        }
-                        tmem_st16(s_tmem + c * 16, pw);
-                        tmem_wait_st();
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(p_chunk(g, c));
-                    }
-                    float a0, a1, a2, a3;
-                    f2unpack(ls2[0], a0, a1);
-                    f2unpack(ls2[1], a2, a3);
-                    l = (a0 + a1) + (a2 + a3);
                 }
                 have_prev = true;
                 prev_h = ch;
