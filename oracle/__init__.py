@@ -63,6 +63,8 @@ def _load():
         lib.oracle_decode.argtypes = [I, I, I, I, I, Dbl, L, P, I, P, P, I, P, L, P]
         lib.oracle_encode_bwd.argtypes = [I, I, I, I, I, Dbl, L, P, I, P, P, I, P,
                                           P, P, P, P, P, P]
+        lib.oracle_decode_bwd.argtypes = [I, I, I, I, I, Dbl, L, P, I, P, P, I, P, I,
+                                          P, P, P]
         lib.oracle_num_threads.restype = I
         _lib = lib
     return _lib
@@ -225,3 +227,23 @@ def encode_bwd(Q, K, V, mask, Z, L, dZ, scale=None):
                               _ptr(mk), _ptr(z), _ptr(l), _ptr(dz), _ptr(dQ), _ptr(dK),
                               _ptr(dV))
     return dQ, dK, dV
+
+
+def decode_bwd(Q, Z, K, dY, scale=None):
+    """Decode backward for the output gradient dY [B,N,H,D]. Returns dQ
+    [B,H,M,D] (per batch element), dZ [B,H,M,D] and dK [B,N,H,D]."""
+    q, qt = _as_input(Q)
+    k, kt = _as_input(K)
+    y, yt = _as_input(dY)
+    z = _f64(Z)
+    B, N, H, D = k.shape
+    M = q.shape[-2]
+    qbs = _query_layout(q, B, H, M, D)
+    assert z.shape == (B, H, M, D) and y.shape == k.shape
+    s = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    dQ = np.empty((B, H, M, D))
+    dZ = np.empty((B, H, M, D))
+    dK = np.empty((B, N, H, D))
+    _load().oracle_decode_bwd(B, H, M, N, D, s, qbs, _ptr(q), qt, _ptr(z), _ptr(k), kt,
+                              _ptr(y), yt, _ptr(dQ), _ptr(dZ), _ptr(dK))
+    return dQ, dZ, dK

@@ -25,6 +25,11 @@
  *       U = sum_r exp(L_r - L_max) O_r, Z = U / a, L = L_max + log a.
  *   decode (FLARE decode paragraph): each token's own key is its query against
  *     the replicated latents: T_nm = s * <K_n, Q_m>, Y_n = sum_m softmax_m(T_n) Z_m.
+ *   decode backward (chain rule of the decode; the pages name the decoder's
+ *     contribution to the gradients of the latents, the formula is stripped):
+ *       A_nm = softmax_m(T_n), g_nm = <dY_n, Z_m>, r_n = sum_m A_nm g_nm,
+ *       dT_nm = A_nm (g_nm - r_n), dZ_m = sum_n A_nm dY_n,
+ *       dK_n = s sum_m dT_nm Q_m, dQ_m = s sum_n dT_nm K_n.
  *   encoder backward (the backward paragraphs): with the global Z, L,
  *       P_mn = exp(S_mn - L_m), c_m = <dZ_m, Z_m>,
  *       dV_n = sum_m P_mn dZ_m, dS_mn = P_mn (<dZ_m, V_n> - c_m),
@@ -247,5 +252,65 @@ void oracle_encode_bwd(int B, int H, int M, int N, int D, double scale, long q_b
         }
         free(c);
         free(Qd);
+    }
+}
+
+/*
+ * Decode backward: the gradients of the local decode for an output gradient
+ * dY [B,N,H,D] (element code yt). Z [B,H,M,D] double. Outputs (double):
+ * dQ [B,H,M,D] (one per batch element, also for a replicated query),
+ * dZ [B,H,M,D] and dK [B,N,H,D]. Every token slot contributes (the decode has
+ * no mask).
+ */
+void oracle_decode_bwd(int B, int H, int M, int N, int D, double scale, long q_bstride,
+                       const void *Q, int qt, const double *Z, const void *K, int kt,
+                       const void *dY, int yt, double *dQ, double *dZ, double *dK) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long bh = 0; bh < (long)B * H; ++bh) {
+        long b = bh / H, h = bh % H;
+        double *Qd = (double *)malloc(sizeof(double) * (size_t)M * D);
+        double *A = (double *)malloc(sizeof(double) * M);
+        double *g = (double *)malloc(sizeof(double) * M);
+        for (int m = 0; m < M; ++m) {
+            size_t qoff = (size_t)b * q_bstride + ((size_t)h * M + m) * D;
+            for (int d = 0; d < D; ++d) Qd[(size_t)m * D + d] = load(Q, qt, qoff + d);
+        }
+        const double *Zb = Z + (size_t)bh * M * D;
+        double *dq = dQ + (size_t)bh * M * D, *dz = dZ + (size_t)bh * M * D;
+        for (size_t j = 0; j < (size_t)M * D; ++j) dq[j] = dz[j] = 0.0;
+        for (long n = 0; n < N; ++n) {
+            size_t to = tok_index(b, n, h, N, H, D);
+            /* A = softmax over the latents of T_nm = s <K_n, Q_m> */
+            double mx = -INFINITY;
+            for (int m = 0; m < M; ++m) {
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d) dot += load(K, kt, to + d) * Qd[(size_t)m * D + d];
+                A[m] = scale * dot;
+                if (A[m] > mx) mx = A[m];
+            }
+            double sum = 0.0;
+            for (int m = 0; m < M; ++m) sum += exp(A[m] - mx);
+            double r = 0.0;
+            for (int m = 0; m < M; ++m) {
+                A[m] = exp(A[m] - mx) / sum;
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d) dot += load(dY, yt, to + d) * Zb[(size_t)m * D + d];
+                g[m] = dot;
+                r += A[m] * g[m];
+            }
+            double *dk = dK + to;
+            for (int d = 0; d < D; ++d) dk[d] = 0.0;
+            for (int m = 0; m < M; ++m) {
+                double dT = A[m] * (g[m] - r);
+                for (int d = 0; d < D; ++d) {
+                    dk[d] += scale * dT * Qd[(size_t)m * D + d];
+                    dq[(size_t)m * D + d] += scale * dT * load(K, kt, to + d);
+                    dz[(size_t)m * D + d] += A[m] * load(dY, yt, to + d);
+                }
+            }
+        }
+        free(Qd);
+        free(A);
+        free(g);
     }
 }
