@@ -87,7 +87,8 @@ typedef enum {
     FLARE_OP_DECODE_FWD = 2,
     FLARE_OP_FWD = 3,
     FLARE_OP_PP_FWD = 4,
-    FLARE_OP_ENCODER_BWD = 5
+    FLARE_OP_ENCODER_BWD = 5,
+    FLARE_OP_DECODE_BWD = 6
 } flare_op_t;
 
 /* Workspace bytes `op` needs for these sizes and shard offsets (host array of
@@ -202,6 +203,27 @@ FLARE_API flare_status_t flare_encoder_bwd(const flare_dims_t *dims, const void 
                                  const int64_t *shard_offsets, int R, const float *Z,
                                  const float *L, const float *dZ, float *dQ, void *dK, void *dV,
                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Decode backward: the chain rule of the local decode (the FLARE decode
+ * paragraph of the appendix; the pages name the decoder's contribution to the
+ * gradients of the latent tensors but print no formula). For the gradient dY
+ * of the decode output, per batch b, head h, token n and latent m:
+ *   A_nm  = softmax_m(s <K_n, Q_m>),  g_nm = <dY_n, Z_m>,  r_n = sum_m A_nm g_nm,
+ *   dT_nm = A_nm (g_nm - r_n),
+ *   dZ_m  = sum_n A_nm dY_n,  dK_n = s sum_m dT_nm Q_m,  dQ_m = s sum_n dT_nm K_n.
+ *   Q   dims->dtype [H,M,D] or [B,H,M,D];  Z fp32 [B,H,M,D];
+ *   K, dY  dims->dtype [B,N,H,D];
+ *   dQ fp32 [B,H,M,D] (one slice per batch element, also when Q is
+ *   replicated); dZ fp32 [B,H,M,D]; dK dims->dtype [B,N,H,D] (the decode's
+ *   share of the key gradient; the encoder backward adds its own).
+ * Every token slot contributes (the decode has no mask). Workspace:
+ * flare_workspace_bytes(FLARE_OP_DECODE_BWD, dims, NULL, 0) bytes.
+ */
+FLARE_API flare_status_t flare_decode_bwd(const flare_dims_t *dims, const void *Q, const float *Z,
+                                          const void *K, const void *dY, float *dQ, float *dZ,
+                                          void *dK, void *workspace, size_t workspace_bytes,
+                                          void *stream);
 
 /*
  * Split-KV encoder without a workspace argument, for callers that cannot

@@ -361,6 +361,16 @@ const char *flare_last_error_string(void) { return t_error.c_str(); }
 size_t flare_workspace_bytes(flare_op_t op, const flare_dims_t *dims, const int64_t *off, int R) {
     const size_t bad = (size_t)-1;
     if (op == FLARE_OP_LSE_MERGE || op == FLARE_OP_DECODE_FWD) return 0;
+    if (op == FLARE_OP_DECODE_BWD) {
+        if (check_dims(dims) != FLARE_OK) return bad;
+        const Problem pr = make_problem(dims);
+        size_t b = decode_bwd_simt_workspace(pr);
+        if (dims->kernel != FLARE_KERNEL_SIMT) {
+            const size_t t = tc_decode_bwd_workspace(pr, planning_sms());
+            if (t > b) b = t;
+        }
+        return b;
+    }
     if (check_dims(dims) != FLARE_OK) return bad;
     if (check_offsets(off, R, dims->N) != FLARE_OK) return bad;
     switch (op) {
@@ -492,6 +502,46 @@ flare_status_t flare_encoder_bwd(const flare_dims_t *dims, const void *Q, const 
                                     workspace_bytes, (cudaStream_t)stream);
     }
     return e == cudaSuccess ? FLARE_OK : cuda_fail(e, "encoder backward launch");
+}
+
+flare_status_t flare_decode_bwd(const flare_dims_t *dims, const void *Q, const float *Z,
+                                const void *K, const void *dY, float *dQ, float *dZ, void *dK,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+    flare_status_t s = check_dims(dims);
+    if (s != FLARE_OK) return s;
+    const Problem pr = make_problem(dims);
+    if (pr.B == 0) return FLARE_OK;
+    if (!Q || !Z || !dQ || !dZ || (pr.N > 0 && (!K || !dY || !dK)))
+        return fail(FLARE_ERR_INVALID_ARG, "NULL tensor");
+    const size_t es = elem_size(dims);
+    if (!aligned(Q, es) || !aligned(K, es) || !aligned(dY, es) || !aligned(dK, es) || !aligned(Z, 4) ||
+        !aligned(dQ, 4) || !aligned(dZ, 4))
+        return fail(FLARE_ERR_INVALID_ARG, "tensors must be aligned to their element size");
+    const bool want_tc = dims->kernel != FLARE_KERNEL_SIMT && tc_decode_bwd_supported(pr.bf16, pr.M, pr.D);
+    if (dims->kernel == FLARE_KERNEL_TENSOR && !want_tc)
+        return fail(FLARE_ERR_UNSUPPORTED, "no tensor-core decode backward for dtype=%d M=%d D=%d",
+                    (int)dims->dtype, dims->M, dims->D);
+    const bool tc = want_tc && tc_pointers_ok(K, dY, dims->H, dims->D) &&
+                    tc_pointers_ok(dK, dK, dims->H, dims->D) && aligned(Q, 16) && aligned(Z, 16) &&
+                    aligned(dQ, 16) && aligned(dZ, 16);
+    if (dims->kernel == FLARE_KERNEL_TENSOR && !tc)
+        return fail(FLARE_ERR_INVALID_ARG,
+                    "tensor-core decode backward needs 16-byte aligned Q, Z, K, dY, dQ, dZ and dK");
+    const size_t need = flare_workspace_bytes(FLARE_OP_DECODE_BWD, dims, nullptr, 0);
+    if (!workspace || workspace_bytes < need)
+        return fail(FLARE_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", need,
+                    workspace_bytes);
+    if (!aligned(workspace, 256)) return fail(FLARE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    cudaError_t e;
+    if (tc) {
+        DeviceInfo di;
+        if ((s = device_info(di)) != FLARE_OK) return s;
+        e = launch_decode_bwd_tc(pr, Q, Z, K, dY, dQ, dZ, dK, workspace, workspace_bytes, di.sms,
+                                 di.status, (cudaStream_t)stream);
+    } else {
+        e = launch_decode_bwd_simt(pr, Q, Z, K, dY, dQ, dZ, dK, workspace, (cudaStream_t)stream);
+    }
+    return e == cudaSuccess ? FLARE_OK : cuda_fail(e, "decode backward launch");
 }
 
 flare_status_t flare_device_status(void *stream) {

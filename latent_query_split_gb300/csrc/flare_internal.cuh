@@ -86,6 +86,10 @@ cudaError_t launch_encoder_bwd_simt(const Problem &pr, const void *Q, const void
                                     const float *L, const float *dZ, float *dQ, void *dK,
                                     void *dV, void *ws, size_t ws_bytes, cudaStream_t st);
 size_t encoder_bwd_simt_workspace(const Problem &pr);
+cudaError_t launch_decode_bwd_simt(const Problem &pr, const void *Q, const float *Z, const void *K,
+                                   const void *dY, float *dQ, float *dZ, void *dK, void *ws,
+                                   cudaStream_t st);
+size_t decode_bwd_simt_workspace(const Problem &pr);
 
 // Rows of latents one SIMT encoder CTA handles.
 constexpr int kSimtRows = 32;

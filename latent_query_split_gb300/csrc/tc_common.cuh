@@ -62,4 +62,11 @@ cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *
                                   const float *dZ, float *dQ, void *dK, void *dV, void *ws,
                                   size_t ws_bytes, int sms, unsigned *status, cudaStream_t st);
 
+// Decode backward on tensor cores: bf16 with D = 64 and M in {64, 128}.
+bool tc_decode_bwd_supported(bool bf16, int M, int D);
+size_t tc_decode_bwd_workspace(const Problem &pr, int sms);
+cudaError_t launch_decode_bwd_tc(const Problem &pr, const void *Q, const float *Z, const void *K,
+                                 const void *dY, float *dQ, float *dZ, void *dK, void *ws,
+                                 size_t ws_bytes, int sms, unsigned *status, cudaStream_t st);
+
 }  // namespace flare

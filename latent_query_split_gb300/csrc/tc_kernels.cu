@@ -343,4 +343,14 @@ cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *
     return cudaGetLastError();
 }
 
+// The tensor-core decode backward is not built yet: the CUDA-core kernels
+// serve every shape.
+bool tc_decode_bwd_supported(bool, int, int) { return false; }
+size_t tc_decode_bwd_workspace(const Problem &, int) { return 0; }
+cudaError_t launch_decode_bwd_tc(const Problem &, const void *, const float *, const void *,
+                                 const void *, float *, float *, void *, void *, size_t, int,
+                                 unsigned *, cudaStream_t) {
+    return cudaErrorNotSupported;
+}
+
 }  // namespace flare

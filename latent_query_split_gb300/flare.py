@@ -23,12 +23,13 @@ FLARE_ERR_WORKSPACE, FLARE_ERR_CUDA, FLARE_ERR_TIMEOUT = 3, 4, 5
 FLARE_F32, FLARE_BF16 = 0, 1
 KERNELS = {"auto": 0, "simt": 1, "tensor": 2}
 (FLARE_OP_ENCODER_FWD, FLARE_OP_LSE_MERGE, FLARE_OP_DECODE_FWD, FLARE_OP_FWD,
- FLARE_OP_PP_FWD, FLARE_OP_ENCODER_BWD) = range(6)
+ FLARE_OP_PP_FWD, FLARE_OP_ENCODER_BWD, FLARE_OP_DECODE_BWD) = range(7)
 FLARE_MAX_SHARDS = 256
 
 # Every symbol the header declares (checked by the test-suite).
 EXPORTS = ("flare_workspace_bytes", "flare_encoder_fwd", "flare_lse_merge", "flare_decode_fwd",
-           "flare_fwd", "flare_pp_fwd", "flare_encoder_bwd", "flare_encoder_fwd_noalloc",
+           "flare_fwd", "flare_pp_fwd", "flare_encoder_bwd", "flare_decode_bwd",
+           "flare_encoder_fwd_noalloc",
            "flare_device_status", "flare_last_error_string", "flare_version",
            "flare_launch_count")
 
@@ -73,6 +74,7 @@ def load_library(build_if_missing: bool = True):
     lib.flare_fwd.argtypes = [D, P, P, P, P, P, I, P, P, P, P, Z, P]
     lib.flare_pp_fwd.argtypes = [D, P, P, P, P, P, P, P, I, P, P, P, P, P, P, Z, P]
     lib.flare_encoder_bwd.argtypes = [D, P, P, P, P, P, I, P, P, P, P, P, P, P, Z, P]
+    lib.flare_decode_bwd.argtypes = [D, P, P, P, P, P, P, P, P, Z, P]
     lib.flare_encoder_fwd_noalloc.argtypes = [D, P, P, P, P, P, I, P, P, P, P, P]
     lib.flare_device_status.argtypes = [P]
     lib.flare_last_error_string.restype = ctypes.c_char_p
@@ -256,6 +258,27 @@ def flare_encoder_bwd(Q, K, V, mask, shard_offsets, Z, L, dZ, *, dQ=None, dK=Non
                                  R, _ptr(Z), _ptr(L), _ptr(dZ), _ptr(dQ), _ptr(dK), _ptr(dV),
                                  _ptr(ws), nbytes, _stream(stream)))
     return dQ, dK, dV
+
+
+def flare_decode_bwd(Q, Z, K, dY, *, dQ=None, dZ=None, dK=None, workspace=None, scale=None,
+                     kernel="auto", stream=None):
+    """Decode backward for the output gradient dY; returns (dQ [B,H,M,D] fp32,
+    dZ [B,H,M,D] fp32, dK [B,N,H,D] in K's dtype)."""
+    lib = load_library()
+    dims = make_dims(Q, K, scale, kernel)
+    B, N, H, D = K.shape
+    M = Q.shape[-2]
+    f32 = dict(dtype=torch.float32, device=K.device)
+    if dQ is None:
+        dQ = torch.empty((B, H, M, D), **f32)
+    if dZ is None:
+        dZ = torch.empty((B, H, M, D), **f32)
+    if dK is None:
+        dK = torch.empty_like(K)
+    ws, nbytes = _workspace(FLARE_OP_DECODE_BWD, dims, None, workspace, K.device)
+    _check(lib.flare_decode_bwd(ctypes.byref(dims), _ptr(Q), _ptr(Z), _ptr(K), _ptr(dY), _ptr(dQ),
+                                _ptr(dZ), _ptr(dK), _ptr(ws), nbytes, _stream(stream)))
+    return dQ, dZ, dK
 
 
 def flare_encoder_fwd_noalloc(Q, K, V, mask=None, shard_offsets=None, *, O_r=None, L_r=None,

@@ -138,3 +138,26 @@ def test_c4_rescale_path_is_exercised(cuda_device):
         Zo, Lo = oracle.encode(Q[h:h + 1].cpu(), _head(K, 0, h), _head(V, 0, h))
         assert_close(f"Z[0,{h}]", Z[0:1, h:h + 1], Zo, "bf16")
         assert_L_close(f"L[0,{h}]", L[0:1, h:h + 1], Lo)
+
+
+def test_decode_bwd_c5_shapes_sampled(cuda_device):
+    """The decode backward on the shapes of the encoder-backward workload
+    (B2 H8 D64 M128 N131072), checked on sampled (b, h) pairs, plus the
+    invariant sum_m dZ_m = sum_n dY_n at full size."""
+    w = workloads.CONFIGS["c5_bwd_bf16"]
+    inp = workloads.make_inputs(w, device="cuda")
+    Q, K = inp["Q"], inp["K"]
+    g = torch.Generator(device="cuda").manual_seed(55)
+    Z = torch.randn((w.B, w.H, w.M, w.D), generator=g, device="cuda")
+    dY = torch.randn(K.shape, generator=g, device="cuda").to(K.dtype)
+    dQ, dZ, dK = flare.flare_decode_bwd(Q, Z, K, dY)
+    flare.flare_device_status()
+    lhs = dZ.double().sum(2)
+    rhs = dY.double().sum(1)
+    assert (lhs - rhs).abs().max().item() <= 2e-3 * rhs.abs().max().item()
+    for b, h in [(0, 1), (1, 7)]:
+        Qh = Q[h:h + 1].cpu()
+        dQo, dZo, dKo = oracle.decode_bwd(Qh, Z[b:b + 1, h:h + 1].cpu(), _head(K, b, h), _head(dY, b, h))
+        assert_close(f"dQ[{b},{h}]", dQ[b:b + 1, h:h + 1], dQo, "bf16")
+        assert_close(f"dZ[{b},{h}]", dZ[b:b + 1, h:h + 1], dZo, "bf16")
+        assert_close(f"dK[{b},:,{h}]", dK[b:b + 1, :, h:h + 1], dKo, "bf16")

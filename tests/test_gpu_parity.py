@@ -168,6 +168,28 @@ def test_encoder_bwd_multi_tile_spans(cuda_device, kernel, M, replicated):
     assert torch.equal(dQ, dQ2) and torch.equal(dK, dK2) and torch.equal(dV, dV2)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dt,M,D,N,replicated", [("f32", 16, 32, 700, True), ("bf16", 128, 64, 3000, True),
+                                                 ("bf16", 64, 64, 2100, False), ("bf16", 64, 128, 1100, True),
+                                                 ("bf16", 256, 64, 900, True), ("f32", 37, 40, 333, False)])
+def test_decode_bwd(cuda_device, kernel, dt, M, D, N, replicated):
+    B, H = 2, 2
+    Q, K, _, _ = _problem(18, B, H, M, N, D, dt, [0, N], pad=0, q_std=1.0, replicated=replicated)
+    g = torch.Generator().manual_seed(19)
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    Z = torch.randn((B, H, M, D), generator=g).cuda()
+    dY = torch.randn((B, N, H, D), generator=g).to(tdt).cuda()
+    dQ, dZ, dK = _call(flare.flare_decode_bwd, Q, Z, K, dY, kernel=kernel)
+    flare.flare_device_status()
+    dQo, dZo, dKo = oracle.decode_bwd(Q, Z, K, dY)
+    assert_close("dQ", dQ, dQo, dt)
+    assert_close("dZ", dZ, dZo, dt)
+    assert_close("dK", dK, dKo, dt)
+    # two runs agree bit for bit (fixed-order sums)
+    dQ2, dZ2, dK2 = _call(flare.flare_decode_bwd, Q, Z, K, dY, kernel=kernel)
+    assert torch.equal(dQ, dQ2) and torch.equal(dZ, dZ2) and torch.equal(dK, dK2)
+
+
 # ---- edge cases ------------------------------------------------------------------------
 
 @pytest.mark.parametrize("kernel", KERNELS)
