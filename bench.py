@@ -9,6 +9,7 @@ One step = one pass of the hot path over one batch of a named workload
   c4_long_bf16       the same forward, B=1 H=8 D=128 M=64 N=4194304, R=64
   c3_pp_bf16         FLARE++ forward (encoder twice, then the decode)
   c5_bwd_bf16        global-normaliser encoder backward (dQ, dK, dV)
+  c5_decbwd_bf16     decode backward (dQ, dZ, dK) on the shapes of c5
 Token tensors of c2-c5 are 256 MiB or more each (larger than the 129 MB L2),
 so no flush is needed between steps; c1 flushes L2 between steps.
 
@@ -46,6 +47,7 @@ KERNEL_SOURCES = {
     "decode": ["tc_decode.cuh", "tc_ptx.cuh", "tc_kernels.cu"],
     "encoder_bwd": ["tc_backward.cuh", "tc_ptx.cuh", "tc_kernels.cu", "simt_kernels.cu"],
     "flare_pp_fwd": ["tc_encoder.cuh", "tc_decode.cuh", "tc_ptx.cuh", "tc_kernels.cu"],
+    "decode_bwd": ["tc_decode_bwd.cuh", "tc_ptx.cuh", "tc_kernels.cu", "simt_decode_bwd.cu"],
 }
 
 
@@ -167,7 +169,8 @@ def weak_scaling_value(tokens_per_replica: int, world: int, ms_per_step: float) 
 def describe(w) -> str:
     what = {"flare_fwd": "FLARE fwd (encoder + merge + decode)",
             "flare_pp_fwd": "FLARE++ fwd (encoder x2 + decode)",
-            "encoder_bwd": "encoder bwd (dQ, dK, dV)"}[w.kind]
+            "encoder_bwd": "encoder bwd (dQ, dK, dV)",
+            "decode_bwd": "decode bwd (dQ, dZ, dK)"}[w.kind]
     extra = []
     if w.pad_frac:
         extra.append(f"{w.pad_frac:.0%} padded slots")
@@ -196,6 +199,8 @@ def algorithmic(w, elem):
         return {"encoder": (2 * tok, pass_flops), "decode": (2 * tok, pass_flops)}
     if w.kind == "flare_pp_fwd":
         return {"flare_pp_fwd": (6 * tok, 3 * pass_flops)}
+    if w.kind == "decode_bwd":      # K, dY read, dK written; five GEMM-shaped products
+        return {"decode_bwd": (3 * tok, 2.5 * pass_flops)}
     return {"encoder_bwd": (4 * tok, 2.5 * pass_flops)}
 
 
@@ -223,6 +228,13 @@ def cpu_oracle_sample(w, inputs, pairs=1):
         oracle.flare_pp_fwd(Qs, Kt, Vt, K, V, mask)
         dt = time.perf_counter() - t0
         what = "FLARE++ forward (two encodes + decode)"
+    elif w.kind == "decode_bwd":
+        Q, K, dY = inputs["Q"][hs].contiguous().cpu(), tok(inputs["K"]), tok(inputs["dY"])
+        Z = inputs["Z"][b:b + 1, hs].contiguous().cpu()
+        t0 = time.perf_counter()
+        oracle.decode_bwd(Q, Z, K, dY)
+        dt = time.perf_counter() - t0
+        what = "decode backward"
     else:
         Q, K, V = inputs["Q"][hs].contiguous().cpu(), tok(inputs["K"]), tok(inputs["V"])
         dZ = inputs["dZ"][b:b + 1, hs].contiguous().cpu()
@@ -283,14 +295,18 @@ class Step:
         Qref = inp["Qseed"] if w.kind == "flare_pp_fwd" else inp["Q"]
         dims = flare.make_dims(Qref, inp["K"], None, kernel)
         op = {"flare_fwd": flare.FLARE_OP_FWD, "flare_pp_fwd": flare.FLARE_OP_PP_FWD,
-              "encoder_bwd": flare.FLARE_OP_ENCODER_BWD}[w.kind]
-        nbytes = flare.flare_workspace_bytes(op, dims, self.off)
+              "encoder_bwd": flare.FLARE_OP_ENCODER_BWD,
+              "decode_bwd": flare.FLARE_OP_DECODE_BWD}[w.kind]
+        nbytes = flare.flare_workspace_bytes(op, dims, None if w.kind == "decode_bwd" else self.off)
         self.ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
         if w.kind == "flare_fwd":
             self.Y = torch.empty_like(inp["K"])
         elif w.kind == "flare_pp_fwd":
             self.Y = torch.empty_like(inp["K"])
             self.Qd, self.L1 = torch.empty((B, H, M, D), **f32), torch.empty((B, H, M), **f32)
+        elif w.kind == "decode_bwd":
+            self.dQ, self.dZ = torch.empty((B, H, M, D), **f32), torch.empty((B, H, M, D), **f32)
+            self.dK = torch.empty_like(inp["K"])
         else:
             self.dQ = torch.empty((B, H, M, D), **f32)
             self.dK, self.dV = torch.empty_like(inp["K"]), torch.empty_like(inp["V"])
@@ -328,6 +344,10 @@ class Step:
                         x["Qseed"], x["Kt"], x["Vt"], x["K"], x["V"], x["mask"], off, Y=self.Y,
                         Qdyn=self.Qd, L1=self.L1, Z=self.Z, L2=self.L, workspace=self.ws,
                         kernel=k, stream=st))]
+        if w.kind == "decode_bwd":
+            return [("decode_bwd", lambda: flare.flare_decode_bwd(
+                        x["Q"], x["Z"], x["K"], x["dY"], dQ=self.dQ, dZ=self.dZ, dK=self.dK,
+                        workspace=self.ws, kernel=k, stream=st))]
         return [("encoder_bwd", lambda: flare.flare_encoder_bwd(
                     x["Q"], x["K"], x["V"], x["mask"], off, x.get("Zs", self.Z),
                     x.get("Ls", self.L), x["dZ"], dQ=self.dQ, dK=self.dK, dV=self.dV,
@@ -340,6 +360,8 @@ class Step:
             return ["Q", "K", "V", "mask"], [self.Y]
         if self.w.kind == "flare_pp_fwd":
             return ["Qseed", "Kt", "Vt", "K", "V", "mask"], [self.Y]
+        if self.w.kind == "decode_bwd":
+            return ["Q", "Z", "K", "dY"], [self.dQ, self.dZ, self.dK]
         return ["Q", "K", "V", "mask", "Zs", "Ls", "dZ"], [self.dQ, self.dK, self.dV]
 
 

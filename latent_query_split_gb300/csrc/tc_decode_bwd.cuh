@@ -1,0 +1,508 @@
+// tc_decode_bwd.cuh -- FLARE decode backward on sm_103a tensor cores.
+//
+// The chain rule of the local decode (FLARE decode paragraph of "FLARE++:
+// Low-rank attention with dynamic attention routing", appendix on context
+// parallelism). For a (b, h), token n and latent m:
+//   A_nm = softmax_m(s <K_n, Q_m>),  g_nm = <dY_n, Z_m>,  r_n = sum_m A_nm g_nm,
+//   dT_nm = A_nm (g_nm - r_n),
+//   dK_n = s sum_m dT_nm Q_m,  dQ_m = s sum_n dT_nm K_n,  dZ_m = sum_n A_nm dY_n.
+//
+// Kernels (D = 64, M in {64, 128}):
+//  * dbw_prep_kernel: Z rounded to bf16 (an MMA operand).
+//  * dbw_tc_kernel: one persistent CTA per SM over a contiguous span of
+//    128-token tiles in (b, h, tile) order. Per tile, token rows in the TMEM
+//    lanes:
+//        S^T = K Q^T,  G^T = dY Z^T                 (A, B from shared memory)
+//        A, s dT from the row softmax (warps 2-9)   (fp32, bf16 operands out)
+//        dK = (s dT) Q                              (A = s dT in TMEM)
+//        dQ += (s dT)^T K,  dZ += A^T dY           (A from shared memory, MN-major)
+//    Eight warps form two latent halves of every token row; the halves
+//    exchange the row maximum, then their partial row sums and <A, g>. dK
+//    leaves through shared memory (one TMA store per 32 rows); dQ and dZ
+//    accumulate in TMEM over the (b, h)'s tiles of the span and are written
+//    as one fp32 piece per (b, h) of the span.
+//  * dbw_reduce_kernel: dQ and dZ = the sums of the pieces in piece order.
+// Warp roles: warp 0 TMA producer (K, dY ring; Q, Z on every (b, h) change),
+// warp 1 TMEM allocator and MMA issuer (lane 0), warps 2-9 the two halves.
+#pragma once
+
+#include "tc_backward.cuh"
+#include "tc_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace flare {
+namespace tc {
+
+struct DbwArgs {
+    int B, H, M, N;
+    float sl2;                  // s * log2(e)
+    float s;                    // score scale
+    int q_per_batch;            // Q has a batch dimension
+    float *part;                // [B*H][P_max][2][M][64]: dQ, then dZ pieces
+    int P_max;
+    int64_t T_bh, T_total;      // 128-token tiles per (b, h), and overall
+    int grid;
+    unsigned *status;
+};
+
+template <int M_, int STAGES_>
+struct DbwCfg {
+    static constexpr int M = M_, D = 64, TILE = 128, STAGES = STAGES_;
+    static constexpr int THREADS = 320;
+    static constexpr uint32_t TILE_BYTES = TILE * 128;     // 128 rows x 64 bf16 (swizzled)
+    static constexpr uint32_t QZ_BYTES = M * 128;          // [M][64] bf16 (swizzled)
+    static constexpr uint32_t Q_OFF = 0;
+    static constexpr uint32_t ZB_OFF = Q_OFF + QZ_BYTES;
+    static constexpr uint32_t STAGE_OFF = ZB_OFF + QZ_BYTES;
+    static constexpr uint32_t STAGE_BYTES = 2 * TILE_BYTES; // K tile, then dY tile
+    // A^T and s dT^T in bf16: token rows of 64-latent atoms (atom a at a * TILE_BYTES)
+    static constexpr uint32_t A_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
+    static constexpr uint32_t DT_OFF = A_OFF + 2 * TILE_BYTES;
+    static constexpr uint32_t OUT_OFF = DT_OFF + 2 * TILE_BYTES;   // dK staging (4 slabs)
+    // row statistics exchanged between the halves: [2 parity][2 half][128]
+    static constexpr uint32_t XM_OFF = OUT_OFF + TILE_BYTES;        // float: maxima
+    static constexpr uint32_t XL_OFF = XM_OFF + 2 * 2 * 128 * 4;    // float2: (sum, <p, g>)
+    static constexpr uint32_t BAR_OFF = XL_OFF + 2 * 2 * 128 * 8;
+    // full[S], empty[S], qz_full, qz_free, s_full, p_full, at_free, dk_full,
+    // dk_free, pz_full, pz_free, drain
+    static constexpr int NBAR = 2 * STAGES + 10;
+    static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr uint32_t BYTES = MISC_OFF + 64;
+    static constexpr uint32_t ALLOC = BYTES + 1024;
+    static_assert(ALLOC <= 232448, "shared memory budget of one CTA exceeded");
+    static_assert(QZ_BYTES % 1024 == 0, "operand tiles must stay 1 KB aligned");
+    // tensor memory columns
+    static constexpr uint32_t S_COL = 0, G_COL = 128, DK_COL = 256, DQ_COL = 320, DZ_COL = 384;
+    static constexpr uint32_t TMEM_COLS = 512;
+};
+
+// Z rounded to bf16, two elements per thread.
+__global__ void __launch_bounds__(256) dbw_prep_kernel(const float *__restrict__ Z,
+                                                       __nv_bfloat16 *__restrict__ Zb, int64_t n2) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n2) return;
+    const float2 z = reinterpret_cast<const float2 *>(Z)[i];
+    reinterpret_cast<uint32_t *>(Zb)[i] = pack_bf16(z.x, z.y);
+}
+
+// dQ (which = 0) and dZ (which = 1) = the sums of the pieces of each (b, h).
+__global__ void __launch_bounds__(256) dbw_reduce_kernel(const float *__restrict__ part,
+                                                         float *__restrict__ dQ, float *__restrict__ dZ,
+                                                         int64_t BH, int M, int P_max, int64_t T_bh,
+                                                         int64_t T_total, int grid) {
+    const int64_t per = (int64_t)M * 16;                    // float4s of one (b, h) tensor
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= 2 * BH * per) return;
+    const int which = (int)(i / (BH * per));
+    const int64_t rest = i - which * BH * per;
+    const int64_t bh = rest / per, rem = rest - bh * per;
+    const int c0 = bwd_cta_of(bh * T_bh, T_total, grid);
+    const int np = bwd_cta_of(bh * T_bh + T_bh - 1, T_total, grid) - c0 + 1;
+    const float4 *src = reinterpret_cast<const float4 *>(part) + (bh * P_max * 2 + which) * per + rem;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p = 0; p < np; ++p) {
+        const float4 v = __ldcg(src + p * 2 * per);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+    }
+    reinterpret_cast<float4 *>(which ? dZ : dQ)[bh * per + rem] = acc;
+}
+
+template <int M, int STAGES>
+__global__ void __launch_bounds__(DbwCfg<M, STAGES>::THREADS, 1)
+dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmdY,
+              const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmZ,
+              const __grid_constant__ CUtensorMap tmdK, const DbwArgs a) {
+    using C = DbwCfg<M, STAGES>;
+    constexpr uint32_t TB = C::TILE_BYTES;
+    constexpr int W = M / 2;                                   // latents of each half
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + C::Q_OFF, sZ = sbase + C::ZB_OFF, sStage = sbase + C::STAGE_OFF;
+    const uint32_t sA = sbase + C::A_OFF, sDT = sbase + C::DT_OFF;
+    const uint32_t bar0 = sbase + C::BAR_OFF;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    const uint32_t qz_full = bar0 + 8u * (2 * STAGES), qz_free = qz_full + 8;
+    const uint32_t s_full = qz_full + 16, p_full = qz_full + 24, at_free = qz_full + 32;
+    const uint32_t dk_full = qz_full + 40, dk_free = qz_full + 48;
+    const uint32_t pz_full = qz_full + 56, pz_free = qz_full + 64, drain = qz_full + 72;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const int64_t tb = ((int64_t)cta * a.T_total + a.grid - 1) / a.grid;
+    const int64_t te = ((int64_t)(cta + 1) * a.T_total + a.grid - 1) / a.grid;
+    const int64_t ntiles = te - tb;
+    const int64_t bh0 = tb / a.T_bh, k0 = tb - bh0 * a.T_bh;
+    Waiter wt{abort_flag, a.status};
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(qz_full, 1);
+        mbar_init(qz_free, 1);
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 8);          // one arrival per softmax warp
+        mbar_init(at_free, 1);
+        mbar_init(dk_full, 1);
+        mbar_init(dk_free, 8);
+        mbar_init(pz_full, 1);
+        mbar_init(pz_free, 8);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmdY);
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmZ);
+        prefetch_tmap(&tmdK);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (M < 128 && warp >= 2) {
+        // latents M..127 of A^T and dT^T stay zero: the dQ and dZ MMAs span 128 rows
+        for (int q = threadIdx.x - 64; q < (int)TB / 16; q += 256) {
+            reinterpret_cast<uint4 *>(smem + C::A_OFF + TB)[q] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4 *>(smem + C::DT_OFF + TB)[q] = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        const uint64_t pol = policy_evict_first();
+        int64_t bh = bh0, kt = k0, cur = -1;
+        int b = (int)(bh0 / a.H), h = (int)(bh0 - (int64_t)b * a.H);   // (b, h) of tile j
+        int u = -1;
+        int64_t j = 0;
+        for (; j < ntiles && !wt.aborted(); ++j) {
+            if (bh != cur) {
+                ++u;
+                cur = bh;
+                // Q and Z of the previous (b, h) are no longer read
+                if (u > 0 && !__all_sync(0xffffffffu, wt.wait(qz_free, (uint32_t)(u - 1) & 1))) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(qz_full, 2 * C::QZ_BYTES);
+                    tma_load_4d(sQ, &tmQ, 0, 0, h, a.q_per_batch ? b : 0, qz_full);
+                    tma_load_4d(sZ, &tmZ, 0, 0, h, b, qz_full);
+                }
+                __syncwarp();
+            }
+            const int s = (int)(j % STAGES);
+            if (!__all_sync(0xffffffffu, wt.wait(empty(s), ((uint32_t)(j / STAGES) & 1) ^ 1))) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full(s), C::STAGE_BYTES);
+                const uint32_t dst = sStage + s * C::STAGE_BYTES;
+                tma_load_4d_hint(dst, &tmK, 0, h, (int)(kt * 128), b, full(s), pol);
+                tma_load_4d_hint(dst + TB, &tmdY, 0, h, (int)(kt * 128), b, full(s), pol);
+            }
+            __syncwarp();
+            if (++kt == a.T_bh) {
+                kt = 0;
+                ++bh;
+                if (++h == a.H) {
+                    h = 0;
+                    ++b;
+                }
+            }
+        }
+        if (wt.aborted() && lane == 0) {
+            // let every issued load land before the CTA exits
+            const uint64_t t0 = globaltimer();
+            for (int64_t jj = (j > STAGES ? j - STAGES : 0); jj < j; ++jj)
+                while (!mbar_try_wait(full((int)(jj % STAGES)), (uint32_t)(jj / STAGES) & 1) &&
+                       globaltimer() - t0 < 500000000ull) {
+                }
+            if (u >= 0)
+                while (!mbar_try_wait(qz_full, (uint32_t)u & 1) && globaltimer() - t0 < 500000000ull) {
+                }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (lane 0) ----------------
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16(128, M, 0, 0);
+            constexpr uint32_t idG = idesc_bf16(128, 64, 0, 1);    // dK: A in TMEM, B MN-major
+            constexpr uint32_t idR = idesc_bf16(128, 64, 1, 1);    // dQ, dZ: A, B MN-major
+            const uint64_t dQk = desc_sw128(sQ, 16, 1024);          // Q, K-major (B of S^T)
+            const uint64_t dZk = desc_sw128(sZ, 16, 1024);          // Z, K-major (B of G^T)
+            const uint64_t dQm = desc_sw128(sQ, TB, 1024);          // Q, MN-major (B of dK)
+            const uint64_t dAm = desc_sw128(sA, TB, 1024);          // A^T, MN-major (A of dZ)
+            const uint64_t dDTm = desc_sw128(sDT, TB, 1024);        // s dT^T, MN-major (A of dQ)
+            int64_t bhS = bh0, ktS = k0, curS = -1;
+            int uS = -1;
+            bool ok = true;
+            auto issue_sg = [&](int64_t jj) -> bool {
+                if (bhS != curS) {
+                    ++uS;
+                    curS = bhS;
+                    if (!wt.wait(qz_full, (uint32_t)uS & 1)) return false;
+                }
+                const int s = (int)(jj % STAGES);
+                if (!wt.wait(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
+                tc_fence_after();
+                const uint64_t dK = desc_sw128(sStage + s * C::STAGE_BYTES, 16, 1024);
+                const uint64_t dY = desc_sw128(sStage + s * C::STAGE_BYTES + TB, 16, 1024);
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb)
+                    umma_bf16_ss(tmem + C::S_COL, dK + 2 * kb, dQk + 2 * kb, idS, kb > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb)
+                    umma_bf16_ss(tmem + C::G_COL, dY + 2 * kb, dZk + 2 * kb, idS, kb > 0 ? 1u : 0u);
+                umma_commit(s_full);
+                if (++ktS == a.T_bh) {
+                    ktS = 0;
+                    ++bhS;
+                }
+                return true;
+            };
+            // s dT of half h's latents sits (bf16 pairs) from column h * M/2 of S
+            auto pcol = [](int kb) -> uint32_t {
+                const int half = 16 * kb / W;
+                return (uint32_t)(W * half + 8 * (kb - half * (W / 16)));
+            };
+            int64_t bhP = bh0, ktP = k0;
+            int uP = 0;
+            if (ntiles > 0) ok = issue_sg(0);
+            for (int64_t j = 0; j < ntiles && ok; ++j) {
+                const bool first = (j == 0) || ktP == 0;
+                int64_t bhN = bhP, ktN = ktP + 1;
+                if (ktN == a.T_bh) {
+                    ktN = 0;
+                    ++bhN;
+                }
+                const bool last = (j + 1 == ntiles) || bhN != bhP;
+                if (!(ok = wt.wait(p_full, (uint32_t)j & 1))) break;
+                tc_fence_after();
+                if (j > 0 && !(ok = wt.wait(dk_free, (uint32_t)(j - 1) & 1))) break;
+                tc_fence_after();
+                // dK = (s dT) Q: K = M latents, 16 per MMA
+#pragma unroll
+                for (int kb = 0; kb < M / 16; ++kb)
+                    umma_bf16_ts(tmem + C::DK_COL, tmem + C::S_COL + pcol(kb), dQm + kb * (2048 >> 4), idG,
+                                 kb > 0 ? 1u : 0u);
+                umma_commit(dk_full);
+                if (last) umma_commit(qz_free);
+                // the next tile's scores overwrite dT in TMEM (MMAs run in issue order)
+                if (j + 1 < ntiles && !(ok = issue_sg(j + 1))) break;
+                // dQ += (s dT)^T K, dZ += A^T dY over the tile's 128 tokens
+                if (first && uP > 0 && !(ok = wt.wait(pz_free, (uint32_t)(uP - 1) & 1))) break;
+                tc_fence_after();
+                const int s = (int)(j % STAGES);
+                const uint64_t dKm = desc_sw128(sStage + s * C::STAGE_BYTES, TB, 1024);
+                const uint64_t dYm = desc_sw128(sStage + s * C::STAGE_BYTES + TB, TB, 1024);
+#pragma unroll
+                for (int kb = 0; kb < 8; ++kb)
+                    umma_bf16_ss(tmem + C::DQ_COL, dDTm + kb * (2048 >> 4), dKm + kb * (2048 >> 4), idR,
+                                 (kb > 0 || !first) ? 1u : 0u);
+#pragma unroll
+                for (int kb = 0; kb < 8; ++kb)
+                    umma_bf16_ss(tmem + C::DZ_COL, dAm + kb * (2048 >> 4), dYm + kb * (2048 >> 4), idR,
+                                 (kb > 0 || !first) ? 1u : 0u);
+                umma_commit(at_free);
+                umma_commit(empty(s));
+                if (last) {
+                    umma_commit(pz_full);
+                    ++uP;
+                }
+                bhP = bhN;
+                ktP = ktN;
+            }
+            if (wt.aborted()) {
+                umma_commit(drain);
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < 500000000ull) {
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- the two latent halves (warps 2-9) ----------------
+        const int hf = (warp - 2) >> 2;                       // latent half
+        const int quad = warp & 3;
+        const int rig = quad * 32 + lane;                     // token row within the tile
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const uint32_t s_tm = tmem + C::S_COL + W * hf + lane_off;
+        const uint32_t g_tm = tmem + C::G_COL + W * hf + lane_off;
+        const float sl2 = a.sl2, sc = a.s;
+        float *xm = reinterpret_cast<float *>(smem + C::XM_OFF);
+        float2 *xl = reinterpret_cast<float2 *>(smem + C::XL_OFF);
+        uint8_t *slab = smem + C::OUT_OFF + quad * (32 * 128);   // the quadrant's 32 dK rows
+        const bool storer = hf == 0 && lane == 0;
+        const int pair_bar = 1 + quad;                         // named barrier of the quadrant
+        auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
+            return __all_sync(0xffffffffu, wt.wait(bar, par));
+        };
+        int64_t bh = bh0, kt = k0;
+        int b = (int)(bh0 / a.H), h = (int)(bh0 - (int64_t)b * a.H);
+        int pieces = 0;
+        uint32_t stores = 0;
+        for (int64_t j = 0; j < ntiles; ++j) {
+            int64_t bhN = bh, ktN = kt + 1;
+            int bN = b, hN = h;
+            if (ktN == a.T_bh) {
+                ktN = 0;
+                ++bhN;
+                if (++hN == a.H) {
+                    hN = 0;
+                    ++bN;
+                }
+            }
+            const bool last = (j + 1 == ntiles) || bhN != bh;
+            const int64_t n = kt * 128 + rig;
+            const bool valid = n < a.N;
+            if (!wwait(s_full, (uint32_t)j & 1)) break;
+            tc_fence_after();
+            // this half's scores: the maximum, exchanged with the other half
+            uint32_t sv[W / 32][32];
+#pragma unroll
+            for (int c = 0; c < W / 32; ++c) tmem_ld32(s_tm + 32 * c, sv[c]);
+            tmem_wait_ld();
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < W / 32; ++c)
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    mx = max3(mx, __uint_as_float(sv[c][2 * i]), __uint_as_float(sv[c][2 * i + 1]));
+            const int par = (int)(j & 1);
+            xm[(par * 2 + hf) * 128 + rig] = mx;
+            named_bar_sync(pair_bar, 64);
+            const float m2 = fmaxf(mx, xm[(par * 2 + (hf ^ 1)) * 128 + rig]) * sl2;
+            // p = 2^(s t log2 e - max), the half's partial sum and <p, g>
+            uint32_t gv[W / 32][32];
+#pragma unroll
+            for (int c = 0; c < W / 32; ++c) tmem_ld32(g_tm + 32 * c, gv[c]);
+            tmem_wait_ld();
+            float ls = 0.f, lr = 0.f;
+#pragma unroll
+            for (int c = 0; c < W / 32; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p = ex2(fmaf(__uint_as_float(sv[c][i]), sl2, -m2));
+                    sv[c][i] = __float_as_uint(p);
+                    ls += p;
+                    lr = fmaf(p, __uint_as_float(gv[c][i]), lr);
+                }
+            xl[(par * 2 + hf) * 128 + rig] = make_float2(ls, lr);
+            named_bar_sync(pair_bar, 64);
+            const float2 o = xl[(par * 2 + (hf ^ 1)) * 128 + rig];
+            const float inv = valid ? 1.f / (ls + o.x) : 0.f;      // tokens past N: A = 0
+            const float r = (lr + o.y) / (ls + o.x);
+            // A and s dT in bf16: dT over this half's TMEM columns, both into
+            // the MN-major operands of dQ and dZ (after the last tile's
+            // products have read them)
+            if (j > 0 && !wwait(at_free, (uint32_t)(j - 1) & 1)) break;
+#pragma unroll
+            for (int c = 0; c < W / 32; ++c) {
+                uint32_t aw[16], tw[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float a0 = __uint_as_float(sv[c][2 * i]) * inv;
+                    const float a1 = __uint_as_float(sv[c][2 * i + 1]) * inv;
+                    const float t0 = sc * a0 * (__uint_as_float(gv[c][2 * i]) - r);
+                    const float t1 = sc * a1 * (__uint_as_float(gv[c][2 * i + 1]) - r);
+                    aw[i] = pack_bf16(a0, a1);
+                    tw[i] = pack_bf16(t0, t1);
+                }
+                tmem_st16(s_tm + 16 * c, tw);
+                const int m0 = W * hf + 32 * c;
+                uint8_t *arow = smem + C::A_OFF + (m0 >> 6) * TB + rig * 128;
+                uint8_t *trow = smem + C::DT_OFF + (m0 >> 6) * TB + rig * 128;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int pos = ((((m0 & 63) >> 3) + q) ^ (rig & 7)) << 4;
+                    *reinterpret_cast<uint4 *>(arow + pos) = make_uint4(aw[4 * q], aw[4 * q + 1], aw[4 * q + 2], aw[4 * q + 3]);
+                    *reinterpret_cast<uint4 *>(trow + pos) = make_uint4(tw[4 * q], tw[4 * q + 1], tw[4 * q + 2], tw[4 * q + 3]);
+                }
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+            // epilogue: dK of the quadrant's 32 rows, half hf converts columns [32 hf, 32 hf + 32)
+            if (!wwait(dk_full, (uint32_t)j & 1)) break;
+            tc_fence_after();
+            uint32_t rk[32];
+            tmem_ld32(tmem + C::DK_COL + 32 * hf + lane_off, rk);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dk_free);
+            if (stores > 0 && storer) bulk_wait_group_read0();    // the slab's last store has read it
+            named_bar_sync(pair_bar, 64);
+            uint8_t *srow = slab + lane * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t *k8 = rk + 8 * q;
+                *reinterpret_cast<uint4 *>(srow + (((4 * hf + q) ^ (lane & 7)) << 4)) = make_uint4(
+                    pack_bf16(__uint_as_float(k8[0]), __uint_as_float(k8[1])),
+                    pack_bf16(__uint_as_float(k8[2]), __uint_as_float(k8[3])),
+                    pack_bf16(__uint_as_float(k8[4]), __uint_as_float(k8[5])),
+                    pack_bf16(__uint_as_float(k8[6]), __uint_as_float(k8[7])));
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(pair_bar, 64);
+            const int n0 = (int)(kt * 128) + quad * 32;
+            if (storer && n0 < a.N) {
+                // rows past N are clipped by the tensor map
+                tma_store_4d(&tmdK, smem_u32(slab), 0, h, n0, b);
+                bulk_commit_group();
+            }
+            ++stores;
+            if (last) {
+                // the (b, h)'s dQ (half 0) and dZ (half 1) pieces of this span,
+                // latent rows in the lanes
+                if (!wwait(pz_full, (uint32_t)pieces & 1)) break;
+                tc_fence_after();
+                uint32_t rq[2][32];
+                tmem_ld32(tmem + (hf ? C::DZ_COL : C::DQ_COL) + lane_off, rq[0]);
+                tmem_ld32(tmem + (hf ? C::DZ_COL : C::DQ_COL) + 32 + lane_off, rq[1]);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pz_free);
+                if (rig < M) {
+                    const int piece = cta - bwd_cta_of(bh * a.T_bh, a.T_total, a.grid);
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        a.part + (((bh * a.P_max + piece) * 2 + hf) * M + rig) * 64);
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[8 * h2 + q] = make_float4(
+                                __uint_as_float(rq[h2][4 * q]), __uint_as_float(rq[h2][4 * q + 1]),
+                                __uint_as_float(rq[h2][4 * q + 2]), __uint_as_float(rq[h2][4 * q + 3]));
+                }
+                ++pieces;
+            }
+            bh = bhN;
+            kt = ktN;
+            b = bN;
+            h = hN;
+        }
+        if (storer) bulk_wait_group0();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+}  // namespace tc
+}  // namespace flare

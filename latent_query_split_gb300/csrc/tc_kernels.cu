@@ -4,6 +4,7 @@
 #include "tc_encoder.cuh"
 #include "tc_decode.cuh"
 #include "tc_backward.cuh"
+#include "tc_decode_bwd.cuh"
 
 #include <cudaTypedefs.h>
 
@@ -343,14 +344,102 @@ cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *
     return cudaGetLastError();
 }
 
-// The tensor-core decode backward is not built yet: the CUDA-core kernels
-// serve every shape.
-bool tc_decode_bwd_supported(bool, int, int) { return false; }
-size_t tc_decode_bwd_workspace(const Problem &, int) { return 0; }
-cudaError_t launch_decode_bwd_tc(const Problem &, const void *, const float *, const void *,
-                                 const void *, float *, float *, void *, void *, size_t, int,
-                                 unsigned *, cudaStream_t) {
-    return cudaErrorNotSupported;
+bool tc_decode_bwd_supported(bool bf16, int M, int D) { return bf16 && D == 64 && (M == 64 || M == 128); }
+
+namespace {
+// Decode-backward workspace: Z in bf16 [B*H*M*64] and the dQ/dZ pieces
+// [B*H][P_max][2][M][64]; tiles and spans as for the encoder backward.
+struct DbwLayout {
+    int64_t T_bh, T_total;
+    int grid, P_max;
+    size_t zb, part, bytes;
+};
+
+void dbw_layout(const Problem &pr, int sms, DbwLayout &l) {
+    l.T_bh = (pr.N + 127) / 128;
+    l.T_total = (int64_t)pr.B * pr.H * l.T_bh;
+    l.grid = (int)(l.T_total < sms ? l.T_total : sms);
+    if (l.grid < 1) l.grid = 1;
+    const int64_t span_min = l.T_total > 0 ? l.T_total / l.grid : 1;
+    l.P_max = l.T_bh > 0 ? (int)((l.T_bh + span_min - 1) / span_min) + 1 : 1;
+    const size_t bhm = (size_t)pr.B * pr.H * pr.M;
+    size_t o = 0;
+    l.zb = o;
+    o += align256(2 * bhm * 64);
+    l.part = o;
+    o += align256(4 * bhm * (size_t)l.P_max * 2 * 64);
+    l.bytes = o;
+}
+
+template <int M>
+cudaError_t launch_dbw(const CUtensorMap *maps, const tc::DbwArgs &a, cudaStream_t st) {
+    using C = tc::DbwCfg<M, 3>;
+    auto k = tc::dbw_tc_kernel<M, 3>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
+    if (e != cudaSuccess) return e;
+    k<<<a.grid, C::THREADS, C::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a);
+    note_launch();
+    return cudaGetLastError();
+}
+}  // namespace
+
+size_t tc_decode_bwd_workspace(const Problem &pr, int sms) {
+    if (!tc_decode_bwd_supported(pr.bf16, pr.M, pr.D)) return 0;
+    DbwLayout l;
+    dbw_layout(pr, sms, l);
+    return l.bytes;
+}
+
+cudaError_t launch_decode_bwd_tc(const Problem &pr, const void *Q, const float *Z, const void *K,
+                                 const void *dY, float *dQ, float *dZ, void *dK, void *ws,
+                                 size_t ws_bytes, int sms, unsigned *status, cudaStream_t st) {
+    if (!tc_decode_bwd_supported(pr.bf16, pr.M, pr.D)) return cudaErrorNotSupported;
+    DbwLayout l;
+    dbw_layout(pr, sms, l);
+    if (ws_bytes < l.bytes) return cudaErrorInvalidValue;
+    const int64_t BH = (int64_t)pr.B * pr.H;
+    if (BH == 0) return cudaSuccess;
+    if (l.T_total == 0) {           // no token: dQ = dZ = 0, no dK
+        cudaError_t e = cudaMemsetAsync(dQ, 0, sizeof(float) * (size_t)BH * pr.M * pr.D, st);
+        return e != cudaSuccess ? e : cudaMemsetAsync(dZ, 0, sizeof(float) * (size_t)BH * pr.M * pr.D, st);
+    }
+    char *w = (char *)ws;
+    __nv_bfloat16 *zb = (__nv_bfloat16 *)(w + l.zb);
+    float *part = (float *)(w + l.part);
+    const int64_t n2 = BH * pr.M * 32;
+    tc::dbw_prep_kernel<<<(unsigned)((n2 + 255) / 256), 256, 0, st>>>(Z, zb, n2);
+    note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t qb = pr.q_bstride == 0 ? 1 : pr.B;
+    CUtensorMap maps[5];
+    if (!make_map(&maps[0], K, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
+        !make_map(&maps[1], dY, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
+        !make_map(&maps[2], Q, pr.D, pr.M, pr.H, qb, (uint32_t)pr.M, 1) ||
+        !make_map(&maps[3], zb, pr.D, pr.M, pr.H, pr.B, (uint32_t)pr.M, 1) ||
+        !make_map(&maps[4], dK, pr.D, pr.H, pr.N, pr.B, 1, 32))
+        return cudaErrorInvalidValue;
+    tc::DbwArgs a;
+    a.B = pr.B;
+    a.H = pr.H;
+    a.M = pr.M;
+    a.N = pr.N;
+    a.s = pr.scale;
+    a.sl2 = pr.scale * 1.4426950408889634f;
+    a.q_per_batch = pr.q_bstride != 0;
+    a.part = part;
+    a.P_max = l.P_max;
+    a.T_bh = l.T_bh;
+    a.T_total = l.T_total;
+    a.grid = l.grid;
+    a.status = status;
+    e = pr.M == 128 ? launch_dbw<128>(maps, a, st) : launch_dbw<64>(maps, a, st);
+    if (e != cudaSuccess) return e;
+    const int64_t n4 = 2 * BH * pr.M * 16;
+    tc::dbw_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(part, dQ, dZ, BH, pr.M, l.P_max,
+                                                                       l.T_bh, l.T_total, l.grid);
+    note_launch();
+    return cudaGetLastError();
 }
 
 }  // namespace flare

@@ -9,7 +9,7 @@ routing" (context-parallel section): token tensors [B, N, H, D] (C = H*D
 channels of the per-token projections), the replicated latent queries or seeds
 [H, M, D], R token shards with unequal sizes and padding excluded by a mask.
 
-The five named workloads:
+The six named workloads:
   c1_fp32_small  FLARE fwd fp32, B1 H2 D32 M16 N1024, R4 equal shards, N(0,1)
   c2_bf16        FLARE fwd bf16, B4 H8 D64 M128 N65536, R8 shards of length
                  ~U[0.5,1.5]*N/R summing to N, 5% padded slots; K,V ~ N(0,1),
@@ -20,6 +20,8 @@ The five named workloads:
                  have their whole key (all heads) scaled by 8
   c5_bwd_bf16    encoder bwd bf16, B2 H8 D64 M128 N131072, R8 with shards 2
                  and 5 empty, shard 3 of batch element 1 all padding; dZ ~ N(0,1)
+  c5_decbwd_bf16 decode bwd bf16 on the shapes of c5_bwd_bf16 (no mask: the
+                 decode has none); Z, dY ~ N(0,1)
 N(0, sigma) is read with sigma the standard deviation.
 """
 from __future__ import annotations
@@ -35,7 +37,7 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str            # "flare_fwd" | "flare_pp_fwd" | "encoder_bwd"
+    kind: str            # "flare_fwd" | "flare_pp_fwd" | "encoder_bwd" | "decode_bwd"
     dtype: str           # "f32" | "bf16"
     B: int
     H: int
@@ -74,6 +76,8 @@ CONFIGS: Dict[str, Workload] = {
     "c5_bwd_bf16": Workload("c5_bwd_bf16", "encoder_bwd", "bf16", B=2, H=8, M=128,
                             N=131072, D=64, R=8, seed=1005, empty_shards=(2, 5),
                             padded_shard=(1, 3)),
+    "c5_decbwd_bf16": Workload("c5_decbwd_bf16", "decode_bwd", "bf16", B=2, H=8, M=128,
+                               N=131072, D=64, R=8, seed=1006),
 }
 
 
@@ -124,7 +128,8 @@ def make_inputs(w: Workload, device="cpu") -> dict:
     Returns a dict with the token tensors ("K", "V", and "Kt", "Vt" for
     FLARE++), the latent query ("Q", or "Qseed"), host "offsets" (list of R+1
     ints), "mask" (uint8 [B,N] tensor on `device`, or None), "scale" (None =
-    D^-1/2) and "dZ" for the backward.
+    D^-1/2), "dZ" for the encoder backward, and "Z" (fp32 [B,H,M,D]) and "dY"
+    (token-shaped) for the decode backward.
     """
     rng = np.random.default_rng(w.seed)
     offsets = shard_offsets(w.N, w.R, rng, equal=w.equal_shards, empty=w.empty_shards)
@@ -162,6 +167,10 @@ def make_inputs(w: Workload, device="cpu") -> dict:
     if w.kind == "encoder_bwd":
         out["dZ"] = torch.randn((w.B, w.H, w.M, w.D), generator=g, device=dev,
                                 dtype=torch.float32)
+    if w.kind == "decode_bwd":
+        out["Z"] = torch.randn((w.B, w.H, w.M, w.D), generator=g, device=dev,
+                               dtype=torch.float32)
+        out["dY"] = normal(tok)
     out["boosted_tokens"] = boosted
     return out
 

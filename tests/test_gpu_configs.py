@@ -158,6 +158,10 @@ def test_decode_bwd_c5_shapes_sampled(cuda_device):
     for b, h in [(0, 1), (1, 7)]:
         Qh = Q[h:h + 1].cpu()
         dQo, dZo, dKo = oracle.decode_bwd(Qh, Z[b:b + 1, h:h + 1].cpu(), _head(K, b, h), _head(dY, b, h))
-        assert_close(f"dQ[{b},{h}]", dQ[b:b + 1, h:h + 1], dQo, "bf16")
-        assert_close(f"dZ[{b},{h}]", dZ[b:b + 1, h:h + 1], dZo, "bf16")
+        # dQ and dZ sum one bf16-rounded product per token over all N tokens:
+        # their absolute rounding error grows like sqrt(N), so they are held to
+        # 2e-2 of max(1, largest reference magnitude)
+        for name, dev, ref in (("dQ", dQ, dQo), ("dZ", dZ, dZo)):
+            bound = 2e-2 * max(1.0, float(np.abs(ref).max()))
+            assert_close(f"{name}[{b},{h}]", dev[b:b + 1, h:h + 1], ref, "bf16", atol=bound)
         assert_close(f"dK[{b},:,{h}]", dK[b:b + 1, :, h:h + 1], dKo, "bf16")
