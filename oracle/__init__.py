@@ -247,3 +247,30 @@ def decode_bwd(Q, Z, K, dY, scale=None):
     _load().oracle_decode_bwd(B, H, M, N, D, s, qbs, _ptr(q), qt, _ptr(z), _ptr(k), kt,
                               _ptr(y), yt, _ptr(dQ), _ptr(dZ), _ptr(dK))
     return dQ, dZ, dK
+
+
+def flare_bwd(Q, K, V, mask, Z, L, dY, scale=None):
+    """FLARE mixer backward (backward paragraphs of the appendix): the
+    gradient of the replicated Z is first summed over its consumers -- in the
+    mixer only the decode -- and then the encoder is differentiated with the
+    forward's global (Z, L). Q is both the encoder's latent query and the
+    decode's latent key, K both the encoder's key and the decode's token
+    query, so their gradients add. Returns dQ [B,H,M,D] (per batch element),
+    dK, dV [B,N,H,D]."""
+    dQ_dec, dZ, dK_dec = decode_bwd(Q, Z, K, dY, scale)
+    dQ_enc, dK_enc, dV = encode_bwd(Q, K, V, mask, Z, L, dZ, scale)
+    return dQ_dec + dQ_enc, dK_dec + dK_enc, dV
+
+
+def flare_pp_bwd(Qseed, Kt, Vt, K, V, mask, Qdyn, L1, Z, L2, dY, scale=None):
+    """FLARE++ mixer backward (FLARE++ backward paragraph of the appendix):
+    the decode with Q(X) gives its shares of dQ(X), dZ and dK; the
+    physical-value encoder (saved Z, L2) adds its shares of dQ(X) and dK and
+    gives dV; the summed dQ(X) is the output gradient of the query-synthesis
+    encoder, differentiated with its own saved output Q(X) and L1. Returns
+    dQseed [B,H,M,D] (per batch element), dKt, dVt, dK, dV, dQdyn."""
+    dQX_dec, dZ, dK_dec = decode_bwd(Qdyn, Z, K, dY, scale)
+    dQX_enc, dK_enc, dV = encode_bwd(Qdyn, K, V, mask, Z, L2, dZ, scale)
+    dQX = dQX_dec + dQX_enc
+    dQs, dKt, dVt = encode_bwd(Qseed, Kt, Vt, mask, Qdyn, L1, dQX, scale)
+    return dQs, dKt, dVt, dK_dec + dK_enc, dV, dQX
