@@ -48,6 +48,10 @@ KERNEL_SOURCES = {
     "encoder_bwd": ["tc_backward.cuh", "tc_ptx.cuh", "tc_kernels.cu", "simt_kernels.cu"],
     "flare_pp_fwd": ["tc_encoder.cuh", "tc_decode.cuh", "tc_ptx.cuh", "tc_kernels.cu"],
     "decode_bwd": ["tc_decode_bwd.cuh", "tc_ptx.cuh", "tc_kernels.cu", "simt_decode_bwd.cu"],
+    "flare_bwd": ["tc_decode_bwd.cuh", "tc_backward.cuh", "tc_ptx.cuh", "tc_kernels.cu",
+                  "simt_decode_bwd.cu", "simt_kernels.cu", "flare_api.cu"],
+    "flare_pp_bwd": ["tc_decode_bwd.cuh", "tc_backward.cuh", "tc_ptx.cuh", "tc_kernels.cu",
+                     "simt_decode_bwd.cu", "simt_kernels.cu", "flare_api.cu"],
 }
 
 
@@ -170,7 +174,9 @@ def describe(w) -> str:
     what = {"flare_fwd": "FLARE fwd (encoder + merge + decode)",
             "flare_pp_fwd": "FLARE++ fwd (encoder x2 + decode)",
             "encoder_bwd": "encoder bwd (dQ, dK, dV)",
-            "decode_bwd": "decode bwd (dQ, dZ, dK)"}[w.kind]
+            "decode_bwd": "decode bwd (dQ, dZ, dK)",
+            "flare_bwd": "FLARE mixer bwd (decode bwd + encoder bwd; dQ, dK, dV)",
+            "flare_pp_bwd": "FLARE++ mixer bwd (decode bwd + two encoder bwd)"}[w.kind]
     extra = []
     if w.pad_frac:
         extra.append(f"{w.pad_frac:.0%} padded slots")
@@ -201,6 +207,10 @@ def algorithmic(w, elem):
         return {"flare_pp_fwd": (6 * tok, 3 * pass_flops)}
     if w.kind == "decode_bwd":      # K, dY read, dK written; five GEMM-shaped products
         return {"decode_bwd": (3 * tok, 2.5 * pass_flops)}
+    if w.kind == "flare_bwd":       # decode bwd, then encoder bwd reading the old dK too
+        return {"flare_bwd": (8 * tok, 5 * pass_flops)}
+    if w.kind == "flare_pp_bwd":    # ... plus the query-synthesis encoder bwd
+        return {"flare_pp_bwd": (12 * tok, 7.5 * pass_flops)}
     return {"encoder_bwd": (4 * tok, 2.5 * pass_flops)}
 
 
@@ -235,6 +245,22 @@ def cpu_oracle_sample(w, inputs, pairs=1):
         oracle.decode_bwd(Q, Z, K, dY)
         dt = time.perf_counter() - t0
         what = "decode backward"
+    elif w.kind == "flare_bwd":
+        Q, K, V, dY = (inputs["Q"][hs].contiguous().cpu(), tok(inputs["K"]), tok(inputs["V"]),
+                       tok(inputs["dY"]))
+        Z, L = oracle.encode(Q, K, V, mask)        # forward statistics, not timed
+        t0 = time.perf_counter()
+        oracle.flare_bwd(Q, K, V, mask, Z, L, dY)
+        dt = time.perf_counter() - t0
+        what = "FLARE mixer backward"
+    elif w.kind == "flare_pp_bwd":
+        Qs = inputs["Qseed"][hs].contiguous().cpu()
+        Kt, Vt, K, V, dY = (tok(inputs[k]) for k in ("Kt", "Vt", "K", "V", "dY"))
+        Qd, L1, Z, L2, _ = oracle.flare_pp_fwd(Qs, Kt, Vt, K, V, mask)   # not timed
+        t0 = time.perf_counter()
+        oracle.flare_pp_bwd(Qs, Kt, Vt, K, V, mask, Qd, L1, Z, L2, dY)
+        dt = time.perf_counter() - t0
+        what = "FLARE++ mixer backward"
     else:
         Q, K, V = inputs["Q"][hs].contiguous().cpu(), tok(inputs["K"]), tok(inputs["V"])
         dZ = inputs["dZ"][b:b + 1, hs].contiguous().cpu()
@@ -292,12 +318,17 @@ class Step:
         self.off = inp["offsets"]
         self.Z = torch.empty((B, H, M, D), **f32)
         self.L = torch.empty((B, H, M), **f32)
-        Qref = inp["Qseed"] if w.kind == "flare_pp_fwd" else inp["Q"]
+        pp = w.kind in ("flare_pp_fwd", "flare_pp_bwd")
+        Qref = inp["Qseed"] if pp else inp["Q"]
         dims = flare.make_dims(Qref, inp["K"], None, kernel)
         op = {"flare_fwd": flare.FLARE_OP_FWD, "flare_pp_fwd": flare.FLARE_OP_PP_FWD,
               "encoder_bwd": flare.FLARE_OP_ENCODER_BWD,
-              "decode_bwd": flare.FLARE_OP_DECODE_BWD}[w.kind]
+              "decode_bwd": flare.FLARE_OP_DECODE_BWD, "flare_bwd": flare.FLARE_OP_BWD,
+              "flare_pp_bwd": flare.FLARE_OP_PP_BWD}[w.kind]
         nbytes = flare.flare_workspace_bytes(op, dims, None if w.kind == "decode_bwd" else self.off)
+        if w.kind in ("flare_bwd", "flare_pp_bwd"):   # the forward that saves the statistics
+            fop = flare.FLARE_OP_PP_FWD if pp else flare.FLARE_OP_ENCODER_FWD
+            nbytes = max(nbytes, flare.flare_workspace_bytes(fop, dims, self.off))
         self.ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
         if w.kind == "flare_fwd":
             self.Y = torch.empty_like(inp["K"])
@@ -307,6 +338,22 @@ class Step:
         elif w.kind == "decode_bwd":
             self.dQ, self.dZ = torch.empty((B, H, M, D), **f32), torch.empty((B, H, M, D), **f32)
             self.dK = torch.empty_like(inp["K"])
+        elif w.kind == "flare_bwd":
+            self.dQ = torch.empty((B, H, M, D), **f32)
+            self.dK, self.dV = torch.empty_like(inp["K"]), torch.empty_like(inp["V"])
+            flare.flare_encoder_fwd(inp["Q"], inp["K"], inp["V"], inp["mask"], self.off,
+                                    Z=self.Z, L=self.L, workspace=self.ws, kernel=kernel,
+                                    stream=stream)
+        elif w.kind == "flare_pp_bwd":
+            self.Qd, self.L1 = torch.empty((B, H, M, D), **f32), torch.empty((B, H, M), **f32)
+            self.dQs = torch.empty((B, H, M, D), **f32)
+            self.dKt, self.dVt = torch.empty_like(inp["Kt"]), torch.empty_like(inp["Vt"])
+            self.dK, self.dV = torch.empty_like(inp["K"]), torch.empty_like(inp["V"])
+            Y = torch.empty_like(inp["K"])
+            flare.flare_pp_fwd(inp["Qseed"], inp["Kt"], inp["Vt"], inp["K"], inp["V"], inp["mask"],
+                               self.off, Y=Y, Qdyn=self.Qd, L1=self.L1, Z=self.Z, L2=self.L,
+                               workspace=self.ws, kernel=kernel, stream=stream)
+            del Y
         else:
             self.dQ = torch.empty((B, H, M, D), **f32)
             self.dK, self.dV = torch.empty_like(inp["K"]), torch.empty_like(inp["V"])
@@ -348,6 +395,18 @@ class Step:
             return [("decode_bwd", lambda: flare.flare_decode_bwd(
                         x["Q"], x["Z"], x["K"], x["dY"], dQ=self.dQ, dZ=self.dZ, dK=self.dK,
                         workspace=self.ws, kernel=k, stream=st))]
+        if w.kind == "flare_bwd":
+            return [("flare_bwd", lambda: flare.flare_bwd(
+                        x["Q"], x["K"], x["V"], x["mask"], off, x.get("Zs", self.Z),
+                        x.get("Ls", self.L), x["dY"], dQ=self.dQ, dK=self.dK, dV=self.dV,
+                        workspace=self.ws, kernel=k, stream=st))]
+        if w.kind == "flare_pp_bwd":
+            return [("flare_pp_bwd", lambda: flare.flare_pp_bwd(
+                        x["Qseed"], x["Kt"], x["Vt"], x["K"], x["V"], x["mask"], off,
+                        x.get("Qds", self.Qd), x.get("L1s", self.L1), x.get("Zs", self.Z),
+                        x.get("Ls", self.L), x["dY"], dQseed=self.dQs, dKt=self.dKt,
+                        dVt=self.dVt, dK=self.dK, dV=self.dV, workspace=self.ws, kernel=k,
+                        stream=st))]
         return [("encoder_bwd", lambda: flare.flare_encoder_bwd(
                     x["Q"], x["K"], x["V"], x["mask"], off, x.get("Zs", self.Z),
                     x.get("Ls", self.L), x["dZ"], dQ=self.dQ, dK=self.dK, dV=self.dV,
@@ -362,6 +421,11 @@ class Step:
             return ["Qseed", "Kt", "Vt", "K", "V", "mask"], [self.Y]
         if self.w.kind == "decode_bwd":
             return ["Q", "Z", "K", "dY"], [self.dQ, self.dZ, self.dK]
+        if self.w.kind == "flare_bwd":
+            return ["Q", "K", "V", "mask", "Zs", "Ls", "dY"], [self.dQ, self.dK, self.dV]
+        if self.w.kind == "flare_pp_bwd":
+            return (["Qseed", "Kt", "Vt", "K", "V", "mask", "Qds", "L1s", "Zs", "Ls", "dY"],
+                    [self.dQs, self.dKt, self.dVt, self.dK, self.dV])
         return ["Q", "K", "V", "mask", "Zs", "Ls", "dZ"], [self.dQ, self.dK, self.dV]
 
 
@@ -471,7 +535,8 @@ def main(argv=None):
     # end to end through the public API with host buffers (pinned), copies timed
     e2e_in, e2e_out = runner.inputs_for_e2e()
     host, dinp = {}, dict(inp)
-    extra = {"Zs": runner.Z, "Ls": runner.L}
+    extra = {"Zs": runner.Z, "Ls": runner.L, "Qds": getattr(runner, "Qd", None),
+             "L1s": getattr(runner, "L1", None)}
     for name in e2e_in:
         t = extra[name] if name in extra else inp[name]
         if t is None:

@@ -88,7 +88,9 @@ typedef enum {
     FLARE_OP_FWD = 3,
     FLARE_OP_PP_FWD = 4,
     FLARE_OP_ENCODER_BWD = 5,
-    FLARE_OP_DECODE_BWD = 6
+    FLARE_OP_DECODE_BWD = 6,
+    FLARE_OP_BWD = 7,
+    FLARE_OP_PP_BWD = 8
 } flare_op_t;
 
 /* Workspace bytes `op` needs for these sizes and shard offsets (host array of
@@ -224,6 +226,55 @@ FLARE_API flare_status_t flare_decode_bwd(const flare_dims_t *dims, const void *
                                           const void *K, const void *dY, float *dQ, float *dZ,
                                           void *dK, void *workspace, size_t workspace_bytes,
                                           void *stream);
+
+/*
+ * FLARE mixer backward. Source: the backward paragraphs of the appendix (the
+ * gradient of the replicated Z is first summed over its consumers, then the
+ * encoder is differentiated with the forward's global Z and L). In the mixer
+ * Z's only consumer is the decode; Q enters the encoder (latent queries) and
+ * the decode (latent keys), K the encoder (keys) and the decode (token
+ * queries). So: flare_decode_bwd gives dQ_dec, dZ, dK_dec; flare_encoder_bwd
+ * with that dZ gives dQ_enc, dK_enc, dV; and
+ *   dQ = dQ_dec + dQ_enc   fp32 [B,H,M,D] (one slice per batch element)
+ *   dK = dK_dec + dK_enc   dims->dtype [B,N,H,D] (the decode's share is stored
+ *                          in dims->dtype, then the encoder's fp32 share is
+ *                          added and the sum rounded once more)
+ *   dV = dV_enc            dims->dtype [B,N,H,D]
+ *   Q, K, V, mask, shard_offsets: as for flare_fwd; Z, L: flare_fwd's outputs;
+ *   dY dims->dtype [B,N,H,D].
+ * Workspace: flare_workspace_bytes(FLARE_OP_BWD, dims, shard_offsets, R) bytes
+ * (dZ, then the scratch of the two passes).
+ */
+FLARE_API flare_status_t flare_bwd(const flare_dims_t *dims, const void *Q, const void *K,
+                                   const void *V, const uint8_t *mask,
+                                   const int64_t *shard_offsets, int R, const float *Z,
+                                   const float *L, const void *dY, float *dQ, void *dK, void *dV,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * FLARE++ mixer backward. Source: the FLARE++ backward paragraph of the
+ * appendix. The decode with the dynamic queries Q(X) gives the decoder's
+ * shares of dQ(X), dZ and dK; the physical-value encoder (its own Z, L2) adds
+ * its shares of dQ(X) and dK and gives dV; the summed dQ(X) is the output
+ * gradient of the query-synthesis encoder, whose backward with its own saved
+ * output Q(X) and L1 gives the seeds' gradient and those of K~, V~:
+ *   Qseed dims->dtype [H,M,D] or [B,H,M,D] (dims->q_batch_stride);
+ *   Kt, Vt, K, V, dY dims->dtype [B,N,H,D]; Qdyn, L1, Z, L2: flare_pp_fwd's
+ *   outputs (Qdyn 16-byte aligned);
+ *   dQseed fp32 [B,H,M,D] (one slice per batch element); dKt, dVt, dK, dV
+ *   dims->dtype [B,N,H,D]; dQdyn: optional fp32 [B,H,M,D] (16-byte aligned)
+ *   receiving the summed gradient of Q(X), or NULL (kept in the workspace).
+ * On the bf16 path Q(X) is rounded to bf16 (nearest even) as the operand of
+ * the decode and physical-value encoder backward, as in the forward.
+ * Workspace: flare_workspace_bytes(FLARE_OP_PP_BWD, dims, shard_offsets, R).
+ */
+FLARE_API flare_status_t flare_pp_bwd(const flare_dims_t *dims, const void *Qseed, const void *Kt,
+                                      const void *Vt, const void *K, const void *V,
+                                      const uint8_t *mask, const int64_t *shard_offsets, int R,
+                                      const float *Qdyn, const float *L1, const float *Z,
+                                      const float *L2, const void *dY, float *dQseed, void *dKt,
+                                      void *dVt, void *dK, void *dV, float *dQdyn, void *workspace,
+                                      size_t workspace_bytes, void *stream);
 
 /*
  * Split-KV encoder without a workspace argument, for callers that cannot

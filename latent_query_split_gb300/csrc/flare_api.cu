@@ -324,6 +324,135 @@ flare_status_t decode_run(const flare_dims_t *d, const void *Q, bool q_is_f32, c
     return e == cudaSuccess ? FLARE_OK : cuda_fail(e, "decode launch");
 }
 
+
+size_t encoder_bwd_ws(const flare_dims_t *d) {
+    const Problem pr = make_problem(d);
+    size_t b = encoder_bwd_simt_workspace(pr);
+    if (d->kernel != FLARE_KERNEL_SIMT) {
+        const size_t t = tc_encoder_bwd_workspace(pr, planning_sms());
+        if (t > b) b = t;
+    }
+    return b;
+}
+
+size_t decode_bwd_ws(const flare_dims_t *d) {
+    const Problem pr = make_problem(d);
+    size_t b = decode_bwd_simt_workspace(pr);
+    if (d->kernel != FLARE_KERNEL_SIMT) {
+        const size_t t = tc_decode_bwd_workspace(pr, planning_sms());
+        if (t > b) b = t;
+    }
+    return b;
+}
+
+// Core of flare_encoder_bwd (dims and offsets already checked). accumulate:
+// dQ and dK already hold another consumer's share and this pass adds its own.
+flare_status_t encoder_bwd_run(const flare_dims_t *dims, const void *Q, const void *K, const void *V,
+                               const uint8_t *mask, const float *Z, const float *L, const float *dZ,
+                               float *dQ, void *dK, void *dV, void *workspace, size_t workspace_bytes,
+                               bool accumulate, cudaStream_t st) {
+    const Problem pr = make_problem(dims);
+    if (pr.B == 0) return FLARE_OK;
+    if (!Q || !Z || !L || !dZ || !dQ || (pr.N > 0 && (!K || !V || !dK || !dV)))
+        return fail(FLARE_ERR_INVALID_ARG, "NULL tensor");
+    const size_t es = elem_size(dims);
+    if (!aligned(Q, es) || !aligned(K, es) || !aligned(V, es) || !aligned(dK, es) ||
+        !aligned(dV, es) || !aligned(Z, 4) || !aligned(L, 4) || !aligned(dZ, 4) || !aligned(dQ, 4))
+        return fail(FLARE_ERR_INVALID_ARG, "tensors must be aligned to their element size");
+    const bool want_tc = dims->kernel != FLARE_KERNEL_SIMT && tc_bwd_supported(pr.bf16, pr.M, pr.D);
+    if (dims->kernel == FLARE_KERNEL_TENSOR && !want_tc)
+        return fail(FLARE_ERR_UNSUPPORTED, "no tensor-core backward for dtype=%d M=%d D=%d",
+                    (int)dims->dtype, dims->M, dims->D);
+    const bool tc = want_tc && tc_pointers_ok(K, V, dims->H, dims->D) &&
+                    tc_pointers_ok(dK, dV, dims->H, dims->D) && aligned(Q, 16) && aligned(Z, 16) &&
+                    aligned(dZ, 16) && aligned(dQ, 16);
+    if (dims->kernel == FLARE_KERNEL_TENSOR && !tc)
+        return fail(FLARE_ERR_INVALID_ARG,
+                    "tensor-core backward needs 16-byte aligned Q, K, V, Z, dZ, dQ, dK and dV");
+    const size_t need = encoder_bwd_ws(dims);
+    if (pr.N > 0 && (!workspace || workspace_bytes < need))
+        return fail(FLARE_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", need,
+                    workspace_bytes);
+    if (workspace && !aligned(workspace, 256))
+        return fail(FLARE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    cudaError_t e;
+    if (tc) {
+        DeviceInfo di;
+        flare_status_t s = device_info(di);
+        if (s != FLARE_OK) return s;
+        e = launch_encoder_bwd_tc(pr, Q, K, V, mask, Z, L, dZ, dQ, dK, dV, workspace,
+                                  workspace_bytes, di.sms, di.status, st, accumulate);
+    } else {
+        e = launch_encoder_bwd_simt(pr, Q, K, V, mask, Z, L, dZ, dQ, dK, dV, workspace,
+                                    workspace_bytes, st, accumulate);
+    }
+    return e == cudaSuccess ? FLARE_OK : cuda_fail(e, "encoder backward launch");
+}
+
+// Core of flare_decode_bwd (dims already checked).
+flare_status_t decode_bwd_run(const flare_dims_t *dims, const void *Q, const float *Z, const void *K,
+                              const void *dY, float *dQ, float *dZ, void *dK, void *workspace,
+                              size_t workspace_bytes, cudaStream_t st) {
+    const Problem pr = make_problem(dims);
+    if (pr.B == 0) return FLARE_OK;
+    if (!Q || !Z || !dQ || !dZ || (pr.N > 0 && (!K || !dY || !dK)))
+        return fail(FLARE_ERR_INVALID_ARG, "NULL tensor");
+    const size_t es = elem_size(dims);
+    if (!aligned(Q, es) || !aligned(K, es) || !aligned(dY, es) || !aligned(dK, es) || !aligned(Z, 4) ||
+        !aligned(dQ, 4) || !aligned(dZ, 4))
+        return fail(FLARE_ERR_INVALID_ARG, "tensors must be aligned to their element size");
+    const bool want_tc = dims->kernel != FLARE_KERNEL_SIMT && tc_decode_bwd_supported(pr.bf16, pr.M, pr.D);
+    if (dims->kernel == FLARE_KERNEL_TENSOR && !want_tc)
+        return fail(FLARE_ERR_UNSUPPORTED, "no tensor-core decode backward for dtype=%d M=%d D=%d",
+                    (int)dims->dtype, dims->M, dims->D);
+    const bool tc = want_tc && tc_pointers_ok(K, dY, dims->H, dims->D) &&
+                    tc_pointers_ok(dK, dK, dims->H, dims->D) && aligned(Q, 16) && aligned(Z, 16) &&
+                    aligned(dQ, 16) && aligned(dZ, 16);
+    if (dims->kernel == FLARE_KERNEL_TENSOR && !tc)
+        return fail(FLARE_ERR_INVALID_ARG,
+                    "tensor-core decode backward needs 16-byte aligned Q, Z, K, dY, dQ, dZ and dK");
+    const size_t need = decode_bwd_ws(dims);
+    if (!workspace || workspace_bytes < need)
+        return fail(FLARE_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", need,
+                    workspace_bytes);
+    if (!aligned(workspace, 256)) return fail(FLARE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    cudaError_t e;
+    if (tc) {
+        DeviceInfo di;
+        flare_status_t s = device_info(di);
+        if (s != FLARE_OK) return s;
+        e = launch_decode_bwd_tc(pr, Q, Z, K, dY, dQ, dZ, dK, workspace, workspace_bytes, di.sms,
+                                 di.status, st);
+    } else {
+        e = launch_decode_bwd_simt(pr, Q, Z, K, dY, dQ, dZ, dK, workspace, st);
+    }
+    return e == cudaSuccess ? FLARE_OK : cuda_fail(e, "decode backward launch");
+}
+
+// Workspace of the mixer backward passes: the latent gradients that pass
+// from one stage to the next, then scratch shared by the stages in turn.
+struct MixerBwdLayout {
+    size_t dz = 0, dqdyn = 0, qdyn_b = 0, scratch = 0, bytes = 0;
+};
+
+void mixer_bwd_layout(const flare_dims_t *d, bool pp, MixerBwdLayout &l) {
+    const size_t lat = (size_t)d->B * d->H * d->M * d->D;
+    size_t o = 0;
+    l.dz = o;
+    o += align256(sizeof(float) * lat);
+    size_t scratch = decode_bwd_ws(d);
+    const size_t enc = encoder_bwd_ws(d);
+    if (enc > scratch) scratch = enc;
+    if (pp) {
+        l.dqdyn = o;
+        o += align256(sizeof(float) * lat);
+        l.qdyn_b = o;
+        if (d->dtype == FLARE_BF16) o += align256(2 * lat);
+    }
+    l.scratch = o;
+    l.bytes = o + scratch;
+}
+
 }  // namespace
 
 // Entry points for the allocation-free encoder (noalloc.cu): the same
@@ -363,13 +492,7 @@ size_t flare_workspace_bytes(flare_op_t op, const flare_dims_t *dims, const int6
     if (op == FLARE_OP_LSE_MERGE || op == FLARE_OP_DECODE_FWD) return 0;
     if (op == FLARE_OP_DECODE_BWD) {
         if (check_dims(dims) != FLARE_OK) return bad;
-        const Problem pr = make_problem(dims);
-        size_t b = decode_bwd_simt_workspace(pr);
-        if (dims->kernel != FLARE_KERNEL_SIMT) {
-            const size_t t = tc_decode_bwd_workspace(pr, planning_sms());
-            if (t > b) b = t;
-        }
-        return b;
+        return decode_bwd_ws(dims);
     }
     if (check_dims(dims) != FLARE_OK) return bad;
     if (check_offsets(off, R, dims->N) != FLARE_OK) return bad;
@@ -378,14 +501,13 @@ size_t flare_workspace_bytes(flare_op_t op, const flare_dims_t *dims, const int6
         case FLARE_OP_FWD:
         case FLARE_OP_PP_FWD:
             return encoder_ws_bytes(dims, off, R);
-        case FLARE_OP_ENCODER_BWD: {
-            const Problem pr = make_problem(dims);
-            size_t b = encoder_bwd_simt_workspace(pr);
-            if (dims->kernel != FLARE_KERNEL_SIMT) {
-                const size_t t = tc_encoder_bwd_workspace(pr, planning_sms());
-                if (t > b) b = t;
-            }
-            return b;
+        case FLARE_OP_ENCODER_BWD:
+            return encoder_bwd_ws(dims);
+        case FLARE_OP_BWD:
+        case FLARE_OP_PP_BWD: {
+            MixerBwdLayout l;
+            mixer_bwd_layout(dims, op == FLARE_OP_PP_BWD, l);
+            return l.bytes;
         }
         default:
             return bad;
@@ -467,41 +589,8 @@ flare_status_t flare_encoder_bwd(const flare_dims_t *dims, const void *Q, const 
     flare_status_t s = check_dims(dims);
     if (s != FLARE_OK) return s;
     if ((s = check_offsets(shard_offsets, R, dims->N)) != FLARE_OK) return s;
-    const Problem pr = make_problem(dims);
-    if (pr.B == 0) return FLARE_OK;
-    if (!Q || !Z || !L || !dZ || !dQ || (pr.N > 0 && (!K || !V || !dK || !dV)))
-        return fail(FLARE_ERR_INVALID_ARG, "NULL tensor");
-    const size_t es = elem_size(dims);
-    if (!aligned(Q, es) || !aligned(K, es) || !aligned(V, es) || !aligned(dK, es) ||
-        !aligned(dV, es) || !aligned(Z, 4) || !aligned(L, 4) || !aligned(dZ, 4) || !aligned(dQ, 4))
-        return fail(FLARE_ERR_INVALID_ARG, "tensors must be aligned to their element size");
-    const bool want_tc = dims->kernel != FLARE_KERNEL_SIMT && tc_bwd_supported(pr.bf16, pr.M, pr.D);
-    if (dims->kernel == FLARE_KERNEL_TENSOR && !want_tc)
-        return fail(FLARE_ERR_UNSUPPORTED, "no tensor-core backward for dtype=%d M=%d D=%d",
-                    (int)dims->dtype, dims->M, dims->D);
-    const bool tc = want_tc && tc_pointers_ok(K, V, dims->H, dims->D) &&
-                    tc_pointers_ok(dK, dV, dims->H, dims->D) && aligned(Q, 16) && aligned(Z, 16) &&
-                    aligned(dZ, 16) && aligned(dQ, 16);
-    if (dims->kernel == FLARE_KERNEL_TENSOR && !tc)
-        return fail(FLARE_ERR_INVALID_ARG,
-                    "tensor-core backward needs 16-byte aligned Q, K, V, Z, dZ, dQ, dK and dV");
-    const size_t need = flare_workspace_bytes(FLARE_OP_ENCODER_BWD, dims, shard_offsets, R);
-    if (pr.N > 0 && (!workspace || workspace_bytes < need))
-        return fail(FLARE_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", need,
-                    workspace_bytes);
-    if (workspace && !aligned(workspace, 256))
-        return fail(FLARE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    cudaError_t e;
-    if (tc) {
-        DeviceInfo di;
-        if ((s = device_info(di)) != FLARE_OK) return s;
-        e = launch_encoder_bwd_tc(pr, Q, K, V, mask, Z, L, dZ, dQ, dK, dV, workspace,
-                                  workspace_bytes, di.sms, di.status, (cudaStream_t)stream);
-    } else {
-        e = launch_encoder_bwd_simt(pr, Q, K, V, mask, Z, L, dZ, dQ, dK, dV, workspace,
-                                    workspace_bytes, (cudaStream_t)stream);
-    }
-    return e == cudaSuccess ? FLARE_OK : cuda_fail(e, "encoder backward launch");
+    return encoder_bwd_run(dims, Q, K, V, mask, Z, L, dZ, dQ, dK, dV, workspace, workspace_bytes,
+                           false, (cudaStream_t)stream);
 }
 
 flare_status_t flare_decode_bwd(const flare_dims_t *dims, const void *Q, const float *Z,
@@ -509,39 +598,81 @@ flare_status_t flare_decode_bwd(const flare_dims_t *dims, const void *Q, const f
                                 void *workspace, size_t workspace_bytes, void *stream) {
     flare_status_t s = check_dims(dims);
     if (s != FLARE_OK) return s;
-    const Problem pr = make_problem(dims);
-    if (pr.B == 0) return FLARE_OK;
-    if (!Q || !Z || !dQ || !dZ || (pr.N > 0 && (!K || !dY || !dK)))
-        return fail(FLARE_ERR_INVALID_ARG, "NULL tensor");
-    const size_t es = elem_size(dims);
-    if (!aligned(Q, es) || !aligned(K, es) || !aligned(dY, es) || !aligned(dK, es) || !aligned(Z, 4) ||
-        !aligned(dQ, 4) || !aligned(dZ, 4))
-        return fail(FLARE_ERR_INVALID_ARG, "tensors must be aligned to their element size");
-    const bool want_tc = dims->kernel != FLARE_KERNEL_SIMT && tc_decode_bwd_supported(pr.bf16, pr.M, pr.D);
-    if (dims->kernel == FLARE_KERNEL_TENSOR && !want_tc)
-        return fail(FLARE_ERR_UNSUPPORTED, "no tensor-core decode backward for dtype=%d M=%d D=%d",
-                    (int)dims->dtype, dims->M, dims->D);
-    const bool tc = want_tc && tc_pointers_ok(K, dY, dims->H, dims->D) &&
-                    tc_pointers_ok(dK, dK, dims->H, dims->D) && aligned(Q, 16) && aligned(Z, 16) &&
-                    aligned(dQ, 16) && aligned(dZ, 16);
-    if (dims->kernel == FLARE_KERNEL_TENSOR && !tc)
-        return fail(FLARE_ERR_INVALID_ARG,
-                    "tensor-core decode backward needs 16-byte aligned Q, Z, K, dY, dQ, dZ and dK");
-    const size_t need = flare_workspace_bytes(FLARE_OP_DECODE_BWD, dims, nullptr, 0);
-    if (!workspace || workspace_bytes < need)
-        return fail(FLARE_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", need,
+    return decode_bwd_run(dims, Q, Z, K, dY, dQ, dZ, dK, workspace, workspace_bytes,
+                          (cudaStream_t)stream);
+}
+
+flare_status_t flare_bwd(const flare_dims_t *dims, const void *Q, const void *K, const void *V,
+                         const uint8_t *mask, const int64_t *shard_offsets, int R, const float *Z,
+                         const float *L, const void *dY, float *dQ, void *dK, void *dV,
+                         void *workspace, size_t workspace_bytes, void *stream) {
+    flare_status_t s = check_dims(dims);
+    if (s != FLARE_OK) return s;
+    if ((s = check_offsets(shard_offsets, R, dims->N)) != FLARE_OK) return s;
+    if (dims->B == 0) return FLARE_OK;
+    MixerBwdLayout l;
+    mixer_bwd_layout(dims, false, l);
+    if (!workspace || workspace_bytes < l.bytes)
+        return fail(FLARE_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", l.bytes,
                     workspace_bytes);
     if (!aligned(workspace, 256)) return fail(FLARE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    cudaError_t e;
-    if (tc) {
-        DeviceInfo di;
-        if ((s = device_info(di)) != FLARE_OK) return s;
-        e = launch_decode_bwd_tc(pr, Q, Z, K, dY, dQ, dZ, dK, workspace, workspace_bytes, di.sms,
-                                 di.status, (cudaStream_t)stream);
-    } else {
-        e = launch_decode_bwd_simt(pr, Q, Z, K, dY, dQ, dZ, dK, workspace, (cudaStream_t)stream);
+    char *w = (char *)workspace;
+    float *dZ = (float *)(w + l.dz);
+    cudaStream_t st = (cudaStream_t)stream;
+    // the decoder's shares of dQ and dK, and dZ (Z's only consumer in the mixer)
+    if ((s = decode_bwd_run(dims, Q, Z, K, dY, dQ, dZ, dK, w + l.scratch, workspace_bytes - l.scratch,
+                            st)) != FLARE_OK)
+        return s;
+    // the encoder with its global (Z, L) adds its shares and gives dV
+    return encoder_bwd_run(dims, Q, K, V, mask, Z, L, dZ, dQ, dK, dV, w + l.scratch,
+                           workspace_bytes - l.scratch, true, st);
+}
+
+flare_status_t flare_pp_bwd(const flare_dims_t *dims, const void *Qseed, const void *Kt,
+                            const void *Vt, const void *K, const void *V, const uint8_t *mask,
+                            const int64_t *shard_offsets, int R, const float *Qdyn,
+                            const float *L1, const float *Z, const float *L2, const void *dY,
+                            float *dQseed, void *dKt, void *dVt, void *dK, void *dV, float *dQdyn,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+    flare_status_t s = check_dims(dims);
+    if (s != FLARE_OK) return s;
+    if ((s = check_offsets(shard_offsets, R, dims->N)) != FLARE_OK) return s;
+    if (dims->B == 0) return FLARE_OK;
+    if (!Qdyn || !L1 || !Z || !L2) return fail(FLARE_ERR_INVALID_ARG, "the forward's Qdyn, L1, Z, L2 are required");
+    if (!aligned(Qdyn, 16) || !aligned(dQdyn, 16))
+        return fail(FLARE_ERR_INVALID_ARG, "Qdyn and dQdyn must be 16-byte aligned");
+    MixerBwdLayout l;
+    mixer_bwd_layout(dims, true, l);
+    if (!workspace || workspace_bytes < l.bytes)
+        return fail(FLARE_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", l.bytes,
+                    workspace_bytes);
+    if (!aligned(workspace, 256)) return fail(FLARE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    char *w = (char *)workspace;
+    float *dZ = (float *)(w + l.dz);
+    float *dQX = dQdyn ? dQdyn : (float *)(w + l.dqdyn);
+    void *scratch = w + l.scratch;
+    const size_t scratch_bytes = workspace_bytes - l.scratch;
+    cudaStream_t st = (cudaStream_t)stream;
+    flare_dims_t d2 = *dims;                                   // Q(X) is per batch element
+    d2.q_batch_stride = (int64_t)dims->H * dims->M * dims->D;
+    // Q(X) as the operand of the decode and physical-value encoder: bf16 on the bf16 path
+    const void *QX = Qdyn;
+    if (dims->dtype == FLARE_BF16) {
+        const cudaError_t e = launch_f32_to_bf16(Qdyn, w + l.qdyn_b,
+                                                 (int64_t)dims->B * dims->H * dims->M * dims->D, st);
+        if (e != cudaSuccess) return cuda_fail(e, "Q(X) conversion launch");
+        QX = w + l.qdyn_b;
     }
-    return e == cudaSuccess ? FLARE_OK : cuda_fail(e, "decode backward launch");
+    // decoder: its shares of dQ(X) and dK, and dZ
+    if ((s = decode_bwd_run(&d2, QX, Z, K, dY, dQX, dZ, dK, scratch, scratch_bytes, st)) != FLARE_OK)
+        return s;
+    // physical-value encoder (Z, L2): adds its shares of dQ(X) and dK, gives dV
+    if ((s = encoder_bwd_run(&d2, QX, K, V, mask, Z, L2, dZ, dQX, dK, dV, scratch, scratch_bytes, true,
+                             st)) != FLARE_OK)
+        return s;
+    // query-synthesis encoder (its output Q(X), L1) with the summed dQ(X)
+    return encoder_bwd_run(dims, Qseed, Kt, Vt, mask, Qdyn, L1, dQX, dQseed, dKt, dVt, scratch,
+                           scratch_bytes, false, st);
 }
 
 flare_status_t flare_device_status(void *stream) {

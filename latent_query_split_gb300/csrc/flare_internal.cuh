@@ -84,7 +84,8 @@ cudaError_t launch_decode_simt(const Problem &pr, const void *Q, bool q_is_f32, 
 cudaError_t launch_encoder_bwd_simt(const Problem &pr, const void *Q, const void *K,
                                     const void *V, const uint8_t *mask, const float *Z,
                                     const float *L, const float *dZ, float *dQ, void *dK,
-                                    void *dV, void *ws, size_t ws_bytes, cudaStream_t st);
+                                    void *dV, void *ws, size_t ws_bytes, cudaStream_t st,
+                                    bool accumulate = false);   // dQ, dK += this share
 size_t encoder_bwd_simt_workspace(const Problem &pr);
 cudaError_t launch_decode_bwd_simt(const Problem &pr, const void *Q, const float *Z, const void *K,
                                    const void *dY, float *dQ, float *dZ, void *dK, void *ws,

@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kThreads)
 bwd_dkdv_simt_kernel(Problem pr, const TQ *__restrict__ Q, const TKV *__restrict__ K,
                      const TKV *__restrict__ V, const uint8_t *__restrict__ mask,
                      const float *__restrict__ Z, const float *__restrict__ L,
-                     const float *__restrict__ dZ, TKV *__restrict__ dK, TKV *__restrict__ dV) {
+                     const float *__restrict__ dZ, TKV *dK, TKV *__restrict__ dV, int accumulate) {
     extern __shared__ float smem[];
     const int D = pr.D, M = pr.M, H = pr.H, N = pr.N, ld = D + 1;
     BwdTile t = bwd_carve(smem, D);
@@ -503,7 +503,8 @@ bwd_dkdv_simt_kernel(Problem pr, const TQ *__restrict__ Q, const TKV *__restrict
         const int64_t n = t0 + tok;
         if (n >= N) continue;
         const int64_t o = (((int64_t)b * N + n) * H + h) * D + d;
-        dK[o] = from_f<TKV>(pr.scale * dKs[tok * ld + d]);
+        const float old = accumulate ? to_f(dK[o]) : 0.f;   // the decode's share
+        dK[o] = from_f<TKV>(old + pr.scale * dKs[tok * ld + d]);
         dV[o] = from_f<TKV>(dVs[tok * ld + d]);
     }
 }
@@ -516,7 +517,7 @@ bwd_dq_simt_kernel(Problem pr, const TQ *__restrict__ Q, const TKV *__restrict__
                    const TKV *__restrict__ V, const uint8_t *__restrict__ mask,
                    const float *__restrict__ Z, const float *__restrict__ L,
                    const float *__restrict__ dZ, float *__restrict__ dQ, unsigned *tickets,
-                   float *part, int chunk_len, int nchunks, int mtiles) {
+                   float *part, int chunk_len, int nchunks, int mtiles, int accumulate) {
     extern __shared__ float smem[];
     __shared__ int s_last;
     const int D = pr.D, M = pr.M, H = pr.H, N = pr.N, ld = D + 1;
@@ -561,10 +562,11 @@ bwd_dq_simt_kernel(Problem pr, const TQ *__restrict__ Q, const TKV *__restrict__
     __threadfence();
     for (int e = threadIdx.x; e < rows * D; e += kThreads) {
         const int row = e / D, d = e % D;
-        float acc = 0.f;
+        float *dst = dQ + (bh * M + m0 + row) * D + d;
+        float acc = accumulate ? *dst : 0.f;
         for (int cc = 0; cc < nchunks; ++cc)
             acc += __ldcg(part + ((bh * nchunks + cc) * M + m0 + row) * D + d);
-        dQ[(bh * M + m0 + row) * D + d] = acc;
+        *dst = acc;
     }
 }
 
@@ -669,7 +671,8 @@ size_t encoder_bwd_simt_workspace(const Problem &pr) {
 cudaError_t launch_encoder_bwd_simt(const Problem &pr, const void *Q, const void *K,
                                     const void *V, const uint8_t *mask, const float *Z,
                                     const float *L, const float *dZ, float *dQ, void *dK,
-                                    void *dV, void *ws, size_t ws_bytes, cudaStream_t st) {
+                                    void *dV, void *ws, size_t ws_bytes, cudaStream_t st,
+                                    bool accumulate) {
     if (pr.B == 0) return cudaSuccess;
     const int mtiles = (pr.M + 31) / 32;
     const int nchunks = bwd_nchunks(pr);
@@ -680,11 +683,13 @@ cudaError_t launch_encoder_bwd_simt(const Problem &pr, const void *Q, const void
     const size_t smem_kv = tile + sizeof(float) * 2 * 32 * (pr.D + 1);
     const size_t smem_q = tile + sizeof(float) * 32 * (pr.D + 1);
     cudaError_t e;
-    if (pr.N == 0) {   // no token: dQ = 0
-        return cudaMemsetAsync(dQ, 0, sizeof(float) * (size_t)pr.B * pr.H * pr.M * pr.D, st);
+    if (pr.N == 0) {   // no token: no share of dQ
+        return accumulate ? cudaSuccess
+                          : cudaMemsetAsync(dQ, 0, sizeof(float) * (size_t)pr.B * pr.H * pr.M * pr.D, st);
     }
     if ((e = cudaMemsetAsync(tickets, 0, tickets_bytes, st)) != cudaSuccess) return e;
     dim3 gkv((pr.N + 31) / 32, pr.H, pr.B), gq(nchunks, pr.H, pr.B * mtiles);
+    const int acc = accumulate ? 1 : 0;
 #define FLARE_BWD_LAUNCH(TQ, TKV)                                                             \
     {                                                                                         \
         auto k1 = bwd_dkdv_simt_kernel<TQ, TKV>;                                              \
@@ -692,11 +697,11 @@ cudaError_t launch_encoder_bwd_simt(const Problem &pr, const void *Q, const void
         if ((e = set_smem(k1, smem_kv)) != cudaSuccess) return e;                             \
         if ((e = set_smem(k2, smem_q)) != cudaSuccess) return e;                              \
         k1<<<gkv, kThreads, smem_kv, st>>>(pr, (const TQ *)Q, (const TKV *)K, (const TKV *)V, \
-                                            mask, Z, L, dZ, (TKV *)dK, (TKV *)dV);            \
+                                            mask, Z, L, dZ, (TKV *)dK, (TKV *)dV, acc);       \
         note_launch();                                                                        \
         k2<<<gq, kThreads, smem_q, st>>>(pr, (const TQ *)Q, (const TKV *)K, (const TKV *)V,   \
                                           mask, Z, L, dZ, dQ, tickets, part, kBwdChunk,       \
-                                          nchunks, mtiles);                                   \
+                                          nchunks, mtiles, acc);                              \
         note_launch();                                                                        \
     }
     if (!pr.bf16) FLARE_BWD_LAUNCH(float, float)

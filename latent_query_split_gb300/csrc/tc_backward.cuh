@@ -26,6 +26,11 @@
 //    partial per (b, h) piece of the span.
 //  * bwd_dq_reduce_kernel: dQ = sum of the pieces of each (b, h), in piece
 //    order (deterministic).
+// With accumulation on (the mixer backward, where the decode's shares of dK
+// and dQ are already in the output buffers) dK = dK + the encoder's share and
+// dQ = dQ + the encoder's share: the dK epilogue prefetches the tile's rows of
+// the old dK with cp.async at the start of the tile and adds them in fp32
+// before rounding once.
 // Warp roles of bwd_tc_kernel: warp 0 TMA producer (K, V ring; Q, dZ and the
 // row statistics on every (b, h) change), warp 1 TMEM allocator and MMA
 // issuer (lane 0), warps 2-9 two halves of four warps, each half owning M/2
@@ -49,6 +54,7 @@ struct BwdArgs {
     const uint8_t *mask;        // [B, N] or null
     const float *lc;            // [B*H][2][M]: -L log2(e) (or -inf), then -s c
     float *part;                // [B*H][P_max][M][64] dQ partials
+    const __nv_bfloat16 *dk_acc;  // with ACC: dK = dk_acc + this share (dk_acc may be dK)
     int P_max;
     int64_t T_bh, T_total;      // 128-token tiles per (b, h), and overall
     int grid;
@@ -75,8 +81,12 @@ struct BwdCfg {
     static constexpr uint32_t DS_BYTES = 2 * TILE_BYTES;
     static constexpr uint32_t OUT_OFF = DS_OFF + DS_BYTES;  // dK tile, then dV tile
     static constexpr uint32_t OUT_BYTES = 2 * TILE_BYTES;
+    // rows of the old dK being accumulated into (one 128-byte row per thread
+    // of the dK half, 16-byte chunks XOR-swizzled by the row)
+    static constexpr uint32_t DKIN_OFF = OUT_OFF + OUT_BYTES;
+    static constexpr uint32_t DKIN_BYTES = TILE_BYTES;
     // row statistics of two (b, h) generations: [2][-L2 (128), -s c (128)]
-    static constexpr uint32_t LC_OFF = OUT_OFF + OUT_BYTES;
+    static constexpr uint32_t LC_OFF = DKIN_OFF + DKIN_BYTES;
     static constexpr uint32_t LC_BYTES = 2 * 2 * 128 * 4;
     static constexpr uint32_t BAR_OFF = LC_OFF + LC_BYTES;
     // full[S], empty[S], qd_full, qd_free, lc_full[2], s_full, p_full,
@@ -122,7 +132,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const float *__restrict__
 __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const float *__restrict__ part,
                                                             float *__restrict__ dQ, int64_t BH, int M,
                                                             int P_max, int64_t T_bh, int64_t T_total,
-                                                            int grid) {
+                                                            int grid, int accumulate) {
     const int64_t per_bh = (int64_t)M * 16;                 // float4s of one (b, h)
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= BH * per_bh) return;
@@ -130,7 +140,7 @@ __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const float *__restr
     const int c0 = bwd_cta_of(bh * T_bh, T_total, grid);
     const int np = bwd_cta_of(bh * T_bh + T_bh - 1, T_total, grid) - c0 + 1;
     const float4 *src = reinterpret_cast<const float4 *>(part) + bh * P_max * per_bh + rem;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = accumulate ? reinterpret_cast<const float4 *>(dQ)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int p = 0; p < np; ++p) {
         const float4 v = __ldcg(src + p * per_bh);
         acc.x += v.x;
@@ -142,7 +152,7 @@ __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const float *__restr
 }
 
 // ---- the tile kernel -------------------------------------------------------------
-template <int M, int STAGES>
+template <int M, int STAGES, bool ACC>
 __global__ void __launch_bounds__(BwdCfg<M, STAGES>::THREADS, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdZ,
@@ -411,12 +421,27 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             if (a.mask != nullptr && n < a.N) v = __ldg(a.mask + (int64_t)t.b * a.N + n);
             return v;
         };
+        // the old dK rows of tile t (this thread's row; read by this thread only,
+        // in the tile's epilogue)
+        auto prefetch_dk = [&](const Cursor &t) {
+            const int64_t n = t.kt * 128 + rig;
+            if (ACC && hf == 1 && n < a.N) {
+                const __nv_bfloat16 *src = a.dk_acc + (((int64_t)t.b * a.N + n) * a.H + t.h) * 64;
+                const uint32_t dst = sbase + C::DKIN_OFF + (uint32_t)rig * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) cp_async16(dst + ((c ^ (rig & 7)) << 4), src + 8 * c);
+                cp_async_commit();
+            }
+        };
         Cursor cu{bh0, k0, (int)(bh0 / a.H), (int)(bh0 - (bh0 / a.H) * a.H)};
         int64_t cur = -1;
         int u = -1, pieces = 0;
         Cursor ca = cu;                                           // tile j + 2
         uint32_t mb0 = 0, mb1 = 0;                                // mask bytes of tiles j, j + 1
-        if (ntiles > 0) mb0 = mask_byte(ca);
+        if (ntiles > 0) {
+            mb0 = mask_byte(ca);
+            prefetch_dk(ca);
+        }
         advance(ca);
         if (ntiles > 1) mb1 = mask_byte(ca);
         advance(ca);
@@ -492,31 +517,70 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             // epilogue: half 0 takes dV, half 1 dK of the warp's 32 token rows
             if (!wwait(dvdk_full, (uint32_t)j & 1)) break;
             tc_fence_after();
-            uint32_t rg[2][32];
-            tmem_ld32(tmem + (hf ? C::DK_COL : C::DV_COL) + lane_off, rg[0]);
-            tmem_ld32(tmem + (hf ? C::DK_COL : C::DV_COL) + 32 + lane_off, rg[1]);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(dvdk_free);
-            // the slab is free once the warp's previous store has read it
-            if (j > 0) {
-                if (lane == 0) bulk_wait_group_read0();
-                __syncwarp();
-            }
+            const uint32_t out_tm = tmem + (hf ? C::DK_COL : C::DV_COL) + lane_off;
             uint8_t *srow = slab + lane * 128;
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2)
+            // 32 fp32 columns [32 h2, 32 h2 + 32) of the row into the slab as bf16;
+            // with `old`, the old dK row's bf16 values are added first
+            auto pack32 = [&](const uint32_t *g, int h2, bool old) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int chunk = 4 * h2 + q;
-                    const uint32_t *g8 = rg[h2] + 8 * q;
-                    *reinterpret_cast<uint4 *>(srow + ((chunk ^ (lane & 7)) << 4)) = make_uint4(
-                        pack_bf16(__uint_as_float(g8[0]), __uint_as_float(g8[1])),
-                        pack_bf16(__uint_as_float(g8[2]), __uint_as_float(g8[3])),
-                        pack_bf16(__uint_as_float(g8[4]), __uint_as_float(g8[5])),
-                        pack_bf16(__uint_as_float(g8[6]), __uint_as_float(g8[7])));
+                    float f[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(g[8 * q + k]);
+                    if (old) {
+                        // bf16 pairs, the even column in the low half
+                        const uint4 o = *reinterpret_cast<const uint4 *>(smem + C::DKIN_OFF + rig * 128 +
+                                                                          ((chunk ^ (rig & 7)) << 4));
+                        const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            f[2 * k] += __uint_as_float(ow[k] << 16);
+                            f[2 * k + 1] += __uint_as_float(ow[k] & 0xffff0000u);
+                        }
+                    }
+                    *reinterpret_cast<uint4 *>(srow + ((chunk ^ (lane & 7)) << 4)) =
+                        make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                                   pack_bf16(f[6], f[7]));
                 }
+            };
+            if constexpr (!ACC) {
+                uint32_t rg[2][32];
+                tmem_ld32(out_tm, rg[0]);
+                tmem_ld32(out_tm + 32, rg[1]);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dvdk_free);
+                // the slab is free once the warp's previous store has read it
+                if (j > 0) {
+                    if (lane == 0) bulk_wait_group_read0();
+                    __syncwarp();
+                }
+                pack32(rg[0], 0, false);
+                pack32(rg[1], 1, false);
+            } else {
+                // one 32-column half at a time (fewer live registers); TMEM is
+                // released after the second half
+                if (j > 0) {
+                    if (lane == 0) bulk_wait_group_read0();
+                    __syncwarp();
+                }
+                const bool acc_row = hf == 1 && kt * 128 + rig < a.N;
+                if (acc_row) cp_async_wait0();
+#pragma unroll 1
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t rg[32];
+                    tmem_ld32(out_tm + 32 * h2, rg);
+                    tmem_wait_ld();
+                    if (h2 == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(dvdk_free);
+                    }
+                    pack32(rg, h2, acc_row);
+                }
+            }
             fence_proxy_async_smem();
             __syncwarp();
             const int n0 = (int)(kt * 128) + quad * 32;
@@ -525,6 +589,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 tma_store_4d(tmOut, smem_u32(slab), 0, h, n0, b);
                 bulk_commit_group();
             }
+            if (j + 1 < ntiles) prefetch_dk(cn);
             if (last) {
                 // the (b, h)'s dQ partial of this span: latent rows in the
                 // lanes, half hf takes columns [32 hf, 32 hf + 32)

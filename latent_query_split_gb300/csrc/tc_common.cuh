@@ -60,9 +60,13 @@ size_t tc_encoder_bwd_workspace(const Problem &pr, int sms);
 cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *K, const void *V,
                                   const uint8_t *mask, const float *Z, const float *L,
                                   const float *dZ, float *dQ, void *dK, void *dV, void *ws,
-                                  size_t ws_bytes, int sms, unsigned *status, cudaStream_t st);
+                                  size_t ws_bytes, int sms, unsigned *status, cudaStream_t st,
+                                  bool accumulate = false);   // dQ, dK += this share
 
 // Decode backward on tensor cores: bf16 with D = 64 and M in {64, 128}.
+// y[i] = x[i] rounded to bf16 (nearest even), n elements.
+cudaError_t launch_f32_to_bf16(const float *x, void *y, int64_t n, cudaStream_t st);
+
 bool tc_decode_bwd_supported(bool bf16, int M, int D);
 size_t tc_decode_bwd_workspace(const Problem &pr, int sms);
 cudaError_t launch_decode_bwd_tc(const Problem &pr, const void *Q, const float *Z, const void *K,

@@ -70,6 +70,17 @@ __global__ void f32_to_bf16_kernel(const float *__restrict__ x, __nv_bfloat16 *_
         y[i] = __float2bfloat16_rn(x[i]);
 }
 
+}  // namespace
+
+cudaError_t launch_f32_to_bf16(const float *x, void *y, int64_t n, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const int64_t blocks = (n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024;
+    f32_to_bf16_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, (__nv_bfloat16 *)y, n);
+    note_launch();
+    return cudaGetLastError();
+}
+
+namespace {
 template <class C, class Kernel>
 cudaError_t launch_enc(Kernel k, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq,
                        const tc::EncArgs &args, int grid, cudaStream_t st) {
@@ -270,10 +281,10 @@ void bwd_layout(const Problem &pr, int sms, BwdLayout &l) {
     l.bytes = o;
 }
 
-template <int M>
+template <int M, bool ACC>
 cudaError_t launch_bwd(const CUtensorMap *maps, const tc::BwdArgs &a, cudaStream_t st) {
     using C = tc::BwdCfg<M, 3>;
-    auto k = tc::bwd_tc_kernel<M, 3>;
+    auto k = tc::bwd_tc_kernel<M, 3, ACC>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
     if (e != cudaSuccess) return e;
     k<<<a.grid, C::THREADS, C::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
@@ -292,15 +303,16 @@ size_t tc_encoder_bwd_workspace(const Problem &pr, int sms) {
 cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *K, const void *V,
                                   const uint8_t *mask, const float *Z, const float *L,
                                   const float *dZ, float *dQ, void *dK, void *dV, void *ws,
-                                  size_t ws_bytes, int sms, unsigned *status, cudaStream_t st) {
+                                  size_t ws_bytes, int sms, unsigned *status, cudaStream_t st,
+                                  bool accumulate) {
     if (!tc_bwd_supported(pr.bf16, pr.M, pr.D)) return cudaErrorNotSupported;
     BwdLayout l;
     bwd_layout(pr, sms, l);
     if (ws_bytes < l.bytes) return cudaErrorInvalidValue;
     const int64_t BH = (int64_t)pr.B * pr.H;
     if (BH == 0) return cudaSuccess;
-    if (l.T_total == 0)            // no token: dQ = 0, no dK / dV
-        return cudaMemsetAsync(dQ, 0, sizeof(float) * (size_t)BH * pr.M * pr.D, st);
+    if (l.T_total == 0)            // no token: no share of dQ, no dK / dV
+        return accumulate ? cudaSuccess : cudaMemsetAsync(dQ, 0, sizeof(float) * (size_t)BH * pr.M * pr.D, st);
     char *w = (char *)ws;
     __nv_bfloat16 *dzb = (__nv_bfloat16 *)(w + l.dzb);
     float *lc = (float *)(w + l.lc), *part = (float *)(w + l.part);
@@ -330,16 +342,21 @@ cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *
     a.mask = mask;
     a.lc = lc;
     a.part = part;
+    a.dk_acc = accumulate ? (const __nv_bfloat16 *)dK : nullptr;
     a.P_max = l.P_max;
     a.T_bh = l.T_bh;
     a.T_total = l.T_total;
     a.grid = l.grid;
     a.status = status;
-    e = pr.M == 128 ? launch_bwd<128>(maps, a, st) : launch_bwd<64>(maps, a, st);
+    if (accumulate)
+        e = pr.M == 128 ? launch_bwd<128, true>(maps, a, st) : launch_bwd<64, true>(maps, a, st);
+    else
+        e = pr.M == 128 ? launch_bwd<128, false>(maps, a, st) : launch_bwd<64, false>(maps, a, st);
     if (e != cudaSuccess) return e;
     const int64_t n4 = BH * pr.M * 16;
     tc::bwd_dq_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(part, dQ, BH, pr.M, l.P_max,
-                                                                          l.T_bh, l.T_total, l.grid);
+                                                                          l.T_bh, l.T_total, l.grid,
+                                                                          accumulate ? 1 : 0);
     note_launch();
     return cudaGetLastError();
 }

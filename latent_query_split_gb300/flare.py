@@ -23,13 +23,14 @@ FLARE_ERR_WORKSPACE, FLARE_ERR_CUDA, FLARE_ERR_TIMEOUT = 3, 4, 5
 FLARE_F32, FLARE_BF16 = 0, 1
 KERNELS = {"auto": 0, "simt": 1, "tensor": 2}
 (FLARE_OP_ENCODER_FWD, FLARE_OP_LSE_MERGE, FLARE_OP_DECODE_FWD, FLARE_OP_FWD,
- FLARE_OP_PP_FWD, FLARE_OP_ENCODER_BWD, FLARE_OP_DECODE_BWD) = range(7)
+ FLARE_OP_PP_FWD, FLARE_OP_ENCODER_BWD, FLARE_OP_DECODE_BWD, FLARE_OP_BWD,
+ FLARE_OP_PP_BWD) = range(9)
 FLARE_MAX_SHARDS = 256
 
 # Every symbol the header declares (checked by the test-suite).
 EXPORTS = ("flare_workspace_bytes", "flare_encoder_fwd", "flare_lse_merge", "flare_decode_fwd",
            "flare_fwd", "flare_pp_fwd", "flare_encoder_bwd", "flare_decode_bwd",
-           "flare_encoder_fwd_noalloc",
+           "flare_bwd", "flare_pp_bwd", "flare_encoder_fwd_noalloc",
            "flare_device_status", "flare_last_error_string", "flare_version",
            "flare_launch_count")
 
@@ -75,6 +76,8 @@ def load_library(build_if_missing: bool = True):
     lib.flare_pp_fwd.argtypes = [D, P, P, P, P, P, P, P, I, P, P, P, P, P, P, Z, P]
     lib.flare_encoder_bwd.argtypes = [D, P, P, P, P, P, I, P, P, P, P, P, P, P, Z, P]
     lib.flare_decode_bwd.argtypes = [D, P, P, P, P, P, P, P, P, Z, P]
+    lib.flare_bwd.argtypes = [D, P, P, P, P, P, I, P, P, P, P, P, P, P, Z, P]
+    lib.flare_pp_bwd.argtypes = [D, P, P, P, P, P, P, P, I, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]
     lib.flare_encoder_fwd_noalloc.argtypes = [D, P, P, P, P, P, I, P, P, P, P, P]
     lib.flare_device_status.argtypes = [P]
     lib.flare_last_error_string.restype = ctypes.c_char_p
@@ -279,6 +282,55 @@ def flare_decode_bwd(Q, Z, K, dY, *, dQ=None, dZ=None, dK=None, workspace=None, 
     _check(lib.flare_decode_bwd(ctypes.byref(dims), _ptr(Q), _ptr(Z), _ptr(K), _ptr(dY), _ptr(dQ),
                                 _ptr(dZ), _ptr(dK), _ptr(ws), nbytes, _stream(stream)))
     return dQ, dZ, dK
+
+
+def flare_bwd(Q, K, V, mask, shard_offsets, Z, L, dY, *, dQ=None, dK=None, dV=None,
+              workspace=None, scale=None, kernel="auto", stream=None):
+    """FLARE mixer backward from the forward's (Z, L) and the output gradient
+    dY; returns (dQ [B,H,M,D] fp32, dK, dV in K's dtype)."""
+    lib = load_library()
+    dims = make_dims(Q, K, scale, kernel)
+    B, N, H, D = K.shape
+    M = Q.shape[-2]
+    shard_offsets = [0, N] if shard_offsets is None else list(shard_offsets)
+    if dQ is None:
+        dQ = torch.empty((B, H, M, D), dtype=torch.float32, device=K.device)
+    if dK is None:
+        dK, dV = torch.empty_like(K), torch.empty_like(V)
+    ws, nbytes = _workspace(FLARE_OP_BWD, dims, shard_offsets, workspace, K.device)
+    arr, R = _offsets(shard_offsets)
+    _check(lib.flare_bwd(ctypes.byref(dims), _ptr(Q), _ptr(K), _ptr(V), _ptr(mask), arr, R,
+                         _ptr(Z), _ptr(L), _ptr(dY), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws),
+                         nbytes, _stream(stream)))
+    return dQ, dK, dV
+
+
+def flare_pp_bwd(Qseed, Kt, Vt, K, V, mask, shard_offsets, Qdyn, L1, Z, L2, dY, *, dQseed=None,
+                 dKt=None, dVt=None, dK=None, dV=None, dQdyn=None, want_dQdyn=False,
+                 workspace=None, scale=None, kernel="auto", stream=None):
+    """FLARE++ mixer backward from the forward's (Qdyn, L1, Z, L2) and dY;
+    returns (dQseed [B,H,M,D] fp32, dKt, dVt, dK, dV, dQdyn or None)."""
+    lib = load_library()
+    dims = make_dims(Qseed, K, scale, kernel)
+    B, N, H, D = K.shape
+    M = Qseed.shape[-2]
+    shard_offsets = [0, N] if shard_offsets is None else list(shard_offsets)
+    f32 = dict(dtype=torch.float32, device=K.device)
+    if dQseed is None:
+        dQseed = torch.empty((B, H, M, D), **f32)
+    if dKt is None:
+        dKt, dVt = torch.empty_like(Kt), torch.empty_like(Vt)
+    if dK is None:
+        dK, dV = torch.empty_like(K), torch.empty_like(V)
+    if dQdyn is None and want_dQdyn:
+        dQdyn = torch.empty((B, H, M, D), **f32)
+    ws, nbytes = _workspace(FLARE_OP_PP_BWD, dims, shard_offsets, workspace, K.device)
+    arr, R = _offsets(shard_offsets)
+    _check(lib.flare_pp_bwd(ctypes.byref(dims), _ptr(Qseed), _ptr(Kt), _ptr(Vt), _ptr(K), _ptr(V),
+                            _ptr(mask), arr, R, _ptr(Qdyn), _ptr(L1), _ptr(Z), _ptr(L2), _ptr(dY),
+                            _ptr(dQseed), _ptr(dKt), _ptr(dVt), _ptr(dK), _ptr(dV), _ptr(dQdyn),
+                            _ptr(ws), nbytes, _stream(stream)))
+    return dQseed, dKt, dVt, dK, dV, dQdyn
 
 
 def flare_encoder_fwd_noalloc(Q, K, V, mask=None, shard_offsets=None, *, O_r=None, L_r=None,

@@ -9,7 +9,7 @@ routing" (context-parallel section): token tensors [B, N, H, D] (C = H*D
 channels of the per-token projections), the replicated latent queries or seeds
 [H, M, D], R token shards with unequal sizes and padding excluded by a mask.
 
-The six named workloads:
+The eight named workloads:
   c1_fp32_small  FLARE fwd fp32, B1 H2 D32 M16 N1024, R4 equal shards, N(0,1)
   c2_bf16        FLARE fwd bf16, B4 H8 D64 M128 N65536, R8 shards of length
                  ~U[0.5,1.5]*N/R summing to N, 5% padded slots; K,V ~ N(0,1),
@@ -22,6 +22,12 @@ The six named workloads:
                  and 5 empty, shard 3 of batch element 1 all padding; dZ ~ N(0,1)
   c5_decbwd_bf16 decode bwd bf16 on the shapes of c5_bwd_bf16 (no mask: the
                  decode has none); Z, dY ~ N(0,1)
+  c5_mixbwd_bf16 FLARE mixer bwd bf16 (decode bwd, then encoder bwd adding
+                 into dQ, dK) on the shapes, shards and mask of c5_bwd_bf16;
+                 Q ~ N(0, 0.5^2), dY ~ N(0,1); Z, L from the forward
+  c5_ppbwd_bf16  FLARE++ mixer bwd bf16 on the same shapes, shards and mask;
+                 seeds ~ N(0, 0.02^2), K~,V~,K,V,dY ~ N(0,1); Q(X), L1, Z, L2
+                 from the forward
 N(0, sigma) is read with sigma the standard deviation.
 """
 from __future__ import annotations
@@ -38,6 +44,7 @@ import torch
 class Workload:
     name: str
     kind: str            # "flare_fwd" | "flare_pp_fwd" | "encoder_bwd" | "decode_bwd"
+                         # | "flare_bwd" | "flare_pp_bwd"
     dtype: str           # "f32" | "bf16"
     B: int
     H: int
@@ -78,6 +85,12 @@ CONFIGS: Dict[str, Workload] = {
                             padded_shard=(1, 3)),
     "c5_decbwd_bf16": Workload("c5_decbwd_bf16", "decode_bwd", "bf16", B=2, H=8, M=128,
                                N=131072, D=64, R=8, seed=1006),
+    "c5_mixbwd_bf16": Workload("c5_mixbwd_bf16", "flare_bwd", "bf16", B=2, H=8, M=128,
+                               N=131072, D=64, R=8, seed=1007, q_std=0.5, empty_shards=(2, 5),
+                               padded_shard=(1, 3)),
+    "c5_ppbwd_bf16": Workload("c5_ppbwd_bf16", "flare_pp_bwd", "bf16", B=2, H=8, M=128,
+                              N=131072, D=64, R=8, seed=1008, q_std=0.02, empty_shards=(2, 5),
+                              padded_shard=(1, 3)),
 }
 
 
@@ -128,8 +141,9 @@ def make_inputs(w: Workload, device="cpu") -> dict:
     Returns a dict with the token tensors ("K", "V", and "Kt", "Vt" for
     FLARE++), the latent query ("Q", or "Qseed"), host "offsets" (list of R+1
     ints), "mask" (uint8 [B,N] tensor on `device`, or None), "scale" (None =
-    D^-1/2), "dZ" for the encoder backward, and "Z" (fp32 [B,H,M,D]) and "dY"
-    (token-shaped) for the decode backward.
+    D^-1/2), "dZ" for the encoder backward, "Z" (fp32 [B,H,M,D]) and "dY"
+    (token-shaped) for the decode backward, and "dY" for the mixer backward
+    passes (their forward statistics come from the forward, not from here).
     """
     rng = np.random.default_rng(w.seed)
     offsets = shard_offsets(w.N, w.R, rng, equal=w.equal_shards, empty=w.empty_shards)
@@ -152,7 +166,7 @@ def make_inputs(w: Workload, device="cpu") -> dict:
     tok = (w.B, w.N, w.H, w.D)
     out = {"offsets": offsets, "scale": None,
            "mask": None if mask_np is None else torch.from_numpy(mask_np).to(dev)}
-    if w.kind == "flare_pp_fwd":
+    if w.kind in ("flare_pp_fwd", "flare_pp_bwd"):
         out["Qseed"] = normal((w.H, w.M, w.D), w.q_std)
         out["Kt"] = normal(tok)
         out["Vt"] = normal(tok)
@@ -170,6 +184,8 @@ def make_inputs(w: Workload, device="cpu") -> dict:
     if w.kind == "decode_bwd":
         out["Z"] = torch.randn((w.B, w.H, w.M, w.D), generator=g, device=dev,
                                dtype=torch.float32)
+        out["dY"] = normal(tok)
+    if w.kind in ("flare_bwd", "flare_pp_bwd"):
         out["dY"] = normal(tok)
     out["boosted_tokens"] = boosted
     return out

@@ -165,3 +165,57 @@ def test_decode_bwd_c5_shapes_sampled(cuda_device):
             bound = 2e-2 * max(1.0, float(np.abs(ref).max()))
             assert_close(f"{name}[{b},{h}]", dev[b:b + 1, h:h + 1], ref, "bf16", atol=bound)
         assert_close(f"dK[{b},:,{h}]", dK[b:b + 1, :, h:h + 1], dKo, "bf16")
+
+
+def _bwd_bound(ref):
+    """dQ-like sums over all N tokens of bf16-rounded products: 2e-2 of
+    max(1, largest reference magnitude) (rounding error grows like sqrt(N))."""
+    return 2e-2 * max(1.0, float(np.abs(ref).max()))
+
+
+def test_c5_flare_bwd_full_size_sampled(cuda_device):
+    """FLARE mixer backward at B2 H8 D64 M128 N131072 with empty shards and an
+    all-padding shard: sampled (b, h) pairs against the oracle's own forward
+    and backward; padded tokens get no dV."""
+    w = workloads.CONFIGS["c5_mixbwd_bf16"]
+    inp = workloads.make_inputs(w, device="cuda")
+    Q, K, V, mask, off, dY = inp["Q"], inp["K"], inp["V"], inp["mask"], inp["offsets"], inp["dY"]
+    _, _, Z, L = flare.flare_encoder_fwd(Q, K, V, mask, off)
+    dQ, dK, dV = flare.flare_bwd(Q, K, V, mask, off, Z, L, dY)
+    flare.flare_device_status()
+    pad = mask == 0
+    assert dV[pad].float().abs().max().item() == 0.0
+    for b, h in [(0, 3), (1, 5)]:
+        Qh = Q[h:h + 1].cpu()
+        Kh, Vh, dYh = _head(K, b, h), _head(V, b, h), _head(dY, b, h)
+        mh = _mask(mask, b)
+        Zo, Lo = oracle.encode(Qh, Kh, Vh, mh)
+        dQo, dKo, dVo = oracle.flare_bwd(Qh, Kh, Vh, mh, Zo, Lo, dYh)
+        assert_close(f"dQ[{b},{h}]", dQ[b:b + 1, h:h + 1], dQo, "bf16", atol=_bwd_bound(dQo))
+        assert_close(f"dK[{b},:,{h}]", dK[b:b + 1, :, h:h + 1], dKo, "bf16")
+        assert_close(f"dV[{b},:,{h}]", dV[b:b + 1, :, h:h + 1], dVo, "bf16")
+
+
+def test_c5_flare_pp_bwd_full_size_sampled(cuda_device):
+    """FLARE++ mixer backward on the same shapes: the library's forward
+    statistics feed the library's backward, the oracle's its own; sampled
+    (b, h) pairs of all five gradients and of dQ(X)."""
+    w = workloads.CONFIGS["c5_ppbwd_bf16"]
+    inp = workloads.make_inputs(w, device="cuda")
+    Qs, Kt, Vt, K, V = inp["Qseed"], inp["Kt"], inp["Vt"], inp["K"], inp["V"]
+    mask, off, dY = inp["mask"], inp["offsets"], inp["dY"]
+    _, Qd, L1, Z, L2 = flare.flare_pp_fwd(Qs, Kt, Vt, K, V, mask, off)
+    out = flare.flare_pp_bwd(Qs, Kt, Vt, K, V, mask, off, Qd, L1, Z, L2, dY, want_dQdyn=True)
+    flare.flare_device_status()
+    for b, h in [(0, 0), (1, 6)]:
+        heads = [_head(x, b, h) for x in (Kt, Vt, K, V, dY)]
+        mh = _mask(mask, b)
+        Qdo, L1o, Zo, L2o, _ = oracle.flare_pp_fwd(Qs[h:h + 1].cpu(), *heads[:4], mh)
+        ref = oracle.flare_pp_bwd(Qs[h:h + 1].cpu(), *heads[:4], mh, Qdo, L1o, Zo, L2o, heads[4])
+        lat = lambda x: x[b:b + 1, h:h + 1]
+        tok = lambda x: x[b:b + 1, :, h:h + 1]
+        for name, dev, r in zip(("dQseed", "dKt", "dVt", "dK", "dV", "dQdyn"),
+                                (lat(out[0]), tok(out[1]), tok(out[2]), tok(out[3]), tok(out[4]), lat(out[5])),
+                                ref):
+            atol = _bwd_bound(r) if name in ("dQseed", "dQdyn") else None
+            assert_close(f"{name}[{b},{h}]", dev, r, "bf16", atol=atol)

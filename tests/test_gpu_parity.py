@@ -190,6 +190,67 @@ def test_decode_bwd(cuda_device, kernel, dt, M, D, N, replicated):
     assert torch.equal(dQ, dQ2) and torch.equal(dZ, dZ2) and torch.equal(dK, dK2)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dt,M,D,N,replicated", [("f32", 16, 32, 700, True), ("bf16", 128, 64, 3000, True),
+                                                 ("bf16", 64, 64, 2100, False), ("bf16", 256, 64, 900, True),
+                                                 ("bf16", 128, 64, 20000, True)])
+def test_flare_bwd(cuda_device, kernel, dt, M, D, N, replicated):
+    """FLARE mixer backward: the decode's shares of dQ and dK are written
+    first and the encoder's are added in place (dK read back and summed in
+    fp32); padded tokens keep the decode's dK and get no dV. The 20000-token
+    case walks several tiles per CTA across (b, h) boundaries."""
+    B, H = 2, 3 if N > 10000 else 2
+    off = [0, N // 4, N // 4, N]
+    Q, K, V, mask = _problem(30, B, H, M, N, D, dt, off, q_std=1.0, replicated=replicated)
+    mask[1, N // 2:] = 0
+    g = torch.Generator().manual_seed(31)
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    dY = torch.randn((B, N, H, D), generator=g).to(tdt).cuda()
+    Zo, Lo = oracle.encode(Q, K, V, mask)
+    Zf = torch.from_numpy(Zo).float().cuda()
+    Lf = torch.from_numpy(Lo).float().cuda()
+    dQ, dK, dV = _call(flare.flare_bwd, Q, K, V, mask, off, Zf, Lf, dY, kernel=kernel)
+    flare.flare_device_status()
+    dQo, dKo, dVo = oracle.flare_bwd(Q, K, V, mask, Zf, Lf, dY)
+    assert_close("dQ", dQ, dQo, dt)
+    assert_close("dK", dK, dKo, dt)
+    assert_close("dV", dV, dVo, dt)
+    pad = mask == 0
+    assert dV[pad].abs().max().item() == 0.0
+    dQ2, dK2, dV2 = _call(flare.flare_bwd, Q, K, V, mask, off, Zf, Lf, dY, kernel=kernel)
+    assert torch.equal(dQ, dQ2) and torch.equal(dK, dK2) and torch.equal(dV, dV2)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dt,M,D,N", [("f32", 16, 32, 700), ("bf16", 128, 64, 2500), ("bf16", 64, 64, 5000)])
+def test_flare_pp_bwd(cuda_device, kernel, dt, M, D, N):
+    """FLARE++ mixer backward from the oracle's forward statistics: the seeds'
+    gradient, the four token gradients and the summed gradient of Q(X)."""
+    B, H = 2, 2
+    off = [0, 600, 600, N]
+    g = torch.Generator().manual_seed(32)
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    Qs = (torch.randn((H, M, D), generator=g) * 0.5).to(tdt).cuda()
+    Kt, Vt, K, V, dY = (torch.randn((B, N, H, D), generator=g).to(tdt).cuda() for _ in range(5))
+    mask = (torch.rand((B, N), generator=g) > 0.1).to(torch.uint8).cuda()
+    Qdo, L1o, Zo, L2o, _ = oracle.flare_pp_fwd(Qs, Kt, Vt, K, V, mask)
+    Qd, L1, Z, L2 = (torch.from_numpy(x).float().cuda() for x in (Qdo, L1o, Zo, L2o))
+    out = _call(flare.flare_pp_bwd, Qs, Kt, Vt, K, V, mask, off, Qd, L1, Z, L2, dY, want_dQdyn=True,
+                kernel=kernel)
+    flare.flare_device_status()
+    # the device rounds Q(X) to bf16 as an operand: the oracle takes the same values
+    Qd_op = Qd.to(tdt).float() if dt == "bf16" else Qd
+    ref = oracle.flare_pp_bwd(Qs, Kt, Vt, K, V, mask, Qd_op, L1, Z, L2, dY)
+    # encoder 1's c = <dZ1, Z1> uses the unrounded Q(X)
+    ref1 = oracle.encode_bwd(Qs, Kt, Vt, mask, Qd, L1, ref[5])
+    for name, dev, r in zip(("dQseed", "dKt", "dVt", "dK", "dV", "dQdyn"), out,
+                            (ref1[0], ref1[1], ref1[2]) + tuple(ref[3:])):
+        assert_close(name, dev, r, dt)
+    out2 = _call(flare.flare_pp_bwd, Qs, Kt, Vt, K, V, mask, off, Qd, L1, Z, L2, dY, want_dQdyn=True,
+                 kernel=kernel)
+    assert all(torch.equal(x, y) for x, y in zip(out, out2))
+
+
 # ---- edge cases ------------------------------------------------------------------------
 
 @pytest.mark.parametrize("kernel", KERNELS)
