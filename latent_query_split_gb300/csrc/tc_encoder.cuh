@@ -8,9 +8,12 @@
 // log-sum-exp paragraph). Scores are never written to memory.
 //
 // One persistent CTA per SM walks a contiguous span of TILE-token tiles (see
-// TcTilePlan; TILE = 128 for D = 64, 64 for D = 128). Ten warps: warp 0 is the
-// TMA producer, warp 1 allocates tensor memory, warps 2-9 form two softmax
-// groups of four warps (one per TMEM lane quadrant, one latent row per thread).
+// TcTilePlan; TILE = 128 for D = 64, 64 for D = 128). Eleven warps: warp 0 is
+// the TMA producer, warp 1 allocates tensor memory and issues the PV MMAs,
+// warp 2 issues the S MMAs (an MMA issue blocks until the tensor pipe accepts
+// it, so two issuing warps overlap one's bookkeeping with the other's issue),
+// warps 3-10 form two softmax groups of four warps (one per TMEM lane quadrant,
+// one latent row per thread).
 //
 // Producer: K/V tiles into a STAGES-deep ring (L2 evict-first). The tile's
 // padding mask (prefetched one tile ahead; tokens past the shard end count as
@@ -21,15 +24,18 @@
 // mask.
 //
 // Two kernels share the producer and the merge:
-//  * enc_cs_kernel (M <= 128): warp 1 also issues every MMA (converged,
-//    elect.sync). S is double-buffered in tensor memory, so S of the next tile
-//    is computed while the softmax of this one runs. The two groups split each
-//    tile's tokens in halves; each keeps its own running max, sum and output
+//  * enc_cs_kernel (M <= 128): S is double-buffered in tensor memory, so S of
+//    the next tile is computed while the softmax of this one runs; S_{j+2}
+//    waits for PV_j, which read P from the same buffer (buf_free). The two
+//    groups split each tile's tokens in halves; each keeps its own running
+//    max, sum and output
 //    accumulator (the PV MMAs of a tile accumulate the first half of its
 //    tokens into O_0 and the second into O_1), so the groups never exchange
 //    anything inside a piece and are combined once when a piece ends.
-//  * enc_halves_kernel (M = 256): each group owns 128 latent rows and issues
-//    its own MMAs from one of its warps; S is single-buffered per group.
+//  * enc_ring_kernel (M = 256): each group owns 128 latent rows; the two
+//    groups' S tiles take turns in a ring of three tensor-memory buffers, so
+//    each group's next S is computed while its softmax runs.
+// A tile without padded tokens skips the bias MMA (the producer flags it).
 // Softmax: the row maximum over S (already scaled into log2 units by one
 // FFMA), lazy rescale (O and l are rescaled only when the row maximum grows by
 // more than kTau), P = exp2(S - m) in bf16 written back into tensor memory
@@ -141,7 +147,8 @@ __device__ __forceinline__ void umma_bias_elect(uint32_t d_tmem, uint32_t s_ones
 }
 
 // ---- producer (one warp): K/V tiles and their mask bias -----------------------
-// full(s) = bar0 + 8 s, empty(s) = bar0 + 8 (STAGES + s).
+// full(s) = bar0 + 8 s, empty(s) = bar0 + 8 (STAGES + s). Beside the bias rows
+// a per-stage word at PADF_OFF says whether the tile has any padded token.
 template <class C>
 __device__ __forceinline__ void produce_kv(const CUtensorMap *tmK, const CUtensorMap *tmV,
                                            const EncArgs &a, int64_t tb, int64_t ntiles,
@@ -179,8 +186,15 @@ __device__ __forceinline__ void produce_kv(const CUtensorMap *tmK, const CUtenso
         if (!__all_sync(0xffffffffu, wt.wait(empty(s), ((uint32_t)(j / STAGES) & 1) ^ 1))) break;
         // bias rows of this stage: bf16 0 (valid) or -inf (padding), then zeros
         uint4 *bs = reinterpret_cast<uint4 *>(smem + C::BIAS_OFF + s * C::BIAS_BYTES);
+        bool pad = false;
 #pragma unroll
-        for (int i = 0; i < MB; ++i) bs[lane + 32 * i] = make_uint4(mb[i] ? 0u : 0xFF80u, 0u, 0u, 0u);
+        for (int i = 0; i < MB; ++i) {
+            bs[lane + 32 * i] = make_uint4(mb[i] ? 0u : 0xFF80u, 0u, 0u, 0u);
+            pad |= mb[i] == 0;
+        }
+        // whether the tile has a padded token (else the MMA warp skips the bias MMA)
+        pad = __any_sync(0xffffffffu, pad);
+        if (lane == 0) reinterpret_cast<volatile uint32_t *>(smem + C::PADF_OFF)[s] = pad ? 1u : 0u;
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -223,7 +237,7 @@ struct CsCfg {
     static constexpr int HALF = TILE / 2;               // tokens of one group in a tile
     static constexpr int KA = D / 64;                   // 64-element atoms along D
     static constexpr int NSOFT = 256;
-    static constexpr int THREADS = 64 + NSOFT;
+    static constexpr int THREADS = 96 + NSOFT;         // producer, PV issuer, S issuer, softmax
     // tensor memory: S buffers b = 0, 1 at b*TILE (P of group g written as
     // bf16 pairs over the first HALF/2 columns of its own half of S), then O_0, O_1
     static constexpr uint32_t O_COL = 2 * TILE;
@@ -238,9 +252,10 @@ struct CsCfg {
     static constexpr uint32_t BIAS_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
     static constexpr uint32_t BIAS_BYTES = TILE * 16;
     static constexpr uint32_t ONES_OFF = BIAS_OFF + STAGES * BIAS_BYTES;
-    static constexpr uint32_t BAR_OFF = ONES_OFF + kOnesBytes;
-    // full[S], empty[S], q_full[2], s_full[2], p_full[2], o_done[2], drain, soft
-    static constexpr int NBAR = 2 * STAGES + 10;
+    static constexpr uint32_t PADF_OFF = ONES_OFF + kOnesBytes;   // per stage: tile has padding
+    static constexpr uint32_t BAR_OFF = PADF_OFF + 16 * ((STAGES * 4 + 15) / 16);
+    // full[S], empty[S], q_full[2], s_full[2], p_full[2], o_done[2], drain, soft, buf_free[2], drain2
+    static constexpr int NBAR = 2 * STAGES + 13;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     // the two groups' (m, l) of each row at a piece end, double-buffered by
     // piece parity: [2][2 groups][128 rows]
@@ -271,6 +286,8 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     auto o_done = [&](int b) { return bar0 + 8u * (2 * STAGES + 6 + b); };
     const uint32_t drain = bar0 + 8u * (2 * STAGES + 8);
     const uint32_t soft = bar0 + 8u * (2 * STAGES + 9);
+    auto buf_free = [&](int b) { return bar0 + 8u * (2 * STAGES + 10 + b); };
+    const uint32_t drain2 = bar0 + 8u * (2 * STAGES + 12);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
     float2 *stat = reinterpret_cast<float2 *>(smem + C::STAT_OFF);
@@ -293,8 +310,10 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             mbar_init(s_full(b), 1);
             mbar_init(p_full(b), 8);          // one arrival per softmax warp
             mbar_init(o_done(b), 1);
+            mbar_init(buf_free(b), 1);
         }
         mbar_init(drain, 1);
+        mbar_init(drain2, 1);
         mbar_init(soft, NSOFT);
         fence_mbar_init();
     }
@@ -307,8 +326,8 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp >= 2) {
-        const int i = threadIdx.x - 64;           // 0 .. 255
+    if (warp >= 3) {
+        const int i = threadIdx.x - 96;           // 0 .. 255
         // rows M..127 of both query buffers stay zero (only M rows are loaded)
         if (a.M < 128)
             for (int q = i; q < 2 * (int)C::Q_BYTES / 16; q += NSOFT) {
@@ -326,112 +345,112 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 
     if (warp == 0) {
         produce_kv<C>(&tmK, &tmV, a, tb, ntiles, smem, bar0, wt, lane);
-    } else if (warp == 1) {
-        // ---------------- MMA issue (whole warp, elect.sync) ----------------
-        // Order: S_0, S_1, then per tile j: PV_j (after P_j is written), S_{j+2}
-        // into the buffer PV_j has just read (MMAs execute in issue order).
-        // Q of generation u (the u-th (b, h) of the span) sits in buffer u & 1;
+    } else if (warp == 1 || warp == 2) {
+        // ---------------- MMA issue: warp 2 every S, warp 1 every PV ----------------
+        // S_{j+2} goes into buffer j & 1 once PV_j (which read P there) has
+        // completed (buf_free). Q of generation u sits in buffer u & 1;
         // generation u + 1 is fetched once S of generation u - 1 has completed.
         auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
             return __all_sync(0xffffffffu, wt.wait(bar, par));
         };
-        const int bh0 = (int)(tb / pl.T_bh);
-        const int last_gen = ntiles > 0 ? (int)((te - 1) / pl.T_bh) - bh0 : -1;
-        int q_req = -1;                          // newest generation requested
-        auto request_q = [&](int u) {
-            if (lane == 0) {
-                const int bh = bh0 + u, b = bh / a.H, h = bh - b * a.H;
-                const int rows = a.M < 128 ? a.M : 128;
-                mbar_arrive_expect_tx(q_full(u & 1), KA * rows * 128);
-#pragma unroll
-                for (int ka = 0; ka < KA; ++ka)
-                    tma_load_4d(sQ + (u & 1) * C::Q_BYTES + ka * C::Q_ATOM, &tmQ, 64 * ka, 0, h,
-                                a.q_per_batch ? b : 0, q_full(u & 1));
-            }
-            __syncwarp();
-            q_req = u;
-        };
         constexpr uint32_t idS = idesc_bf16_m128(TILE, 0);
         constexpr uint32_t idPV = idesc_bf16_m128(D, 1);
-        TileCursor cs, cp;                       // cursors of the next S tile and the PV tile
-        cs.init(pl, tb);
-        cp = cs;
-        int64_t js = 0;
-        int s_bh = -1;                           // (b, h) of the last S issued
-        auto issue_s = [&]() -> bool {           // S of tile js into buffer js & 1
-            const int u = cs.bh - bh0;
-            const bool gen_start = cs.bh != s_bh;
-            // Q of a generation is waited for once, before its first S
-            if (gen_start && !wwait(q_full(u & 1), (uint32_t)(u >> 1) & 1)) return false;
-            const int s = (int)(js % STAGES);
-            if (!wwait(full(s), (uint32_t)(js / STAGES) & 1)) return false;
-            tc_fence_after();
-            const uint32_t tS = tmem + (uint32_t)(js & 1) * TILE;
-            umma_bias_elect(tS, sOnes, sBias + s * C::BIAS_BYTES, idS);
-            const uint64_t dQ = desc_sw128(sQ + (u & 1) * C::Q_BYTES, 16, 1024);
-            const uint64_t dK = desc_sw128(sStage + s * C::STAGE_BYTES, 16, 1024);
-#pragma unroll
-            for (int kb = 0; kb < D / 16; ++kb) {
-                const uint64_t offQ = (uint64_t)((kb >> 2) * C::Q_ATOM + (kb & 3) * 32) >> 4;
-                const uint64_t offK = (uint64_t)((kb >> 2) * C::KV_ATOM + (kb & 3) * 32) >> 4;
-                umma_ss_elect(tS, dQ + offQ, dK + offK, idS, 1u);
-            }
-            umma_commit_elect(s_full((int)(js & 1)));
-            s_bh = cs.bh;
-            // a new generation started: once S of the previous one has
-            // completed, its Q buffer takes the generation after this one
-            if (gen_start && u + 1 <= last_gen && q_req < u + 1) {
-                if (u >= 1 && !wwait(s_full((int)((js - 1) & 1)), (uint32_t)((js - 1) >> 1) & 1)) return false;
-                request_q(u + 1);
-            }
-            if (++js < ntiles) cs.next(pl);
-            return true;
-        };
+        const uint32_t my_drain = warp == 1 ? drain : drain2;
         bool ok = true;
-        if (ntiles > 0) {
-            request_q(0);
-            if (last_gen >= 1) request_q(1);
-        }
-        for (int i = 0; i < 2 && js < ntiles && ok; ++i) ok = issue_s();
-        for (int64_t j = 0; j < ntiles && ok; ++j) {
-            const int b = (int)(j & 1);
-            ok = __all_sync(0xffffffffu, wt.spin(p_full(b), (uint32_t)(j >> 1) & 1));
-            if (!ok) break;
-            tc_fence_after();
-            // O_g += P_g V_g over the tile's two halves; a piece's first tile
-            // starts both accumulators afresh
-            const bool first = (j == 0) || cp.k == 0;
-            const int s = (int)(j % STAGES);
-            const uint64_t dV = desc_sw128(sStage + s * C::STAGE_BYTES + KA * C::KV_ATOM, C::KV_ATOM, 1024);
-            const uint32_t tP = tmem + (uint32_t)b * TILE;
+        int q_req = -1;
+        if (warp == 2) {
+            const int bh0 = (int)(tb / pl.T_bh);
+            const int last_gen = ntiles > 0 ? (int)((te - 1) / pl.T_bh) - bh0 : -1;
+            auto request_q = [&](int u) {
+                if (lane == 0) {
+                    const int bh = bh0 + u, b = bh / a.H, h = bh - b * a.H;
+                    const int rows = a.M < 128 ? a.M : 128;
+                    mbar_arrive_expect_tx(q_full(u & 1), KA * rows * 128);
 #pragma unroll
-            for (int g = 0; g < 2; ++g)
+                    for (int ka = 0; ka < KA; ++ka)
+                        tma_load_4d(sQ + (u & 1) * C::Q_BYTES + ka * C::Q_ATOM, &tmQ, 64 * ka, 0, h,
+                                    a.q_per_batch ? b : 0, q_full(u & 1));
+                }
+                __syncwarp();
+                q_req = u;
+            };
+            TileCursor cs;
+            cs.init(pl, tb);
+            int s_bh = -1;
+            if (ntiles > 0) {
+                request_q(0);
+                if (last_gen >= 1) request_q(1);
+            }
+            for (int64_t js = 0; js < ntiles && ok; ++js) {
+                const int u = cs.bh - bh0;
+                const bool gen_start = cs.bh != s_bh;
+                const int b = (int)(js & 1);
+                if (js >= 2 && !(ok = wwait(buf_free(b), (uint32_t)((js >> 1) - 1) & 1))) break;
+                if (gen_start && !(ok = wwait(q_full(u & 1), (uint32_t)(u >> 1) & 1))) break;
+                const int s = (int)(js % STAGES);
+                if (!(ok = wwait(full(s), (uint32_t)(js / STAGES) & 1))) break;
+                tc_fence_after();
+                const uint32_t tS = tmem + (uint32_t)b * TILE;
+                const bool pad = reinterpret_cast<const volatile uint32_t *>(smem + C::PADF_OFF)[s] != 0;
+                if (pad) umma_bias_elect(tS, sOnes, sBias + s * C::BIAS_BYTES, idS);
+                const uint64_t dQ = desc_sw128(sQ + (u & 1) * C::Q_BYTES, 16, 1024);
+                const uint64_t dK = desc_sw128(sStage + s * C::STAGE_BYTES, 16, 1024);
 #pragma unroll
-                for (int kb = 0; kb < HALF / 16; ++kb)
-                    umma_ts_elect(tmem + C::O_COL + g * D, tP + g * HALF + kb * 8,
-                                  dV + (uint64_t)((g * HALF + kb * 16) * 128 >> 4), idPV,
-                                  (kb > 0 || !first) ? 1u : 0u);
-            umma_commit_elect(o_done(b));
-            umma_commit_elect(empty(s));
-            if (js < ntiles) ok = issue_s();
-            if (j + 1 < ntiles) cp.next(pl);
+                for (int kb = 0; kb < D / 16; ++kb) {
+                    const uint64_t offQ = (uint64_t)((kb >> 2) * C::Q_ATOM + (kb & 3) * 32) >> 4;
+                    const uint64_t offK = (uint64_t)((kb >> 2) * C::KV_ATOM + (kb & 3) * 32) >> 4;
+                    umma_ss_elect(tS, dQ + offQ, dK + offK, idS, (pad || kb > 0) ? 1u : 0u);
+                }
+                umma_commit_elect(s_full(b));
+                s_bh = cs.bh;
+                if (gen_start && u + 1 <= last_gen && q_req < u + 1) {
+                    if (u >= 1 && !(ok = wwait(s_full((int)((js - 1) & 1)), (uint32_t)((js - 1) >> 1) & 1))) break;
+                    request_q(u + 1);
+                }
+                if (js + 1 < ntiles) cs.next(pl);
+            }
+        } else {
+            TileCursor cp;
+            cp.init(pl, tb);
+            for (int64_t j = 0; j < ntiles && ok; ++j) {
+                const int b = (int)(j & 1);
+                if (!(ok = wwait(p_full(b), (uint32_t)(j >> 1) & 1))) break;
+                tc_fence_after();
+                // O_g += P_g V_g over the tile's two halves; a piece's first tile
+                // starts both accumulators afresh
+                const bool first = (j == 0) || cp.k == 0;
+                const int s = (int)(j % STAGES);
+                const uint64_t dV = desc_sw128(sStage + s * C::STAGE_BYTES + KA * C::KV_ATOM, C::KV_ATOM, 1024);
+                const uint32_t tP = tmem + (uint32_t)b * TILE;
+#pragma unroll
+                for (int g = 0; g < 2; ++g)
+#pragma unroll
+                    for (int kb = 0; kb < HALF / 16; ++kb)
+                        umma_ts_elect(tmem + C::O_COL + g * D, tP + g * HALF + kb * 8,
+                                      dV + (uint64_t)((g * HALF + kb * 16) * 128 >> 4), idPV,
+                                      (kb > 0 || !first) ? 1u : 0u);
+                umma_commit_elect(o_done(b));
+                umma_commit_elect(buf_free(b));
+                umma_commit_elect(empty(s));
+                if (j + 1 < ntiles) cp.next(pl);
+            }
         }
         if (wt.aborted()) {
-            umma_commit_elect(drain);
+            umma_commit_elect(my_drain);
             if (lane == 0) {
                 const uint64_t t0 = globaltimer();
                 for (int u = (q_req > 0 ? q_req - 1 : 0); u <= q_req; ++u)
                     while (!mbar_try_wait(q_full(u & 1), (uint32_t)(u >> 1) & 1) &&
                            globaltimer() - t0 < 500000000ull) {
                     }
-                while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < 500000000ull) {
+                while (!mbar_try_wait(my_drain, 0) && globaltimer() - t0 < 500000000ull) {
                 }
             }
         }
         __syncwarp();
     } else {
         // ---------------- softmax groups (column halves) ----------------
-        const int g = (warp - 2) >> 2;            // group: tokens [g*HALF, (g+1)*HALF) of a tile
+        const int g = (warp - 3) >> 2;            // group: tokens [g*HALF, (g+1)*HALF) of a tile
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
         const int rig = quad * 32 + lane;         // latent row (TMEM lane)
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
@@ -597,32 +616,39 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 }
 
 // ===============================================================================
-// enc_halves_kernel: M = 256, D = 64 (each group owns 128 latent rows)
+// enc_ring_kernel: M = 256, D = 64 (two groups of 128 latent rows, three S buffers)
 // ===============================================================================
+// Group g owns latent rows [128 g, 128 g + 128) and its own accumulator O_g.
+// S of (tile j, group g) is the q-th S computed, q = 2 j + g, and lives in
+// tensor-memory buffer q mod 3; P is written as bf16 pairs over the first
+// half of that buffer. Warp 2 issues S(0), S(1), ... (S(q + 3) once PV(q),
+// which read the same buffer, has completed: buf_free); warp 1 issues PV(q)
+// once P(q) is written. A group's next S is thus computed while its softmax
+// of this tile runs.
 template <int STAGES_>
-struct HalvesCfg {
+struct RingCfg {
     static constexpr int STAGES = STAGES_;
     static constexpr int D = 64;
     static constexpr int TILE = 128;
     static constexpr int KA = 1;
     static constexpr int NCH = TILE / 32;
     static constexpr int NSOFT = 256;
-    static constexpr int THREADS = 64 + NSOFT;
-    // tensor memory of group g (256 columns): S, P (bf16 pairs), O
-    static constexpr uint32_t S_COL = 0, P_COL = TILE, O_COL = TILE + TILE / 2;
-    static_assert(O_COL + D <= 256, "tensor-memory columns of one group exceeded");
+    static constexpr int THREADS = 96 + NSOFT;         // producer, PV issuer, S issuer, softmax
+    static constexpr uint32_t O_COL = 3 * TILE;         // O_0, O_1 after the three S buffers
+    static_assert(O_COL + 2 * D <= 512, "tensor-memory columns exceeded");
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t Q_ATOM = kAtom;
     static constexpr uint32_t KV_ATOM = TILE * 128;
-    static constexpr uint32_t Q_OFF = 0;                // rows 0-127 (group 0), 128-255 (group 1)
-    static constexpr uint32_t STAGE_OFF = Q_OFF + 2 * Q_ATOM;
-    static constexpr uint32_t STAGE_BYTES = 2 * KA * KV_ATOM;
+    static constexpr uint32_t Q_OFF = 0;                // two Q buffers (consecutive (b, h)) of 256 rows
+    static constexpr uint32_t Q_BYTES = 2 * kAtom;
+    static constexpr uint32_t STAGE_OFF = Q_OFF + 2 * Q_BYTES;
+    static constexpr uint32_t STAGE_BYTES = 2 * KV_ATOM;   // K atom, then V atom
     static constexpr uint32_t BIAS_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
     static constexpr uint32_t BIAS_BYTES = TILE * 16;
     static constexpr uint32_t ONES_OFF = BIAS_OFF + STAGES * BIAS_BYTES;
-    static constexpr uint32_t BAR_OFF = ONES_OFF + kOnesBytes;
-    // full[S], empty[S], q_full[2], s_full[2], p_full[2], o_done[2], drain[2], turn[2]
-    static constexpr int NBAR = 2 * STAGES + 14;
+    static constexpr uint32_t PADF_OFF = ONES_OFF + kOnesBytes;   // per stage: tile has padding
+    static constexpr uint32_t BAR_OFF = PADF_OFF + 16 * ((STAGES * 4 + 15) / 16);
+    // full[S], empty[S], q_full[2], s_full[3], p_full[3], o_done[2], drain[2], buf_free[3]
+    static constexpr int NBAR = 2 * STAGES + 15;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t BYTES = MISC_OFF + 64;
     static constexpr uint32_t ALLOC = BYTES + 1024;
@@ -630,11 +656,11 @@ struct HalvesCfg {
 };
 
 template <int STAGES>
-__global__ void __launch_bounds__(HalvesCfg<STAGES>::THREADS, 1)
-enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                  const __grid_constant__ CUtensorMap tmQ, const EncArgs a) {
-    using C = HalvesCfg<STAGES>;
-    constexpr int D = C::D, KA = C::KA, TILE = C::TILE, NCH = C::NCH;
+__global__ void __launch_bounds__(RingCfg<STAGES>::THREADS, 1)
+enc_ring_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                const __grid_constant__ CUtensorMap tmQ, const EncArgs a) {
+    using C = RingCfg<STAGES>;
+    constexpr int D = C::D, TILE = C::TILE, NCH = C::NCH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -644,12 +670,12 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const uint32_t bar0 = sbase + C::BAR_OFF;
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    auto q_full = [&](int g) { return bar0 + 8u * (2 * STAGES + g); };
-    auto s_full = [&](int g) { return bar0 + 8u * (2 * STAGES + 2 + g); };
-    auto p_full = [&](int g) { return bar0 + 8u * (2 * STAGES + 4 + g); };
-    auto o_done = [&](int g) { return bar0 + 8u * (2 * STAGES + 6 + g); };
-    auto drain = [&](int g) { return bar0 + 8u * (2 * STAGES + 8 + g); };
-    auto turn = [&](int g) { return bar0 + 8u * (2 * STAGES + 10 + g); };
+    auto q_full = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto s_full = [&](int u) { return bar0 + 8u * (2 * STAGES + 2 + u); };
+    auto p_full = [&](int u) { return bar0 + 8u * (2 * STAGES + 5 + u); };
+    auto o_done = [&](int g) { return bar0 + 8u * (2 * STAGES + 8 + g); };
+    auto drain = [&](int w) { return bar0 + 8u * (2 * STAGES + 10 + w); };
+    auto buf_free = [&](int u) { return bar0 + 8u * (2 * STAGES + 12 + u); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
 
@@ -664,16 +690,19 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         *abort_flag = 0;
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(empty(s), 2);               // one PV commit per group on the tile
+            mbar_init(empty(s), 1);               // committed after the tile's second PV
         }
-        for (int g = 0; g < 2; ++g) {
-            mbar_init(q_full(g), 1);
-            mbar_init(s_full(g), 1);
-            mbar_init(p_full(g), 4);
-            mbar_init(o_done(g), 1);
-            mbar_init(drain(g), 1);
-            mbar_init(turn(g), 4);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(q_full(b), 1);
+            mbar_init(o_done(b), 1);
         }
+        for (int u = 0; u < 3; ++u) {
+            mbar_init(s_full(u), 1);
+            mbar_init(p_full(u), 4);              // the owning group's four warps
+            mbar_init(buf_free(u), 1);            // PV of the buffer's P has completed
+        }
+        mbar_init(drain(0), 1);
+        mbar_init(drain(1), 1);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -685,8 +714,8 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp >= 2) {
-        const int i = threadIdx.x - 64;
+    if (warp >= 3) {
+        const int i = threadIdx.x - 96;
         reinterpret_cast<uint4 *>(smem + C::ONES_OFF)[i] = make_uint4(i < 128 ? 0x3F80u : 0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
     }
@@ -697,80 +726,128 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
 
     if (warp == 0) {
         produce_kv<C>(&tmK, &tmV, a, tb, ntiles, smem, bar0, wt, lane);
-    } else if (warp >= 2) {
-        // ---------------- softmax groups (row halves) ----------------
-        const int g = (warp - 2) >> 2;            // group: latent rows [128 g, 128 g + 128)
+    } else if (warp == 1 || warp == 2) {
+        // ---------------- MMA issue: warp 2 the S MMAs, warp 1 the PV MMAs ----------------
+        // (whole warps, elect.sync). S(q + 3) goes into the buffer of PV(q)
+        // once PV(q) has completed (buf_free); the two warps issue concurrently.
+        auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
+            return __all_sync(0xffffffffu, wt.wait(bar, par));
+        };
+        constexpr uint32_t idS = idesc_bf16_m128(TILE, 0);
+        constexpr uint32_t idPV = idesc_bf16_m128(D, 1);
+        const int64_t nq = 2 * ntiles;
+        const int me = warp - 1;                 // drain barrier of this warp
+        bool ok = true;
+        int q_req = -1;                          // newest Q generation requested (warp 2)
+        if (warp == 2) {
+            // Q of generation u (the u-th (b, h) of the span, both row halves)
+            // sits in buffer u & 1; generation u + 1 is fetched once S of
+            // generation u - 1 has completed.
+            const int bh0 = (int)(tb / pl.T_bh);
+            const int last_gen = ntiles > 0 ? (int)((te - 1) / pl.T_bh) - bh0 : -1;
+            auto request_q = [&](int u) {
+                if (lane == 0) {
+                    const int bh = bh0 + u, b = bh / a.H, h = bh - b * a.H;
+                    mbar_arrive_expect_tx(q_full(u & 1), 256 * 128);
+                    for (int g = 0; g < 2; ++g)
+                        tma_load_4d(sQ + (u & 1) * C::Q_BYTES + g * kAtom, &tmQ, 0, 128 * g, h,
+                                    a.q_per_batch ? b : 0, q_full(u & 1));
+                }
+                __syncwarp();
+                q_req = u;
+            };
+            const volatile uint32_t *padf = reinterpret_cast<const volatile uint32_t *>(smem + C::PADF_OFF);
+            TileCursor cs;
+            cs.init(pl, tb);
+            int s_bh = -1;
+            if (ntiles > 0) {
+                request_q(0);
+                if (last_gen >= 1) request_q(1);
+            }
+            for (int64_t qs = 0; qs < nq && ok; ++qs) {
+                const int64_t j = qs >> 1;
+                const int g = (int)(qs & 1);
+                const int u = cs.bh - bh0;
+                const int s = (int)(j % STAGES);
+                const int buf = (int)(qs % 3);
+                const bool gen_start = g == 0 && cs.bh != s_bh;
+                if (qs >= 3 && !(ok = wwait(buf_free(buf), (uint32_t)(qs / 3 - 1) & 1))) break;
+                if (gen_start && !(ok = wwait(q_full(u & 1), (uint32_t)(u >> 1) & 1))) break;
+                if (g == 0 && !(ok = wwait(full(s), (uint32_t)(j / STAGES) & 1))) break;
+                tc_fence_after();
+                const uint32_t tS = tmem + (uint32_t)buf * TILE;
+                const bool pad = padf[s] != 0;
+                if (pad) umma_bias_elect(tS, sOnes, sBias + s * C::BIAS_BYTES, idS);
+                const uint64_t dQ = desc_sw128(sQ + (u & 1) * C::Q_BYTES + g * kAtom, 16, 1024);
+                const uint64_t dK = desc_sw128(sStage + s * C::STAGE_BYTES, 16, 1024);
+#pragma unroll
+                for (int kb = 0; kb < D / 16; ++kb)
+                    umma_ss_elect(tS, dQ + (uint64_t)(kb * 32 >> 4), dK + (uint64_t)(kb * 32 >> 4), idS,
+                                  (pad || kb > 0) ? 1u : 0u);
+                umma_commit_elect(s_full(buf));
+                s_bh = cs.bh;
+                if (gen_start && u + 1 <= last_gen && q_req < u + 1) {
+                    if (u >= 1 && !(ok = wwait(s_full((int)((qs - 1) % 3)), (uint32_t)((qs - 1) / 3) & 1))) break;
+                    request_q(u + 1);
+                }
+                if (g == 1 && j + 1 < ntiles) cs.next(pl);
+            }
+        } else {
+            TileCursor cp;
+            cp.init(pl, tb);
+            for (int64_t q = 0; q < nq && ok; ++q) {
+                const int64_t j = q >> 1;
+                const int g = (int)(q & 1);
+                const int buf = (int)(q % 3);
+                if (!(ok = wwait(p_full(buf), (uint32_t)(q / 3) & 1))) break;
+                tc_fence_after();
+                // O_g += P V; a piece's first tile starts the accumulator afresh
+                const bool first = (j == 0) || cp.k == 0;
+                const int s = (int)(j % STAGES);
+                const uint64_t dV = desc_sw128(sStage + s * C::STAGE_BYTES + C::KV_ATOM, C::KV_ATOM, 1024);
+                const uint32_t tP = tmem + (uint32_t)buf * TILE;
+#pragma unroll
+                for (int kb = 0; kb < TILE / 16; ++kb)
+                    umma_ts_elect(tmem + C::O_COL + g * D, tP + kb * 8, dV + (uint64_t)(kb * (2048 >> 4)), idPV,
+                                  (kb > 0 || !first) ? 1u : 0u);
+                umma_commit_elect(o_done(g));
+                umma_commit_elect(buf_free(buf));
+                if (g == 1) {
+                    umma_commit_elect(empty(s));
+                    if (j + 1 < ntiles) cp.next(pl);
+                }
+            }
+        }
+        if (wt.aborted()) {
+            umma_commit_elect(drain(me));
+            if (lane == 0) {
+                const uint64_t t0 = globaltimer();
+                for (int u = (q_req > 0 ? q_req - 1 : 0); u <= q_req; ++u)
+                    while (!mbar_try_wait(q_full(u & 1), (uint32_t)(u >> 1) & 1) &&
+                           globaltimer() - t0 < 500000000ull) {
+                    }
+                while (!mbar_try_wait(drain(me), 0) && globaltimer() - t0 < 500000000ull) {
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- softmax groups (latent-row halves) ----------------
+        const int g = (warp - 3) >> 2;            // group: latent rows [128 g, 128 g + 128)
         const int quad = warp & 3;
         const int rig = quad * 32 + lane;
         const int row = g * 128 + rig;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        const uint32_t s_tmem = tmem + g * 256 + C::S_COL + lane_off;
-        const uint32_t p_tmem = tmem + g * 256 + C::P_COL + lane_off;
-        const uint32_t o_tmem = tmem + g * 256 + C::O_COL + lane_off;
+        const uint32_t o_tmem = tmem + C::O_COL + g * D + lane_off;
         auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
             return __all_sync(0xffffffffu, wt.wait(bar, par));
         };
         float m_ref = -INFINITY, l = 0.f;
         bool has = false;
-        int64_t k_last = -1;
 
-        // ---- tensor-core issue: one converged warp of the group (warps 2 and
-        // 7), elect.sync picking the issuing lane ----
-        const bool issuer_warp = warp == 2 + 5 * g;
-        const uint32_t tS = tmem + g * 256 + C::S_COL, tP = tmem + g * 256 + C::P_COL;
-        const uint32_t tO = tmem + g * 256 + C::O_COL;
-        const uint32_t sQg = sQ + g * C::Q_ATOM;              // this group's rows of Q
-        TileCursor cn;                            // issuer: the group's next tile to issue S for
-        cn.init(pl, tb);
-        int64_t jn = 0;
-        int q_bh = -1;                            // (b, h) whose Q the copy holds (or is loading)
-        uint32_t q_loads = 0;
-        auto load_q = [&](int bh) {               // the copy must not be read by a pending MMA
-            if (lane == 0) {
-                const int b = bh / a.H, h = bh - b * a.H;
-                mbar_arrive_expect_tx(q_full(g), 128 * 128);
-                tma_load_4d(sQg, &tmQ, 0, 128 * g, h, a.q_per_batch ? b : 0, q_full(g));
-            }
-            __syncwarp();
-            ++q_loads;
-            q_bh = bh;
-        };
-        uint32_t q_waited = 0;                    // Q loads already waited for
-        auto issue_s = [&]() -> bool {            // (warp-collective) S of tile jn
-            if (cn.bh != q_bh) load_q(cn.bh);
-            if (q_waited != q_loads) {
-                if (!wwait(q_full(g), (q_loads - 1) & 1)) return false;
-                q_waited = q_loads;
-            }
-            const int s = (int)(jn % STAGES);
-            if (!wwait(full(s), (uint32_t)(jn / STAGES) & 1)) return false;
-            tc_fence_after();
-            constexpr uint32_t idS = idesc_bf16_m128(TILE, 0);
-            umma_bias_elect(tS, sOnes, sBias + s * C::BIAS_BYTES, idS);
-            const uint64_t dQ = desc_sw128(sQg, 16, 1024);
-            const uint64_t dK = desc_sw128(sStage + s * C::STAGE_BYTES, 16, 1024);
-#pragma unroll
-            for (int kb = 0; kb < D / 16; ++kb)
-                umma_ss_elect(tS, dQ + (uint64_t)(kb * 32 >> 4), dK + (uint64_t)(kb * 32 >> 4), idS, 1u);
-            umma_commit_elect(s_full(g));
-            if (++jn < ntiles) cn.next(pl);
-            return true;
-        };
-        auto issue_pv = [&](int64_t j, bool acc) {   // (warp-collective) O += P V of tile j
-            constexpr uint32_t idPV = idesc_bf16_m128(D, 1);
-            const int s = (int)(j % STAGES);
-            const uint64_t dV = desc_sw128(sStage + s * C::STAGE_BYTES + KA * C::KV_ATOM, C::KV_ATOM, 1024);
-#pragma unroll
-            for (int kb = 0; kb < TILE / 16; ++kb)
-                umma_ts_elect(tO, tP + kb * 8, dV + kb * (2048 >> 4), idPV, (kb > 0 || acc) ? 1u : 0u);
-            umma_commit_elect(o_done(g));
-            umma_commit_elect(empty(s));
-        };
-        bool ok = true;
-        if (issuer_warp && ntiles > 0) ok = issue_s();
-
-        auto finalize_piece = [&](const TileCursor &ti) -> bool {
-            if (has && !wwait(o_done(g), (uint32_t)k_last & 1)) return false;
+        auto finalize_piece = [&](const TileCursor &ti, int64_t j) -> bool {
+            // the group's PV of the piece's last tile must be complete
+            if (!wwait(o_done(g), (uint32_t)j & 1)) return false;
             tc_fence_after();
             const int64_t slot = piece_slot_of(pl, ti, cta);
             float *part_row = a.part_O + (slot * a.M + row) * D;
@@ -795,7 +872,7 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         TileCursor ti;
         ti.init(pl, tb);
         const uint64_t c2 = f2pack(a.sl2, a.sl2);
-        for (int64_t j = 0; j < ntiles && ok; ++j) {
+        for (int64_t j = 0; j < ntiles; ++j) {
             const bool first = (j == 0) || ti.k == 0;
             const bool last = (j + 1 == ntiles) || ti.k == ti.nt - 1;
             if (first) {
@@ -803,15 +880,11 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 l = 0.f;
                 has = false;
             }
-            const int64_t k = j;
-            // the groups take turns on the ALUs (group 0 first): while one
-            // computes a softmax, the other's MMAs run
-            if ((g == 1 || k > 0) && !wwait(turn(g), (uint32_t)(g == 1 ? k : k - 1) & 1)) break;
-            if (!wwait(s_full(g), (uint32_t)k & 1)) break;
+            const int64_t q = 2 * j + g;
+            const int buf = (int)(q % 3);
+            const uint32_t s_tmem = tmem + (uint32_t)buf * TILE + lane_off;
+            if (!wwait(s_full(buf), (uint32_t)(q / 3) & 1)) break;
             tc_fence_after();
-            // S of this tile has completed, so the group's Q copy is free:
-            // fetch the next (b, h)'s Q while this tile is processed
-            if (issuer_warp && jn < ntiles && cn.bh != q_bh) load_q(cn.bh);
             // pass 1: the row maximum (padding is -inf in S already)
             float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -829,14 +902,14 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                     }
             }
             const float mt = fmaxf(mx[0], mx[1]) * a.sl2;
-            // the previous PV of this group reads P and writes O: let it finish
-            if (k_last >= 0 && !wwait(o_done(g), (uint32_t)k_last & 1)) break;
-            tc_fence_after();
             const bool need = mt > m_ref + kTau;
             if (__any_sync(0xffffffffu, need)) {
                 const float m_new = need ? mt : m_ref;
                 const float f = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
                 if (__any_sync(0xffffffffu, has)) {
+                    // O holds the group's PV of the previous tile once it completed
+                    if (!wwait(o_done(g), (uint32_t)(j - 1) & 1)) break;
+                    tc_fence_after();
 #pragma unroll
                     for (int c = 0; c < D / 16; ++c) {
                         uint32_t r[16];
@@ -850,7 +923,9 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 l *= f;
                 m_ref = m_new;
             }
-            // pass 2: P = exp2(t - m) in bf16 into P's columns
+            // pass 2: P = exp2(t - m) in bf16 over the buffer's first 64 columns
+            // (chunk c of S is loaded before P of chunk c is stored over S
+            // columns [16 c, 16 c + 16), which belong to chunks <= c)
             const bool live = __all_sync(0xffffffffu, m_ref != -INFINITY);
             const uint64_t nm2 = live ? f2pack(-m_ref, -m_ref) : f2pack(0.f, 0.f);
             uint64_t ls2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
@@ -881,50 +956,23 @@ enc_halves_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
 #pragma unroll
                         for (int i = 0; i < 16; ++i) pw[i] = 0u;
                     }
-                    tmem_st16(p_tmem + (c0 + b) * 16, pw);
+                    tmem_st16(s_tmem + (c0 + b) * 16, pw);
                 }
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {                     // one arrival per warp on each
-                mbar_arrive(p_full(g));
-                mbar_arrive(turn(g ^ 1));
-            }
+            if (lane == 0) mbar_arrive(p_full(buf));  // one arrival per warp
             {
                 float a0, a1, a2, a3;
                 f2unpack(ls2[0], a0, a1);
                 f2unpack(ls2[1], a2, a3);
                 l += (a0 + a1) + (a2 + a3);
             }
-            const bool acc = has;                // the group's first tile of a piece starts O afresh
             has = true;
-            k_last = k;
-            if (issuer_warp) {
-                ok = __all_sync(0xffffffffu, wt.spin(p_full(g), (uint32_t)k & 1));
-                if (ok) {
-                    tc_fence_after();
-                    issue_pv(j, acc);
-                    if (jn < ntiles) ok = issue_s();
-                }
-                if (!ok) break;
-            }
-            if (last && !finalize_piece(ti)) break;
+            if (last && !finalize_piece(ti, j)) break;
             if (j + 1 < ntiles) ti.next(pl);
         }
-        // after an abort: let the group's own copies and MMAs land before the CTA exits
-        if (issuer_warp && wt.aborted()) {
-            umma_commit_elect(drain(g));
-            if (lane == 0) {
-                const uint64_t t0 = globaltimer();
-                if (q_loads > 0)
-                    while (!mbar_try_wait(q_full(g), (q_loads - 1) & 1) && globaltimer() - t0 < 500000000ull) {
-                    }
-                while (!mbar_try_wait(drain(g), 0) && globaltimer() - t0 < 500000000ull) {
-                }
-            }
-        }
-        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();

@@ -196,7 +196,7 @@ cudaError_t launch_encoder_tc(const Problem &pr, const TcTilePlan &plan, const T
     else if (pr.D == 128 && pr.M <= 128)
         e = launch_enc<tc::CsCfg<128, 4>>(tc::enc_cs_kernel<128, 4>, mk, mv, mq, a, plan.grid, st);
     else if (pr.D == 64 && pr.M == 256)
-        e = launch_enc<tc::HalvesCfg<5>>(tc::enc_halves_kernel<5>, mk, mv, mq, a, plan.grid, st);
+        e = launch_enc<tc::RingCfg<4>>(tc::enc_ring_kernel<4>, mk, mv, mq, a, plan.grid, st);
     else
         return cudaErrorNotSupported;
     if (e != cudaSuccess) return e;
