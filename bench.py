@@ -439,12 +439,16 @@ def main(argv=None):
     ap.add_argument("--kernel", choices=["auto", "simt", "tensor"], default="auto")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--n", type=int, default=None,
+                    help="run the workload's structure at N tokens (small cases for profiler captures)")
     args = ap.parse_args(argv)
 
     from latent_query_split_gb300 import workloads
     if args.workload not in workloads.CONFIGS:
         raise SystemExit(f"unknown workload {args.workload}: {sorted(workloads.CONFIGS)}")
     w = workloads.CONFIGS[args.workload]
+    if args.n is not None:
+        w = w.scaled(N=args.n)
     if args.impl == "reference":
         return run_reference(args, w)
     if args.warmup < 3:
