@@ -19,8 +19,12 @@
 //    in the 128 TMEM lanes:
 //        S^T = K Q^T,  dP^T = V dZ^T                    (A, B from shared memory)
 //        P = exp2(S^T s log2e - L2), s dS = P (s dP - s c)  (softmax warps, fp32)
-//        dV = P^T dZ,  dK = (s dS)^T Q                  (A = bf16 P / dS in TMEM)
-//        dQ += (s dS) K                                 (A = dS in shared memory)
+//        dV = P^T dZ                                    (A = bf16 P^T in its own TMEM columns)
+//        dK = (s dS)^T Q,  dQ += (s dS) K               (A = bf16 dS^T in shared memory)
+//    Because P and dS leave S/dP's columns, S/dP of the next tile (same
+//    (b, h)) is issued as soon as the softmax warps have read this tile's,
+//    ahead of this tile's gradient MMAs; the softmax warps store a tile's
+//    dK/dV (its epilogue) after publishing the next tile's P and dS.
 //    dK and dV leave through shared memory by TMA stores; dQ accumulates in
 //    TMEM over the (b, h)'s tiles of the span and is written as one fp32
 //    partial per (b, h) piece of the span.
@@ -34,10 +38,11 @@
 // Warp roles of bwd_tc_kernel: warp 0 TMA producer (K, V ring; Q, dZ and the
 // row statistics on every (b, h) change), warp 1 TMEM allocator and MMA
 // issuer (lane 0), warps 2-9 two halves of four warps, each half owning M/2
-// latents of every token row (one token row per thread): the half's P and
-// s dS (written as bf16 into the half's own TMEM columns), then the tile's
-// epilogue (half 0 stores dV, half 1 dK, one TMA store per warp of 32 rows)
-// and, at the end of a (b, h) piece, half of the dQ partial's columns.
+// latents of every token row (one token row per thread): the half's P (bf16
+// into its half of P's TMEM columns) and s dS (bf16 into shared memory), then
+// the previous tile's epilogue (half 0 stores dV, half 1 dK, one TMA store
+// per warp of 32 rows) and, at the end of a (b, h) piece, half of the dQ
+// partial's columns.
 #pragma once
 
 #include "tc_common.cuh"
@@ -90,15 +95,17 @@ struct BwdCfg {
     static constexpr uint32_t LC_BYTES = 2 * 2 * 128 * 4;
     static constexpr uint32_t BAR_OFF = LC_OFF + LC_BYTES;
     // full[S], empty[S], qd_full, qd_free, lc_full[2], s_full, p_full,
-    // ds_free, dvdk_full, dvdk_free, dq_full, dq_free, drain
-    static constexpr int NBAR = 2 * STAGES + 13;
+    // ds_free, dvdk_full, dvdk_free, dq_full, dq_free, drain, sdp_free
+    static constexpr int NBAR = 2 * STAGES + 14;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t BYTES = MISC_OFF + 64;
     static constexpr uint32_t ALLOC = BYTES + 1024;
     static_assert(ALLOC <= 232448, "shared memory budget of one CTA exceeded");
     static_assert(QZ_BYTES % 1024 == 0, "operand tiles must stay 1 KB aligned");
     // tensor memory columns
-    static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 320, DQ_COL = 384;
+    // (P^T of a tile in bf16 pairs at P_COL, so S/dP of the next tile can
+    // overwrite S_COL/DP_COL while dV reads P)
+    static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 320, DQ_COL = 384, P_COL = 448;
     static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -174,6 +181,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     const uint32_t s_full = bar0 + 8u * (2 * STAGES + 4), p_full = s_full + 8, ds_free = s_full + 16;
     const uint32_t dvdk_full = s_full + 24, dvdk_free = s_full + 32;
     const uint32_t dq_full = s_full + 40, dq_free = s_full + 48, drain = s_full + 56;
+    const uint32_t sdp_free = s_full + 64;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
     float *lcs = reinterpret_cast<float *>(smem + C::LC_OFF);
@@ -204,6 +212,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         mbar_init(dq_full, 1);
         mbar_init(dq_free, 8);
         mbar_init(drain, 1);
+        mbar_init(sdp_free, 8);        // every softmax warp has read S and dP of the tile
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -294,6 +303,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             const uint64_t dQm = desc_sw128(sQ, TB, 1024);          // Q, MN-major (B of dK)
             const uint64_t dZm = desc_sw128(sdZ, TB, 1024);         // dZ, MN-major (B of dV)
             const uint64_t dDS = desc_sw128(sDS, TB, 1024);         // s dS^T, MN-major (A of dQ)
+            const uint64_t dDSk = desc_sw128(sDS, 16, 1024);        // s dS^T, K-major (A of dK)
             int64_t bhS = bh0, ktS = k0, curS = -1;                  // cursor of the S tiles
             int uS = -1;
             bool ok = true;
@@ -332,29 +342,30 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                     ++bhN;
                 }
                 const bool last = (j + 1 == ntiles) || bhN != bhP;
+                // tile j + 1 of the same (b, h): its S/dP as soon as S/dP of tile j is read
+                const bool early = j + 1 < ntiles && !last;
+                if (early) {
+                    if (!(ok = wt.wait(sdp_free, (uint32_t)j & 1))) break;
+                    if (!(ok = issue_sdp(j + 1))) break;
+                }
                 if (!(ok = wt.wait(p_full, (uint32_t)j & 1))) break;
                 tc_fence_after();
                 if (j > 0 && !(ok = wt.wait(dvdk_free, (uint32_t)(j - 1) & 1))) break;
                 tc_fence_after();
-                // dV = P^T dZ, dK = (s dS)^T Q: K = M latents, 16 per MMA; half h's
-                // latents sit (bf16 pairs) from column h * M/2 of S and of dP
-                auto pcol = [](int kb) -> uint32_t {
-                    constexpr int W = M / 2;
-                    const int half = 16 * kb / W;
-                    return (uint32_t)(W * half + 8 * (kb - half * (W / 16)));
-                };
+                // dV = P^T dZ (A = P^T from tensor memory), dK = (s dS)^T Q (A = dS^T
+                // from shared memory): K = M latents, 16 per MMA
 #pragma unroll
                 for (int kb = 0; kb < M / 16; ++kb)
-                    umma_bf16_ts(tmem + C::DV_COL, tmem + C::S_COL + pcol(kb), dZm + kb * (2048 >> 4), idG,
+                    umma_bf16_ts(tmem + C::DV_COL, tmem + C::P_COL + 8 * kb, dZm + kb * (2048 >> 4), idG,
                                  kb > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kb = 0; kb < M / 16; ++kb)
-                    umma_bf16_ts(tmem + C::DK_COL, tmem + C::DP_COL + pcol(kb), dQm + kb * (2048 >> 4), idG,
-                                 kb > 0 ? 1u : 0u);
+                    umma_bf16_ss(tmem + C::DK_COL, dDSk + (uint64_t)(((kb >> 2) * TB + (kb & 3) * 32) >> 4),
+                                 dQm + kb * (2048 >> 4), idG, kb > 0 ? 1u : 0u);
                 umma_commit(dvdk_full);
                 if (last) umma_commit(qd_free);
-                // the next tile's scores overwrite P and dS in TMEM (MMAs run in issue order)
-                if (j + 1 < ntiles && !(ok = issue_sdp(j + 1))) break;
+                // a tile of the next (b, h): its Q and dZ arrive once qd_free fired
+                if (j + 1 < ntiles && !early && !(ok = issue_sdp(j + 1))) break;
                 // dQ += (s dS) K over the tile's 128 tokens, 16 per MMA
                 if (first && uP > 0 && !(ok = wt.wait(dq_free, (uint32_t)(uP - 1) & 1))) break;
                 tc_fence_after();
@@ -382,7 +393,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         }
         __syncwarp();
     } else {
-        // ---------------- softmax halves + epilogue (warps 2-9) ----------------
+        // ---------------- softmax halves + deferred epilogue (warps 2-9) ----------------
+        // Per tile j: S and dP loaded (then sdp_free, so S/dP of tile j + 1 can
+        // be computed), P into P_COL once dV of tile j - 1 is done, s dS^T into
+        // shared memory once dK and dQ of tile j - 1 are done, p_full; then the
+        // epilogue of tile j - 1, whose dV, dK were computed meanwhile.
         constexpr int W = M / 2;                              // latents of each half
         const int hf = (warp - 2) >> 2;                       // latent half
         const int quad = warp & 3;
@@ -390,6 +405,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const uint32_t s_tm = tmem + C::S_COL + W * hf + lane_off;
         const uint32_t dp_tm = tmem + C::DP_COL + W * hf + lane_off;
+        const uint32_t p_tm = tmem + C::P_COL + (W / 2) * hf + lane_off;   // this half's P^T (bf16 pairs)
         const uint64_t c2 = f2pack(a.sl2, a.sl2), sc2 = f2pack(a.s, a.s);
         // this warp's 32-row slab of the dV (half 0) or dK (half 1) staging tile
         uint8_t *slab = smem + C::OUT_OFF + (hf * 4 + quad) * (32 * 128);
@@ -433,89 +449,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 cp_async_commit();
             }
         };
-        Cursor cu{bh0, k0, (int)(bh0 / a.H), (int)(bh0 - (bh0 / a.H) * a.H)};
-        int64_t cur = -1;
-        int u = -1, pieces = 0;
-        Cursor ca = cu;                                           // tile j + 2
-        uint32_t mb0 = 0, mb1 = 0;                                // mask bytes of tiles j, j + 1
-        if (ntiles > 0) {
-            mb0 = mask_byte(ca);
-            prefetch_dk(ca);
-        }
-        advance(ca);
-        if (ntiles > 1) mb1 = mask_byte(ca);
-        advance(ca);
-        for (int64_t j = 0; j < ntiles; ++j) {
-            const int64_t bh = cu.bh, kt = cu.kt;
-            const int b = cu.b, h = cu.h;
-            if (bh != cur) {
-                ++u;
-                cur = bh;
-                if (!wwait(lc_full(u & 1), (uint32_t)(u >> 1) & 1)) break;
-            }
-            Cursor cn = cu;
-            advance(cn);
-            const bool last = (j + 1 == ntiles) || cn.bh != bh;
-            const float *nl2 = lcs + (u & 1) * 256, *ncs = nl2 + 128;
-            const bool valid = mb0 != 0;
-            mb0 = mb1;
-            mb1 = j + 2 < ntiles ? mask_byte(ca) : 0u;
-            advance(ca);
-            if (!wwait(s_full, (uint32_t)j & 1)) break;
-            tc_fence_after();
-            bool ok = true;
-#pragma unroll
-            for (int c = 0; c < W / 32; ++c) {
-                uint32_t rs[32], rp[32];
-                tmem_ld32(s_tm + 32 * c, rs);
-                tmem_ld32(dp_tm + 32 * c, rp);
-                tmem_wait_ld();
-                uint32_t pw[16], dw[16];
-                const int m0 = W * hf + 32 * c;                   // first latent of the chunk
-                if (valid) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = m0 + 2 * i;
-                        const uint64_t nl = *reinterpret_cast<const uint64_t *>(nl2 + m);
-                        const uint64_t nc = *reinterpret_cast<const uint64_t *>(ncs + m);
-                        float t0, t1;
-                        f2unpack(fma2(f2pack(__uint_as_float(rs[2 * i]), __uint_as_float(rs[2 * i + 1])), c2, nl),
-                                 t0, t1);
-                        const uint64_t p2 = f2pack(ex2(t0), ex2(t1));
-                        const uint64_t g2 =
-                            fma2(f2pack(__uint_as_float(rp[2 * i]), __uint_as_float(rp[2 * i + 1])), sc2, nc);
-                        float p0, p1, d0, d1;
-                        f2unpack(p2, p0, p1);
-                        f2unpack(mul2(p2, g2), d0, d1);
-                        pw[i] = pack_bf16(p0, p1);
-                        dw[i] = pack_bf16(d0, d1);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) pw[i] = dw[i] = 0u;
-                }
-                // over this half's own, already loaded, columns
-                tmem_st16(s_tm + 16 * c, pw);
-                tmem_st16(dp_tm + 16 * c, dw);
-                // the previous tile's dQ MMA has read the shared dS buffer
-                if (c == 0 && j > 0 && !(ok = wwait(ds_free, (uint32_t)(j - 1) & 1))) break;
-                // s dS^T row into the MN-major A operand of dQ
-                uint8_t *row = smem + C::DS_OFF + (m0 >> 6) * TB + rig * 128;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int chunk = ((m0 & 63) >> 3) + q;
-                    *reinterpret_cast<uint4 *>(row + ((chunk ^ (rig & 7)) << 4)) =
-                        make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]);
-                }
-            }
-            if (!ok) break;
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
-            // epilogue: half 0 takes dV, half 1 dK of the warp's 32 token rows
-            if (!wwait(dvdk_full, (uint32_t)j & 1)) break;
+        int pieces = 0;
+        // Epilogue of tile jp (cursor t): half 0 stores dV, half 1 dK of the
+        // warp's 32 token rows; at the end of a (b, h) piece, half hf writes
+        // columns [32 hf, 32 hf + 32) of the piece's dQ partial. `nxt`: the tile
+        // whose epilogue comes next (its old dK rows are prefetched), or null.
+        auto epilogue = [&](int64_t jp, const Cursor &t, bool lastp, const Cursor *nxt) -> bool {
+            if (!wwait(dvdk_full, (uint32_t)jp & 1)) return false;
             tc_fence_after();
             const uint32_t out_tm = tmem + (hf ? C::DK_COL : C::DV_COL) + lane_off;
             uint8_t *srow = slab + lane * 128;
@@ -544,6 +484,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                                    pack_bf16(f[6], f[7]));
                 }
             };
+            // the slab is free once the warp's previous store has read it
+            if (jp > 0) {
+                if (lane == 0) bulk_wait_group_read0();
+                __syncwarp();
+            }
             if constexpr (!ACC) {
                 uint32_t rg[2][32];
                 tmem_ld32(out_tm, rg[0]);
@@ -552,21 +497,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(dvdk_free);
-                // the slab is free once the warp's previous store has read it
-                if (j > 0) {
-                    if (lane == 0) bulk_wait_group_read0();
-                    __syncwarp();
-                }
                 pack32(rg[0], 0, false);
                 pack32(rg[1], 1, false);
             } else {
                 // one 32-column half at a time (fewer live registers); TMEM is
                 // released after the second half
-                if (j > 0) {
-                    if (lane == 0) bulk_wait_group_read0();
-                    __syncwarp();
-                }
-                const bool acc_row = hf == 1 && kt * 128 + rig < a.N;
+                const bool acc_row = hf == 1 && t.kt * 128 + rig < a.N;
                 if (acc_row) cp_async_wait0();
 #pragma unroll 1
                 for (int h2 = 0; h2 < 2; ++h2) {
@@ -583,17 +519,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             }
             fence_proxy_async_smem();
             __syncwarp();
-            const int n0 = (int)(kt * 128) + quad * 32;
+            const int n0 = (int)(t.kt * 128) + quad * 32;
             if (lane == 0 && n0 < a.N) {
                 // rows past N are clipped by the tensor map
-                tma_store_4d(tmOut, smem_u32(slab), 0, h, n0, b);
+                tma_store_4d(tmOut, smem_u32(slab), 0, t.h, n0, t.b);
                 bulk_commit_group();
             }
-            if (j + 1 < ntiles) prefetch_dk(cn);
-            if (last) {
+            if (nxt != nullptr) prefetch_dk(*nxt);
+            if (lastp) {
                 // the (b, h)'s dQ partial of this span: latent rows in the
                 // lanes, half hf takes columns [32 hf, 32 hf + 32)
-                if (!wwait(dq_full, (uint32_t)pieces & 1)) break;
+                if (!wwait(dq_full, (uint32_t)pieces & 1)) return false;
                 tc_fence_after();
                 uint32_t rq[32];
                 tmem_ld32(tmem + C::DQ_COL + 32 * hf + lane_off, rq);
@@ -602,8 +538,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 __syncwarp();
                 if (lane == 0) mbar_arrive(dq_free);
                 if (rig < M) {
-                    const int piece = cta - bwd_cta_of(bh * a.T_bh, a.T_total, a.grid);
-                    float4 *dst = reinterpret_cast<float4 *>(a.part + ((bh * a.P_max + piece) * M + rig) * 64 + 32 * hf);
+                    const int piece = cta - bwd_cta_of(t.bh * a.T_bh, a.T_total, a.grid);
+                    float4 *dst = reinterpret_cast<float4 *>(a.part + ((t.bh * a.P_max + piece) * M + rig) * 64 + 32 * hf);
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
                         dst[q] = make_float4(__uint_as_float(rq[4 * q]), __uint_as_float(rq[4 * q + 1]),
@@ -611,8 +547,103 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 }
                 ++pieces;
             }
+            return true;
+        };
+        Cursor cu{bh0, k0, (int)(bh0 / a.H), (int)(bh0 - (bh0 / a.H) * a.H)};
+        int64_t cur = -1;
+        int u = -1;
+        Cursor ca = cu;                                           // tile j + 2
+        uint32_t mb0 = 0, mb1 = 0;                                // mask bytes of tiles j, j + 1
+        if (ntiles > 0) {
+            mb0 = mask_byte(ca);
+            prefetch_dk(ca);
+        }
+        advance(ca);
+        if (ntiles > 1) mb1 = mask_byte(ca);
+        advance(ca);
+        Cursor pv = cu;                                           // the previous tile
+        bool pv_last = false;
+        bool ok = true;
+        for (int64_t j = 0; j < ntiles; ++j) {
+            const int64_t bh = cu.bh;
+            if (bh != cur) {
+                ++u;
+                cur = bh;
+                if (!(ok = wwait(lc_full(u & 1), (uint32_t)(u >> 1) & 1))) break;
+            }
+            Cursor cn = cu;
+            advance(cn);
+            const bool last = (j + 1 == ntiles) || cn.bh != bh;
+            const float *nl2 = lcs + (u & 1) * 256, *ncs = nl2 + 128;
+            const bool valid = mb0 != 0;
+            mb0 = mb1;
+            mb1 = j + 2 < ntiles ? mask_byte(ca) : 0u;
+            advance(ca);
+            if (!(ok = wwait(s_full, (uint32_t)j & 1))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < W / 32; ++c) {
+                uint32_t rs[32], rp[32];
+                tmem_ld32(s_tm + 32 * c, rs);
+                tmem_ld32(dp_tm + 32 * c, rp);
+                tmem_wait_ld();
+                if (c == W / 32 - 1) {
+                    // S and dP of this tile are in registers: the next tile's may be computed
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sdp_free);
+                }
+                uint32_t pw[16], dw[16];
+                const int m0 = W * hf + 32 * c;                   // first latent of the chunk
+                if (valid) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int m = m0 + 2 * i;
+                        const uint64_t nl = *reinterpret_cast<const uint64_t *>(nl2 + m);
+                        const uint64_t nc = *reinterpret_cast<const uint64_t *>(ncs + m);
+                        float t0, t1;
+                        f2unpack(fma2(f2pack(__uint_as_float(rs[2 * i]), __uint_as_float(rs[2 * i + 1])), c2, nl),
+                                 t0, t1);
+                        const uint64_t p2 = f2pack(ex2(t0), ex2(t1));
+                        const uint64_t g2 =
+                            fma2(f2pack(__uint_as_float(rp[2 * i]), __uint_as_float(rp[2 * i + 1])), sc2, nc);
+                        float p0, p1, d0, d1;
+                        f2unpack(p2, p0, p1);
+                        f2unpack(mul2(p2, g2), d0, d1);
+                        pw[i] = pack_bf16(p0, p1);
+                        dw[i] = pack_bf16(d0, d1);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pw[i] = dw[i] = 0u;
+                }
+                // P^T into P_COL once dV of the previous tile (which read it) is done
+                if (c == 0 && j > 0 && !(ok = wwait(dvdk_full, (uint32_t)(j - 1) & 1))) break;
+                tmem_st16(p_tm + 16 * c, pw);
+                // the previous tile's dK and dQ MMAs have read the shared dS buffer
+                if (c == 0 && j > 0 && !(ok = wwait(ds_free, (uint32_t)(j - 1) & 1))) break;
+                // s dS^T row: the K-major A of dK and the MN-major A of dQ
+                uint8_t *row = smem + C::DS_OFF + (m0 >> 6) * TB + rig * 128;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int chunk = ((m0 & 63) >> 3) + q;
+                    *reinterpret_cast<uint4 *>(row + ((chunk ^ (rig & 7)) << 4)) =
+                        make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]);
+                }
+            }
+            if (!ok) break;
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+            // the previous tile's epilogue (its dV, dK were computed meanwhile)
+            if (j > 0 && !(ok = epilogue(j - 1, pv, pv_last, &cu))) break;
+            pv = cu;
+            pv_last = last;
             cu = cn;
         }
+        if (ok && ntiles > 0) epilogue(ntiles - 1, pv, pv_last, nullptr);
         if (lane == 0) bulk_wait_group0();
     }
     tc_fence_before();
