@@ -14,11 +14,15 @@
 //    lanes:
 //        S^T = K Q^T,  G^T = dY Z^T                 (A, B from shared memory)
 //        A, s dT from the row softmax (warps 2-9)   (fp32, bf16 operands out)
-//        dK = (s dT) Q                              (A = s dT in TMEM)
+//        dK = (s dT) Q                              (A = s dT in its own TMEM columns)
 //        dQ += (s dT)^T K,  dZ += A^T dY           (A from shared memory, MN-major)
 //    Eight warps form two latent halves of every token row; the halves
-//    exchange the row maximum, then their partial row sums and <A, g>. dK
-//    leaves through shared memory (one TMA store per 32 rows); dQ and dZ
+//    exchange the row maximum, then their partial row sums and <A, g>.
+//    Because s dT leaves S's columns, S/G of the next tile (same (b, h)) is
+//    issued as soon as the halves have read this tile's, ahead of this tile's
+//    gradient MMAs; a tile's dK is stored (its epilogue) after the next tile's
+//    operands are out. dK leaves through shared memory (one TMA store per 32
+//    rows); dQ and dZ
 //    accumulate in TMEM over the (b, h)'s tiles of the span and are written
 //    as one fp32 piece per (b, h) of the span.
 //  * dbw_reduce_kernel: dQ and dZ = the sums of the pieces in piece order.
@@ -64,15 +68,17 @@ struct DbwCfg {
     static constexpr uint32_t XL_OFF = XM_OFF + 2 * 2 * 128 * 4;    // float2: (sum, <p, g>)
     static constexpr uint32_t BAR_OFF = XL_OFF + 2 * 2 * 128 * 8;
     // full[S], empty[S], qz_full, qz_free, s_full, p_full, at_free, dk_full,
-    // dk_free, pz_full, pz_free, drain
-    static constexpr int NBAR = 2 * STAGES + 10;
+    // dk_free, pz_full, pz_free, drain, sg_free
+    static constexpr int NBAR = 2 * STAGES + 11;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t BYTES = MISC_OFF + 64;
     static constexpr uint32_t ALLOC = BYTES + 1024;
     static_assert(ALLOC <= 232448, "shared memory budget of one CTA exceeded");
     static_assert(QZ_BYTES % 1024 == 0, "operand tiles must stay 1 KB aligned");
     // tensor memory columns
-    static constexpr uint32_t S_COL = 0, G_COL = 128, DK_COL = 256, DQ_COL = 320, DZ_COL = 384;
+    // (s dT of a tile in bf16 pairs at DT_COL, so S/G of the next tile can
+    // overwrite S_COL/G_COL while dK reads s dT)
+    static constexpr uint32_t S_COL = 0, G_COL = 128, DK_COL = 256, DQ_COL = 320, DZ_COL = 384, DT_COL = 448;
     static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -131,6 +137,7 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     const uint32_t s_full = qz_full + 16, p_full = qz_full + 24, at_free = qz_full + 32;
     const uint32_t dk_full = qz_full + 40, dk_free = qz_full + 48;
     const uint32_t pz_full = qz_full + 56, pz_free = qz_full + 64, drain = qz_full + 72;
+    const uint32_t sg_free = qz_full + 80;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
 
@@ -158,6 +165,7 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         mbar_init(pz_full, 1);
         mbar_init(pz_free, 8);
         mbar_init(drain, 1);
+        mbar_init(sg_free, 8);         // every softmax warp has read S and G of the tile
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -271,11 +279,6 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 }
                 return true;
             };
-            // s dT of half h's latents sits (bf16 pairs) from column h * M/2 of S
-            auto pcol = [](int kb) -> uint32_t {
-                const int half = 16 * kb / W;
-                return (uint32_t)(W * half + 8 * (kb - half * (W / 16)));
-            };
             int64_t bhP = bh0, ktP = k0;
             int uP = 0;
             if (ntiles > 0) ok = issue_sg(0);
@@ -287,19 +290,25 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                     ++bhN;
                 }
                 const bool last = (j + 1 == ntiles) || bhN != bhP;
+                // tile j + 1 of the same (b, h): its S/G as soon as S/G of tile j is read
+                const bool early = j + 1 < ntiles && !last;
+                if (early) {
+                    if (!(ok = wt.wait(sg_free, (uint32_t)j & 1))) break;
+                    if (!(ok = issue_sg(j + 1))) break;
+                }
                 if (!(ok = wt.wait(p_full, (uint32_t)j & 1))) break;
                 tc_fence_after();
                 if (j > 0 && !(ok = wt.wait(dk_free, (uint32_t)(j - 1) & 1))) break;
                 tc_fence_after();
-                // dK = (s dT) Q: K = M latents, 16 per MMA
+                // dK = (s dT) Q: K = M latents, 16 per MMA (A = s dT from its TMEM columns)
 #pragma unroll
                 for (int kb = 0; kb < M / 16; ++kb)
-                    umma_bf16_ts(tmem + C::DK_COL, tmem + C::S_COL + pcol(kb), dQm + kb * (2048 >> 4), idG,
+                    umma_bf16_ts(tmem + C::DK_COL, tmem + C::DT_COL + 8 * kb, dQm + kb * (2048 >> 4), idG,
                                  kb > 0 ? 1u : 0u);
                 umma_commit(dk_full);
                 if (last) umma_commit(qz_free);
-                // the next tile's scores overwrite dT in TMEM (MMAs run in issue order)
-                if (j + 1 < ntiles && !(ok = issue_sg(j + 1))) break;
+                // a tile of the next (b, h): its Q and Z arrive once qz_free fired
+                if (j + 1 < ntiles && !early && !(ok = issue_sg(j + 1))) break;
                 // dQ += (s dT)^T K, dZ += A^T dY over the tile's 128 tokens
                 if (first && uP > 0 && !(ok = wt.wait(pz_free, (uint32_t)(uP - 1) & 1))) break;
                 tc_fence_after();
@@ -333,12 +342,18 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         __syncwarp();
     } else {
         // ---------------- the two latent halves (warps 2-9) ----------------
+        // Per tile j: S and G loaded (then sg_free, so S/G of tile j + 1 can be
+        // computed), A and s dT formed, s dT into DT_COL once dK of tile j - 1
+        // is done, A^T and s dT^T into shared memory once dQ, dZ of tile j - 1
+        // are done, p_full; then the epilogue of tile j - 1, whose dK was
+        // computed meanwhile.
         const int hf = (warp - 2) >> 2;                       // latent half
         const int quad = warp & 3;
         const int rig = quad * 32 + lane;                     // token row within the tile
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const uint32_t s_tm = tmem + C::S_COL + W * hf + lane_off;
         const uint32_t g_tm = tmem + C::G_COL + W * hf + lane_off;
+        const uint32_t t_tm = tmem + C::DT_COL + (W / 2) * hf + lane_off;   // this half's s dT (bf16 pairs)
         const float sl2 = a.sl2, sc = a.s;
         float *xm = reinterpret_cast<float *>(smem + C::XM_OFF);
         float2 *xl = reinterpret_cast<float2 *>(smem + C::XL_OFF);
@@ -348,95 +363,13 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
             return __all_sync(0xffffffffu, wt.wait(bar, par));
         };
-        int64_t bh = bh0, kt = k0;
-        int b = (int)(bh0 / a.H), h = (int)(bh0 - (int64_t)b * a.H);
         int pieces = 0;
         uint32_t stores = 0;
-        for (int64_t j = 0; j < ntiles; ++j) {
-            int64_t bhN = bh, ktN = kt + 1;
-            int bN = b, hN = h;
-            if (ktN == a.T_bh) {
-                ktN = 0;
-                ++bhN;
-                if (++hN == a.H) {
-                    hN = 0;
-                    ++bN;
-                }
-            }
-            const bool last = (j + 1 == ntiles) || bhN != bh;
-            const int64_t n = kt * 128 + rig;
-            const bool valid = n < a.N;
-            if (!wwait(s_full, (uint32_t)j & 1)) break;
-            tc_fence_after();
-            // this half's scores: the maximum, exchanged with the other half
-            uint32_t sv[W / 32][32];
-#pragma unroll
-            for (int c = 0; c < W / 32; ++c) tmem_ld32(s_tm + 32 * c, sv[c]);
-            tmem_wait_ld();
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < W / 32; ++c)
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    mx = max3(mx, __uint_as_float(sv[c][2 * i]), __uint_as_float(sv[c][2 * i + 1]));
-            const int par = (int)(j & 1);
-            xm[(par * 2 + hf) * 128 + rig] = mx;
-            named_bar_sync(pair_bar, 64);
-            const float m2 = fmaxf(mx, xm[(par * 2 + (hf ^ 1)) * 128 + rig]) * sl2;
-            // p = 2^(s t log2 e - max), the half's partial sum and <p, g>
-            uint32_t gv[W / 32][32];
-#pragma unroll
-            for (int c = 0; c < W / 32; ++c) tmem_ld32(g_tm + 32 * c, gv[c]);
-            tmem_wait_ld();
-            float ls = 0.f, lr = 0.f;
-#pragma unroll
-            for (int c = 0; c < W / 32; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float p = ex2(fmaf(__uint_as_float(sv[c][i]), sl2, -m2));
-                    sv[c][i] = __float_as_uint(p);
-                    ls += p;
-                    lr = fmaf(p, __uint_as_float(gv[c][i]), lr);
-                }
-            xl[(par * 2 + hf) * 128 + rig] = make_float2(ls, lr);
-            named_bar_sync(pair_bar, 64);
-            const float2 o = xl[(par * 2 + (hf ^ 1)) * 128 + rig];
-            const float inv = valid ? 1.f / (ls + o.x) : 0.f;      // tokens past N: A = 0
-            const float r = (lr + o.y) / (ls + o.x);
-            // A and s dT in bf16: dT over this half's TMEM columns, both into
-            // the MN-major operands of dQ and dZ (after the last tile's
-            // products have read them)
-            if (j > 0 && !wwait(at_free, (uint32_t)(j - 1) & 1)) break;
-#pragma unroll
-            for (int c = 0; c < W / 32; ++c) {
-                uint32_t aw[16], tw[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float a0 = __uint_as_float(sv[c][2 * i]) * inv;
-                    const float a1 = __uint_as_float(sv[c][2 * i + 1]) * inv;
-                    const float t0 = sc * a0 * (__uint_as_float(gv[c][2 * i]) - r);
-                    const float t1 = sc * a1 * (__uint_as_float(gv[c][2 * i + 1]) - r);
-                    aw[i] = pack_bf16(a0, a1);
-                    tw[i] = pack_bf16(t0, t1);
-                }
-                tmem_st16(s_tm + 16 * c, tw);
-                const int m0 = W * hf + 32 * c;
-                uint8_t *arow = smem + C::A_OFF + (m0 >> 6) * TB + rig * 128;
-                uint8_t *trow = smem + C::DT_OFF + (m0 >> 6) * TB + rig * 128;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int pos = ((((m0 & 63) >> 3) + q) ^ (rig & 7)) << 4;
-                    *reinterpret_cast<uint4 *>(arow + pos) = make_uint4(aw[4 * q], aw[4 * q + 1], aw[4 * q + 2], aw[4 * q + 3]);
-                    *reinterpret_cast<uint4 *>(trow + pos) = make_uint4(tw[4 * q], tw[4 * q + 1], tw[4 * q + 2], tw[4 * q + 3]);
-                }
-            }
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
-            // epilogue: dK of the quadrant's 32 rows, half hf converts columns [32 hf, 32 hf + 32)
-            if (!wwait(dk_full, (uint32_t)j & 1)) break;
+        // Epilogue of tile jp at (bhp, ktp, bp, hp): dK of the quadrant's 32
+        // rows (half hf converts columns [32 hf, 32 hf + 32)); at the end of a
+        // (b, h) piece, the span's dQ (half 0) and dZ (half 1) pieces.
+        auto epilogue = [&](int64_t jp, int64_t bhp, int64_t ktp, int bp, int hp, bool lastp) -> bool {
+            if (!wwait(dk_full, (uint32_t)jp & 1)) return false;
             tc_fence_after();
             uint32_t rk[32];
             tmem_ld32(tmem + C::DK_COL + 32 * hf + lane_off, rk);
@@ -458,17 +391,15 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             }
             fence_proxy_async_smem();
             named_bar_sync(pair_bar, 64);
-            const int n0 = (int)(kt * 128) + quad * 32;
+            const int n0 = (int)(ktp * 128) + quad * 32;
             if (storer && n0 < a.N) {
                 // rows past N are clipped by the tensor map
-                tma_store_4d(&tmdK, smem_u32(slab), 0, h, n0, b);
+                tma_store_4d(&tmdK, smem_u32(slab), 0, hp, n0, bp);
                 bulk_commit_group();
             }
             ++stores;
-            if (last) {
-                // the (b, h)'s dQ (half 0) and dZ (half 1) pieces of this span,
-                // latent rows in the lanes
-                if (!wwait(pz_full, (uint32_t)pieces & 1)) break;
+            if (lastp) {
+                if (!wwait(pz_full, (uint32_t)pieces & 1)) return false;
                 tc_fence_after();
                 uint32_t rq[2][32];
                 tmem_ld32(tmem + (hf ? C::DZ_COL : C::DQ_COL) + lane_off, rq[0]);
@@ -478,9 +409,9 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 __syncwarp();
                 if (lane == 0) mbar_arrive(pz_free);
                 if (rig < M) {
-                    const int piece = cta - bwd_cta_of(bh * a.T_bh, a.T_total, a.grid);
+                    const int piece = cta - bwd_cta_of(bhp * a.T_bh, a.T_total, a.grid);
                     float4 *dst = reinterpret_cast<float4 *>(
-                        a.part + (((bh * a.P_max + piece) * 2 + hf) * M + rig) * 64);
+                        a.part + (((bhp * a.P_max + piece) * 2 + hf) * M + rig) * 64);
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
@@ -491,11 +422,116 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 }
                 ++pieces;
             }
+            return true;
+        };
+        int64_t bh = bh0, kt = k0;
+        int b = (int)(bh0 / a.H), h = (int)(bh0 - (int64_t)b * a.H);
+        // the previous tile, whose epilogue runs after this tile's operands are out
+        int64_t bhp = bh, ktp = kt;
+        int bp = b, hp = h;
+        bool lastp = false;
+        bool ok = true;
+        for (int64_t j = 0; j < ntiles; ++j) {
+            int64_t bhN = bh, ktN = kt + 1;
+            int bN = b, hN = h;
+            if (ktN == a.T_bh) {
+                ktN = 0;
+                ++bhN;
+                if (++hN == a.H) {
+                    hN = 0;
+                    ++bN;
+                }
+            }
+            const bool last = (j + 1 == ntiles) || bhN != bh;
+            const int64_t n = kt * 128 + rig;
+            const bool valid = n < a.N;
+            if (!(ok = wwait(s_full, (uint32_t)j & 1))) break;
+            tc_fence_after();
+            // this half's scores: the maximum, exchanged with the other half
+            uint32_t sv[W / 32][32];
+#pragma unroll
+            for (int c = 0; c < W / 32; ++c) tmem_ld32(s_tm + 32 * c, sv[c]);
+            tmem_wait_ld();
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < W / 32; ++c)
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    mx = max3(mx, __uint_as_float(sv[c][2 * i]), __uint_as_float(sv[c][2 * i + 1]));
+            const int par = (int)(j & 1);
+            xm[(par * 2 + hf) * 128 + rig] = mx;
+            named_bar_sync(pair_bar, 64);
+            const float m2 = fmaxf(mx, xm[(par * 2 + (hf ^ 1)) * 128 + rig]) * sl2;
+            // p = 2^(s t log2 e - max), the half's partial sum and <p, g>
+            uint32_t gv[W / 32][32];
+#pragma unroll
+            for (int c = 0; c < W / 32; ++c) tmem_ld32(g_tm + 32 * c, gv[c]);
+            tmem_wait_ld();
+            // S and G of this tile are in registers: the next tile's may be computed
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sg_free);
+            float ls = 0.f, lr = 0.f;
+#pragma unroll
+            for (int c = 0; c < W / 32; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p = ex2(fmaf(__uint_as_float(sv[c][i]), sl2, -m2));
+                    sv[c][i] = __float_as_uint(p);
+                    ls += p;
+                    lr = fmaf(p, __uint_as_float(gv[c][i]), lr);
+                }
+            xl[(par * 2 + hf) * 128 + rig] = make_float2(ls, lr);
+            named_bar_sync(pair_bar, 64);
+            const float2 o = xl[(par * 2 + (hf ^ 1)) * 128 + rig];
+            const float inv = valid ? 1.f / (ls + o.x) : 0.f;      // tokens past N: A = 0
+            const float r = (lr + o.y) / (ls + o.x);
+            // s dT into DT_COL once dK of the previous tile (which read it) is
+            // done; A^T and s dT^T into the MN-major operands of dZ and dQ once
+            // the previous tile's products have read them
+            if (j > 0 && !(ok = wwait(dk_full, (uint32_t)(j - 1) & 1))) break;
+            if (j > 0 && !(ok = wwait(at_free, (uint32_t)(j - 1) & 1))) break;
+#pragma unroll
+            for (int c = 0; c < W / 32; ++c) {
+                uint32_t aw[16], tw[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float a0 = __uint_as_float(sv[c][2 * i]) * inv;
+                    const float a1 = __uint_as_float(sv[c][2 * i + 1]) * inv;
+                    const float t0 = sc * a0 * (__uint_as_float(gv[c][2 * i]) - r);
+                    const float t1 = sc * a1 * (__uint_as_float(gv[c][2 * i + 1]) - r);
+                    aw[i] = pack_bf16(a0, a1);
+                    tw[i] = pack_bf16(t0, t1);
+                }
+                tmem_st16(t_tm + 16 * c, tw);
+                const int m0 = W * hf + 32 * c;
+                uint8_t *arow = smem + C::A_OFF + (m0 >> 6) * TB + rig * 128;
+                uint8_t *trow = smem + C::DT_OFF + (m0 >> 6) * TB + rig * 128;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int pos = ((((m0 & 63) >> 3) + q) ^ (rig & 7)) << 4;
+                    *reinterpret_cast<uint4 *>(arow + pos) = make_uint4(aw[4 * q], aw[4 * q + 1], aw[4 * q + 2], aw[4 * q + 3]);
+                    *reinterpret_cast<uint4 *>(trow + pos) = make_uint4(tw[4 * q], tw[4 * q + 1], tw[4 * q + 2], tw[4 * q + 3]);
+                }
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+            // the previous tile's epilogue (its dK was computed meanwhile)
+            if (j > 0 && !(ok = epilogue(j - 1, bhp, ktp, bp, hp, lastp))) break;
+            bhp = bh;
+            ktp = kt;
+            bp = b;
+            hp = h;
+            lastp = last;
             bh = bhN;
             kt = ktN;
             b = bN;
             h = hN;
         }
+        if (ok && ntiles > 0) epilogue(ntiles - 1, bhp, ktp, bp, hp, lastp);
         if (storer) bulk_wait_group0();
     }
     tc_fence_before();
