@@ -160,8 +160,13 @@ __device__ __forceinline__ void produce_kv(const CUtensorMap *tmK, const CUtenso
     auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
     const uint32_t sStage = smem_u32(smem + C::STAGE_OFF);
     const uint64_t pol = policy_evict_first();
-    // mask bytes of the next tile are loaded one iteration ahead
+    // Mask bytes are fetched AHEAD tiles before their tile is issued, into
+    // one of AHEAD register sets taken in turn (the loop is unrolled AHEAD
+    // times, so no set is read before its loads have had AHEAD iterations
+    // to land): a load consumed in the next iteration put its whole latency
+    // on every tile.
     constexpr int MB = TILE / 32;
+    constexpr int AHEAD = 4;
     auto load_mask = [&](const TileCursor &ti, uint8_t (&mb)[MB]) {
         const int b = ti.bh / a.H;
 #pragma unroll
@@ -170,20 +175,29 @@ __device__ __forceinline__ void produce_kv(const CUtensorMap *tmK, const CUtenso
             mb[i] = (n < ti.n1) ? (a.mask ? a.mask[(int64_t)b * a.N + n] : (uint8_t)1) : (uint8_t)0;
         }
     };
-    uint8_t mb[MB], mb_next[MB];
-    TileCursor ti, tn;
+    uint8_t m0[MB], m1[MB], m2[MB], m3[MB];
+    TileCursor ti, tl;                  // the tile being issued; the next tile whose mask is fetched
     ti.init(pl, tb);
-    tn = ti;
-    load_mask(ti, mb);
-    int64_t j = 0;
-    for (; j < ntiles && !wt.aborted(); ++j) {
-        if (j + 1 < ntiles) {
-            tn.next(pl);
-            load_mask(tn, mb_next);
+    tl = ti;
+    int64_t jl = 0;                     // index of tile tl
+    auto fetch = [&](uint8_t (&mb)[MB]) {
+        if (jl < ntiles) {
+            load_mask(tl, mb);
+            if (jl + 1 < ntiles) tl.next(pl);
         }
+        ++jl;
+    };
+    fetch(m0);
+    fetch(m1);
+    fetch(m2);
+    fetch(m3);
+    int64_t j = 0;
+    // issues tile j with its mask bytes mb, then fetches tile j + AHEAD's into mb
+    auto step = [&](uint8_t (&mb)[MB]) -> bool {
+        if (j >= ntiles || wt.aborted()) return false;
         const int b = ti.bh / a.H, h = ti.bh - b * a.H;
         const int s = (int)(j % STAGES);
-        if (!__all_sync(0xffffffffu, wt.wait(empty(s), ((uint32_t)(j / STAGES) & 1) ^ 1))) break;
+        if (!__all_sync(0xffffffffu, wt.wait(empty(s), ((uint32_t)(j / STAGES) & 1) ^ 1))) return false;
         // bias rows of this stage: bf16 0 (valid) or -inf (padding), then zeros
         uint4 *bs = reinterpret_cast<uint4 *>(smem + C::BIAS_OFF + s * C::BIAS_BYTES);
         bool pad = false;
@@ -206,9 +220,13 @@ __device__ __forceinline__ void produce_kv(const CUtensorMap *tmK, const CUtenso
             }
         }
         __syncwarp();
-        ti = tn;
-#pragma unroll
-        for (int i = 0; i < MB; ++i) mb[i] = mb_next[i];
+        fetch(mb);
+        if (j + 1 < ntiles) ti.next(pl);
+        ++j;
+        return true;
+    };
+    static_assert(AHEAD == 4, "the unrolled loop below takes the four register sets in turn");
+    while (step(m0) && step(m1) && step(m2) && step(m3)) {
     }
     // after an abort: let every issued load land before the CTA exits
     if (wt.aborted() && lane == 0) {
