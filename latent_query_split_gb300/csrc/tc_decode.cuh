@@ -104,11 +104,12 @@ __device__ __forceinline__ uint4 load_chunk8(const float *src) {
     return make_uint4(pack_bf16(lo.x, lo.y), pack_bf16(lo.z, lo.w), pack_bf16(hi.x, hi.y),
                       pack_bf16(hi.z, hi.w));
 }
+// Threads t0, t0 + step, ... of the cooperating threads take the chunks.
 template <int M, int D, typename T>
-__device__ __forceinline__ void stage_rows_bf16(uint8_t *dst, const T *src, int lane) {
+__device__ __forceinline__ void stage_rows_bf16(uint8_t *dst, const T *src, int t0, int step) {
     constexpr int CHUNKS = M * D / 8;                   // 16-byte output chunks
 #pragma unroll 8
-    for (int c = lane; c < CHUNKS; c += 32) {
+    for (int c = t0; c < CHUNKS; c += step) {
         const int row = c / (D / 8), j = c % (D / 8);    // chunk j covers cols 8j..8j+7
         const int atom = j >> 3, jj = j & 7;
         uint8_t *p = dst + atom * (M * 128) + row * 128 + ((jj ^ (row & 7)) << 4);
@@ -131,24 +132,31 @@ __device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
 // c = 2^-e where 2^e <= max|Z| < 2^(e+1) (e clamped to [-14, 24], so c and
 // every scaled element stay within fp16 range), plus atom D/64 whose first
 // column is c in every row (the row-sum block). c cancels in Y = (c Y)/(c l).
+// In two steps so that several warps can share them: z_absmax_part (this
+// thread's share of max|Z|), then z_stage_f16 with c = z_scale(max|Z|).
 template <int M, int D>
-__device__ __forceinline__ void stage_z_f16(uint8_t *dst, const float *src, int lane) {
+__device__ __forceinline__ float z_absmax_part(const float *src, int t0, int step) {
     constexpr int CHUNKS = M * D / 8;
     float mx = 0.f;
 #pragma unroll 8
-    for (int q = lane; q < CHUNKS; q += 32) {
+    for (int q = t0; q < CHUNKS; q += step) {
         const float4 lo = __ldg(reinterpret_cast<const float4 *>(src) + 2 * q);
         const float4 hi = __ldg(reinterpret_cast<const float4 *>(src) + 2 * q + 1);
         mx = fmaxf(mx, fmaxf(fmaxf(fabsf(lo.x), fabsf(lo.y)), fmaxf(fabsf(lo.z), fabsf(lo.w))));
         mx = fmaxf(mx, fmaxf(fmaxf(fabsf(hi.x), fabsf(hi.y)), fmaxf(fabsf(hi.z), fabsf(hi.w))));
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    return mx;
+}
+__device__ __forceinline__ float z_scale(float mx) {
     int e = mx > 0.f ? ((__float_as_int(mx) >> 23) & 0xff) - 127 : 0;   // floor(log2 max|Z|)
     e = e < -14 ? -14 : (e > 24 ? 24 : e);
-    const float c = __int_as_float((127 - e) << 23);                  // 2^-e, exact
+    return __int_as_float((127 - e) << 23);                            // 2^-e, exact
+}
+template <int M, int D>
+__device__ __forceinline__ void z_stage_f16(uint8_t *dst, const float *src, float c, int t0, int step) {
+    constexpr int CHUNKS = M * D / 8;
 #pragma unroll 8
-    for (int q = lane; q < CHUNKS; q += 32) {
+    for (int q = t0; q < CHUNKS; q += step) {
         const int row = q / (D / 8), j = q % (D / 8);
         const int atom = j >> 3, jj = j & 7;
         const float4 lo = __ldg(reinterpret_cast<const float4 *>(src) + 2 * q);
@@ -159,9 +167,44 @@ __device__ __forceinline__ void stage_z_f16(uint8_t *dst, const float *src, int 
     }
     // the row-sum block: columns D..D+15 = [c, 0, ..., 0] (chunks 0 and 1 of the atom)
     uint8_t *ones = dst + (D / 64) * (M * 128);
-    for (int row = lane; row < M; row += 32) {
+    for (int row = t0; row < M; row += step) {
         *reinterpret_cast<uint4 *>(ones + row * 128 + ((0 ^ (row & 7)) << 4)) = make_uint4(pack_f16(c, 0.f), 0u, 0u, 0u);
         *reinterpret_cast<uint4 *>(ones + row * 128 + ((1 ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// Q and Z of (b, h) index bh (head-major: bh = h * B + b) into Q/Z buffer q,
+// by threads t0, t0 + step, ...; `wid` >= 0: the index of this thread's warp
+// among the cooperating warps 2..STAGER (max|Z| is combined through shared
+// memory), -1: one warp alone. Not inlined: it runs once per (b, h) and would
+// otherwise add its registers to the tile loops'.
+template <class C, int M, int D>
+__device__ __noinline__ void dec_stage_qz(uint8_t *smem, const void *Q, const float *Z, int q_f32,
+                                          int q_per_batch, int B, int H, int64_t bh, int q, int t0,
+                                          int step, int wid, int lane) {
+    constexpr int KA = C::KA;
+    const int h = (int)(bh / B), b = (int)(bh - (int64_t)h * B);
+    uint8_t *qdst = smem + q * C::QZ_BYTES, *zdst = qdst + KA * C::QZ_ATOM;
+    const int64_t qoff = ((int64_t)(q_per_batch ? b : 0) * H + h) * M * D;
+    const float *zsrc = Z + ((int64_t)b * H + h) * M * D;
+    if (q_f32)
+        stage_rows_bf16<M, D>(qdst, reinterpret_cast<const float *>(Q) + qoff, t0, step);
+    else
+        stage_rows_bf16<M, D>(qdst, reinterpret_cast<const __nv_bfloat16 *>(Q) + qoff, t0, step);
+    if constexpr (C::F16P) {
+        float mx = z_absmax_part<M, D>(zsrc, t0, step);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (wid >= 0) {
+            float *xz = reinterpret_cast<float *>(smem + C::MISC_OFF + 16);   // one per warp
+            if (lane == 0) xz[wid] = mx;
+            named_bar_sync(5, 32 * (C::STAGER - 1));
+#pragma unroll
+            for (int w = 0; w < C::STAGER - 1; ++w) mx = fmaxf(mx, xz[w]);
+        }
+        z_stage_f16<M, D>(zdst, zsrc, z_scale(mx), t0, step);
+    } else {
+        stage_rows_bf16<M, D>(zdst, zsrc, t0, step);
     }
 }
 
@@ -229,6 +272,23 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const int64_t bh0 = tb / a.T_bh;
     const int64_t k0 = tb - bh0 * a.T_bh;
     const int64_t n_gen = ntiles > 0 ? (te - 1) / a.T_bh - bh0 + 1 : 0;   // (b, h) of the span
+    auto stage_qz = [&](int64_t u, int t0, int step, int wid) {
+        dec_stage_qz<C, M, D>(smem, a.Q, a.Z, a.q_f32, a.q_per_batch, a.B, a.H, bh0 + u, (int)(u % QZB), t0,
+                              step, wid, lane);
+    };
+    // The first (b, h) is staged by warps 2..STAGER together (idle until its
+    // first S anyway). Inside the library's forward the decode is launched as
+    // a programmatic dependent of the merge that writes Z: only these warps
+    // read Z or Q, so only they wait, and the K stream starts during the
+    // merge's tail.
+    if (warp >= 2 && warp <= C::STAGER && n_gen > 0) {
+        pdl_wait();
+        const int wid = warp - 2;
+        stage_qz(0, 32 * wid + lane, 32 * (C::STAGER - 1), wid);
+        fence_proxy_async_smem();
+        named_bar_sync(5, 32 * (C::STAGER - 1));
+        if (warp == C::STAGER && lane == 0) mbar_arrive(qz_full(0));
+    }
 
     if (warp == 0) {
         // ---------------- producer: K tiles ----------------
@@ -263,27 +323,12 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 }
         }
     } else if (warp == C::STAGER) {
-        // ---------------- stager: Q and Z of each (b, h) ----------------
-        // Inside the library's forward the decode is launched as a programmatic
-        // dependent of the merge that writes Z: only this warp reads Z or Q, so
-        // only it waits, and the K stream starts during the merge's tail.
-        pdl_wait();
-        for (int64_t u = 0; u < n_gen && !wt.aborted(); ++u) {
+        // ---------------- stager: Q and Z of each later (b, h) ----------------
+        for (int64_t u = 1; u < n_gen && !wt.aborted(); ++u) {
             const int q = (int)(u % QZB);
             // the buffer's previous (b, h) has had its last P Z issued and done
             if (u >= QZB && !__all_sync(0xffffffffu, wt.wait(qz_free(q), (uint32_t)(u / QZB - 1) & 1))) break;
-            const int64_t bh = bh0 + u;
-            const int h = (int)(bh / a.B), b = (int)(bh - (int64_t)h * a.B);
-            uint8_t *qdst = smem + q * C::QZ_BYTES, *zdst = qdst + KA * C::QZ_ATOM;
-            const int64_t qoff = ((int64_t)(a.q_per_batch ? b : 0) * a.H + h) * M * D;
-            if (a.q_f32)
-                stage_rows_bf16<M, D>(qdst, reinterpret_cast<const float *>(a.Q) + qoff, lane);
-            else
-                stage_rows_bf16<M, D>(qdst, reinterpret_cast<const __nv_bfloat16 *>(a.Q) + qoff, lane);
-            if constexpr (C::F16P)
-                stage_z_f16<M, D>(zdst, a.Z + ((int64_t)b * a.H + h) * M * D, lane);
-            else
-                stage_rows_bf16<M, D>(zdst, a.Z + ((int64_t)b * a.H + h) * M * D, lane);
+            stage_qz(u, lane, 32, -1);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(qz_full(q));

@@ -160,11 +160,13 @@ __device__ __forceinline__ void produce_kv(const CUtensorMap *tmK, const CUtenso
     auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
     const uint32_t sStage = smem_u32(smem + C::STAGE_OFF);
     const uint64_t pol = policy_evict_first();
-    // Mask bytes are fetched AHEAD tiles before their tile is issued, into
-    // one of AHEAD register sets taken in turn (the loop is unrolled AHEAD
-    // times, so no set is read before its loads have had AHEAD iterations
-    // to land): a load consumed in the next iteration put its whole latency
-    // on every tile.
+    // With a mask, its bytes are fetched AHEAD tiles before their tile is
+    // issued, into one of AHEAD register sets taken in turn (the loop is
+    // unrolled AHEAD times, so no set is read before its loads have had AHEAD
+    // iterations to land): a load consumed in the next iteration put its
+    // whole latency on every tile. Without a mask (only shard ends to mark,
+    // no loads) the plain loop with one set is kept: the unrolled one was
+    // measurably slower there.
     constexpr int MB = TILE / 32;
     constexpr int AHEAD = 4;
     auto load_mask = [&](const TileCursor &ti, uint8_t (&mb)[MB]) {
@@ -188,9 +190,11 @@ __device__ __forceinline__ void produce_kv(const CUtensorMap *tmK, const CUtenso
         ++jl;
     };
     fetch(m0);
-    fetch(m1);
-    fetch(m2);
-    fetch(m3);
+    if (a.mask != nullptr) {
+        fetch(m1);
+        fetch(m2);
+        fetch(m3);
+    }
     int64_t j = 0;
     // issues tile j with its mask bytes mb, then fetches tile j + AHEAD's into mb
     auto step = [&](uint8_t (&mb)[MB]) -> bool {
@@ -226,7 +230,13 @@ __device__ __forceinline__ void produce_kv(const CUtensorMap *tmK, const CUtenso
         return true;
     };
     static_assert(AHEAD == 4, "the unrolled loop below takes the four register sets in turn");
-    while (step(m0) && step(m1) && step(m2) && step(m3)) {
+    if (a.mask != nullptr) {
+        while (step(m0) && step(m1) && step(m2) && step(m3)) {
+        }
+    } else {
+        // no mask loads to hide: one register set (the masks only mark shard ends)
+        while (step(m0)) {
+        }
     }
     // after an abort: let every issued load land before the CTA exits
     if (wt.aborted() && lane == 0) {
