@@ -1069,6 +1069,61 @@ __global__ void __launch_bounds__(256) enc_merge_kernel(const EncArgs a) {
         const uint32_t e = piece[q];
         return ((int64_t)bh * pl.R + (e >> 16)) * pl.P_max + (e & 0xffffu);
     };
+    if (a.O_r == nullptr && a.L_r == nullptr) {
+        // Only (Z, L): every piece of the (b, h) straight into the global rule
+        // (the same log-sum-exp, without the per-shard level), one thread per
+        // row quad; each batch issues the log-normalisers and outputs of 16
+        // pieces together and is folded in with a running maximum, in piece
+        // order (deterministic).
+        const int i = tid / Q4, d4 = tid - i * Q4;
+        if (i0 + i >= M) return;
+        const int64_t orow = (int64_t)(i0 + i) * D;
+        float m = -INFINITY, sum = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int qb = 0; qb < P; qb += 16) {
+            float lp[16];
+            float4 v[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int q = qb + u;
+                lp[u] = -INFINITY;
+                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (q < P) {
+                    const int64_t sl = slot(q);
+                    lp[u] = __ldcg(a.part_L + sl * M + i0 + i);
+                    v[u] = __ldcg(reinterpret_cast<const float4 *>(a.part_O + sl * M * D + orow) + d4);
+                }
+            }
+            float mb = m;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) mb = fmaxf(mb, lp[u]);
+            if (mb == -INFINITY) continue;                 // no valid token so far
+            if (mb > m) {
+                const float f = m == -INFINITY ? 0.f : expf(m - mb);
+                sum *= f;
+                acc.x *= f;
+                acc.y *= f;
+                acc.z *= f;
+                acc.w *= f;
+                m = mb;
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const float w = lp[u] == -INFINITY ? 0.f : expf(lp[u] - m);
+                sum += w;
+                acc.x = fmaf(w, v[u].x, acc.x);
+                acc.y = fmaf(w, v[u].y, acc.y);
+                acc.z = fmaf(w, v[u].z, acc.z);
+                acc.w = fmaf(w, v[u].w, acc.w);
+            }
+        }
+        const float inv = sum > 0.f ? 1.f / sum : 0.f;
+        if (a.Z)
+            reinterpret_cast<float4 *>(a.Z + (int64_t)bh * M * D + orow)[d4] =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (a.L && d4 == 0) a.L[(int64_t)bh * M + i0 + i] = sum > 0.f ? m + logf(sum) : -INFINITY;
+        return;
+    }
     for (int x = tid; x < P * RB; x += 256) {
         const int q = x / RB, i = x - q * RB;
         Lp[x] = (i0 + i < M) ? __ldcg(a.part_L + slot(q) * M + i0 + i) : -INFINITY;
