@@ -14,9 +14,11 @@
 //   warp 1     TMEM allocator and MMA issuer (converged warp, elect.sync):
 //                S_g = K Q^T   (A = K tile, B = Q, both shared memory)
 //                Y_g = P_g Z   (A = P from tensor memory, B = Z shared memory)
-//   warps 2..  one or two groups of four warps take alternate tiles (one token
-//              row per thread = TMEM lane): row max, exp2, P over S in tensor
-//              memory. The epilogue of a tile (Y / l rounded to bf16, staged
+//   warps 2..  M <= 128: two groups of four warps take alternate tiles (one
+//              token row per thread = TMEM lane): row max, exp2, P over S in
+//              tensor memory. M > 128: one group of eight warps, two per lane
+//              quadrant (latent halves); S single-buffered but free as soon
+//              as its scores are in registers, P and Y in columns of their own. The epilogue of a tile (Y / l rounded to bf16, staged
 //              in shared memory, one TMA store per warp of 32 token rows) runs
 //              in the group's next iteration, once that tile's scores have
 //              arrived, so the group never waits for its own P Z product.
@@ -67,9 +69,9 @@ struct DecCfg {
     static constexpr uint32_t QZ_BYTES = (KA + ZA) * QZ_ATOM;   // one Q + Z buffer
     static constexpr uint32_t STAGE_BYTES = KA * 128 * 128;     // one K tile
     static constexpr int NCH = M / 32;                  // P chunks of 32 latents
-    // full[S], empty[S], qz_full[2], qz_free[2], s_full[2], p_chunk[2][8], o_done[2]
-    // + epi_done[2] (M > 128: Y of a tile lives in its S buffer, see Y_COL)
-    static constexpr int NBAR = 2 * STAGES + 4 + 2 + 16 + 2 + 2;
+    // full[S], empty[S], qz_full[2], qz_free[2], s_full[2], p_chunk[2][8], o_done[2],
+    // epi_done[2], s_free (M > 128: the single S buffer has been read)
+    static constexpr int NBAR = 2 * STAGES + 4 + 2 + 16 + 2 + 2 + 1;
     static constexpr uint32_t STAGE_OFF = QZB * QZ_BYTES;
     // Y staging of each group for the TMA stores: 128 token rows, KA atoms
     static constexpr uint32_t OUT_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
@@ -82,14 +84,17 @@ struct DecCfg {
     static constexpr uint32_t BYTES = MISC_OFF + 64;
     static constexpr uint32_t ALLOC = BYTES + 1024;
     static_assert(ALLOC <= 232448, "shared memory budget of one CTA exceeded");
-    // Two TMEM buffers b = tile parity, 256 columns each: S (and P over its
-    // first M/2 columns) at 256 b, Y at 256 b + Y_COL. For M <= 128 Y sits
-    // after S; for M > 128 it reuses the upper half of S, dead once the
-    // softmax has read every score, so the buffer is only reused for S two
-    // tiles later after that tile's Y has been read (epi_done).
+    // M <= 128: two TMEM buffers b = tile parity, 256 columns each: S (and P
+    // over its first M/2 columns) at 256 b, Y at 256 b + Y_COL.
+    // M > 128: one S buffer (M columns) at 0, P (fp16 pairs, M/2 columns) at
+    // P_COL and Y at Y_COL: S of the next tile is computed as soon as the
+    // softmax has read this tile's scores, P waits only for the previous
+    // tile's P Z and Y for the previous tile's epilogue.
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t Y_COL = NG == 2 ? M : M / 2;
-    static_assert(Y_COL + YN <= 256, "tensor-memory columns of one buffer exceeded");
+    static constexpr uint32_t P_COL = NG == 2 ? 0 : M;
+    static constexpr uint32_t Y_COL = NG == 2 ? M : M + M / 2;
+    static_assert(NG == 1 || Y_COL + YN <= 256, "tensor-memory columns of one buffer exceeded");
+    static_assert(NG == 2 || Y_COL + YN <= TMEM_COLS, "tensor-memory columns exceeded");
 };
 
 // Writes rows [0, M) x D of a row-major matrix into the 128-byte-swizzled bf16
@@ -228,6 +233,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     auto p_chunk = [&](int g, int c) { return bar0 + 8u * (2 * STAGES + 6 + 8 * g + c); };
     auto o_done = [&](int g) { return bar0 + 8u * (2 * STAGES + 22 + g); };
     auto epi_done = [&](int g) { return bar0 + 8u * (2 * STAGES + 24 + g); };
+    const uint32_t s_free = bar0 + 8u * (2 * STAGES + 26);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
 
@@ -254,6 +260,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             for (int c = 0; c < 8; ++c) mbar_init(p_chunk(g, c), C::GW);   // one arrival per softmax warp
             mbar_init(o_done(g), 1);
         }
+        mbar_init(s_free, C::GW);            // M > 128: every softmax warp has read S
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -356,9 +363,9 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             }
             if (!wwait(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
             tc_fence_after();
-            const int g = (int)(jj & 1);               // TMEM buffer
-            // M > 128: the buffer's previous tile (jj - 2) must have had its Y read
-            if (NG == 1 && jj >= 2 && !wwait(epi_done(g), (uint32_t)((jj >> 1) - 1) & 1)) return false;
+            const int g = NG == 1 ? 0 : (int)(jj & 1);   // TMEM buffer
+            // M > 128: the single S buffer is free once the previous tile's scores are read
+            if (NG == 1 && jj >= 1 && !wwait(s_free, (uint32_t)(jj - 1) & 1)) return false;
             tc_fence_after();
             const uint64_t dK = dK0 + kStageDesc * s;
             const uint64_t dQ0 = desc_sw128(sbase + (uint32_t)(uS % QZB) * C::QZ_BYTES, 16, 1024);
@@ -387,22 +394,25 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         ok = pump_s();
         for (; nP < ntiles && ok;) {
             const int64_t jP = nP;
-            const int g = (int)(jP & 1);
-            const int64_t kP = jP >> 1;
+            const int g = NG == 1 ? 0 : (int)(jP & 1);
+            const int64_t kP = NG == 1 ? jP : jP >> 1;
             const uint64_t dZ0 = desc_sw128(sbase + (uint32_t)(uP % QZB) * C::QZ_BYTES + KA * C::QZ_ATOM,
                                             C::QZ_ATOM, 1024);
             for (int c = 0; c < NCH && ok; ++c) {
                 // P arrives whole, published by every softmax warp at once
                 if (c == 0) {
                     ok = wwait(p_chunk(g, 0), (uint32_t)kP & 1);
+                    // M > 128: Y of the previous tile has been read by its epilogue
+                    if (ok && NG == 1 && jP >= 1) ok = wwait(epi_done(0), (uint32_t)(jP - 1) & 1);
                     if (!ok) break;
                     tc_fence_after();
                 }
+                const uint32_t y_t = NG == 1 ? tmem + C::Y_COL : tmem + g * 256 + C::Y_COL;
+                const uint32_t p_t = NG == 1 ? tmem + C::P_COL : tmem + g * 256;
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
                     const int kb = 2 * c + kk;       // 16 latents per MMA
-                    umma_ts_elect(tmem + g * 256 + C::Y_COL, tmem + g * 256 + kb * 8, dZ0 + kb * (2048 >> 4), idPV,
-                                  kb > 0 ? 1u : 0u);
+                    umma_ts_elect(y_t, p_t + kb * 8, dZ0 + kb * (2048 >> 4), idPV, kb > 0 ? 1u : 0u);
                 }
             }
             if (!ok) break;
@@ -420,18 +430,19 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         }
         // make every issued MMA finish before TMEM is released
         if (ok && ntiles > 0) {
-            const int gl = (int)((ntiles - 1) & 1);
-            const int64_t kl = (ntiles - 1) >> 1;
+            const int gl = NG == 1 ? 0 : (int)((ntiles - 1) & 1);
+            const int64_t kl = NG == 1 ? ntiles - 1 : (ntiles - 1) >> 1;
             wwait(o_done(gl), (uint32_t)kl & 1);
         }
         __syncwarp();
     } else if (NG == 1) {
         // ---------------- softmax halves + epilogue (M > 128) ----------------
         // Warps w and w + 4 share a TMEM lane quadrant (32 token rows); half h
-        // owns latents [M/2 h, M/2 (h + 1)). After both have loaded their
-        // scores into registers and exchanged the row maximum, P of latent m
-        // is written at column m / 2 (fp16 pairs): every score is then in
-        // registers, so the halves can overwrite each other's columns.
+        // owns latents [M/2 h, M/2 (h + 1)). Both load their scores into
+        // registers (then s_free: S of the next tile may be computed) and
+        // exchange the row maximum; P of latent m goes to column P_COL + m / 2
+        // (fp16 pairs) once the previous tile's P Z is done; the previous
+        // tile's Y is stored after this tile's P is out.
         constexpr int HM = M / 2;                     // latents of a half
         const int half = (warp - 2) >> 2;
         const int quad = warp & 3;
@@ -452,17 +463,16 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         // Y / l of the previous tile: half h converts columns [32 h, 32 h + 32)
         // of each row (D = 64), half 0's lane 0 stores the quadrant's 32 rows
         auto epilogue = [&]() -> bool {
-            const int pb = (int)(prev_k & 1);                   // the previous tile's buffer
-            if (!wwait(o_done(pb), (uint32_t)(prev_k >> 1) & 1)) return false;
+            if (!wwait(o_done(0), (uint32_t)prev_k & 1)) return false;
             tc_fence_after();
-            const uint32_t y_tmem = tmem + pb * 256 + C::Y_COL + lane_off;
+            const uint32_t y_tmem = tmem + C::Y_COL + lane_off;
             uint32_t r[32];
             tmem_ld32(y_tmem + 32 * half, r);
             const uint32_t lw = tmem_ld1(y_tmem + D);              // c * l from the row-sum block
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(epi_done(pb));              // the buffer may take S again
+            if (lane == 0) mbar_arrive(epi_done(0));               // Y may take the next tile's P Z
             if (stores > 0 && storer) bulk_wait_group_read0();     // the slab's last store has read it
             named_bar_sync(pair_bar, 64);
             const float inv = 1.f / __uint_as_float(lw);
@@ -492,16 +502,18 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         int ch = (int)(bh0 / a.B), cb = (int)(bh0 - (int64_t)ch * a.B);   // tile j's head and batch
         bool ok = true;
         for (int64_t j = 0; j < ntiles && ok; ++j) {
-            const int bb = (int)(j & 1);                        // TMEM buffer of tile j
-            const uint32_t s_tmem = tmem + bb * 256 + HM * half + lane_off;
-            const uint32_t p_tmem = tmem + bb * 256 + (HM / 2) * half + lane_off;
-            if (!wwait(s_full(bb), (uint32_t)(j >> 1) & 1)) break;
+            const uint32_t s_tmem = tmem + HM * half + lane_off;
+            const uint32_t p_tmem = tmem + C::P_COL + (HM / 2) * half + lane_off;
+            if (!wwait(s_full(0), (uint32_t)j & 1)) break;
             tc_fence_after();
-            if (have_prev && !(ok = epilogue())) break;
             uint32_t r[HM / 32][32];
 #pragma unroll
             for (int c = 0; c < HM / 32; ++c) tmem_ld32(s_tmem + c * 32, r[c]);
             tmem_wait_ld();
+            // the scores are in registers: S of the next tile may be computed
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free);
             float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
             for (int c = 0; c < HM / 32; ++c)
@@ -513,6 +525,9 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             named_bar_sync(pair_bar, 64);                 // both halves' scores are in registers
             const float m = fmaxf(xm[rig], xm[128 + rig]) * a.sl2;
             const uint64_t nm2 = f2pack(-m, -m);
+            // P's columns are free once the previous tile's P Z is done
+            if (have_prev && !(ok = wwait(o_done(0), (uint32_t)prev_k & 1))) break;
+            tc_fence_after();
 #pragma unroll
             for (int c = 0; c < HM / 32; ++c) {
                 uint32_t pw[16];
@@ -527,7 +542,9 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_chunk(bb, 0));
+            if (lane == 0) mbar_arrive(p_chunk(0, 0));
+            // the previous tile's Y (its P Z ran during this softmax)
+            if (have_prev && !(ok = epilogue())) break;
             have_prev = true;
             prev_h = ch;
             prev_b = cb;
