@@ -16,7 +16,8 @@
 //                Y_g = P_g Z   (A = P from tensor memory, B = Z shared memory)
 //   warps 2..  M <= 128: two groups of four warps take alternate tiles (one
 //              token row per thread = TMEM lane): row max, exp2, P over S in
-//              tensor memory. M > 128: one group of eight warps, two per lane
+//              tensor memory; where 3 M + 2 D columns fit, S rotates through
+//              three TMEM buffers so the MMA chain spans three tiles. M > 128: one group of eight warps, two per lane
 //              quadrant (latent halves); S single-buffered but free as soon
 //              as its scores are in registers, P and Y in columns of their own. The epilogue of a tile (Y / l rounded to bf16, staged
 //              in shared memory, one TMA store per warp of 32 token rows) runs
@@ -63,7 +64,12 @@ struct DecCfg {
     // holding the constant c (the power of two Z was scaled by, see
     // stage_z_f16), so the same MMA also returns c * l, the row sum of P,
     // next to c * Y. Needs D + 16 more tensor-memory columns per group.
-    static constexpr bool F16P = NG == 2 ? (M + D + 16 <= 256) : (M + D + 16 <= 512);
+    // RING (M <= 128): S tiles rotate through three TMEM buffers of M
+    // columns (P over the first M/2), each group keeps one Y, when 3 M + 2 D
+    // columns fit; fp16 P with the row-sum block when 3 M + 2 (D + 16) fit too.
+    static constexpr bool RING = NG == 2 && 3 * M + 2 * D <= 512;
+    static constexpr bool F16P = RING ? (3 * M + 2 * (D + 16) <= 512)
+                                      : (NG == 2 ? (M + D + 16 <= 256) : (M + D + 16 <= 512));
     static constexpr int YN = F16P ? D + 16 : D;        // N of the P Z product
     static constexpr int ZA = F16P ? KA + 1 : KA;       // atoms of the staged Z
     static constexpr uint32_t QZ_BYTES = (KA + ZA) * QZ_ATOM;   // one Q + Z buffer
@@ -71,7 +77,7 @@ struct DecCfg {
     static constexpr int NCH = M / 32;                  // P chunks of 32 latents
     // full[S], empty[S], qz_full[2], qz_free[2], s_full[2], p_chunk[2][8], o_done[2],
     // epi_done[2], s_free (M > 128: the single S buffer has been read)
-    static constexpr int NBAR = 2 * STAGES + 4 + 2 + 16 + 2 + 2 + 1;
+    static constexpr int NBAR = 2 * STAGES + 4 + 2 + 16 + 2 + 2 + 1 + 1;   // + the third s_full
     static constexpr uint32_t STAGE_OFF = QZB * QZ_BYTES;
     // Y staging of each group for the TMA stores: 128 token rows, KA atoms
     static constexpr uint32_t OUT_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
@@ -93,6 +99,15 @@ struct DecCfg {
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t P_COL = NG == 2 ? 0 : M;
     static constexpr uint32_t Y_COL = NG == 2 ? M : M + M / 2;
+    static constexpr int NSB = RING ? 3 : (NG == 2 ? 2 : 1);   // S buffers
+    // column of S buffer b, and of group g's Y
+    static __host__ __device__ constexpr uint32_t s_col(int b) {
+        return RING ? (uint32_t)(b * M) : (NG == 2 ? (uint32_t)(b * 256) : 0u);
+    }
+    static __host__ __device__ constexpr uint32_t y_col(int g) {
+        return RING ? (uint32_t)(3 * M + g * YN) : (NG == 2 ? (uint32_t)(g * 256) + Y_COL : Y_COL);
+    }
+    static_assert(!RING || 3 * M + 2 * YN <= TMEM_COLS, "tensor-memory columns exceeded");
     static_assert(NG == 1 || Y_COL + YN <= 256, "tensor-memory columns of one buffer exceeded");
     static_assert(NG == 2 || Y_COL + YN <= TMEM_COLS, "tensor-memory columns exceeded");
 };
@@ -229,7 +244,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto qz_full = [&](int q) { return bar0 + 8u * (2 * STAGES + q); };
     auto qz_free = [&](int q) { return bar0 + 8u * (2 * STAGES + 2 + q); };
-    auto s_full = [&](int g) { return bar0 + 8u * (2 * STAGES + 4 + g); };
+    auto s_full = [&](int g) { return bar0 + 8u * (2 * STAGES + (g < 2 ? 4 + g : 27)); };
     auto p_chunk = [&](int g, int c) { return bar0 + 8u * (2 * STAGES + 6 + 8 * g + c); };
     auto o_done = [&](int g) { return bar0 + 8u * (2 * STAGES + 22 + g); };
     auto epi_done = [&](int g) { return bar0 + 8u * (2 * STAGES + 24 + g); };
@@ -260,6 +275,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             for (int c = 0; c < 8; ++c) mbar_init(p_chunk(g, c), C::GW);   // one arrival per softmax warp
             mbar_init(o_done(g), 1);
         }
+        mbar_init(s_full(2), 1);
         mbar_init(s_free, C::GW);            // M > 128: every softmax warp has read S
         fence_mbar_init();
     }
@@ -363,7 +379,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             }
             if (!wwait(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
             tc_fence_after();
-            const int g = NG == 1 ? 0 : (int)(jj & 1);   // TMEM buffer
+            const int g = C::RING ? (int)(jj % 3) : (NG == 1 ? 0 : (int)(jj & 1));   // S buffer
             // M > 128: the single S buffer is free once the previous tile's scores are read
             if (NG == 1 && jj >= 1 && !wwait(s_free, (uint32_t)(jj - 1) & 1)) return false;
             tc_fence_after();
@@ -373,7 +389,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             for (int kb = 0; kb < D / 16; ++kb) {
                 const uint64_t offK = (uint64_t)((kb >> 2) * (128 * 128) + (kb & 3) * 32) >> 4;
                 const uint64_t offQ = (uint64_t)((kb >> 2) * C::QZ_ATOM + (kb & 3) * 32) >> 4;
-                umma_ss_elect(tmem + g * 256, dK + offK, dQ0 + offQ, idS, kb > 0 ? 1u : 0u);
+                umma_ss_elect(tmem + C::s_col(g), dK + offK, dQ0 + offQ, idS, kb > 0 ? 1u : 0u);
             }
             umma_commit_elect(s_full(g));
             umma_commit_elect(empty(s));            // the K tile is only read by S
@@ -387,7 +403,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         // a new (b, h) also waits until every older tile's P Z is issued
         int64_t jS = 0, nP = 0;
         auto pump_s = [&]() -> bool {
-            while (jS < ntiles && jS < nP + 2 && (QZB == 2 || bhS - bh0 == uS || nP == jS))
+            while (jS < ntiles && jS < nP + (C::RING ? 3 : 2) && (QZB == 2 || bhS - bh0 == uS || nP == jS))
                 if (!issue_s(jS++)) return false;
             return true;
         };
@@ -407,8 +423,8 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                     if (!ok) break;
                     tc_fence_after();
                 }
-                const uint32_t y_t = NG == 1 ? tmem + C::Y_COL : tmem + g * 256 + C::Y_COL;
-                const uint32_t p_t = NG == 1 ? tmem + C::P_COL : tmem + g * 256;
+                const uint32_t y_t = tmem + C::y_col(g);
+                const uint32_t p_t = NG == 1 ? tmem + C::P_COL : tmem + C::s_col(C::RING ? (int)(jP % 3) : g);
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
                     const int kb = 2 * c + kk;       // 16 latents per MMA
@@ -566,8 +582,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         const int quad = warp & 3;
         const int rig = quad * 32 + lane;            // token row within the tile (TMEM lane)
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        const uint32_t s_tmem = tmem + g * 256 + lane_off;
-        const uint32_t y_tmem = tmem + g * 256 + C::Y_COL + lane_off;
+        const uint32_t y_tmem = tmem + C::y_col(g) + lane_off;
         const uint64_t c2 = f2pack(a.sl2, a.sl2);
         // each warp stages and stores its own 32 token rows (a 4 KB slab per atom)
         uint8_t *stage_out = smem + C::OUT_OFF + g * C::OUT_BYTES + quad * 32 * 128;
@@ -630,7 +645,9 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             const bool mine = NG == 1 || (int)(j & 1) == g;
             if (mine) {
                 const int64_t k = NG == 2 ? (j >> 1) : j;
-                if (!wwait(s_full(g), (uint32_t)k & 1)) break;
+                const int sb = C::RING ? (int)(j % 3) : g;        // S buffer of tile j
+                const uint32_t s_tmem = tmem + C::s_col(sb) + lane_off;
+                if (!wwait(s_full(sb), (uint32_t)(C::RING ? j / 3 : k) & 1)) break;
                 tc_fence_after();
                 if (have_prev && !(ok = epilogue())) break;
                 float l;
