@@ -10,6 +10,9 @@ One step = one pass of the hot path over one batch of a named workload
   c3_pp_bf16         FLARE++ forward (encoder twice, then the decode)
   c5_bwd_bf16        global-normaliser encoder backward (dQ, dK, dV)
   c5_decbwd_bf16     decode backward (dQ, dZ, dK) on the shapes of c5
+  c5_mixbwd_bf16     FLARE mixer backward on the shapes of c5
+  c5_ppbwd_bf16      FLARE++ mixer backward on the shapes of c5
+--n N runs a workload's structure at N tokens (small cases for profilers).
 Token tensors of c2-c5 are 256 MiB or more each (larger than the 129 MB L2),
 so no flush is needed between steps; c1 flushes L2 between steps.
 
@@ -536,9 +539,14 @@ def main(argv=None):
     tokens_per_step = w.B * w.N * world
     value = weak_scaling_value(w.B * w.N, world, ms_per_step)
 
-    # end to end through the public API with host buffers (pinned), copies timed
+    # end to end through the public API with host buffers (pinned), copies timed:
+    # every step copies its inputs in and reads its result back; the copy-in
+    # of step i + 1 (on a copy stream, into the other of two device input
+    # sets) overlaps step i, as a training or serving loop prefetches its
+    # next batch
     e2e_in, e2e_out = runner.inputs_for_e2e()
-    host, dinp = {}, dict(inp)
+    host = {}
+    sets = [dict(inp), dict(inp)]
     extra = {"Zs": runner.Z, "Ls": runner.L, "Qds": getattr(runner, "Qd", None),
              "L1s": getattr(runner, "L1", None)}
     for name in e2e_in:
@@ -546,29 +554,52 @@ def main(argv=None):
         if t is None:
             continue
         host[name] = t.cpu().pin_memory()
-        dinp[name] = torch.empty_like(t)
+        for st_ in sets:
+            st_[name] = torch.empty_like(t)
     hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in e2e_out]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in hout)
-    def e2e_step():
-        with torch.cuda.stream(stream):
+    cstream = torch.cuda.Stream(device=dev)
+    h2d_ev = [torch.cuda.Event(), torch.cuda.Event()]
+    done_ev = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def copy_in(i):
+        k = i % 2
+        with torch.cuda.stream(cstream):
+            if i >= 2:
+                cstream.wait_event(done_ev[k])       # step i - 2 has read this set
             for name, t in host.items():
-                dinp[name].copy_(t, non_blocking=True)
-            runner.full_step(dinp)
+                sets[k][name].copy_(t, non_blocking=True)
+            h2d_ev[k].record(cstream)
+
+    def compute(i):
+        k = i % 2
+        with torch.cuda.stream(stream):
+            stream.wait_event(h2d_ev[k])
+            runner.full_step(sets[k])
+            done_ev[k].record(stream)
             for h, d in zip(hout, e2e_out):
                 h.copy_(d, non_blocking=True)
 
+    def e2e_run(n, start_ev=None):
+        with torch.cuda.stream(cstream):
+            if start_ev is not None:
+                cstream.wait_event(start_ev)
+            copy_in(0)
+        for i in range(n):
+            if i + 1 < n:
+                copy_in(i + 1)
+            compute(i)
+
     big = h2d > (8 << 30)
-    for _ in range(1 if big else 3):
-        e2e_step()
+    e2e_run(1 if big else 3)
     torch.cuda.synchronize(dev)
     e2e_steps = 3 if big else max(3, min(args.steps, args.e2e_steps))
     if world > 1:
         dist.barrier()
     s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s2.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    e2e_run(e2e_steps, s2)
     e2.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = s2.elapsed_time(e2) / e2e_steps
@@ -606,7 +637,9 @@ def main(argv=None):
             "clocks": clock_info,
             "e2e": {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms},
+                    "ms_per_step": e2e_ms,
+                    "copies": "each step's inputs copied in from pinned host memory (step i + 1's "
+                              "on a second stream, overlapping step i) and its result read back"},
             "gpu_launches": launches,
             "roofline": roofline}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -343,6 +343,29 @@ def test_mixer_bwd_no_tokens(cuda_device):
     assert dK.numel() == 0 and dV.numel() == 0 and torch.all(dQ == 0)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_flare_pp_shared_projection(cuda_device, kernel):
+    """The shared-projection FLARE++ variant (K~ = K, V~ = V; the FLARE++
+    page's closing remark): the same tensors passed as K~, V~ and K, V. The
+    gradient of each shared projection is the sum of its two shares."""
+    B, H, M, N, D = 2, 2, 128, 3000, 64
+    off = [0, 1000, 3000]
+    g = torch.Generator().manual_seed(33)
+    Qs = (torch.randn((H, M, D), generator=g) * 0.5).bfloat16().cuda()
+    K, V, dY = (torch.randn((B, N, H, D), generator=g).bfloat16().cuda() for _ in range(3))
+    mask = (torch.rand((B, N), generator=g) > 0.1).to(torch.uint8).cuda()
+    Y, Qd, L1, Z, L2 = _call(flare.flare_pp_fwd, Qs, K, V, K, V, mask, off, kernel=kernel)
+    Qdo, L1o, Zo, L2o, Yo = oracle.flare_pp_fwd(Qs, K, V, K, V, mask)
+    assert_close("Y", Y, Yo, "bf16")
+    out = _call(flare.flare_pp_bwd, Qs, K, V, K, V, mask, off, Qd, L1, Z, L2, dY, kernel=kernel)
+    flare.flare_device_status()
+    ref = oracle.flare_pp_bwd(Qs, K, V, K, V, mask, Qd.bfloat16().float(), L1, Z, L2, dY)
+    ref1 = oracle.encode_bwd(Qs, K, V, mask, Qd, L1, ref[5])
+    assert_close("dQseed", out[0], ref1[0], "bf16")
+    assert_close("dK + dK~", out[1].float() + out[3].float(), ref1[1] + ref[3], "bf16")
+    assert_close("dV + dV~", out[2].float() + out[4].float(), ref1[2] + ref[4], "bf16")
+
+
 def test_max_shards_and_single_token_shards(cuda_device):
     N = 300
     off = list(range(0, 256)) + [N]              # 255 one-token shards + one long shard
