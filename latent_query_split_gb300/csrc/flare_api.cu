@@ -193,7 +193,8 @@ void encoder_layout(const flare_dims_t *d, const int64_t *off, int R, bool tc, E
         return;
     }
     lay.mtiles = (d->M + kSimtRows - 1) / kSimtRows;
-    make_plan(off, R, d->N, kSimtTile, 256, (int64_t)bh * lay.mtiles, (int64_t)sms * 8, lay.plan);
+    // chunks of at least two tiles: small problems still spread over many CTAs
+    make_plan(off, R, d->N, kSimtTile, 2 * kSimtTile, (int64_t)bh * lay.mtiles, (int64_t)sms * 8, lay.plan);
     size_t o = 0;
     w.tickets = (unsigned *)o;
     o += align256(sizeof(unsigned) * bh * lay.mtiles);

@@ -53,12 +53,23 @@ __device__ __forceinline__ void online_tile(const float *Rs, const float *Ks, co
                                             float (*acc)[kMaxDPerLane]) {
     const int lane = threadIdx.x & 31;
     const int ld = D + 1;
-#pragma unroll 1
+    const float *k = Ks + lane * ld;
+    // fully unrolled: the per-row state m, l, acc is indexed by constants and
+    // stays in registers (a run-time row index put it in local memory)
+#pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
         const float *r = Rs + (row0 + i) * ld;
-        const float *k = Ks + lane * ld;
-        float s = 0.f;
-        for (int d = 0; d < D; ++d) s = fmaf(r[d], k[d], s);
+        // four independent partial sums keep the FMA chain short
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        int d = 0;
+        for (; d + 4 <= D; d += 4) {
+            s0 = fmaf(r[d], k[d], s0);
+            s1 = fmaf(r[d + 1], k[d + 1], s1);
+            s2 = fmaf(r[d + 2], k[d + 2], s2);
+            s3 = fmaf(r[d + 3], k[d + 3], s3);
+        }
+        for (; d < D; ++d) s0 = fmaf(r[d], k[d], s0);
+        float s = (s0 + s1) + (s2 + s3);
         s = key_ok ? s : -INFINITY;
         const float mnew = fmaxf(m[i], warp_max(s));
         if (mnew == -INFINITY) continue;                 // nothing valid yet
@@ -68,6 +79,8 @@ __device__ __forceinline__ void online_tile(const float *Rs, const float *Ks, co
         m[i] = mnew;
 #pragma unroll
         for (int j = 0; j < kMaxDPerLane; ++j) acc[i][j] *= corr;
+        // unrolled so that several broadcasts are in flight at once
+#pragma unroll 8
         for (int t = 0; t < 32; ++t) {
             const float pt = __shfl_sync(0xffffffffu, p, t);
             const float *v = Vs + t * D;
@@ -111,11 +124,14 @@ __device__ void merge_rows(const MergeArgs &a, int m0, int rows, float *s_lmax, 
         float lmax = -INFINITY;
         for (int r = 0; r < a.R; ++r) {
             const int c0 = a.chunk_start[r], c1 = a.chunk_start[r + 1];
+            // (unrolled: several partials' loads in flight at once)
             float cmax = -INFINITY;
+#pragma unroll 8
             for (int c = c0; c < c1; ++c) cmax = fmaxf(cmax, __ldcg(a.part_L + (int64_t)c * a.M + m));
             float Lr = -INFINITY;
             if (cmax != -INFINITY) {
                 float sum = 0.f;
+#pragma unroll 8
                 for (int c = c0; c < c1; ++c) {
                     const float lc = __ldcg(a.part_L + (int64_t)c * a.M + m);
                     if (lc != -INFINITY) sum += expf(lc - cmax);
@@ -144,6 +160,7 @@ __device__ void merge_rows(const MergeArgs &a, int m0, int rows, float *s_lmax, 
             const float Lr = a.Lr_out[r * a.Lr_shard_stride + m];
             float o = 0.f;
             if (Lr != -INFINITY) {
+#pragma unroll 8
                 for (int c = a.chunk_start[r]; c < a.chunk_start[r + 1]; ++c) {
                     const float lc = __ldcg(a.part_L + (int64_t)c * a.M + m);
                     if (lc != -INFINITY)
