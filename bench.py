@@ -217,6 +217,35 @@ def algorithmic(w, elem):
     return {"encoder_bwd": (4 * tok, 2.5 * pass_flops)}
 
 
+def algorithmic_exps(w):
+    """Exponentials per step and phase (one per latent-token pair and pass):
+    the third, diagnostic ceiling beside HBM and the tensor pipe."""
+    pair = float(w.B * w.H * w.M * w.N)
+    passes = {"flare_fwd": None, "flare_pp_fwd": 3, "decode_bwd": 1, "flare_bwd": 2,
+              "flare_pp_bwd": 3, "encoder_bwd": 1}[w.kind]
+    if passes is None:
+        return {"encoder": pair, "decode": pair}
+    return {w.kind: passes * pair}
+
+
+def cpu_model() -> str:
+    """The host CPU's model string (for the CPU baseline's record)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model", "CPU part"):
+            for line in info.splitlines():
+                if line.startswith(key) and ":" in line:
+                    val = line.split(":", 1)[1].strip()
+                    arm = {"0xd4f": "Arm Neoverse-V2", "0xd40": "Arm Neoverse-V1",
+                           "0xd0c": "Arm Neoverse-N1", "0xd49": "Arm Neoverse-N2"}
+                    return f"{arm[val]} (CPU part {val})" if val in arm else val
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 # ---- the fp64 oracle on a bounded sample --------------------------------------
 def cpu_oracle_sample(w, inputs, pairs=1):
     """Time the fp64 oracle on `pairs` (batch, head) pairs of the workload (every
@@ -300,7 +329,7 @@ def run_reference(args, w):
             "config": {"workload": describe(w) + "; one step = a bounded sample "
                                                  "(one batch-head pair)"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": desc},
+                             "sample": desc, "cpu": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -609,13 +638,18 @@ def main(argv=None):
     # roofline of the dominant phase: algorithmic bytes / its event time
     hbm_gbs, bf16_tf, peak_kind = _peaks()
     algo = algorithmic(w, elem)
+    exps = algorithmic_exps(w)
+    # ex2 ceiling: 32 results per clock per SM (measured on this part), at the sampled SM clock
+    sm_mhz = clock_info.get("sm_mhz") or clock_info.get("sm_max_mhz") or 2070.0
+    exp_peak = 32.0 * torch.cuda.get_device_properties(dev).multi_processor_count * sm_mhz * 1e6
     dominant = max(phase_ms, key=phase_ms.get)
     per_phase = {}
     for name, ms in phase_ms.items():
         b, f = algo[name]
         per_phase[name] = {"ms": ms, "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_gbs,
                            "tensor_frac": f / (ms * 1e-3) / 1e12 / bf16_tf,
-                           "algo_bytes": b, "algo_flops": f}
+                           "exp_frac": exps[name] / (ms * 1e-3) / exp_peak,
+                           "algo_bytes": b, "algo_flops": f, "algo_exps": exps[name]}
     bytes_dom = algo[dominant][0]
     achieved = bytes_dom / (phase_ms[dominant] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
@@ -625,12 +659,15 @@ def main(argv=None):
                           f"{reps} calls", "phases": per_phase}
 
     dt_name = {"f32": "f32", "bf16": "bf16"}[w.dtype]
+    # token slots include padding; the rate over valid (unpadded) tokens too
+    valid_frac = 1.0 if inp["mask"] is None else float(inp["mask"].float().mean().item())
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dt_name,
             "data": "synthetic (seeded, on device)",
             "config": {"workload": describe(w), "kernel": args.kernel,
                        "tokens_per_step": tokens_per_step,
+                       "valid_token_fraction": valid_frac,
                        "l2": ("512 MiB L2 flush between steps (not timed)" if flush is not None
                               else "inputs larger than L2 (token tensors >= 256 MiB), no flush"),
                        "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
@@ -641,11 +678,12 @@ def main(argv=None):
                     "copies": "each step's inputs copied in from pinned host memory (step i + 1's "
                               "on a second stream, overlapping step i) and its result read back"},
             "gpu_launches": launches,
+            "valid_tokens_per_s": value * valid_frac,
             "roofline": roofline}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, desc, cores, _ = cpu_oracle_sample(w, inp, pairs=1 if w.N > 1 << 20 else 2)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": desc}
+                                "sample": desc, "cpu": cpu_model()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
