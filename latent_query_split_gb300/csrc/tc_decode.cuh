@@ -194,14 +194,13 @@ __device__ __forceinline__ void z_stage_f16(uint8_t *dst, const float *src, floa
 }
 
 // Q and Z of (b, h) index bh (head-major: bh = h * B + b) into Q/Z buffer q,
-// by threads t0, t0 + step, ...; `wid` >= 0: the index of this thread's warp
-// among the cooperating warps 2..STAGER (max|Z| is combined through shared
-// memory), -1: one warp alone. Not inlined: it runs once per (b, h) and would
-// otherwise add its registers to the tile loops'.
+// by the 32 lanes of one warp (the stager, for every (b, h) after the first).
+// Not inlined: it runs once per (b, h) and would otherwise add its registers
+// to the tile loops'.
 template <class C, int M, int D>
 __device__ __noinline__ void dec_stage_qz(uint8_t *smem, const void *Q, const float *Z, int q_f32,
-                                          int q_per_batch, int B, int H, int64_t bh, int q, int t0,
-                                          int step, int wid, int lane) {
+                                          int q_per_batch, int B, int H, int64_t bh, int q, int lane) {
+    const int t0 = lane, step = 32;
     constexpr int KA = C::KA;
     const int h = (int)(bh / B), b = (int)(bh - (int64_t)h * B);
     uint8_t *qdst = smem + q * C::QZ_BYTES, *zdst = qdst + KA * C::QZ_ATOM;
@@ -215,16 +214,80 @@ __device__ __noinline__ void dec_stage_qz(uint8_t *smem, const void *Q, const fl
         float mx = z_absmax_part<M, D>(zsrc, t0, step);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (wid >= 0) {
-            float *xz = reinterpret_cast<float *>(smem + C::MISC_OFF + 16);   // one per warp
-            if (lane == 0) xz[wid] = mx;
-            named_bar_sync(5, 32 * (C::STAGER - 1));
-#pragma unroll
-            for (int w = 0; w < C::STAGER - 1; ++w) mx = fmaxf(mx, xz[w]);
-        }
         z_stage_f16<M, D>(zdst, zsrc, z_scale(mx), t0, step);
     } else {
         stage_rows_bf16<M, D>(zdst, zsrc, t0, step);
+    }
+}
+
+// The first (b, h), staged by the cooperating warps 2..STAGER in one pass:
+// every thread loads all of its Q and Z chunks before it stores any (one
+// round trip to memory instead of one per matrix and pass), max|Z| (fp16 Z)
+// is combined through shared memory, and the chunks go to shared memory from
+// registers. Thread t0 takes chunks t0, t0 + STEP, ...
+template <class C, int M, int D>
+__device__ __noinline__ void dec_stage_qz_first(uint8_t *smem, const void *Q, const float *Z, int q_f32,
+                                                int q_per_batch, int B, int H, int64_t bh, int t0, int wid,
+                                                int lane) {
+    constexpr int KA = C::KA, CHUNKS = M * D / 8, STEP = 32 * (C::STAGER - 1);
+    constexpr int NC = (CHUNKS + STEP - 1) / STEP;
+    const int h = (int)(bh / B), b = (int)(bh - (int64_t)h * B);
+    uint8_t *qdst = smem, *zdst = smem + KA * C::QZ_ATOM;   // Q/Z buffer 0
+    const int64_t qoff = ((int64_t)(q_per_batch ? b : 0) * H + h) * M * D;
+    const float4 *zsrc = reinterpret_cast<const float4 *>(Z + ((int64_t)b * H + h) * M * D);
+    uint4 qv[NC];
+    float4 zv[NC][2];
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+        const int c = t0 + i * STEP;   // chunk c: elements 8c .. 8c + 7 of the row-major matrix
+        if (c < CHUNKS) {
+            qv[i] = q_f32 ? load_chunk8(reinterpret_cast<const float *>(Q) + qoff + 8 * c)
+                          : load_chunk8(reinterpret_cast<const __nv_bfloat16 *>(Q) + qoff + 8 * c);
+            zv[i][0] = __ldg(zsrc + 2 * c);
+            zv[i][1] = __ldg(zsrc + 2 * c + 1);
+        }
+    }
+    float cz = 1.f;
+    if constexpr (C::F16P) {
+        float mx = 0.f;
+#pragma unroll
+        for (int i = 0; i < NC; ++i)
+            if (t0 + i * STEP < CHUNKS)
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(zv[i][k].x), fabsf(zv[i][k].y)),
+                                         fmaxf(fabsf(zv[i][k].z), fabsf(zv[i][k].w))));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float *xz = reinterpret_cast<float *>(smem + C::MISC_OFF + 16);   // one per warp
+        if (lane == 0) xz[wid] = mx;
+        named_bar_sync(5, STEP);
+#pragma unroll
+        for (int w = 0; w < C::STAGER - 1; ++w) mx = fmaxf(mx, xz[w]);
+        cz = z_scale(mx);
+    }
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+        const int c = t0 + i * STEP;
+        if (c < CHUNKS) {
+            const int row = c / (D / 8), j = c % (D / 8);
+            const uint32_t o = (uint32_t)((j >> 3) * (M * 128) + row * 128 + (((j & 7) ^ (row & 7)) << 4));
+            *reinterpret_cast<uint4 *>(qdst + o) = qv[i];
+            const float4 lo = zv[i][0], hi = zv[i][1];
+            *reinterpret_cast<uint4 *>(zdst + o) =
+                C::F16P ? make_uint4(pack_f16(lo.x * cz, lo.y * cz), pack_f16(lo.z * cz, lo.w * cz),
+                                     pack_f16(hi.x * cz, hi.y * cz), pack_f16(hi.z * cz, hi.w * cz))
+                        : make_uint4(pack_bf16(lo.x, lo.y), pack_bf16(lo.z, lo.w), pack_bf16(hi.x, hi.y),
+                                     pack_bf16(hi.z, hi.w));
+        }
+    }
+    if constexpr (C::F16P) {
+        // the row-sum block: columns D..D+15 = [c, 0, ..., 0]
+        uint8_t *ones = zdst + KA * (M * 128);
+        for (int row = t0; row < M; row += STEP) {
+            *reinterpret_cast<uint4 *>(ones + row * 128 + ((0 ^ (row & 7)) << 4)) = make_uint4(pack_f16(cz, 0.f), 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(ones + row * 128 + ((1 ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+        }
     }
 }
 
@@ -295,10 +358,6 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const int64_t bh0 = tb / a.T_bh;
     const int64_t k0 = tb - bh0 * a.T_bh;
     const int64_t n_gen = ntiles > 0 ? (te - 1) / a.T_bh - bh0 + 1 : 0;   // (b, h) of the span
-    auto stage_qz = [&](int64_t u, int t0, int step, int wid) {
-        dec_stage_qz<C, M, D>(smem, a.Q, a.Z, a.q_f32, a.q_per_batch, a.B, a.H, bh0 + u, (int)(u % QZB), t0,
-                              step, wid, lane);
-    };
     // The first (b, h) is staged by warps 2..STAGER together (idle until its
     // first S anyway). Inside the library's forward the decode is launched as
     // a programmatic dependent of the merge that writes Z: only these warps
@@ -307,7 +366,8 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     if (warp >= 2 && warp <= C::STAGER && n_gen > 0) {
         pdl_wait();
         const int wid = warp - 2;
-        stage_qz(0, 32 * wid + lane, 32 * (C::STAGER - 1), wid);
+        dec_stage_qz_first<C, M, D>(smem, a.Q, a.Z, a.q_f32, a.q_per_batch, a.B, a.H, bh0, 32 * wid + lane, wid,
+                                    lane);
         fence_proxy_async_smem();
         named_bar_sync(5, 32 * (C::STAGER - 1));
         if (warp == C::STAGER && lane == 0) mbar_arrive(qz_full(0));
@@ -351,7 +411,8 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             const int q = (int)(u % QZB);
             // the buffer's previous (b, h) has had its last P Z issued and done
             if (u >= QZB && !__all_sync(0xffffffffu, wt.wait(qz_free(q), (uint32_t)(u / QZB - 1) & 1))) break;
-            stage_qz(u, lane, 32, -1);
+            dec_stage_qz<C, M, D>(smem, a.Q, a.Z, a.q_f32, a.q_per_batch, a.B, a.H, bh0 + u, (int)(u % QZB),
+                                  lane);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(qz_full(q));
