@@ -250,7 +250,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 ++u;
                 cur = bh;
                 // Q, dZ and the statistics of the previous (b, h) are no longer read
-                if (u > 0 && !__all_sync(0xffffffffu, wt.wait(qd_free, (uint32_t)(u - 1) & 1))) break;
+                if (u > 0 && !__all_sync(0xffffffffu, wt.wait_inline(qd_free, (uint32_t)(u - 1) & 1))) break;
                 float *dst = lcs + (u & 1) * 256;
                 const float *src = a.lc + bh * 2 * M;
                 for (int i = lane; i < 2 * M; i += 32) dst[(i / M) * 128 + (i % M)] = src[i];
@@ -264,7 +264,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 __syncwarp();
             }
             const int s = (int)(j % STAGES);
-            if (!__all_sync(0xffffffffu, wt.wait(empty(s), ((uint32_t)(j / STAGES) & 1) ^ 1))) break;
+            if (!__all_sync(0xffffffffu, wt.wait_inline(empty(s), ((uint32_t)(j / STAGES) & 1) ^ 1))) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(full(s), C::STAGE_BYTES);
                 const uint32_t dst = sStage + s * C::STAGE_BYTES;
@@ -311,10 +311,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 if (bhS != curS) {
                     ++uS;
                     curS = bhS;
-                    if (!wt.wait(qd_full, (uint32_t)uS & 1)) return false;
+                    if (!wt.wait_inline(qd_full, (uint32_t)uS & 1)) return false;
                 }
                 const int s = (int)(jj % STAGES);
-                if (!wt.wait(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
+                if (!wt.wait_inline(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
                 tc_fence_after();
                 const uint64_t dK = desc_sw128(sStage + s * C::STAGE_BYTES, 16, 1024);
                 const uint64_t dV = desc_sw128(sStage + s * C::STAGE_BYTES + TB, 16, 1024);
@@ -345,12 +345,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 // tile j + 1 of the same (b, h): its S/dP as soon as S/dP of tile j is read
                 const bool early = j + 1 < ntiles && !last;
                 if (early) {
-                    if (!(ok = wt.wait(sdp_free, (uint32_t)j & 1))) break;
+                    if (!(ok = wt.wait_inline(sdp_free, (uint32_t)j & 1))) break;
                     if (!(ok = issue_sdp(j + 1))) break;
                 }
-                if (!(ok = wt.wait(p_full, (uint32_t)j & 1))) break;
+                if (!(ok = wt.wait_inline(p_full, (uint32_t)j & 1))) break;
                 tc_fence_after();
-                if (j > 0 && !(ok = wt.wait(dvdk_free, (uint32_t)(j - 1) & 1))) break;
+                if (j > 0 && !(ok = wt.wait_inline(dvdk_free, (uint32_t)(j - 1) & 1))) break;
                 tc_fence_after();
                 // dV = P^T dZ (A = P^T from tensor memory), dK = (s dS)^T Q (A = dS^T
                 // from shared memory): K = M latents, 16 per MMA
@@ -367,7 +367,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 // a tile of the next (b, h): its Q and dZ arrive once qd_free fired
                 if (j + 1 < ntiles && !early && !(ok = issue_sdp(j + 1))) break;
                 // dQ += (s dS) K over the tile's 128 tokens, 16 per MMA
-                if (first && uP > 0 && !(ok = wt.wait(dq_free, (uint32_t)(uP - 1) & 1))) break;
+                if (first && uP > 0 && !(ok = wt.wait_inline(dq_free, (uint32_t)(uP - 1) & 1))) break;
                 tc_fence_after();
                 const int s = (int)(j % STAGES);
                 const uint64_t dKm = desc_sw128(sStage + s * C::STAGE_BYTES, TB, 1024);
@@ -411,7 +411,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         uint8_t *slab = smem + C::OUT_OFF + (hf * 4 + quad) * (32 * 128);
         const CUtensorMap *tmOut = hf ? &tmdK : &tmdV;
         auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
-            return __all_sync(0xffffffffu, wt.wait(bar, par));
+            return __all_sync(0xffffffffu, wt.wait_inline(bar, par));
         };
         // The mask byte of this thread's token is loaded two tiles ahead and
         // only compared when its tile comes up, so the load's latency is never

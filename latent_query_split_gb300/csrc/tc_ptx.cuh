@@ -82,6 +82,22 @@ struct Waiter {
         if (mbar_try_wait(bar, parity)) return true;
         return wait_slow(bar, parity);
     }
+    // The same wait with its bounded loop inline: no call, so no registers are
+    // saved around it. Pays where a kernel's register budget is tight and its
+    // waits often block (the encoder backward); elsewhere the call is cheaper.
+    __device__ __forceinline__ bool wait_inline(uint32_t bar, uint32_t parity) const {
+        if (mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = globaltimer();
+        while (true) {
+            if (mbar_try_wait(bar, parity)) return true;
+            if (*abort) return false;
+            if (globaltimer() - t0 > kWaitNs) {
+                *abort = 1;
+                atomicExch(status, 1u);
+                return false;
+            }
+        }
+    }
     // Spin with test_wait (no suspension): for a thread whose reaction time
     // is on the critical path and whose warp has nothing else to do.
     __device__ __forceinline__ bool spin(uint32_t bar, uint32_t parity) const {
