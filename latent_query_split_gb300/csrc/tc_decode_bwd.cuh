@@ -204,7 +204,7 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 ++u;
                 cur = bh;
                 // Q and Z of the previous (b, h) are no longer read
-                if (u > 0 && !__all_sync(0xffffffffu, wt.wait(qz_free, (uint32_t)(u - 1) & 1))) break;
+                if (u > 0 && !__all_sync(0xffffffffu, wt.wait_inline(qz_free, (uint32_t)(u - 1) & 1))) break;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(qz_full, 2 * C::QZ_BYTES);
                     tma_load_4d(sQ, &tmQ, 0, 0, h, a.q_per_batch ? b : 0, qz_full);
@@ -213,7 +213,7 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 __syncwarp();
             }
             const int s = (int)(j % STAGES);
-            if (!__all_sync(0xffffffffu, wt.wait(empty(s), ((uint32_t)(j / STAGES) & 1) ^ 1))) break;
+            if (!__all_sync(0xffffffffu, wt.wait_inline(empty(s), ((uint32_t)(j / STAGES) & 1) ^ 1))) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(full(s), C::STAGE_BYTES);
                 const uint32_t dst = sStage + s * C::STAGE_BYTES;
@@ -259,10 +259,10 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 if (bhS != curS) {
                     ++uS;
                     curS = bhS;
-                    if (!wt.wait(qz_full, (uint32_t)uS & 1)) return false;
+                    if (!wt.wait_inline(qz_full, (uint32_t)uS & 1)) return false;
                 }
                 const int s = (int)(jj % STAGES);
-                if (!wt.wait(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
+                if (!wt.wait_inline(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
                 tc_fence_after();
                 const uint64_t dK = desc_sw128(sStage + s * C::STAGE_BYTES, 16, 1024);
                 const uint64_t dY = desc_sw128(sStage + s * C::STAGE_BYTES + TB, 16, 1024);
@@ -293,12 +293,12 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 // tile j + 1 of the same (b, h): its S/G as soon as S/G of tile j is read
                 const bool early = j + 1 < ntiles && !last;
                 if (early) {
-                    if (!(ok = wt.wait(sg_free, (uint32_t)j & 1))) break;
+                    if (!(ok = wt.wait_inline(sg_free, (uint32_t)j & 1))) break;
                     if (!(ok = issue_sg(j + 1))) break;
                 }
-                if (!(ok = wt.wait(p_full, (uint32_t)j & 1))) break;
+                if (!(ok = wt.wait_inline(p_full, (uint32_t)j & 1))) break;
                 tc_fence_after();
-                if (j > 0 && !(ok = wt.wait(dk_free, (uint32_t)(j - 1) & 1))) break;
+                if (j > 0 && !(ok = wt.wait_inline(dk_free, (uint32_t)(j - 1) & 1))) break;
                 tc_fence_after();
                 // dK = (s dT) Q: K = M latents, 16 per MMA (A = s dT from its TMEM columns)
 #pragma unroll
@@ -310,7 +310,7 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 // a tile of the next (b, h): its Q and Z arrive once qz_free fired
                 if (j + 1 < ntiles && !early && !(ok = issue_sg(j + 1))) break;
                 // dQ += (s dT)^T K, dZ += A^T dY over the tile's 128 tokens
-                if (first && uP > 0 && !(ok = wt.wait(pz_free, (uint32_t)(uP - 1) & 1))) break;
+                if (first && uP > 0 && !(ok = wt.wait_inline(pz_free, (uint32_t)(uP - 1) & 1))) break;
                 tc_fence_after();
                 const int s = (int)(j % STAGES);
                 const uint64_t dKm = desc_sw128(sStage + s * C::STAGE_BYTES, TB, 1024);
@@ -361,7 +361,7 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         const bool storer = hf == 0 && lane == 0;
         const int pair_bar = 1 + quad;                         // named barrier of the quadrant
         auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
-            return __all_sync(0xffffffffu, wt.wait(bar, par));
+            return __all_sync(0xffffffffu, wt.wait_inline(bar, par));
         };
         int pieces = 0;
         uint32_t stores = 0;
@@ -471,16 +471,34 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(sg_free);
-            float ls = 0.f, lr = 0.f;
+            // two latents per packed instruction; two partial sums of each kind
+            const uint64_t sl2x2 = f2pack(sl2, sl2), nm2x2 = f2pack(-m2, -m2);
+            uint64_t ls2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+            uint64_t lr2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
 #pragma unroll
             for (int c = 0; c < W / 32; ++c)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float p = ex2(fmaf(__uint_as_float(sv[c][i]), sl2, -m2));
-                    sv[c][i] = __float_as_uint(p);
-                    ls += p;
-                    lr = fmaf(p, __uint_as_float(gv[c][i]), lr);
+                for (int i = 0; i < 16; ++i) {
+                    float t0, t1;
+                    f2unpack(fma2(f2pack(__uint_as_float(sv[c][2 * i]), __uint_as_float(sv[c][2 * i + 1])), sl2x2,
+                                  nm2x2),
+                             t0, t1);
+                    const float p0 = ex2(t0), p1 = ex2(t1);
+                    sv[c][2 * i] = __float_as_uint(p0);
+                    sv[c][2 * i + 1] = __float_as_uint(p1);
+                    const uint64_t p2 = f2pack(p0, p1);
+                    ls2[i & 1] = add2(ls2[i & 1], p2);
+                    lr2[i & 1] = fma2(p2, f2pack(__uint_as_float(gv[c][2 * i]), __uint_as_float(gv[c][2 * i + 1])),
+                                      lr2[i & 1]);
                 }
+            float ls, lr;
+            {
+                float x0, x1, x2, x3;
+                f2unpack(add2(ls2[0], ls2[1]), x0, x1);
+                f2unpack(add2(lr2[0], lr2[1]), x2, x3);
+                ls = x0 + x1;
+                lr = x2 + x3;
+            }
             xl[(par * 2 + hf) * 128 + rig] = make_float2(ls, lr);
             named_bar_sync(pair_bar, 64);
             const float2 o = xl[(par * 2 + (hf ^ 1)) * 128 + rig];
@@ -491,15 +509,20 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             // the previous tile's products have read them
             if (j > 0 && !(ok = wwait(dk_full, (uint32_t)(j - 1) & 1))) break;
             if (j > 0 && !(ok = wwait(at_free, (uint32_t)(j - 1) & 1))) break;
+            // A = p inv and s dT = A (s g - s r), two latents per instruction
+            const uint64_t inv2 = f2pack(inv, inv), sc2 = f2pack(sc, sc), nsr2 = f2pack(-sc * r, -sc * r);
 #pragma unroll
             for (int c = 0; c < W / 32; ++c) {
                 uint32_t aw[16], tw[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float a0 = __uint_as_float(sv[c][2 * i]) * inv;
-                    const float a1 = __uint_as_float(sv[c][2 * i + 1]) * inv;
-                    const float t0 = sc * a0 * (__uint_as_float(gv[c][2 * i]) - r);
-                    const float t1 = sc * a1 * (__uint_as_float(gv[c][2 * i + 1]) - r);
+                    const uint64_t a2 =
+                        mul2(f2pack(__uint_as_float(sv[c][2 * i]), __uint_as_float(sv[c][2 * i + 1])), inv2);
+                    const uint64_t t2 = mul2(
+                        a2, fma2(f2pack(__uint_as_float(gv[c][2 * i]), __uint_as_float(gv[c][2 * i + 1])), sc2, nsr2));
+                    float a0, a1, t0, t1;
+                    f2unpack(a2, a0, a1);
+                    f2unpack(t2, t0, t1);
                     aw[i] = pack_bf16(a0, a1);
                     tw[i] = pack_bf16(t0, t1);
                 }
