@@ -240,11 +240,13 @@ __global__ void fill_empty_kernel(float *O_r, int64_t nO, float *L_r, int64_t nL
 
 // Core of flare_encoder_fwd, also used by flare_fwd and flare_pp_fwd.
 // q_is_f32: the query is fp32 even though the token tensors are bf16 (the
-// FLARE++ dynamic queries).
+// FLARE++ dynamic queries). check_only: validate every argument and return
+// before anything is launched (the composite calls check all of their
+// stages before the first launch).
 flare_status_t encoder_run(const flare_dims_t *d, const void *Q, bool q_is_f32, const void *K,
                            const void *V, const uint8_t *mask, const int64_t *off, int R,
                            float *O_r, float *L_r, float *Z, float *L, void *ws, size_t ws_bytes,
-                           cudaStream_t st) {
+                           cudaStream_t st, bool check_only = false) {
     if ((O_r == nullptr) != (L_r == nullptr))
         return fail(FLARE_ERR_INVALID_ARG, "O_r and L_r must be given together");
     if ((Z == nullptr) != (L == nullptr))
@@ -272,6 +274,7 @@ flare_status_t encoder_run(const flare_dims_t *d, const void *Q, bool q_is_f32, 
     const size_t need = encoder_ws_bytes(d, off, R);
     const int64_t bhm = (int64_t)pr.B * pr.H * pr.M;
     if (pr.N == 0) {                           // no token: every row is empty
+        if (check_only) return FLARE_OK;
         fill_empty_kernel<<<64, 256, 0, st>>>(O_r, O_r ? R * bhm * pr.D : 0, L_r, L_r ? R * bhm : 0,
                                                Z, Z ? bhm * pr.D : 0, L, L ? bhm : 0);
         note_launch();
@@ -281,6 +284,7 @@ flare_status_t encoder_run(const flare_dims_t *d, const void *Q, bool q_is_f32, 
     if (!ws || ws_bytes < need)
         return fail(FLARE_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", need, ws_bytes);
     if (!aligned(ws, 256)) return fail(FLARE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (check_only) return FLARE_OK;
     EncoderWorkspace w = bind(lay.ws, ws);
     EncoderOut out{O_r, L_r, Z, L};
     cudaError_t e;
@@ -299,7 +303,8 @@ flare_status_t encoder_run(const flare_dims_t *d, const void *Q, bool q_is_f32, 
 }
 
 flare_status_t decode_run(const flare_dims_t *d, const void *Q, bool q_is_f32, const float *Z,
-                          const void *K, void *Y, bool after_merge, cudaStream_t st) {
+                          const void *K, void *Y, bool after_merge, cudaStream_t st,
+                          bool check_only = false) {
     const Problem pr = make_problem(d);
     if (pr.B == 0 || pr.N == 0) return FLARE_OK;
     if (!Q || !Z || !K || !Y) return fail(FLARE_ERR_INVALID_ARG, "NULL tensor");
@@ -313,6 +318,7 @@ flare_status_t decode_run(const flare_dims_t *d, const void *Q, bool q_is_f32, c
     const bool tc = want_tc && tc_pointers_ok(K, Y, d->H, d->D) && aligned(Q, 16) && aligned(Z, 16);
     if (d->kernel == FLARE_KERNEL_TENSOR && !tc)
         return fail(FLARE_ERR_INVALID_ARG, "tensor-core decode needs 16-byte aligned Q, Z, K and Y");
+    if (check_only) return FLARE_OK;
     cudaError_t e;
     if (tc) {
         DeviceInfo di;
@@ -348,10 +354,11 @@ size_t decode_bwd_ws(const flare_dims_t *d) {
 
 // Core of flare_encoder_bwd (dims and offsets already checked). accumulate:
 // dQ and dK already hold another consumer's share and this pass adds its own.
+// check_only: as for encoder_run.
 flare_status_t encoder_bwd_run(const flare_dims_t *dims, const void *Q, const void *K, const void *V,
                                const uint8_t *mask, const float *Z, const float *L, const float *dZ,
                                float *dQ, void *dK, void *dV, void *workspace, size_t workspace_bytes,
-                               bool accumulate, cudaStream_t st) {
+                               bool accumulate, cudaStream_t st, bool check_only = false) {
     const Problem pr = make_problem(dims);
     if (pr.B == 0) return FLARE_OK;
     if (!Q || !Z || !L || !dZ || !dQ || (pr.N > 0 && (!K || !V || !dK || !dV)))
@@ -376,6 +383,7 @@ flare_status_t encoder_bwd_run(const flare_dims_t *dims, const void *Q, const vo
                     workspace_bytes);
     if (workspace && !aligned(workspace, 256))
         return fail(FLARE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (check_only) return FLARE_OK;
     cudaError_t e;
     if (tc) {
         DeviceInfo di;
@@ -390,10 +398,10 @@ flare_status_t encoder_bwd_run(const flare_dims_t *dims, const void *Q, const vo
     return e == cudaSuccess ? FLARE_OK : cuda_fail(e, "encoder backward launch");
 }
 
-// Core of flare_decode_bwd (dims already checked).
+// Core of flare_decode_bwd (dims already checked). check_only: as for encoder_run.
 flare_status_t decode_bwd_run(const flare_dims_t *dims, const void *Q, const float *Z, const void *K,
                               const void *dY, float *dQ, float *dZ, void *dK, void *workspace,
-                              size_t workspace_bytes, cudaStream_t st) {
+                              size_t workspace_bytes, cudaStream_t st, bool check_only = false) {
     const Problem pr = make_problem(dims);
     if (pr.B == 0) return FLARE_OK;
     if (!Q || !Z || !dQ || !dZ || (pr.N > 0 && (!K || !dY || !dK)))
@@ -417,6 +425,7 @@ flare_status_t decode_bwd_run(const flare_dims_t *dims, const void *Q, const flo
         return fail(FLARE_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", need,
                     workspace_bytes);
     if (!aligned(workspace, 256)) return fail(FLARE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (check_only) return FLARE_OK;
     cudaError_t e;
     if (tc) {
         DeviceInfo di;
@@ -555,10 +564,14 @@ flare_status_t flare_fwd(const flare_dims_t *dims, const void *Q, const void *K,
     if ((s = check_offsets(shard_offsets, R, dims->N)) != FLARE_OK) return s;
     if (!Z || !L) return fail(FLARE_ERR_INVALID_ARG, "flare_fwd needs Z and L");
     cudaStream_t st = (cudaStream_t)stream;
-    if ((s = encoder_run(dims, Q, false, K, V, mask, shard_offsets, R, nullptr, nullptr, Z, L,
-                         workspace, workspace_bytes, st)) != FLARE_OK)
-        return s;
-    return decode_run(dims, Q, false, Z, K, Y, true, st);
+    // both stages' arguments are checked before the first launch
+    for (const bool check : {true, false}) {
+        if ((s = encoder_run(dims, Q, false, K, V, mask, shard_offsets, R, nullptr, nullptr, Z, L,
+                             workspace, workspace_bytes, st, check)) != FLARE_OK)
+            return s;
+        if ((s = decode_run(dims, Q, false, Z, K, Y, true, st, check)) != FLARE_OK) return s;
+    }
+    return FLARE_OK;
 }
 
 flare_status_t flare_pp_fwd(const flare_dims_t *dims, const void *Qseed, const void *Kt,
@@ -571,15 +584,19 @@ flare_status_t flare_pp_fwd(const flare_dims_t *dims, const void *Qseed, const v
     if ((s = check_offsets(shard_offsets, R, dims->N)) != FLARE_OK) return s;
     if (!Qdyn || !L1 || !Z || !L2) return fail(FLARE_ERR_INVALID_ARG, "flare_pp_fwd outputs are required");
     cudaStream_t st = (cudaStream_t)stream;
-    if ((s = encoder_run(dims, Qseed, false, Kt, Vt, mask, shard_offsets, R, nullptr, nullptr, Qdyn,
-                         L1, workspace, workspace_bytes, st)) != FLARE_OK)
-        return s;
     flare_dims_t d2 = *dims;                                   // Q(X) is per batch element
     d2.q_batch_stride = (int64_t)dims->H * dims->M * dims->D;
-    if ((s = encoder_run(&d2, Qdyn, true, K, V, mask, shard_offsets, R, nullptr, nullptr, Z, L2,
-                         workspace, workspace_bytes, st)) != FLARE_OK)
-        return s;
-    return decode_run(&d2, Qdyn, true, Z, K, Y, true, st);
+    // the three stages' arguments are checked before the first launch
+    for (const bool check : {true, false}) {
+        if ((s = encoder_run(dims, Qseed, false, Kt, Vt, mask, shard_offsets, R, nullptr, nullptr, Qdyn,
+                             L1, workspace, workspace_bytes, st, check)) != FLARE_OK)
+            return s;
+        if ((s = encoder_run(&d2, Qdyn, true, K, V, mask, shard_offsets, R, nullptr, nullptr, Z, L2,
+                             workspace, workspace_bytes, st, check)) != FLARE_OK)
+            return s;
+        if ((s = decode_run(&d2, Qdyn, true, Z, K, Y, true, st, check)) != FLARE_OK) return s;
+    }
+    return FLARE_OK;
 }
 
 flare_status_t flare_encoder_bwd(const flare_dims_t *dims, const void *Q, const void *K,
@@ -620,13 +637,18 @@ flare_status_t flare_bwd(const flare_dims_t *dims, const void *Q, const void *K,
     char *w = (char *)workspace;
     float *dZ = (float *)(w + l.dz);
     cudaStream_t st = (cudaStream_t)stream;
-    // the decoder's shares of dQ and dK, and dZ (Z's only consumer in the mixer)
-    if ((s = decode_bwd_run(dims, Q, Z, K, dY, dQ, dZ, dK, w + l.scratch, workspace_bytes - l.scratch,
-                            st)) != FLARE_OK)
-        return s;
-    // the encoder with its global (Z, L) adds its shares and gives dV
-    return encoder_bwd_run(dims, Q, K, V, mask, Z, L, dZ, dQ, dK, dV, w + l.scratch,
-                           workspace_bytes - l.scratch, true, st);
+    // both stages' arguments are checked before the first launch
+    for (const bool check : {true, false}) {
+        // the decoder's shares of dQ and dK, and dZ (Z's only consumer in the mixer)
+        if ((s = decode_bwd_run(dims, Q, Z, K, dY, dQ, dZ, dK, w + l.scratch,
+                                workspace_bytes - l.scratch, st, check)) != FLARE_OK)
+            return s;
+        // the encoder with its global (Z, L) adds its shares and gives dV
+        if ((s = encoder_bwd_run(dims, Q, K, V, mask, Z, L, dZ, dQ, dK, dV, w + l.scratch,
+                                 workspace_bytes - l.scratch, true, st, check)) != FLARE_OK)
+            return s;
+    }
+    return FLARE_OK;
 }
 
 flare_status_t flare_pp_bwd(const flare_dims_t *dims, const void *Qseed, const void *Kt,
@@ -657,23 +679,29 @@ flare_status_t flare_pp_bwd(const flare_dims_t *dims, const void *Qseed, const v
     flare_dims_t d2 = *dims;                                   // Q(X) is per batch element
     d2.q_batch_stride = (int64_t)dims->H * dims->M * dims->D;
     // Q(X) as the operand of the decode and physical-value encoder: bf16 on the bf16 path
-    const void *QX = Qdyn;
-    if (dims->dtype == FLARE_BF16) {
-        const cudaError_t e = launch_f32_to_bf16(Qdyn, w + l.qdyn_b,
-                                                 (int64_t)dims->B * dims->H * dims->M * dims->D, st);
-        if (e != cudaSuccess) return cuda_fail(e, "Q(X) conversion launch");
-        QX = w + l.qdyn_b;
+    const bool convert = dims->dtype == FLARE_BF16;
+    const void *QX = convert ? (const void *)(w + l.qdyn_b) : (const void *)Qdyn;
+    // the three stages' arguments are checked before the first launch
+    for (const bool check : {true, false}) {
+        if (!check && convert) {
+            const cudaError_t e = launch_f32_to_bf16(Qdyn, w + l.qdyn_b,
+                                                     (int64_t)dims->B * dims->H * dims->M * dims->D, st);
+            if (e != cudaSuccess) return cuda_fail(e, "Q(X) conversion launch");
+        }
+        // decoder: its shares of dQ(X) and dK, and dZ
+        if ((s = decode_bwd_run(&d2, QX, Z, K, dY, dQX, dZ, dK, scratch, scratch_bytes, st, check)) !=
+            FLARE_OK)
+            return s;
+        // physical-value encoder (Z, L2): adds its shares of dQ(X) and dK, gives dV
+        if ((s = encoder_bwd_run(&d2, QX, K, V, mask, Z, L2, dZ, dQX, dK, dV, scratch, scratch_bytes,
+                                 true, st, check)) != FLARE_OK)
+            return s;
+        // query-synthesis encoder (its output Q(X), L1) with the summed dQ(X)
+        if ((s = encoder_bwd_run(dims, Qseed, Kt, Vt, mask, Qdyn, L1, dQX, dQseed, dKt, dVt, scratch,
+                                 scratch_bytes, false, st, check)) != FLARE_OK)
+            return s;
     }
-    // decoder: its shares of dQ(X) and dK, and dZ
-    if ((s = decode_bwd_run(&d2, QX, Z, K, dY, dQX, dZ, dK, scratch, scratch_bytes, st)) != FLARE_OK)
-        return s;
-    // physical-value encoder (Z, L2): adds its shares of dQ(X) and dK, gives dV
-    if ((s = encoder_bwd_run(&d2, QX, K, V, mask, Z, L2, dZ, dQX, dK, dV, scratch, scratch_bytes, true,
-                             st)) != FLARE_OK)
-        return s;
-    // query-synthesis encoder (its output Q(X), L1) with the summed dQ(X)
-    return encoder_bwd_run(dims, Qseed, Kt, Vt, mask, Qdyn, L1, dQX, dQseed, dKt, dVt, scratch,
-                           scratch_bytes, false, st);
+    return FLARE_OK;
 }
 
 flare_status_t flare_device_status(void *stream) {

@@ -98,3 +98,84 @@ def test_merge_rejects_bad_sizes(lib):
 def test_binding_refuses_host_tensors(lib):
     with pytest.raises(ValueError):
         flare._ptr(torch.zeros(3))
+
+
+# The composite calls check the arguments of every stage before the first
+# launch: a bad argument of a later stage is reported as such, with nothing
+# launched (here, without a GPU, a launch attempt would fail as FLARE_ERR_CUDA).
+_A = [1 << (12 + i) for i in range(24)]      # fake, aligned, distinct device addresses
+
+
+def _bigws(lib, op, dims, offs):
+    arr = (ctypes.c_int64 * len(offs))(*offs) if offs is not None else None
+    n = lib.flare_workspace_bytes(op, ctypes.byref(dims), arr, len(offs) - 1 if offs else 0)
+    assert n != BAD
+    return 1 << 40, max(n, 1)
+
+
+def _offs(offs):
+    return (ctypes.c_int64 * len(offs))(*offs)
+
+
+@pytest.mark.parametrize("dtype", [flare.FLARE_F32, flare.FLARE_BF16])
+def test_flare_fwd_checks_the_decode_before_launching(lib, dtype):
+    d = _dims(dtype=dtype, M=64, D=64, N=256)
+    offs = [0, 100, 256]
+    ws, nb = _bigws(lib, flare.FLARE_OP_FWD, d, offs)
+    before = lib.flare_launch_count()
+    s = lib.flare_fwd(ctypes.byref(d), _A[0], _A[1], _A[2], None, _offs(offs), 2,
+                      None, _A[3], _A[4], ws, nb, None)       # Y missing
+    assert s == flare.FLARE_ERR_INVALID_ARG
+    assert b"NULL" in lib.flare_last_error_string()
+    assert lib.flare_launch_count() == before
+
+
+@pytest.mark.parametrize("dtype", [flare.FLARE_F32, flare.FLARE_BF16])
+def test_flare_pp_fwd_checks_every_stage_before_launching(lib, dtype):
+    d = _dims(dtype=dtype, M=64, D=64, N=256)
+    offs = [0, 100, 256]
+    ws, nb = _bigws(lib, flare.FLARE_OP_PP_FWD, d, offs)
+    before = lib.flare_launch_count()
+    # K missing: the first encoder (over K~, V~) is fine, the second is not
+    s = lib.flare_pp_fwd(ctypes.byref(d), _A[0], _A[1], _A[2], None, _A[3], None, _offs(offs), 2,
+                         _A[4], _A[5], _A[6], _A[7], _A[8], ws, nb, None)
+    assert s == flare.FLARE_ERR_INVALID_ARG
+    # Y missing: only the decode stage sees it
+    s = lib.flare_pp_fwd(ctypes.byref(d), _A[0], _A[1], _A[2], _A[9], _A[3], None, _offs(offs), 2,
+                         None, _A[5], _A[6], _A[7], _A[8], ws, nb, None)
+    assert s == flare.FLARE_ERR_INVALID_ARG
+    assert lib.flare_launch_count() == before
+
+
+@pytest.mark.parametrize("dtype", [flare.FLARE_F32, flare.FLARE_BF16])
+def test_flare_bwd_checks_the_encoder_stage_before_launching(lib, dtype):
+    d = _dims(dtype=dtype, M=64, D=64, N=256)
+    offs = [0, 100, 256]
+    ws, nb = _bigws(lib, flare.FLARE_OP_BWD, d, offs)
+    before = lib.flare_launch_count()
+    # dV missing: the decode backward (first stage) needs no V or dV
+    s = lib.flare_bwd(ctypes.byref(d), _A[0], _A[1], _A[2], None, _offs(offs), 2, _A[3], _A[4],
+                      _A[5], _A[6], _A[7], None, ws, nb, None)
+    assert s == flare.FLARE_ERR_INVALID_ARG
+    # a workspace that is too small is reported before anything runs
+    s = lib.flare_bwd(ctypes.byref(d), _A[0], _A[1], _A[2], None, _offs(offs), 2, _A[3], _A[4],
+                      _A[5], _A[6], _A[7], _A[8], ws, 1024, None)
+    assert s == flare.FLARE_ERR_WORKSPACE
+    assert lib.flare_launch_count() == before
+
+
+@pytest.mark.parametrize("dtype", [flare.FLARE_F32, flare.FLARE_BF16])
+def test_flare_pp_bwd_checks_every_stage_before_launching(lib, dtype):
+    d = _dims(dtype=dtype, M=64, D=64, N=256)
+    offs = [0, 100, 256]
+    ws, nb = _bigws(lib, flare.FLARE_OP_PP_BWD, d, offs)
+    before = lib.flare_launch_count()
+
+    def call(dKt=_A[15], dV=_A[18], Vt=_A[2]):
+        return lib.flare_pp_bwd(ctypes.byref(d), _A[0], _A[1], Vt, _A[3], _A[4], None, _offs(offs), 2,
+                                _A[5], _A[6], _A[7], _A[8], _A[9], _A[10], dKt, _A[16], _A[17], dV,
+                                None, ws, nb, None)
+    assert call(dV=None) == flare.FLARE_ERR_INVALID_ARG     # second stage
+    assert call(dKt=None) == flare.FLARE_ERR_INVALID_ARG    # third stage
+    assert call(Vt=None) == flare.FLARE_ERR_INVALID_ARG     # third stage's input
+    assert lib.flare_launch_count() == before
