@@ -30,7 +30,9 @@
  *    workspaces.
  *  - stream is a cudaStream_t (NULL = legacy default stream). Calls are
  *    stream-ordered and asynchronous: argument errors are reported
- *    synchronously before anything is launched; launch failures are returned
+ *    synchronously before anything is launched (for the calls that chain
+ *    several passes, the arguments of every pass are checked before the
+ *    first launch); launch failures are returned
  *    as FLARE_ERR_CUDA; a kernel that abandoned a bounded wait records
  *    FLARE_ERR_TIMEOUT on the device, reported by flare_device_status().
  *  - On any error flare_last_error_string() describes it (thread-local).
