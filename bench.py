@@ -2,11 +2,13 @@
 
 One step = one pass of the hot path over one batch of a named workload
 (latent_query_split_gb300.workloads.CONFIGS), inputs resident in HBM:
-  c2_bf16 (default)  FLARE forward bf16, B=4 H=8 D=64 M=128 N=65536, R=8
-                     ragged shards, 5% padded tokens: the split-KV encoder with
-                     its log-sum-exp merge, then the local decode of every token
+  c4_long_bf16 (default)  FLARE forward bf16, B=1 H=8 D=128 M=64 N=4194304,
+                     R=64 ragged shards, 1% of keys x8: the split-KV encoder
+                     with its log-sum-exp merge, then the local decode of
+                     every token (the largest FLARE encode+decode workload)
+  c2_bf16            the same forward, B=4 H=8 D=64 M=128 N=65536, R=8
+                     ragged shards, 5% padded tokens
   c1_fp32_small      the same forward on the small fp32 workload
-  c4_long_bf16       the same forward, B=1 H=8 D=128 M=64 N=4194304, R=64
   c3_pp_bf16         FLARE++ forward (encoder twice, then the decode)
   c5_bwd_bf16        global-normaliser encoder backward (dQ, dK, dV)
   c5_decbwd_bf16     decode backward (dQ, dZ, dK) on the shapes of c5
@@ -16,9 +18,14 @@ One step = one pass of the hot path over one batch of a named workload
 Token tensors of c2-c5 are 256 MiB or more each (larger than the 129 MB L2),
 so no flush is needed between steps; c1 flushes L2 between steps.
 
-Prints one JSON line (rank 0). Under torchrun each rank runs an independent
-replica of the workload on its own GPU (weak scaling, no collective on the
-data path); the reported time is the max over ranks.
+Prints one JSON line (rank 0). Under torchrun (N > 1 GPUs) the FLARE forward
+workloads run context-parallel by default (--mode cp): every rank holds its
+own slice of N tokens of one problem of N x ranks tokens and a replica of the
+latent queries, the ranks all-gather their partial (O_r, L_r) over NCCL and
+each merges them and decodes its own tokens (weak scaling: the tokens per GPU
+are fixed). --mode replicas, and every other workload, runs an independent
+replica per GPU with no collective on the data path. The reported time is the
+max over ranks.
 
 --impl reference times the fp64 CPU oracle on a bounded sample of the same
 workload (the oracle is the reference implementation here).
@@ -43,7 +50,7 @@ if ROOT not in sys.path:
 
 METRIC = "FLARE encode+decode tokens/s at 1 GB300; % of roofline (HBM GB/s or tensor-pipe)"
 UNIT = "tokens/s"
-DEFAULT_WORKLOAD = "c2_bf16"
+DEFAULT_WORKLOAD = "c4_long_bf16"
 # library sources whose content a committed ncu traffic figure belongs to
 KERNEL_SOURCES = {
     "encoder": ["tc_encoder.cuh", "tc_ptx.cuh", "tc_kernels.cu"],
@@ -341,10 +348,11 @@ class Step:
     """Builds the phases of one step (each a call of the public API) for a
     workload, over device tensors."""
 
-    def __init__(self, w, inp, dev, kernel, stream):
+    def __init__(self, w, inp, dev, kernel, stream, ex=None):
         import torch
         from latent_query_split_gb300 import flare
         self.w, self.inp, self.kernel, self.stream = w, inp, kernel, stream
+        self.ex = ex            # context-parallel exchange (FLARE forward over ranks), or None
         B, N, H, D, M = w.B, w.N, w.H, w.D, w.M
         f32 = dict(dtype=torch.float32, device=dev)
         self.off = inp["offsets"]
@@ -399,7 +407,11 @@ class Step:
         from latent_query_split_gb300 import flare
         x = inp or self.inp
         w, k, st, off = self.w, self.kernel, self.stream, self.off
-        if w.kind == "flare_fwd":
+        if w.kind == "flare_fwd" and self.ex is not None:
+            from latent_query_split_gb300 import cp
+            cp.cp_fwd(self.ex, x["Q"], x["K"], x["V"], x["mask"], off, Y=self.Y, Z=self.Z,
+                      L=self.L, workspace=self.ws, kernel=k, stream=st)
+        elif w.kind == "flare_fwd":
             flare.flare_fwd(x["Q"], x["K"], x["V"], x["mask"], off, Y=self.Y, Z=self.Z, L=self.L,
                             workspace=self.ws, kernel=k, stream=st)
         else:
@@ -471,6 +483,9 @@ def main(argv=None):
     ap.add_argument("--kernel", choices=["auto", "simt", "tensor"], default="auto")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", choices=["auto", "cp", "replicas"], default="auto",
+                    help="multi-GPU layout: context-parallel token slices (FLARE forward) or "
+                         "independent replicas; auto = cp for the FLARE forward")
     ap.add_argument("--n", type=int, default=None,
                     help="run the workload's structure at N tokens (small cases for profiler captures)")
     args = ap.parse_args(argv)
@@ -496,9 +511,22 @@ def main(argv=None):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
+    mode = args.mode
+    if mode == "auto":
+        mode = "cp" if w.kind == "flare_fwd" else "replicas"
+    if mode == "cp" and w.kind != "flare_fwd":
+        raise SystemExit("--mode cp runs the FLARE forward workloads")
+    cp_on = mode == "cp" and world > 1
     inp = workloads.make_inputs(replica_workload(w, rank), device=dev)
+    ex = None
+    if cp_on:
+        # one problem of N x world tokens: this rank's slice is its own draw,
+        # the latent queries are rank 0's on every rank
+        from latent_query_split_gb300 import cp
+        dist.broadcast(inp["Q"], src=0)
+        ex = cp.Exchange()
     stream = torch.cuda.Stream(device=dev)
-    runner = Step(w, inp, dev, args.kernel, stream)
+    runner = Step(w, inp, dev, args.kernel, stream, ex)
     phases = runner.phases()
     # an L2 flush between steps for workloads whose tensors fit in L2
     elem = inp["K"].element_size()
@@ -670,7 +698,10 @@ def main(argv=None):
                        "valid_token_fraction": valid_frac,
                        "l2": ("512 MiB L2 flush between steps (not timed)" if flush is not None
                               else "inputs larger than L2 (token tensors >= 256 MiB), no flush"),
-                       "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
+                       "parallelism": (("context-parallel over %d GPUs: %d tokens per GPU, "
+                                        "NCCL all-gather of (O_r, L_r), merge and decode on "
+                                        "every rank" % (world, w.N)) if cp_on else
+                                       f"{world} independent replicas" if world > 1 else "1 GPU")},
             "clocks": clock_info,
             "e2e": {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -209,6 +209,28 @@ FLARE_API flare_status_t flare_encoder_bwd(const flare_dims_t *dims, const void 
                                  void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * flare_encoder_bwd that adds its shares to gradients another consumer has
+ * already written. Source: the backward paragraphs of the appendix (a
+ * replicated tensor's gradient is the sum of its consumers' contributions;
+ * dQ is summed over shards and ranks). Arguments, layouts and workspace are
+ * those of flare_encoder_bwd, except:
+ *   dQ  fp32 [B,H,M,D] is read and the encoder's share added to it;
+ *   dK  dims->dtype [B,N,H,D] is read and the encoder's share added to it
+ *       (the sum taken in fp32 and rounded once to dims->dtype);
+ *   dV  dims->dtype [B,N,H,D] is written (V has no other consumer).
+ * A context-parallel rank uses it after its decode backward: the decode's
+ * shares of dQ and dK are in place, the all-reduced dZ is the input.
+ */
+FLARE_API flare_status_t flare_encoder_bwd_accumulate(const flare_dims_t *dims, const void *Q,
+                                                      const void *K, const void *V,
+                                                      const uint8_t *mask,
+                                                      const int64_t *shard_offsets, int R,
+                                                      const float *Z, const float *L,
+                                                      const float *dZ, float *dQ, void *dK,
+                                                      void *dV, void *workspace,
+                                                      size_t workspace_bytes, void *stream);
+
+/*
  * Decode backward: the chain rule of the local decode (the FLARE decode
  * paragraph of the appendix; the pages name the decoder's contribution to the
  * gradients of the latent tensors but print no formula). For the gradient dY
@@ -288,8 +310,11 @@ FLARE_API flare_status_t flare_pp_bwd(const flare_dims_t *dims, const void *Qsee
  * this library, held by every GPU that loads the library until the process
  * exits. Problems whose flare_workspace_bytes(FLARE_OP_ENCODER_FWD, ...)
  * exceeds it are rejected with FLARE_ERR_WORKSPACE. The first call on a
- * device looks the array's device address up (cudaGetSymbolAddress), so make
- * that first call before any stream capture. Every call on a device shares
+ * device looks the array's device address up (cudaGetSymbolAddress) and keeps
+ * it for the life of the process, so make that first call before any stream
+ * capture, and do not go on calling this entry point after cudaDeviceReset or
+ * from another CUDA context of the same device (the module may then be loaded
+ * at another address than the one kept). Every call on a device shares
  * the array: calls that may overlap on the GPU (other streams, other host
  * threads) race and give wrong results; serialise them. Nothing is allocated
  * or freed; the ticket counters are cleared with cudaMemsetAsync each call.
@@ -298,6 +323,18 @@ FLARE_API flare_status_t flare_encoder_fwd_noalloc(const flare_dims_t *dims, con
                                                    const void *K, const void *V, const uint8_t *mask,
                                                    const int64_t *shard_offsets, int R, float *O_r,
                                                    float *L_r, float *Z, float *L, void *stream);
+
+/* Failure-path check of the bounded waits (no counterpart on the pages).
+ * Launches, on `stream`, one small kernel whose only work is a wait on an
+ * mbarrier that nothing arrives on; after limit_us microseconds (1..1000000)
+ * it gives the wait up exactly as the library's kernels do when an expected
+ * copy or MMA never completes: the CTA unwinds and FLARE_ERR_TIMEOUT is
+ * recorded in the device status word, to be read (and cleared) by
+ * flare_device_status. Nothing faults and the context stays usable, so a
+ * caller can test its handling of FLARE_ERR_TIMEOUT. Returns
+ * FLARE_ERR_INVALID_ARG for a limit out of range, FLARE_ERR_CUDA if the
+ * launch fails. */
+FLARE_API flare_status_t flare_check_bounded_wait(unsigned limit_us, void *stream);
 
 /* Synchronises `stream`, then reads and clears the device status word that
  * kernels set when they abandon a bounded wait: FLARE_OK, FLARE_ERR_TIMEOUT,

@@ -611,6 +611,19 @@ flare_status_t flare_encoder_bwd(const flare_dims_t *dims, const void *Q, const 
                            false, (cudaStream_t)stream);
 }
 
+flare_status_t flare_encoder_bwd_accumulate(const flare_dims_t *dims, const void *Q, const void *K,
+                                            const void *V, const uint8_t *mask,
+                                            const int64_t *shard_offsets, int R, const float *Z,
+                                            const float *L, const float *dZ, float *dQ, void *dK,
+                                            void *dV, void *workspace, size_t workspace_bytes,
+                                            void *stream) {
+    flare_status_t s = check_dims(dims);
+    if (s != FLARE_OK) return s;
+    if ((s = check_offsets(shard_offsets, R, dims->N)) != FLARE_OK) return s;
+    return encoder_bwd_run(dims, Q, K, V, mask, Z, L, dZ, dQ, dK, dV, workspace, workspace_bytes,
+                           true, (cudaStream_t)stream);
+}
+
 flare_status_t flare_decode_bwd(const flare_dims_t *dims, const void *Q, const float *Z,
                                 const void *K, const void *dY, float *dQ, float *dZ, void *dK,
                                 void *workspace, size_t workspace_bytes, void *stream) {
@@ -702,6 +715,16 @@ flare_status_t flare_pp_bwd(const flare_dims_t *dims, const void *Qseed, const v
             return s;
     }
     return FLARE_OK;
+}
+
+flare_status_t flare_check_bounded_wait(unsigned limit_us, void *stream) {
+    if (limit_us < 1 || limit_us > 1000000)
+        return fail(FLARE_ERR_INVALID_ARG, "limit_us=%u outside [1, 1000000]", limit_us);
+    DeviceInfo di;
+    flare_status_t s = device_info(di);
+    if (s != FLARE_OK) return s;
+    cudaError_t e = launch_bounded_wait_probe(1000ull * limit_us, di.status, (cudaStream_t)stream);
+    return e == cudaSuccess ? FLARE_OK : cuda_fail(e, "bounded-wait probe launch");
 }
 
 flare_status_t flare_device_status(void *stream) {

@@ -63,10 +63,15 @@ cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *
                                   size_t ws_bytes, int sms, unsigned *status, cudaStream_t st,
                                   bool accumulate = false);   // dQ, dK += this share
 
-// Decode backward on tensor cores: bf16 with D = 64 and M in {64, 128}.
+// One small kernel that waits on an mbarrier nothing arrives on and gives the
+// wait up after limit_ns (the library's bounded-wait path, with no other work).
+cudaError_t launch_bounded_wait_probe(unsigned long long limit_ns, unsigned *status,
+                                      cudaStream_t st);
+
 // y[i] = x[i] rounded to bf16 (nearest even), n elements.
 cudaError_t launch_f32_to_bf16(const float *x, void *y, int64_t n, cudaStream_t st);
 
+// Decode backward on tensor cores: bf16 with D = 64 and M in {64, 128}.
 bool tc_decode_bwd_supported(bool bf16, int M, int D);
 size_t tc_decode_bwd_workspace(const Problem &pr, int sms);
 cudaError_t launch_decode_bwd_tc(const Problem &pr, const void *Q, const float *Z, const void *K,

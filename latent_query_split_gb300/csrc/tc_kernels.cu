@@ -70,7 +70,33 @@ __global__ void f32_to_bf16_kernel(const float *__restrict__ x, __nv_bfloat16 *_
         y[i] = __float2bfloat16_rn(x[i]);
 }
 
+// A CTA whose only work is a bounded wait on an mbarrier that nothing ever
+// arrives on: the wait gives up after limit_ns exactly as the library's
+// kernels do (abort flag, timeout in the device status word) and the kernel
+// returns. No copy or MMA is in flight, so giving up leaves nothing behind.
+__global__ void bounded_wait_probe_kernel(unsigned long long limit_ns, unsigned *status) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    const uint32_t b = tc::smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        tc::mbar_init(b, 1);             // one arrival expected, none ever made
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    const tc::Waiter wt{&abort_flag, status};
+    if (threadIdx.x == 0) wt.wait_for(b, 0, limit_ns);
+    __syncthreads();
+}
+
 }  // namespace
+
+cudaError_t launch_bounded_wait_probe(unsigned long long limit_ns, unsigned *status,
+                                      cudaStream_t st) {
+    bounded_wait_probe_kernel<<<1, 32, 0, st>>>(limit_ns, status);
+    note_launch();
+    return cudaGetLastError();
+}
 
 cudaError_t launch_f32_to_bf16(const float *x, void *y, int64_t n, cudaStream_t st) {
     if (n == 0) return cudaSuccess;

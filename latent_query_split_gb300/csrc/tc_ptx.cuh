@@ -118,11 +118,18 @@ struct Waiter {
         }
     }
     __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity) const {
+        return wait_for(bar, parity, kWaitNs);
+    }
+    // The bounded loop with an explicit limit in nanoseconds: gives up once
+    // `limit_ns` have passed, marks the CTA aborted and records the timeout in
+    // the device status word.
+    __device__ __forceinline__ bool wait_for(uint32_t bar, uint32_t parity,
+                                             unsigned long long limit_ns) const {
         const uint64_t t0 = globaltimer();
         while (true) {
             if (mbar_try_wait(bar, parity)) return true;
             if (*abort) return false;
-            if (globaltimer() - t0 > kWaitNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 *abort = 1;
                 atomicExch(status, 1u);
                 return false;

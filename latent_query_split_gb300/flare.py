@@ -31,6 +31,7 @@ FLARE_MAX_SHARDS = 256
 EXPORTS = ("flare_workspace_bytes", "flare_encoder_fwd", "flare_lse_merge", "flare_decode_fwd",
            "flare_fwd", "flare_pp_fwd", "flare_encoder_bwd", "flare_decode_bwd",
            "flare_bwd", "flare_pp_bwd", "flare_encoder_fwd_noalloc",
+           "flare_encoder_bwd_accumulate", "flare_check_bounded_wait",
            "flare_device_status", "flare_last_error_string", "flare_version",
            "flare_launch_count")
 
@@ -75,10 +76,12 @@ def load_library(build_if_missing: bool = True):
     lib.flare_fwd.argtypes = [D, P, P, P, P, P, I, P, P, P, P, Z, P]
     lib.flare_pp_fwd.argtypes = [D, P, P, P, P, P, P, P, I, P, P, P, P, P, P, Z, P]
     lib.flare_encoder_bwd.argtypes = [D, P, P, P, P, P, I, P, P, P, P, P, P, P, Z, P]
+    lib.flare_encoder_bwd_accumulate.argtypes = [D, P, P, P, P, P, I, P, P, P, P, P, P, P, Z, P]
     lib.flare_decode_bwd.argtypes = [D, P, P, P, P, P, P, P, P, Z, P]
     lib.flare_bwd.argtypes = [D, P, P, P, P, P, I, P, P, P, P, P, P, P, Z, P]
     lib.flare_pp_bwd.argtypes = [D, P, P, P, P, P, P, P, I, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]
     lib.flare_encoder_fwd_noalloc.argtypes = [D, P, P, P, P, P, I, P, P, P, P, P]
+    lib.flare_check_bounded_wait.argtypes = [ctypes.c_uint, P]
     lib.flare_device_status.argtypes = [P]
     lib.flare_last_error_string.restype = ctypes.c_char_p
     lib.flare_version.restype = I
@@ -263,6 +266,26 @@ def flare_encoder_bwd(Q, K, V, mask, shard_offsets, Z, L, dZ, *, dQ=None, dK=Non
     return dQ, dK, dV
 
 
+def flare_encoder_bwd_accumulate(Q, K, V, mask, shard_offsets, Z, L, dZ, dQ, dK, *, dV=None,
+                                 workspace=None, scale=None, kernel="auto", stream=None):
+    """Encoder backward adding its shares to the given dQ (fp32) and dK (K's
+    dtype), which hold another consumer's shares; dV is written. Returns
+    (dQ, dK, dV)."""
+    lib = load_library()
+    dims = make_dims(Q, K, scale, kernel)
+    N = K.shape[1]
+    shard_offsets = [0, N] if shard_offsets is None else list(shard_offsets)
+    if dV is None:
+        dV = torch.empty_like(V)
+    ws, nbytes = _workspace(FLARE_OP_ENCODER_BWD, dims, shard_offsets, workspace, K.device)
+    arr, R = _offsets(shard_offsets)
+    _check(lib.flare_encoder_bwd_accumulate(ctypes.byref(dims), _ptr(Q), _ptr(K), _ptr(V),
+                                            _ptr(mask), arr, R, _ptr(Z), _ptr(L), _ptr(dZ),
+                                            _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), nbytes,
+                                            _stream(stream)))
+    return dQ, dK, dV
+
+
 def flare_decode_bwd(Q, Z, K, dY, *, dQ=None, dZ=None, dK=None, workspace=None, scale=None,
                      kernel="auto", stream=None):
     """Decode backward for the output gradient dY; returns (dQ [B,H,M,D] fp32,
@@ -355,6 +378,13 @@ def flare_encoder_fwd_noalloc(Q, K, V, mask=None, shard_offsets=None, *, O_r=Non
                                          arr, R, _ptr(O_r), _ptr(L_r), _ptr(Z), _ptr(L),
                                          _stream(stream)))
     return O_r, L_r, Z, L
+
+
+def flare_check_bounded_wait(limit_us: int, stream=None):
+    """Launch the bounded-wait check kernel (see include/flare.h): it gives
+    up a wait that never completes after limit_us and records
+    FLARE_ERR_TIMEOUT for flare_device_status."""
+    _check(load_library().flare_check_bounded_wait(int(limit_us), _stream(stream)))
 
 
 def flare_device_status(stream=None):

@@ -179,3 +179,22 @@ def test_flare_pp_bwd_checks_every_stage_before_launching(lib, dtype):
     assert call(dKt=None) == flare.FLARE_ERR_INVALID_ARG    # third stage
     assert call(Vt=None) == flare.FLARE_ERR_INVALID_ARG     # third stage's input
     assert lib.flare_launch_count() == before
+
+
+def test_bounded_wait_check_rejects_limits_out_of_range(lib):
+    for limit in (0, 1000001):
+        assert lib.flare_check_bounded_wait(limit, None) == flare.FLARE_ERR_INVALID_ARG
+        assert b"limit_us" in lib.flare_last_error_string()
+
+
+def test_accumulating_encoder_bwd_validates_before_launch(lib):
+    dims = _dims()
+    arr = (ctypes.c_int64 * 3)(0, 50, 100)
+    # NULL tensors are rejected before anything is launched
+    assert lib.flare_encoder_bwd_accumulate(ctypes.byref(dims), None, None, None, None, arr, 2,
+                                            None, None, None, None, None, None, None, 0,
+                                            None) == flare.FLARE_ERR_INVALID_ARG
+    bad = (ctypes.c_int64 * 3)(0, 50, 99)
+    assert lib.flare_encoder_bwd_accumulate(ctypes.byref(dims), None, None, None, None, bad, 2,
+                                            None, None, None, None, None, None, None, 0,
+                                            None) == flare.FLARE_ERR_INVALID_ARG
