@@ -14,16 +14,26 @@
 //   warp 1     TMEM allocator and MMA issuer (converged warp, elect.sync):
 //                S_g = K Q^T   (A = K tile, B = Q, both shared memory)
 //                Y_g = P_g Z   (A = P from tensor memory, B = Z shared memory)
-//   warps 2..  M <= 128: two groups of four warps take alternate tiles (one
+//   warps 2..9 M <= 128: two groups of four warps take alternate tiles (one
 //              token row per thread = TMEM lane): row max, exp2, P over S in
 //              tensor memory; where 3 M + 2 D columns fit, S rotates through
-//              three TMEM buffers so the MMA chain spans three tiles. M > 128: one group of eight warps, two per lane
-//              quadrant (latent halves); S single-buffered but free as soon
-//              as its scores are in registers, P and Y in columns of their own. The epilogue of a tile (Y / l rounded to bf16, staged
-//              in shared memory, one TMA store per warp of 32 token rows) runs
-//              in the group's next iteration, once that tile's scores have
-//              arrived, so the group never waits for its own P Z product.
-//   last warp  stager: converts each (b, h)'s Q and Z into swizzled operand
+//              three TMEM buffers so the MMA chain spans three tiles. The
+//              epilogue of a tile (Y / l rounded to bf16, staged in shared
+//              memory, one TMA store per warp of 32 token rows) runs in the
+//              group's next iteration, once that tile's scores have arrived,
+//              so the group never waits for its own P Z product.
+//              M > 128: two warps per lane quadrant (latent halves, the row
+//              maximum exchanged through shared memory); S is single-buffered
+//              but free once its scores are read, P (fp16) and Y have columns
+//              of their own, so S of tile j + 1 and P Z of tile j - 1 run on
+//              the tensor pipe while the softmax of tile j takes its
+//              exponentials.
+//   warp 10    stager (below).
+//   warps 11.. M > 128 only: warps 11..14 the epilogue, one warp per lane
+//              quadrant, so the softmax warps never wait for a Y store; warp
+//              15 issues the S MMAs (warp 1 then issues only P Z), so S of the
+//              next tile never waits behind this tile's P Z issue.
+//   stager     converts each (b, h)'s Q and Z into swizzled operand
 //              tiles, into one of two buffers while the other is in use, so a
 //              (b, h) change does not stall the tile stream.
 #pragma once
@@ -58,7 +68,15 @@ struct DecCfg {
     // owning M/2 latents of its token rows (a row maximum is exchanged)
     static constexpr int GW = NG == 2 ? 4 : 8;          // warps per group
     static constexpr int STAGER = 2 + 8;                // warp index of the stager
-    static constexpr int THREADS = 32 * (STAGER + 1);
+    // M > 128: four more warps (11..14, one per TMEM lane quadrant) take the
+    // epilogue, so the softmax warps never wait for a Y store
+    static constexpr int EPI0 = STAGER + 1;
+    static constexpr int NEPI = NG == 1 ? 4 : 0;
+    // M > 128: warp 15 issues the S MMAs, warp 1 only the P Z MMAs (an MMA
+    // issue blocks until the tensor pipe accepts it, so one warp issuing both
+    // held each tile's S back behind the previous tile's P Z)
+    static constexpr int SISS = NG == 1 ? EPI0 + NEPI : -1;
+    static constexpr int THREADS = 32 * (STAGER + 1 + NEPI + (NG == 1 ? 1 : 0));
     static constexpr uint32_t QZ_ATOM = M * 128;        // bytes of one M-row x 64-col atom
     // F16P: P and Z enter Y = P Z as fp16, and Z gets one more 16-column block
     // holding the constant c (the power of two Z was scaled by, see
@@ -77,7 +95,7 @@ struct DecCfg {
     static constexpr int NCH = M / 32;                  // P chunks of 32 latents
     // full[S], empty[S], qz_full[2], qz_free[2], s_full[2], p_chunk[2][8], o_done[2],
     // epi_done[2], s_free (M > 128: the single S buffer has been read)
-    static constexpr int NBAR = 2 * STAGES + 4 + 2 + 16 + 2 + 2 + 1 + 1;   // + the third s_full
+    static constexpr int NBAR = 2 * STAGES + 4 + 2 + 16 + 2 + 2 + 1 + 1 + 1;   // + the third s_full, drain
     static constexpr uint32_t STAGE_OFF = QZB * QZ_BYTES;
     // Y staging of each group for the TMA stores: 128 token rows, KA atoms
     static constexpr uint32_t OUT_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
@@ -312,6 +330,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     auto o_done = [&](int g) { return bar0 + 8u * (2 * STAGES + 22 + g); };
     auto epi_done = [&](int g) { return bar0 + 8u * (2 * STAGES + 24 + g); };
     const uint32_t s_free = bar0 + 8u * (2 * STAGES + 26);
+    const uint32_t drain_s = bar0 + 8u * (2 * STAGES + 28);   // M > 128: the S issuer's MMAs
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
 
@@ -333,13 +352,16 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             mbar_init(qz_free(q), 1);
         }
         for (int g = 0; g < 2; ++g) {
-            mbar_init(epi_done(g), C::GW);   // one arrival per softmax warp
+            // one arrival per warp that reads Y: the softmax warps (M <= 128),
+            // the four epilogue warps (M > 128)
+            mbar_init(epi_done(g), NG == 1 ? C::NEPI : C::GW);
             mbar_init(s_full(g), 1);
             for (int c = 0; c < 8; ++c) mbar_init(p_chunk(g, c), C::GW);   // one arrival per softmax warp
             mbar_init(o_done(g), 1);
         }
         mbar_init(s_full(2), 1);
         mbar_init(s_free, C::GW);            // M > 128: every softmax warp has read S
+        mbar_init(drain_s, 1);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -464,6 +486,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         // a new (b, h) also waits until every older tile's P Z is issued
         int64_t jS = 0, nP = 0;
         auto pump_s = [&]() -> bool {
+            if (NG == 1) return true;                // M > 128: the S issuer warp
             while (jS < ntiles && jS < nP + (C::RING ? 3 : 2) && (QZB == 2 || bhS - bh0 == uS || nP == jS))
                 if (!issue_s(jS++)) return false;
             return true;
@@ -512,121 +535,188 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             wwait(o_done(gl), (uint32_t)kl & 1);
         }
         __syncwarp();
-    } else if (NG == 1) {
-        // ---------------- softmax halves + epilogue (M > 128) ----------------
+    } else if (NG == 1 && warp < C::STAGER) {
+        // ---------------- softmax halves (M > 128) ----------------
         // Warps w and w + 4 share a TMEM lane quadrant (32 token rows); half h
-        // owns latents [M/2 h, M/2 (h + 1)). Both load their scores into
-        // registers (then s_free: S of the next tile may be computed) and
-        // exchange the row maximum; P of latent m goes to column P_COL + m / 2
-        // (fp16 pairs) once the previous tile's P Z is done; the previous
-        // tile's Y is stored after this tile's P is out.
+        // owns latents [M/2 h, M/2 (h + 1)). Per tile j: a first pass over
+        // the half's scores (32 columns at a time) gives its row maximum,
+        // which the halves exchange; a second pass turns the scores into the
+        // fp16 exponents t = s log2(e) S - m, packed in pairs; then S is
+        // free (s_free: S of tile j + 1 may be computed) and the exponentials
+        // are taken in registers while the tensor pipe still runs P Z of tile
+        // j - 1. Once that product is done P's columns are free and P of tile
+        // j is stored (which starts its P Z). Two passes over tensor memory
+        // keep a thread's registers at one chunk of scores plus the packed
+        // exponents; the epilogue warps take Y.
         constexpr int HM = M / 2;                     // latents of a half
+        constexpr int NC = HM / 32;                   // 32-column chunks of a half
         const int half = (warp - 2) >> 2;
         const int quad = warp & 3;
         const int rig = quad * 32 + lane;             // token row within the tile
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const uint64_t c2 = f2pack(a.sl2, a.sl2);
         float *xmax = reinterpret_cast<float *>(smem + C::XMAX_OFF);   // [2 parity][2 half][128 rows]
-        uint8_t *slab = smem + C::OUT_OFF + quad * 32 * 128;         // the quadrant's 32 Y rows
-        const bool storer = half == 0 && lane == 0;
         const int pair_bar = 1 + quad;                // named barrier of the quadrant's two warps
+        const uint32_t s_tmem = tmem + HM * half + lane_off;
+        const uint32_t p_tmem = tmem + C::P_COL + (HM / 2) * half + lane_off;
         auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
             return __all_sync(0xffffffffu, wt.wait(bar, par));
         };
-        bool have_prev = false;
-        int prev_b = 0, prev_h = 0, prev_n0 = 0;
-        int64_t prev_k = 0;
-        uint32_t stores = 0;
-        // Y / l of the previous tile: half h converts columns [32 h, 32 h + 32)
-        // of each row (D = 64), half 0's lane 0 stores the quadrant's 32 rows
-        auto epilogue = [&]() -> bool {
-            if (!wwait(o_done(0), (uint32_t)prev_k & 1)) return false;
-            tc_fence_after();
-            const uint32_t y_tmem = tmem + C::Y_COL + lane_off;
-            uint32_t r[32];
-            tmem_ld32(y_tmem + 32 * half, r);
-            const uint32_t lw = tmem_ld1(y_tmem + D);              // c * l from the row-sum block
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(epi_done(0));               // Y may take the next tile's P Z
-            if (stores > 0 && storer) bulk_wait_group_read0();     // the slab's last store has read it
-            named_bar_sync(pair_bar, 64);
-            const float inv = 1.f / __uint_as_float(lw);
-            uint8_t *row = slab + lane * 128;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int chunk = 4 * half + q;
-                const uint32_t *v = r + 8 * q;
-                *reinterpret_cast<uint4 *>(row + ((chunk ^ (lane & 7)) << 4)) = make_uint4(
-                    pack_bf16(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
-                    pack_bf16(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
-                    pack_bf16(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
-                    pack_bf16(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
-            }
-            fence_proxy_async_smem();
-            named_bar_sync(pair_bar, 64);
-            const int n0 = prev_n0 + quad * 32;
-            if (storer && n0 < a.N) {
-                // token rows past N are clipped by the tensor map
-                tma_store_4d(&tmY, smem_u32(slab), 0, prev_h, n0, prev_b);
-                bulk_commit_group();
-            }
-            ++stores;
-            return true;
-        };
-        int64_t kt = k0;
-        int ch = (int)(bh0 / a.B), cb = (int)(bh0 - (int64_t)ch * a.B);   // tile j's head and batch
-        bool ok = true;
-        for (int64_t j = 0; j < ntiles && ok; ++j) {
-            const uint32_t s_tmem = tmem + HM * half + lane_off;
-            const uint32_t p_tmem = tmem + C::P_COL + (HM / 2) * half + lane_off;
+        for (int64_t j = 0; j < ntiles; ++j) {
             if (!wwait(s_full(0), (uint32_t)j & 1)) break;
             tc_fence_after();
-            uint32_t r[HM / 32][32];
+            // pass 1: the half's row maximum
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < HM / 32; ++c) tmem_ld32(s_tmem + c * 32, r[c]);
-            tmem_wait_ld();
-            // the scores are in registers: S of the next tile may be computed
+            for (int c = 0; c < NC; c += 2) {
+                uint32_t r[2][32];
+                tmem_ld32(s_tmem + c * 32, r[0]);
+                tmem_ld32(s_tmem + c * 32 + 32, r[1]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int b = 0; b < 2; ++b)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        mx[(2 * b) & 3] = max3(mx[(2 * b) & 3], __uint_as_float(r[b][4 * i]), __uint_as_float(r[b][4 * i + 1]));
+                        mx[(2 * b + 1) & 3] = max3(mx[(2 * b + 1) & 3], __uint_as_float(r[b][4 * i + 2]), __uint_as_float(r[b][4 * i + 3]));
+                    }
+            }
+            float *xm = xmax + (j & 1) * 256;
+            xm[half * 128 + rig] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            named_bar_sync(pair_bar, 64);                 // both halves' maxima are published
+            const float m = fmaxf(xm[rig], xm[128 + rig]) * a.sl2;
+            const uint64_t nm2 = f2pack(-m, -m);
+            // pass 2: the exponents in fp16 pairs
+            uint32_t pw[NC][16];
+#pragma unroll
+            for (int c = 0; c < NC; c += 2) {
+                uint32_t r[2][32];
+                tmem_ld32(s_tmem + c * 32, r[0]);
+                tmem_ld32(s_tmem + c * 32 + 32, r[1]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int b = 0; b < 2; ++b)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float t0, t1;
+                        f2unpack(fma2(f2pack(__uint_as_float(r[b][2 * i]), __uint_as_float(r[b][2 * i + 1])), c2, nm2), t0, t1);
+                        pw[c + b][i] = pack_f16(t0, t1);
+                    }
+            }
+            // the scores are read: S of the next tile may be computed
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free);
-            float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < HM / 32; ++c)
+            for (int c = 0; c < NC; ++c)
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    mx[i & 1] = max3(mx[i & 1], __uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1]));
-            float *xm = xmax + (j & 1) * 256;
-            xm[half * 128 + rig] = fmaxf(mx[0], mx[1]);
-            named_bar_sync(pair_bar, 64);                 // both halves' scores are in registers
-            const float m = fmaxf(xm[rig], xm[128 + rig]) * a.sl2;
-            const uint64_t nm2 = f2pack(-m, -m);
-            // P's columns are free once the previous tile's P Z is done
-            if (have_prev && !(ok = wwait(o_done(0), (uint32_t)prev_k & 1))) break;
+                for (int i = 0; i < 16; ++i) pw[c][i] = ex2_f16x2(pw[c][i]);
+            // P's columns are free once the previous tile's P Z is done (an
+            // inline wait: P is live in registers, and registers live across
+            // the out-of-line wait's call would be saved to memory)
+            if (j > 0 && !__all_sync(0xffffffffu, wt.wait_inline(o_done(0), (uint32_t)(j - 1) & 1))) break;
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < HM / 32; ++c) {
-                uint32_t pw[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float t0, t1;
-                    f2unpack(fma2(f2pack(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1])), c2, nm2), t0, t1);
-                    pw[i] = ex2_f16x2(pack_f16(t0, t1));
-                }
-                tmem_st16(p_tmem + c * 16, pw);
-            }
+            for (int c = 0; c < NC; ++c) tmem_st16(p_tmem + c * 16, pw[c]);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_chunk(0, 0));
-            // the previous tile's Y (its P Z ran during this softmax)
-            if (have_prev && !(ok = epilogue())) break;
-            have_prev = true;
-            prev_h = ch;
-            prev_b = cb;
-            prev_n0 = (int)(kt * 128);
-            prev_k = j;
+        }
+    } else if (NG == 1 && warp == C::SISS) {
+        // ---------------- S issuer (M > 128; whole warp, elect.sync issues) ----------------
+        // S of tile j once its K tile has landed, the single S buffer has been
+        // read by the softmax (s_free of tile j - 1) and, at the first tile of
+        // a (b, h), the stager has put that (b, h)'s Q in place.
+        auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
+            return __all_sync(0xffffffffu, wt.wait(bar, par));
+        };
+        constexpr uint32_t idS = idesc_bf16_m128(M, 0);
+        const uint64_t dK0 = desc_sw128(sStage, 16, 1024);
+        constexpr uint64_t kStageDesc = C::STAGE_BYTES >> 4;
+        int64_t ktS = k0, u = 0;
+        bool issued = false;
+        for (int64_t jj = 0; jj < ntiles; ++jj) {
+            const int s = (int)(jj % STAGES);
+            if (jj == 0 || ktS == 0) {
+                if (jj > 0) ++u;
+                if (!wwait(qz_full((int)(u % QZB)), (uint32_t)(u / QZB) & 1)) break;
+            }
+            if (!wwait(full(s), (uint32_t)(jj / STAGES) & 1)) break;
+            if (jj >= 1 && !wwait(s_free, (uint32_t)(jj - 1) & 1)) break;
+            tc_fence_after();
+            const uint64_t dK = dK0 + kStageDesc * s;
+            const uint64_t dQ0 = desc_sw128(sbase + (uint32_t)(u % QZB) * C::QZ_BYTES, 16, 1024);
+#pragma unroll
+            for (int kb = 0; kb < D / 16; ++kb) {
+                const uint64_t offK = (uint64_t)((kb >> 2) * (128 * 128) + (kb & 3) * 32) >> 4;
+                const uint64_t offQ = (uint64_t)((kb >> 2) * C::QZ_ATOM + (kb & 3) * 32) >> 4;
+                umma_ss_elect(tmem + C::s_col(0), dK + offK, dQ0 + offQ, idS, kb > 0 ? 1u : 0u);
+            }
+            umma_commit_elect(s_full(0));
+            umma_commit_elect(empty(s));            // the K tile is only read by S
+            issued = true;
+            if (++ktS == a.T_bh) ktS = 0;
+        }
+        // every S this warp issued completes before TMEM is released
+        if (issued) {
+            umma_commit_elect(drain_s);
+            wwait(drain_s, 0);
+        }
+        __syncwarp();
+    } else if (NG == 1) {
+        // ---------------- epilogue (M > 128) ----------------
+        // One warp per TMEM lane quadrant: once P Z of tile j is done it reads
+        // the quadrant's 32 rows of Y and c * l (then Y is free for the next
+        // tile's P Z), divides, rounds to bf16 into its shared-memory slab and
+        // stores the 32 token rows with one TMA store.
+        const int quad = warp & 3;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const uint32_t y_tmem = tmem + C::Y_COL + lane_off;
+        uint8_t *slab = smem + C::OUT_OFF + quad * 32 * 128;         // the quadrant's 32 Y rows
+        auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
+            return __all_sync(0xffffffffu, wt.wait(bar, par));
+        };
+        int64_t kt = k0;
+        int ch = (int)(bh0 / a.B), cb = (int)(bh0 - (int64_t)ch * a.B);   // tile j's head and batch
+        for (int64_t j = 0; j < ntiles; ++j) {
+            if (!wwait(o_done(0), (uint32_t)j & 1)) break;
+            tc_fence_after();
+            uint32_t yr[2][32];
+            tmem_ld32(y_tmem, yr[0]);
+            tmem_ld32(y_tmem + 32, yr[1]);
+            const uint32_t lw = tmem_ld1(y_tmem + D);             // c * l from the row-sum block
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(epi_done(0));               // Y may take the next tile's P Z
+            // the slab is free once the warp's previous store has read it
+            if (j > 0) {
+                if (lane == 0) bulk_wait_group_read0();
+                __syncwarp();
+            }
+            const float inv = 1.f / __uint_as_float(lw);
+            uint8_t *row = slab + lane * 128;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int chunk = 4 * h + q;
+                    const uint32_t *v = yr[h] + 8 * q;
+                    *reinterpret_cast<uint4 *>(row + ((chunk ^ (lane & 7)) << 4)) = make_uint4(
+                        pack_bf16(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                        pack_bf16(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                        pack_bf16(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                        pack_bf16(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
+                }
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int n0 = (int)(kt * 128) + quad * 32;
+            if (lane == 0 && n0 < a.N) {
+                // token rows past N are clipped by the tensor map
+                tma_store_4d(&tmY, smem_u32(slab), 0, ch, n0, cb);
+                bulk_commit_group();
+            }
             if (++kt == a.T_bh) {
                 kt = 0;
                 if (++cb == a.B) {
@@ -635,8 +725,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 }
             }
         }
-        if (ok && have_prev && !wt.aborted()) epilogue();
-        if (storer) bulk_wait_group0();
+        if (lane == 0) bulk_wait_group0();
     } else {
         // ---------------- softmax + epilogue warps ----------------
         const int g = (warp - 2) >> 2;
