@@ -675,8 +675,9 @@ struct RingCfg {
     static constexpr uint32_t ONES_OFF = BIAS_OFF + STAGES * BIAS_BYTES;
     static constexpr uint32_t PADF_OFF = ONES_OFF + kOnesBytes;   // per stage: tile has padding
     static constexpr uint32_t BAR_OFF = PADF_OFF + 16 * ((STAGES * 4 + 15) / 16);
-    // full[S], empty[S], q_full[2], s_full[3], p_full[3], o_done[2], drain[2], buf_free[3]
-    static constexpr int NBAR = 2 * STAGES + 15;
+    // full[S], empty[S], q_full[2], s_full[3], p_full[3], o_done[2], drain[2], buf_free[3],
+    // p_half[3]
+    static constexpr int NBAR = 2 * STAGES + 18;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t BYTES = MISC_OFF + 64;
     static constexpr uint32_t ALLOC = BYTES + 1024;
@@ -704,6 +705,8 @@ enc_ring_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
     auto o_done = [&](int g) { return bar0 + 8u * (2 * STAGES + 8 + g); };
     auto drain = [&](int w) { return bar0 + 8u * (2 * STAGES + 10 + w); };
     auto buf_free = [&](int u) { return bar0 + 8u * (2 * STAGES + 12 + u); };
+    // the first half of P (tokens 0..63 of the tile) is in place
+    auto p_half = [&](int u) { return bar0 + 8u * (2 * STAGES + 15 + u); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
 
@@ -727,6 +730,7 @@ enc_ring_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
         for (int u = 0; u < 3; ++u) {
             mbar_init(s_full(u), 1);
             mbar_init(p_full(u), 4);              // the owning group's four warps
+            mbar_init(p_half(u), 4);
             mbar_init(buf_free(u), 1);            // PV of the buffer's P has completed
         }
         mbar_init(drain(0), 1);
@@ -827,7 +831,9 @@ enc_ring_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
                 const int64_t j = q >> 1;
                 const int g = (int)(q & 1);
                 const int buf = (int)(q % 3);
-                if (!(ok = wwait(p_full(buf), (uint32_t)(q / 3) & 1))) break;
+                // the first half of P: its PV MMAs overlap the second half's
+                // exponentials
+                if (!(ok = wwait(p_half(buf), (uint32_t)(q / 3) & 1))) break;
                 tc_fence_after();
                 // O_g += P V; a piece's first tile starts the accumulator afresh
                 const bool first = (j == 0) || cp.k == 0;
@@ -835,9 +841,15 @@ enc_ring_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
                 const uint64_t dV = desc_sw128(sStage + s * C::STAGE_BYTES + C::KV_ATOM, C::KV_ATOM, 1024);
                 const uint32_t tP = tmem + (uint32_t)buf * TILE;
 #pragma unroll
-                for (int kb = 0; kb < TILE / 16; ++kb)
+                for (int kb = 0; kb < TILE / 16; ++kb) {
+                    if (kb == TILE / 32) {
+                        if (!(ok = wwait(p_full(buf), (uint32_t)(q / 3) & 1))) break;
+                        tc_fence_after();
+                    }
                     umma_ts_elect(tmem + C::O_COL + g * D, tP + kb * 8, dV + (uint64_t)(kb * (2048 >> 4)), idPV,
                                   (kb > 0 || !first) ? 1u : 0u);
+                }
+                if (!ok) break;
                 umma_commit_elect(o_done(g));
                 umma_commit_elect(buf_free(buf));
                 if (g == 1) {
@@ -985,6 +997,13 @@ enc_ring_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
                         for (int i = 0; i < 16; ++i) pw[i] = 0u;
                     }
                     tmem_st16(s_tmem + (c0 + b) * 16, pw);
+                }
+                if (c0 + 2 == NCH / 2) {
+                    // the first half of P is in place: PV may start on it
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(p_half(buf));
                 }
             }
             tmem_wait_st();
