@@ -61,7 +61,10 @@ typedef enum {
     FLARE_ERR_UNSUPPORTED = 2,  /* valid, but no kernel for this shape or dtype  */
     FLARE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required    */
     FLARE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed          */
-    FLARE_ERR_TIMEOUT = 5       /* a kernel gave up a bounded wait (device flag) */
+    FLARE_ERR_TIMEOUT = 5,      /* a kernel gave up a bounded wait (device flag) */
+    FLARE_ERR_DEVICE_CHECK = 6  /* a device-side check of a FLARE_DEBUG build of
+                                   the library failed (device flag); the access
+                                   it guarded was skipped                        */
 } flare_status_t;
 
 typedef enum { FLARE_F32 = 0, FLARE_BF16 = 1 } flare_dtype_t;
@@ -337,8 +340,11 @@ FLARE_API flare_status_t flare_encoder_fwd_noalloc(const flare_dims_t *dims, con
 FLARE_API flare_status_t flare_check_bounded_wait(unsigned limit_us, void *stream);
 
 /* Synchronises `stream`, then reads and clears the device status word that
- * kernels set when they abandon a bounded wait: FLARE_OK, FLARE_ERR_TIMEOUT,
- * or FLARE_ERR_CUDA if the synchronisation itself failed. */
+ * kernels set when they abandon a bounded wait (or, in a FLARE_DEBUG build,
+ * when a device-side check of a tile's place or a workspace index fails; the
+ * first error recorded wins): FLARE_OK, FLARE_ERR_TIMEOUT,
+ * FLARE_ERR_DEVICE_CHECK, or FLARE_ERR_CUDA if the synchronisation itself
+ * failed. */
 FLARE_API flare_status_t flare_device_status(void *stream);
 
 /* Text of the calling thread's most recent error (empty if none). */

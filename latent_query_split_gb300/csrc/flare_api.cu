@@ -736,6 +736,9 @@ flare_status_t flare_device_status(void *stream) {
     if (v != kDevOk) {
         const unsigned zero = 0;
         cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero);
+        if (v & 0x100u)
+            return fail(FLARE_ERR_DEVICE_CHECK, "a device-side check failed (check %u); the access was skipped",
+                        v & 0xffu);
         return fail(FLARE_ERR_TIMEOUT, "a kernel abandoned a bounded wait (code %u)", v);
     }
     return FLARE_OK;

@@ -258,8 +258,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 if (lane == 0) {
                     mbar_arrive(lc_full(u & 1));
                     mbar_arrive_expect_tx(qd_full, 2 * C::QZ_BYTES);
-                    tma_load_4d(sQ, &tmQ, 0, 0, h, a.q_per_batch ? b : 0, qd_full);
-                    tma_load_4d(sdZ, &tmdZ, 0, 0, h, b, qd_full);
+                    if (dcheck(h >= 0 && h < a.H && b >= 0 && b < a.B, kChkBwdQ, a.status)) {
+                        tma_load_4d(sQ, &tmQ, 0, 0, h, a.q_per_batch ? b : 0, qd_full);
+                        tma_load_4d(sdZ, &tmdZ, 0, 0, h, b, qd_full);
+                    }
                 }
                 __syncwarp();
             }
@@ -268,8 +270,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             if (lane == 0) {
                 mbar_arrive_expect_tx(full(s), C::STAGE_BYTES);
                 const uint32_t dst = sStage + s * C::STAGE_BYTES;
-                tma_load_4d_hint(dst, &tmK, 0, h, (int)(kt * 128), b, full(s), pol);
-                tma_load_4d_hint(dst + TB, &tmV, 0, h, (int)(kt * 128), b, full(s), pol);
+                if (dcheck(tile_in_tensor(0, h, kt * 128, b, a.H, a.N, a.B) && kt < a.T_bh, kChkBwdKV, a.status)) {
+                    tma_load_4d_hint(dst, &tmK, 0, h, (int)(kt * 128), b, full(s), pol);
+                    tma_load_4d_hint(dst + TB, &tmV, 0, h, (int)(kt * 128), b, full(s), pol);
+                }
             }
             __syncwarp();
             if (++kt == a.T_bh) {
@@ -520,7 +524,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             fence_proxy_async_smem();
             __syncwarp();
             const int n0 = (int)(t.kt * 128) + quad * 32;
-            if (lane == 0 && n0 < a.N) {
+            if (lane == 0 && n0 < a.N &&
+                dcheck(tile_in_tensor(0, t.h, n0, t.b, a.H, a.N, a.B), kChkBwdOut, a.status)) {
                 // rows past N are clipped by the tensor map
                 tma_store_4d(tmOut, smem_u32(slab), 0, t.h, n0, t.b);
                 bulk_commit_group();

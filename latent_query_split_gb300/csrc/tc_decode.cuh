@@ -407,7 +407,9 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             if (lane == 0) {
                 mbar_arrive_expect_tx(full(s), C::STAGE_BYTES);
                 const uint32_t dst = sStage + s * C::STAGE_BYTES;
-                for (int ka = 0; ka < KA; ++ka)
+                const bool ok_k = dcheck(tile_in_tensor(64 * (KA - 1), h, kt * 128, b, a.H, a.N, a.B) && kt < a.T_bh,
+                                         kChkDecK, a.status);
+                for (int ka = 0; ka < KA && ok_k; ++ka)
                     tma_load_4d_hint(dst + ka * (128 * 128), &tmK, 64 * ka, h, (int)(kt * 128), b, full(s), pol);
             }
             __syncwarp();
@@ -712,7 +714,8 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             fence_proxy_async_smem();
             __syncwarp();
             const int n0 = (int)(kt * 128) + quad * 32;
-            if (lane == 0 && n0 < a.N) {
+            if (lane == 0 && n0 < a.N &&
+                dcheck(tile_in_tensor(0, ch, n0, cb, a.H, a.N, a.B), kChkDecY, a.status)) {
                 // token rows past N are clipped by the tensor map
                 tma_store_4d(&tmY, smem_u32(slab), 0, ch, n0, cb);
                 bulk_commit_group();
@@ -778,7 +781,8 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             fence_proxy_async_smem();
             __syncwarp();
             const int n0 = prev_n0 + quad * 32;
-            if (lane == 0 && n0 < a.N) {
+            if (lane == 0 && n0 < a.N &&
+                dcheck(tile_in_tensor(64 * (KA - 1), prev_h, n0, prev_b, a.H, a.N, a.B), kChkDecY, a.status)) {
                 // token rows past N are clipped by the tensor map
 #pragma unroll
                 for (int ka = 0; ka < KA; ++ka)

@@ -207,8 +207,10 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 if (u > 0 && !__all_sync(0xffffffffu, wt.wait_inline(qz_free, (uint32_t)(u - 1) & 1))) break;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(qz_full, 2 * C::QZ_BYTES);
-                    tma_load_4d(sQ, &tmQ, 0, 0, h, a.q_per_batch ? b : 0, qz_full);
-                    tma_load_4d(sZ, &tmZ, 0, 0, h, b, qz_full);
+                    if (dcheck(h >= 0 && h < a.H && b >= 0 && b < a.B, kChkDbwQ, a.status)) {
+                        tma_load_4d(sQ, &tmQ, 0, 0, h, a.q_per_batch ? b : 0, qz_full);
+                        tma_load_4d(sZ, &tmZ, 0, 0, h, b, qz_full);
+                    }
                 }
                 __syncwarp();
             }
@@ -217,8 +219,10 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             if (lane == 0) {
                 mbar_arrive_expect_tx(full(s), C::STAGE_BYTES);
                 const uint32_t dst = sStage + s * C::STAGE_BYTES;
-                tma_load_4d_hint(dst, &tmK, 0, h, (int)(kt * 128), b, full(s), pol);
-                tma_load_4d_hint(dst + TB, &tmdY, 0, h, (int)(kt * 128), b, full(s), pol);
+                if (dcheck(tile_in_tensor(0, h, kt * 128, b, a.H, a.N, a.B) && kt < a.T_bh, kChkDbwKV, a.status)) {
+                    tma_load_4d_hint(dst, &tmK, 0, h, (int)(kt * 128), b, full(s), pol);
+                    tma_load_4d_hint(dst + TB, &tmdY, 0, h, (int)(kt * 128), b, full(s), pol);
+                }
             }
             __syncwarp();
             if (++kt == a.T_bh) {
@@ -392,7 +396,7 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             fence_proxy_async_smem();
             named_bar_sync(pair_bar, 64);
             const int n0 = (int)(ktp * 128) + quad * 32;
-            if (storer && n0 < a.N) {
+            if (storer && n0 < a.N && dcheck(tile_in_tensor(0, hp, n0, bp, a.H, a.N, a.B), kChkDbwOut, a.status)) {
                 // rows past N are clipped by the tensor map
                 tma_store_4d(&tmdK, smem_u32(slab), 0, hp, n0, bp);
                 bulk_commit_group();

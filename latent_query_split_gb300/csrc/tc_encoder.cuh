@@ -215,10 +215,15 @@ __device__ __forceinline__ void produce_kv(const CUtensorMap *tmK, const CUtenso
         if (lane == 0) reinterpret_cast<volatile uint32_t *>(smem + C::PADF_OFF)[s] = pad ? 1u : 0u;
         fence_proxy_async_smem();
         __syncwarp();
+        const bool place_ok =
+            dcheck(tile_in_tensor(64 * (KA - 1), h, ti.n0, b, a.H, a.N, a.B) && ti.n0 < ti.n1 && ti.n1 <= a.N,
+                   kChkEncKV, a.status) &&
+            dcheck(ti.r >= 0 && ti.r < pl.R && ti.n0 >= pl.off[ti.r] && ti.n1 <= pl.off[ti.r + 1],
+                   kChkEncCursor, a.status);
         if (lane == 0) {
             mbar_arrive_expect_tx(full(s), C::STAGE_BYTES);
             const uint32_t dst = sStage + s * C::STAGE_BYTES;
-            for (int ka = 0; ka < KA; ++ka) {
+            for (int ka = 0; ka < KA && place_ok; ++ka) {
                 tma_load_4d_hint(dst + ka * C::KV_ATOM, tmK, 64 * ka, h, (int)ti.n0, b, full(s), pol);
                 tma_load_4d_hint(dst + (KA + ka) * C::KV_ATOM, tmV, 64 * ka, h, (int)ti.n0, b, full(s), pol);
             }
@@ -394,8 +399,9 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                     const int bh = bh0 + u, b = bh / a.H, h = bh - b * a.H;
                     const int rows = a.M < 128 ? a.M : 128;
                     mbar_arrive_expect_tx(q_full(u & 1), KA * rows * 128);
+                    const bool q_ok = dcheck(bh < a.B * a.H && h >= 0 && b >= 0, kChkEncQ, a.status);
 #pragma unroll
-                    for (int ka = 0; ka < KA; ++ka)
+                    for (int ka = 0; ka < KA && q_ok; ++ka)
                         tma_load_4d(sQ + (u & 1) * C::Q_BYTES + ka * C::Q_ATOM, &tmQ, 64 * ka, 0, h,
                                     a.q_per_batch ? b : 0, q_full(u & 1));
                 }
@@ -502,6 +508,8 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             if (!wwait(o_done((int)(j & 1)), (uint32_t)(j >> 1) & 1)) return false;
             tc_fence_after();
             const int64_t slot = piece_slot_of(pl, ti, cta);
+            const int64_t piece = slot - ((int64_t)ti.bh * pl.R + ti.r) * pl.P_max;
+            const bool slot_ok = dcheck(ti.bh < a.B * a.H && piece >= 0 && piece < pl.P_max, kChkEncPiece, a.status);
             float *part_row = a.part_O + (slot * a.M + rig) * D;
             float2 *st = stat + (pieces++ & 1) * 256;
             st[g * 128 + rig] = make_float2(has ? m_ref : -INFINITY, has ? l : 0.f);
@@ -521,7 +529,7 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 tmem_ld32(tmem + C::O_COL + lane_off + col, r0);
                 tmem_ld32(tmem + C::O_COL + D + lane_off + col, r1);
                 tmem_wait_ld();
-                if (rig < a.M) {
+                if (rig < a.M && slot_ok) {
                     float4 *dst = reinterpret_cast<float4 *>(part_row + col);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
@@ -536,7 +544,7 @@ enc_cs_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                     }
                 }
             }
-            if (g == 0 && rig < a.M)
+            if (g == 0 && rig < a.M && slot_ok)
                 a.part_L[slot * a.M + rig] = lt > 0.f ? (m + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
             return true;
         };
@@ -781,7 +789,8 @@ enc_ring_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
                 if (lane == 0) {
                     const int bh = bh0 + u, b = bh / a.H, h = bh - b * a.H;
                     mbar_arrive_expect_tx(q_full(u & 1), 256 * 128);
-                    for (int g = 0; g < 2; ++g)
+                    const bool q_ok = dcheck(bh < a.B * a.H && h >= 0 && b >= 0, kChkEncQ, a.status);
+                    for (int g = 0; g < 2 && q_ok; ++g)
                         tma_load_4d(sQ + (u & 1) * C::Q_BYTES + g * kAtom, &tmQ, 0, 128 * g, h,
                                     a.q_per_batch ? b : 0, q_full(u & 1));
                 }
@@ -890,6 +899,9 @@ enc_ring_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
             if (!wwait(o_done(g), (uint32_t)j & 1)) return false;
             tc_fence_after();
             const int64_t slot = piece_slot_of(pl, ti, cta);
+            const int64_t piece = slot - ((int64_t)ti.bh * pl.R + ti.r) * pl.P_max;
+            if (!dcheck(ti.bh < a.B * a.H && piece >= 0 && piece < pl.P_max, kChkEncPiece, a.status))
+                return true;                     // FLARE_DEBUG: the write is skipped
             float *part_row = a.part_O + (slot * a.M + row) * D;
             const bool live = l > 0.f;
             const float inv = live ? 1.f / l : 0.f;

@@ -21,6 +21,52 @@ namespace tc {
 
 constexpr unsigned long long kWaitNs = 4000000000ull;   // 4 s per wait at most
 
+// ---- FLARE_DEBUG device checks -----------------------------------------------
+// A build with -DFLARE_DEBUG=1 checks the place of every TMA tile (its token
+// row, head and batch coordinates inside the tensor, the innermost coordinate
+// on a 16-byte boundary), the cursors that walk the tiles and every index
+// into the workspace before the access. A failed check records 0x100 | code
+// in the device status word (the first error recorded wins), and the caller
+// skips the access; the kernel then unwinds through its bounded waits and
+// flare_device_status reports FLARE_ERR_DEVICE_CHECK. Without FLARE_DEBUG a
+// check is the constant true and compiles away.
+#ifndef FLARE_DEBUG
+#define FLARE_DEBUG 0
+#endif
+enum : unsigned {
+    kChkEncKV = 1,       // encoder K/V tile
+    kChkEncQ = 2,        // encoder query tile
+    kChkEncPiece = 3,    // encoder partial slot in the workspace
+    kChkEncCursor = 4,   // encoder tile cursor inside its shard
+    kChkDecK = 5,        // decode K tile
+    kChkDecY = 6,        // decode Y store
+    kChkBwdQ = 7,        // encoder backward Q / dZ tiles
+    kChkBwdKV = 8,       // encoder backward K / V tiles
+    kChkBwdOut = 9,      // encoder backward dK / dV store
+    kChkDbwQ = 10,       // decode backward Q / Z tiles
+    kChkDbwKV = 11,      // decode backward K / dY tiles
+    kChkDbwOut = 12,     // decode backward dK store
+    kChkTmem = 13,       // tensor-memory column
+};
+__device__ __forceinline__ bool dcheck(bool ok, unsigned code, unsigned *status) {
+#if FLARE_DEBUG
+    if (!ok) {
+        atomicCAS(status, 0u, 0x100u | code);
+        return false;
+    }
+#else
+    (void)ok;
+    (void)code;
+    (void)status;
+#endif
+    return true;
+}
+// A TMA tile of `rows` token rows starting at token n0 of a [B, N, H, D]
+// tensor, at head h and batch b, innermost coordinate x (bf16 elements).
+__device__ __forceinline__ bool tile_in_tensor(int x, int h, int64_t n0, int b, int H, int64_t N, int B) {
+    return x >= 0 && (x & 7) == 0 && h >= 0 && h < H && n0 >= 0 && n0 < N && b >= 0 && b < B;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -93,7 +139,7 @@ struct Waiter {
             if (*abort) return false;
             if (globaltimer() - t0 > kWaitNs) {
                 *abort = 1;
-                atomicExch(status, 1u);
+                atomicCAS(status, 0u, 1u);
                 return false;
             }
         }
@@ -112,7 +158,7 @@ struct Waiter {
             if (*abort) return false;
             if (globaltimer() - t0 > kWaitNs) {
                 *abort = 1;
-                atomicExch(status, 1u);
+                atomicCAS(status, 0u, 1u);
                 return false;
             }
         }
@@ -131,7 +177,7 @@ struct Waiter {
             if (*abort) return false;
             if (globaltimer() - t0 > limit_ns) {
                 *abort = 1;
-                atomicExch(status, 1u);
+                atomicCAS(status, 0u, 1u);
                 return false;
             }
         }

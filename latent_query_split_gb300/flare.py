@@ -20,6 +20,7 @@ from . import build as _build
 
 FLARE_OK, FLARE_ERR_INVALID_ARG, FLARE_ERR_UNSUPPORTED = 0, 1, 2
 FLARE_ERR_WORKSPACE, FLARE_ERR_CUDA, FLARE_ERR_TIMEOUT = 3, 4, 5
+FLARE_ERR_DEVICE_CHECK = 6
 FLARE_F32, FLARE_BF16 = 0, 1
 KERNELS = {"auto": 0, "simt": 1, "tensor": 2}
 (FLARE_OP_ENCODER_FWD, FLARE_OP_LSE_MERGE, FLARE_OP_DECODE_FWD, FLARE_OP_FWD,
@@ -52,8 +53,13 @@ class FlareDims(ctypes.Structure):
 _lib = None
 
 
+def _debug_variant() -> bool:
+    """FLARE_LIBRARY_VARIANT=debug selects the checking build (FLARE_DEBUG)."""
+    return os.environ.get("FLARE_LIBRARY_VARIANT", "release") == "debug"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.lib_path(_debug_variant())
 
 
 def load_library(build_if_missing: bool = True):
@@ -61,11 +67,13 @@ def load_library(build_if_missing: bool = True):
     global _lib
     if _lib is not None:
         return _lib
-    if build_if_missing and not _build.up_to_date():
-        _build.build()
-    if not os.path.exists(_build.LIB):
-        raise RuntimeError(f"{_build.LIB} is missing: run latent_query_split_gb300.build.build()")
-    lib = ctypes.CDLL(_build.LIB)
+    debug = _debug_variant()
+    path = _build.lib_path(debug)
+    if build_if_missing and not _build.up_to_date(debug):
+        _build.build(debug=debug)
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: run latent_query_split_gb300.build.build()")
+    lib = ctypes.CDLL(path)
     P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     D = ctypes.POINTER(FlareDims)
     lib.flare_workspace_bytes.argtypes = [I, D, P, I]

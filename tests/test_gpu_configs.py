@@ -163,7 +163,10 @@ def test_decode_bwd_c5_shapes_sampled(cuda_device):
         # 2e-2 of max(1, largest reference magnitude)
         for name, dev, ref in (("dQ", dQ, dQo), ("dZ", dZ, dZo)):
             bound = 2e-2 * max(1.0, float(np.abs(ref).max()))
-            assert_close(f"{name}[{b},{h}]", dev[b:b + 1, h:h + 1], ref, "bf16", atol=bound)
+            err = assert_close(f"{name}[{b},{h}]", dev[b:b + 1, h:h + 1], ref, "bf16", atol=bound)
+            # the error this bound admits is reported beside it (run with -s)
+            print(f"decode bwd {name}[{b},{h}]: max abs err {err:.3e}, bound {bound:.3e}, "
+                  f"max |ref| {np.abs(ref).max():.3e}")
         assert_close(f"dK[{b},:,{h}]", dK[b:b + 1, :, h:h + 1], dKo, "bf16")
 
 
@@ -191,7 +194,8 @@ def test_c5_flare_bwd_full_size_sampled(cuda_device):
         mh = _mask(mask, b)
         Zo, Lo = oracle.encode(Qh, Kh, Vh, mh)
         dQo, dKo, dVo = oracle.flare_bwd(Qh, Kh, Vh, mh, Zo, Lo, dYh)
-        assert_close(f"dQ[{b},{h}]", dQ[b:b + 1, h:h + 1], dQo, "bf16", atol=_bwd_bound(dQo))
+        err = assert_close(f"dQ[{b},{h}]", dQ[b:b + 1, h:h + 1], dQo, "bf16", atol=_bwd_bound(dQo))
+        print(f"FLARE bwd dQ[{b},{h}]: max abs err {err:.3e}, bound {_bwd_bound(dQo):.3e}")
         assert_close(f"dK[{b},:,{h}]", dK[b:b + 1, :, h:h + 1], dKo, "bf16")
         assert_close(f"dV[{b},:,{h}]", dV[b:b + 1, :, h:h + 1], dVo, "bf16")
 
@@ -218,4 +222,6 @@ def test_c5_flare_pp_bwd_full_size_sampled(cuda_device):
                                 (lat(out[0]), tok(out[1]), tok(out[2]), tok(out[3]), tok(out[4]), lat(out[5])),
                                 ref):
             atol = _bwd_bound(r) if name in ("dQseed", "dQdyn") else None
-            assert_close(f"{name}[{b},{h}]", dev, r, "bf16", atol=atol)
+            err = assert_close(f"{name}[{b},{h}]", dev, r, "bf16", atol=atol)
+            if atol is not None:
+                print(f"FLARE++ bwd {name}[{b},{h}]: max abs err {err:.3e}, bound {atol:.3e}")
