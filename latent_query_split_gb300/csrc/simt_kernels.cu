@@ -20,7 +20,11 @@ namespace {
 
 constexpr int kThreads = 128;        // 4 warps
 constexpr int kRowsPerWarp = 8;      // 4 warps x 8 rows = kSimtRows
-constexpr int kMaxDPerLane = 4;      // D <= 128 = 32 lanes x 4
+// The encoder and decode are compiled for a D capacity DC in {32, 64, 128}
+// (the smallest that holds D): a lane accumulates DC / 32 output components,
+// and a thread moves DC / 4 elements of a 32-row tile.
+template <int DC> constexpr int per_lane() { return DC / 32; }
+template <int DC> constexpr int tile_elems() { return 32 * DC / kThreads; }
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -48,9 +52,11 @@ __device__ __forceinline__ float warp_sum(float v) {
 //   key_ok         this lane's key is valid
 // State per row i: running max m[i], running sum l[i] (relative to m[i]) and
 // the unnormalised accumulator acc[i][j] for value component d = lane + 32 j.
+template <int DC>
 __device__ __forceinline__ void online_tile(const float *Rs, const float *Ks, const float *Vs,
                                             bool key_ok, int D, int row0, float *m, float *l,
-                                            float (*acc)[kMaxDPerLane]) {
+                                            float (*acc)[per_lane<DC>()]) {
+    constexpr int kMaxDPerLane = per_lane<DC>();
     const int lane = threadIdx.x & 31;
     const int ld = D + 1;
     const float *k = Ks + lane * ld;
@@ -118,26 +124,38 @@ struct MergeArgs {
 };
 
 __device__ void merge_rows(const MergeArgs &a, int m0, int rows, float *s_lmax, float *s_a) {
+    // Every loop below issues the loads of up to kMergeBatch chunks together
+    // and only then uses them (no load waits on another load's value, no
+    // branch on a loaded value before the next load): the partials were
+    // written by other CTAs a moment ago and sit in L2, so the merge's time
+    // is a few round trips to L2 per shard instead of two per chunk.
+    constexpr int kMergeBatch = 8;
     const int tid = threadIdx.x, nth = blockDim.x;
     for (int i = tid; i < rows; i += nth) {
         const int m = m0 + i;
         float lmax = -INFINITY;
         for (int r = 0; r < a.R; ++r) {
             const int c0 = a.chunk_start[r], c1 = a.chunk_start[r + 1];
-            // (unrolled: several partials' loads in flight at once)
-            float cmax = -INFINITY;
-#pragma unroll 8
-            for (int c = c0; c < c1; ++c) cmax = fmaxf(cmax, __ldcg(a.part_L + (int64_t)c * a.M + m));
-            float Lr = -INFINITY;
-            if (cmax != -INFINITY) {
-                float sum = 0.f;
-#pragma unroll 8
-                for (int c = c0; c < c1; ++c) {
-                    const float lc = __ldcg(a.part_L + (int64_t)c * a.M + m);
-                    if (lc != -INFINITY) sum += expf(lc - cmax);
+            // one pass: running maximum and the sum rescaled to it
+            float cmax = -INFINITY, sum = 0.f;
+            for (int cb = c0; cb < c1; cb += kMergeBatch) {
+                float lc[kMergeBatch];
+#pragma unroll
+                for (int u = 0; u < kMergeBatch; ++u)
+                    lc[u] = (cb + u < c1) ? __ldcg(a.part_L + (int64_t)(cb + u) * a.M + m) : -INFINITY;
+                float bm = cmax;
+#pragma unroll
+                for (int u = 0; u < kMergeBatch; ++u) bm = fmaxf(bm, lc[u]);
+                if (bm == -INFINITY) continue;
+                if (bm > cmax) {
+                    sum = (cmax == -INFINITY) ? 0.f : sum * expf(cmax - bm);
+                    cmax = bm;
                 }
-                Lr = cmax + logf(sum);
+#pragma unroll
+                for (int u = 0; u < kMergeBatch; ++u)
+                    if (lc[u] != -INFINITY) sum += expf(lc[u] - cmax);
             }
+            const float Lr = (cmax == -INFINITY) ? -INFINITY : cmax + logf(sum);
             a.Lr_out[r * a.Lr_shard_stride + m] = Lr;
             lmax = fmaxf(lmax, Lr);
         }
@@ -158,13 +176,23 @@ __device__ void merge_rows(const MergeArgs &a, int m0, int rows, float *s_lmax, 
         float U = 0.f;
         for (int r = 0; r < a.R; ++r) {
             const float Lr = a.Lr_out[r * a.Lr_shard_stride + m];
+            const int c0 = a.chunk_start[r], c1 = a.chunk_start[r + 1];
             float o = 0.f;
             if (Lr != -INFINITY) {
-#pragma unroll 8
-                for (int c = a.chunk_start[r]; c < a.chunk_start[r + 1]; ++c) {
-                    const float lc = __ldcg(a.part_L + (int64_t)c * a.M + m);
-                    if (lc != -INFINITY)
-                        o = fmaf(expf(lc - Lr), __ldcg(a.part_O + ((int64_t)c * a.M + m) * a.D + d), o);
+                // every chunk's output slot was written (zeros for an empty
+                // chunk), so it is loaded unconditionally and weighted
+                for (int cb = c0; cb < c1; cb += kMergeBatch) {
+                    float lc[kMergeBatch], oc[kMergeBatch];
+#pragma unroll
+                    for (int u = 0; u < kMergeBatch; ++u) {
+                        const bool in = cb + u < c1;
+                        const int64_t c = cb + u;
+                        lc[u] = in ? __ldcg(a.part_L + c * a.M + m) : -INFINITY;
+                        oc[u] = in ? __ldcg(a.part_O + (c * a.M + m) * a.D + d) : 0.f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < kMergeBatch; ++u)
+                        o = fmaf(lc[u] == -INFINITY ? 0.f : expf(lc[u] - Lr), oc[u], o);
                 }
                 U = fmaf(expf(Lr - lmax), o, U);
             }
@@ -178,12 +206,13 @@ namespace {
 
 // ---------------------------------------------------------------------------
 // Encoder: one CTA per (token chunk, head, batch x row tile of 32 latents).
-template <typename TQ, typename TKV>
+template <typename TQ, typename TKV, int DC>
 __global__ void __launch_bounds__(kThreads)
 enc_fwd_simt_kernel(Problem pr, ShardPlan plan, const TQ *__restrict__ Q,
                     const TKV *__restrict__ K, const TKV *__restrict__ V,
                     const uint8_t *__restrict__ mask, EncoderWorkspace ws, EncoderOut out,
                     int mtiles) {
+    constexpr int kMaxDPerLane = per_lane<DC>(), kTileElems = tile_elems<DC>();
     extern __shared__ float smem[];
     const int D = pr.D, M = pr.M, H = pr.H, N = pr.N;
     const int ld = D + 1;
@@ -202,9 +231,19 @@ enc_fwd_simt_kernel(Problem pr, ShardPlan plan, const TQ *__restrict__ Q,
     chunk_range(plan, c, n0, n1);
 
     const TQ *Qb = Q + (int64_t)b * pr.q_bstride + (int64_t)h * M * D;
-    for (int e = tid; e < kSimtRows * D; e += kThreads) {
-        const int i = e / D, d = e % D;
-        Qs[i * ld + d] = (m0 + i < M) ? pr.scale * to_f(Qb[(int64_t)(m0 + i) * D + d]) : 0.f;
+    {
+        // all of this thread's loads first, then the stores (one round trip)
+        float qv[kTileElems];
+#pragma unroll
+        for (int k = 0; k < kTileElems; ++k) {
+            const int e = tid + k * kThreads, i = e / D, d = e - i * D;
+            qv[k] = (e < kSimtRows * D && m0 + i < M) ? pr.scale * to_f(Qb[(int64_t)(m0 + i) * D + d]) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kTileElems; ++k) {
+            const int e = tid + k * kThreads, i = e / D, d = e - i * D;
+            if (e < kSimtRows * D) Qs[i * ld + d] = qv[k];
+        }
     }
     float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][kMaxDPerLane];
 #pragma unroll
@@ -214,26 +253,40 @@ enc_fwd_simt_kernel(Problem pr, ShardPlan plan, const TQ *__restrict__ Q,
 #pragma unroll
         for (int j = 0; j < kMaxDPerLane; ++j) acc[i][j] = 0.f;
     }
+    // The next tile's K, V and mask are loaded into registers while this one
+    // is computed (its loads are in flight during the tile's arithmetic).
+    float kr[kTileElems], vr[kTileElems];
+    bool okr = false;
+    auto fetch = [&](int64_t t0) {
+#pragma unroll
+        for (int k = 0; k < kTileElems; ++k) {
+            const int e = tid + k * kThreads, t = e / D, d = e - t * D;
+            const int64_t n = t0 + t;
+            kr[k] = vr[k] = 0.f;
+            if (e < kSimtTile * D && n < n1) {
+                const int64_t o = (((int64_t)b * N + n) * H + h) * D + d;
+                kr[k] = to_f(K[o]);
+                vr[k] = to_f(V[o]);
+            }
+        }
+        const int64_t n = t0 + tid;
+        okr = tid < kSimtTile && n < n1 && (!mask || mask[(int64_t)b * N + n]);
+    };
+    if (n0 < n1) fetch(n0);
     for (int64_t t0 = n0; t0 < n1; t0 += kSimtTile) {
         __syncthreads();
-        for (int e = tid; e < kSimtTile * D; e += kThreads) {
-            const int t = e / D, d = e % D;
-            const int64_t n = t0 + t;
-            float kv = 0.f, vv = 0.f;
-            if (n < n1) {
-                const int64_t o = (((int64_t)b * N + n) * H + h) * D + d;
-                kv = to_f(K[o]);
-                vv = to_f(V[o]);
+#pragma unroll
+        for (int k = 0; k < kTileElems; ++k) {
+            const int e = tid + k * kThreads, t = e / D, d = e - t * D;
+            if (e < kSimtTile * D) {
+                Ks[t * ld + d] = kr[k];
+                Vs[t * D + d] = vr[k];
             }
-            Ks[t * ld + d] = kv;
-            Vs[t * D + d] = vv;
         }
-        if (tid < kSimtTile) {
-            const int64_t n = t0 + tid;
-            s_ok[tid] = (n < n1) && (!mask || mask[(int64_t)b * N + n]);
-        }
+        if (tid < kSimtTile) s_ok[tid] = okr;
         __syncthreads();
-        online_tile(Qs, Ks, Vs, s_ok[lane] != 0, D, warp * kRowsPerWarp, m, l, acc);
+        if (t0 + kSimtTile < n1) fetch(t0 + kSimtTile);
+        online_tile<DC>(Qs, Ks, Vs, s_ok[lane] != 0, D, warp * kRowsPerWarp, m, l, acc);
     }
 
     // chunk partial: normalised output and log-normaliser (empty row: -inf, 0)
@@ -329,10 +382,11 @@ lse_merge_kernel(const float *__restrict__ O_r, const float *__restrict__ L_r, i
 
 // ---------------------------------------------------------------------------
 // Decode: rows are 32 tokens, keys are the M latents (tiles of 32), values Z.
-template <typename TQ, typename TK>
+template <typename TQ, typename TK, int DC>
 __global__ void __launch_bounds__(kThreads)
 dec_fwd_simt_kernel(Problem pr, const TQ *__restrict__ Q, const float *__restrict__ Z,
                     const TK *__restrict__ K, TK *__restrict__ Y) {
+    constexpr int kMaxDPerLane = per_lane<DC>(), kTileElems = tile_elems<DC>();
     extern __shared__ float smem[];
     const int D = pr.D, M = pr.M, H = pr.H, N = pr.N;
     const int ld = D + 1;
@@ -342,10 +396,19 @@ dec_fwd_simt_kernel(Problem pr, const TQ *__restrict__ Q, const float *__restric
     const int64_t t0 = (int64_t)blockIdx.x * kSimtTile;
     const int h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int e = tid; e < kSimtTile * D; e += kThreads) {
-        const int t = e / D, d = e % D;
-        const int64_t n = t0 + t;
-        Rs[t * ld + d] = (n < N) ? pr.scale * to_f(K[(((int64_t)b * N + n) * H + h) * D + d]) : 0.f;
+    {
+        float kv[kTileElems];
+#pragma unroll
+        for (int k = 0; k < kTileElems; ++k) {
+            const int e = tid + k * kThreads, t = e / D, d = e - t * D;
+            const int64_t n = t0 + t;
+            kv[k] = (e < kSimtTile * D && n < N) ? pr.scale * to_f(K[(((int64_t)b * N + n) * H + h) * D + d]) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kTileElems; ++k) {
+            const int e = tid + k * kThreads, t = e / D, d = e - t * D;
+            if (e < kSimtTile * D) Rs[t * ld + d] = kv[k];
+        }
     }
     float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][kMaxDPerLane];
 #pragma unroll
@@ -358,15 +421,25 @@ dec_fwd_simt_kernel(Problem pr, const TQ *__restrict__ Q, const float *__restric
     const TQ *Qb = Q + (int64_t)b * pr.q_bstride + (int64_t)h * M * D;
     const float *Zb = Z + ((int64_t)b * H + h) * M * D;
     for (int l0 = 0; l0 < M; l0 += kSimtRows) {
-        __syncthreads();
-        for (int e = tid; e < kSimtRows * D; e += kThreads) {
-            const int j = e / D, d = e % D;
-            const bool ok = l0 + j < M;
-            Ls[j * ld + d] = ok ? to_f(Qb[(int64_t)(l0 + j) * D + d]) : 0.f;
-            Zs[j * D + d] = ok ? Zb[(int64_t)(l0 + j) * D + d] : 0.f;
+        float qv[kTileElems], zv[kTileElems];
+#pragma unroll
+        for (int k = 0; k < kTileElems; ++k) {
+            const int e = tid + k * kThreads, j = e / D, d = e - j * D;
+            const bool ok = e < kSimtRows * D && l0 + j < M;
+            qv[k] = ok ? to_f(Qb[(int64_t)(l0 + j) * D + d]) : 0.f;
+            zv[k] = ok ? Zb[(int64_t)(l0 + j) * D + d] : 0.f;
         }
         __syncthreads();
-        online_tile(Rs, Ls, Zs, l0 + lane < M, D, warp * kRowsPerWarp, m, l, acc);
+#pragma unroll
+        for (int k = 0; k < kTileElems; ++k) {
+            const int e = tid + k * kThreads, j = e / D, d = e - j * D;
+            if (e < kSimtRows * D) {
+                Ls[j * ld + d] = qv[k];
+                Zs[j * D + d] = zv[k];
+            }
+        }
+        __syncthreads();
+        online_tile<DC>(Rs, Ls, Zs, l0 + lane < M, D, warp * kRowsPerWarp, m, l, acc);
     }
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
@@ -602,6 +675,62 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 
 // ---- launchers -------------------------------------------------------------
 
+namespace {
+template <int DC>
+cudaError_t launch_encoder_simt_dc(const Problem &pr, const ShardPlan &plan, const void *Q,
+                                   bool q_is_f32, const void *K, const void *V, const uint8_t *mask,
+                                   const EncoderWorkspace &ws, const EncoderOut &out, dim3 grid,
+                                   int mtiles, cudaStream_t st) {
+    const size_t smem = enc_smem_bytes(pr.D);
+    cudaError_t e;
+    if (!pr.bf16) {
+        auto k = enc_fwd_simt_kernel<float, float, DC>;
+        if ((e = set_smem(k, smem)) != cudaSuccess) return e;
+        k<<<grid, kThreads, smem, st>>>(pr, plan, (const float *)Q, (const float *)K,
+                                        (const float *)V, mask, ws, out, mtiles);
+    } else if (q_is_f32) {
+        auto k = enc_fwd_simt_kernel<float, __nv_bfloat16, DC>;
+        if ((e = set_smem(k, smem)) != cudaSuccess) return e;
+        k<<<grid, kThreads, smem, st>>>(pr, plan, (const float *)Q, (const __nv_bfloat16 *)K,
+                                        (const __nv_bfloat16 *)V, mask, ws, out, mtiles);
+    } else {
+        auto k = enc_fwd_simt_kernel<__nv_bfloat16, __nv_bfloat16, DC>;
+        if ((e = set_smem(k, smem)) != cudaSuccess) return e;
+        k<<<grid, kThreads, smem, st>>>(pr, plan, (const __nv_bfloat16 *)Q,
+                                        (const __nv_bfloat16 *)K, (const __nv_bfloat16 *)V, mask,
+                                        ws, out, mtiles);
+    }
+    note_launch();
+    return cudaGetLastError();
+}
+
+template <int DC>
+cudaError_t launch_decode_simt_dc(const Problem &pr, const void *Q, bool q_is_f32, const float *Z,
+                                  const void *K, void *Y, cudaStream_t st) {
+    dim3 grid((pr.N + kSimtTile - 1) / kSimtTile, pr.H, pr.B);
+    const size_t smem = sizeof(float) * ((size_t)kSimtTile * (pr.D + 1) +
+                                         (size_t)kSimtRows * (pr.D + 1) + (size_t)kSimtRows * pr.D);
+    cudaError_t e;
+    if (!pr.bf16) {
+        auto k = dec_fwd_simt_kernel<float, float, DC>;
+        if ((e = set_smem(k, smem)) != cudaSuccess) return e;
+        k<<<grid, kThreads, smem, st>>>(pr, (const float *)Q, Z, (const float *)K, (float *)Y);
+    } else if (q_is_f32) {
+        auto k = dec_fwd_simt_kernel<float, __nv_bfloat16, DC>;
+        if ((e = set_smem(k, smem)) != cudaSuccess) return e;
+        k<<<grid, kThreads, smem, st>>>(pr, (const float *)Q, Z, (const __nv_bfloat16 *)K,
+                                        (__nv_bfloat16 *)Y);
+    } else {
+        auto k = dec_fwd_simt_kernel<__nv_bfloat16, __nv_bfloat16, DC>;
+        if ((e = set_smem(k, smem)) != cudaSuccess) return e;
+        k<<<grid, kThreads, smem, st>>>(pr, (const __nv_bfloat16 *)Q, Z,
+                                        (const __nv_bfloat16 *)K, (__nv_bfloat16 *)Y);
+    }
+    note_launch();
+    return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_encoder_simt(const Problem &pr, const ShardPlan &plan, const void *Q,
                                 bool q_is_f32, const void *K, const void *V, const uint8_t *mask,
                                 const EncoderWorkspace &ws, const EncoderOut &out,
@@ -609,29 +738,11 @@ cudaError_t launch_encoder_simt(const Problem &pr, const ShardPlan &plan, const 
     const int mtiles = (pr.M + kSimtRows - 1) / kSimtRows;
     if (plan.total_chunks == 0 || pr.B == 0) return cudaSuccess;
     dim3 grid(plan.total_chunks, pr.H, pr.B * mtiles);
-    const size_t smem = enc_smem_bytes(pr.D);
-    cudaError_t e;
-    if (!pr.bf16) {
-        auto k = enc_fwd_simt_kernel<float, float>;
-        if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-        k<<<grid, kThreads, smem, st>>>(pr, plan, (const float *)Q, (const float *)K,
-                                        (const float *)V, mask, ws, out, mtiles);
-        note_launch();
-    } else if (q_is_f32) {
-        auto k = enc_fwd_simt_kernel<float, __nv_bfloat16>;
-        if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-        k<<<grid, kThreads, smem, st>>>(pr, plan, (const float *)Q, (const __nv_bfloat16 *)K,
-                                        (const __nv_bfloat16 *)V, mask, ws, out, mtiles);
-        note_launch();
-    } else {
-        auto k = enc_fwd_simt_kernel<__nv_bfloat16, __nv_bfloat16>;
-        if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-        k<<<grid, kThreads, smem, st>>>(pr, plan, (const __nv_bfloat16 *)Q,
-                                        (const __nv_bfloat16 *)K, (const __nv_bfloat16 *)V, mask,
-                                        ws, out, mtiles);
-        note_launch();
-    }
-    return cudaGetLastError();
+    if (pr.D <= 32)
+        return launch_encoder_simt_dc<32>(pr, plan, Q, q_is_f32, K, V, mask, ws, out, grid, mtiles, st);
+    if (pr.D <= 64)
+        return launch_encoder_simt_dc<64>(pr, plan, Q, q_is_f32, K, V, mask, ws, out, grid, mtiles, st);
+    return launch_encoder_simt_dc<128>(pr, plan, Q, q_is_f32, K, V, mask, ws, out, grid, mtiles, st);
 }
 
 cudaError_t launch_lse_merge(const float *O_r, const float *L_r, int R, int B, int H, int M,
@@ -647,29 +758,9 @@ cudaError_t launch_lse_merge(const float *O_r, const float *L_r, int R, int B, i
 cudaError_t launch_decode_simt(const Problem &pr, const void *Q, bool q_is_f32, const float *Z,
                                const void *K, void *Y, cudaStream_t st) {
     if (pr.B == 0 || pr.N == 0) return cudaSuccess;
-    dim3 grid((pr.N + kSimtTile - 1) / kSimtTile, pr.H, pr.B);
-    const size_t smem = sizeof(float) * ((size_t)kSimtTile * (pr.D + 1) +
-                                         (size_t)kSimtRows * (pr.D + 1) + (size_t)kSimtRows * pr.D);
-    cudaError_t e;
-    if (!pr.bf16) {
-        auto k = dec_fwd_simt_kernel<float, float>;
-        if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-        k<<<grid, kThreads, smem, st>>>(pr, (const float *)Q, Z, (const float *)K, (float *)Y);
-        note_launch();
-    } else if (q_is_f32) {
-        auto k = dec_fwd_simt_kernel<float, __nv_bfloat16>;
-        if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-        k<<<grid, kThreads, smem, st>>>(pr, (const float *)Q, Z, (const __nv_bfloat16 *)K,
-                                        (__nv_bfloat16 *)Y);
-        note_launch();
-    } else {
-        auto k = dec_fwd_simt_kernel<__nv_bfloat16, __nv_bfloat16>;
-        if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-        k<<<grid, kThreads, smem, st>>>(pr, (const __nv_bfloat16 *)Q, Z,
-                                        (const __nv_bfloat16 *)K, (__nv_bfloat16 *)Y);
-        note_launch();
-    }
-    return cudaGetLastError();
+    if (pr.D <= 32) return launch_decode_simt_dc<32>(pr, Q, q_is_f32, Z, K, Y, st);
+    if (pr.D <= 64) return launch_decode_simt_dc<64>(pr, Q, q_is_f32, Z, K, Y, st);
+    return launch_decode_simt_dc<128>(pr, Q, q_is_f32, Z, K, Y, st);
 }
 
 namespace {

@@ -38,9 +38,22 @@ def test_long_context_and_small_workloads():
 
 
 def test_flare_pp_forward_is_three_passes():
-    a = _alg("c3_pp_bf16")["flare_pp_fwd"]
+    al = _alg("c3_pp_bf16")
+    a = al["flare_pp_fwd"]
     assert a[0] / 1e9 == pytest.approx(3 * 2.147, abs=0.01)
     assert a[1] / 1e12 == pytest.approx(1.65, abs=0.01)
+    # one encoder pass and the decode, timed alone: a third each
+    assert al["encoder"][0] == al["decode"][0] == a[0] / 3
+    assert al["encoder"][1] == al["decode"][1] == a[1] / 3
+
+
+def test_dominant_kernel_of_a_composite_step():
+    # the FLARE++ step launches the encoder twice and the decode once
+    ms = {"flare_pp_fwd": 1.6, "encoder": 0.5, "decode": 0.55}
+    assert bench.dominant_phase(ms, "flare_pp_fwd") == "encoder"
+    ms["decode"] = 1.1
+    assert bench.dominant_phase(ms, "flare_pp_fwd") == "decode"
+    assert bench.dominant_phase({"encoder": 0.1, "decode": 0.2}, "flare_fwd") == "decode"
 
 
 def test_backward_counts():
