@@ -18,13 +18,19 @@
 namespace flare {
 namespace {
 
-constexpr int kThreads = 128;        // 4 warps
-constexpr int kRowsPerWarp = 8;      // 4 warps x 8 rows = kSimtRows
+constexpr int kThreads = 128;        // 4 warps (backward kernels)
+// The encoder and decode spread a tile's 32 rows over 16 warps of 2 rows:
+// each warp's chain of dependent steps (dot products, shuffle reductions,
+// exponentials, broadcasts) is short, and a small problem, where each SM
+// holds one CTA, still has four warps per sub-partition to interleave.
+constexpr int kFwdThreads = 512;
+constexpr int kRowsPerWarp = 2;      // 16 warps x 2 rows = kSimtRows
+static_assert(kFwdThreads / 32 * kRowsPerWarp == 32, "a tile's 32 rows over the CTA's warps");
 // The encoder and decode are compiled for a D capacity DC in {32, 64, 128}
 // (the smallest that holds D): a lane accumulates DC / 32 output components,
 // and a thread moves DC / 4 elements of a 32-row tile.
 template <int DC> constexpr int per_lane() { return DC / 32; }
-template <int DC> constexpr int tile_elems() { return 32 * DC / kThreads; }
+template <int DC> constexpr int tile_elems() { return 32 * DC / kFwdThreads; }
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -133,7 +139,7 @@ __device__ void merge_rows(const MergeArgs &a, int m0, int rows, float *s_lmax, 
     const int tid = threadIdx.x, nth = blockDim.x;
     for (int i = tid; i < rows; i += nth) {
         const int m = m0 + i;
-        float lmax = -INFINITY;
+        float lmax = -INFINITY, asum = 0.f;
         for (int r = 0; r < a.R; ++r) {
             const int c0 = a.chunk_start[r], c1 = a.chunk_start[r + 1];
             // one pass: running maximum and the sum rescaled to it
@@ -157,19 +163,65 @@ __device__ void merge_rows(const MergeArgs &a, int m0, int rows, float *s_lmax, 
             }
             const float Lr = (cmax == -INFINITY) ? -INFINITY : cmax + logf(sum);
             a.Lr_out[r * a.Lr_shard_stride + m] = Lr;
-            lmax = fmaxf(lmax, Lr);
-        }
-        float asum = 0.f;
-        if (lmax != -INFINITY)
-            for (int r = 0; r < a.R; ++r) {
-                const float Lr = a.Lr_out[r * a.Lr_shard_stride + m];
-                if (Lr != -INFINITY) asum += expf(Lr - lmax);
+            // the row's (L_max, a) folded in shard order as each shard is done
+            if (Lr != -INFINITY) {
+                if (Lr > lmax) {
+                    asum = (lmax == -INFINITY) ? 0.f : asum * expf(lmax - Lr);
+                    lmax = Lr;
+                }
+                asum += expf(Lr - lmax);
             }
+        }
         s_lmax[i] = lmax;
         s_a[i] = asum;
         if (a.L) a.L[m] = (lmax == -INFINITY) ? -INFINITY : lmax + logf(asum);
     }
     __syncthreads();
+    if (a.Or_out == nullptr) {
+        // Only (Z, L): Z = sum_c exp(L_c - L_max) O_c / a over every chunk of
+        // the row, so no load waits on a shard-level value; each thread
+        // takes kElems outputs at once and issues the loads of a batch of
+        // chunks for all of them together.
+        constexpr int kElems = 4;
+        const int total = a.chunk_start[a.R];
+        for (int e0 = tid; e0 < rows * a.D; e0 += kElems * nth) {
+            int m[kElems], d[kElems];
+            float lm[kElems], U[kElems];
+#pragma unroll
+            for (int k = 0; k < kElems; ++k) {
+                const int e = e0 + k * nth, i = e / a.D;
+                const bool in = e < rows * a.D;
+                m[k] = m0 + (in ? i : 0);
+                d[k] = in ? e - i * a.D : 0;
+                lm[k] = in ? s_lmax[i] : -INFINITY;
+                U[k] = 0.f;
+            }
+            for (int cb = 0; cb < total; cb += kMergeBatch) {
+                float lc[kElems][kMergeBatch], oc[kElems][kMergeBatch];
+#pragma unroll
+                for (int k = 0; k < kElems; ++k)
+#pragma unroll
+                    for (int u = 0; u < kMergeBatch; ++u) {
+                        const int64_t c = cb + u;
+                        const bool in = cb + u < total && lm[k] != -INFINITY;
+                        lc[k][u] = in ? __ldcg(a.part_L + c * a.M + m[k]) : -INFINITY;
+                        oc[k][u] = in ? __ldcg(a.part_O + (c * a.M + m[k]) * a.D + d[k]) : 0.f;
+                    }
+#pragma unroll
+                for (int k = 0; k < kElems; ++k)
+#pragma unroll
+                    for (int u = 0; u < kMergeBatch; ++u)
+                        U[k] = fmaf(lc[k][u] == -INFINITY ? 0.f : expf(lc[k][u] - lm[k]), oc[k][u], U[k]);
+            }
+#pragma unroll
+            for (int k = 0; k < kElems; ++k) {
+                const int e = e0 + k * nth;
+                if (e < rows * a.D && a.Z)
+                    a.Z[(int64_t)m[k] * a.D + d[k]] = (lm[k] == -INFINITY) ? 0.f : U[k] / s_a[m[k] - m0];
+            }
+        }
+        return;
+    }
     for (int e = tid; e < rows * a.D; e += nth) {
         const int i = e / a.D, d = e % a.D, m = m0 + i;
         const float lmax = s_lmax[i];
@@ -207,7 +259,7 @@ namespace {
 // ---------------------------------------------------------------------------
 // Encoder: one CTA per (token chunk, head, batch x row tile of 32 latents).
 template <typename TQ, typename TKV, int DC>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kFwdThreads)
 enc_fwd_simt_kernel(Problem pr, ShardPlan plan, const TQ *__restrict__ Q,
                     const TKV *__restrict__ K, const TKV *__restrict__ V,
                     const uint8_t *__restrict__ mask, EncoderWorkspace ws, EncoderOut out,
@@ -236,12 +288,12 @@ enc_fwd_simt_kernel(Problem pr, ShardPlan plan, const TQ *__restrict__ Q,
         float qv[kTileElems];
 #pragma unroll
         for (int k = 0; k < kTileElems; ++k) {
-            const int e = tid + k * kThreads, i = e / D, d = e - i * D;
+            const int e = tid + k * kFwdThreads, i = e / D, d = e - i * D;
             qv[k] = (e < kSimtRows * D && m0 + i < M) ? pr.scale * to_f(Qb[(int64_t)(m0 + i) * D + d]) : 0.f;
         }
 #pragma unroll
         for (int k = 0; k < kTileElems; ++k) {
-            const int e = tid + k * kThreads, i = e / D, d = e - i * D;
+            const int e = tid + k * kFwdThreads, i = e / D, d = e - i * D;
             if (e < kSimtRows * D) Qs[i * ld + d] = qv[k];
         }
     }
@@ -260,7 +312,7 @@ enc_fwd_simt_kernel(Problem pr, ShardPlan plan, const TQ *__restrict__ Q,
     auto fetch = [&](int64_t t0) {
 #pragma unroll
         for (int k = 0; k < kTileElems; ++k) {
-            const int e = tid + k * kThreads, t = e / D, d = e - t * D;
+            const int e = tid + k * kFwdThreads, t = e / D, d = e - t * D;
             const int64_t n = t0 + t;
             kr[k] = vr[k] = 0.f;
             if (e < kSimtTile * D && n < n1) {
@@ -277,7 +329,7 @@ enc_fwd_simt_kernel(Problem pr, ShardPlan plan, const TQ *__restrict__ Q,
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < kTileElems; ++k) {
-            const int e = tid + k * kThreads, t = e / D, d = e - t * D;
+            const int e = tid + k * kFwdThreads, t = e / D, d = e - t * D;
             if (e < kSimtTile * D) {
                 Ks[t * ld + d] = kr[k];
                 Vs[t * D + d] = vr[k];
@@ -341,7 +393,7 @@ enc_fwd_simt_kernel(Problem pr, ShardPlan plan, const TQ *__restrict__ Q,
 
 // ---------------------------------------------------------------------------
 // Standalone merge of R given shard results: one CTA per (b, h, 32 rows).
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kFwdThreads)
 lse_merge_kernel(const float *__restrict__ O_r, const float *__restrict__ L_r, int R, int B,
                  int H, int M, int D, float *Z, float *L) {
     __shared__ float s_lmax[kSimtRows], s_a[kSimtRows];
@@ -383,7 +435,7 @@ lse_merge_kernel(const float *__restrict__ O_r, const float *__restrict__ L_r, i
 // ---------------------------------------------------------------------------
 // Decode: rows are 32 tokens, keys are the M latents (tiles of 32), values Z.
 template <typename TQ, typename TK, int DC>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kFwdThreads)
 dec_fwd_simt_kernel(Problem pr, const TQ *__restrict__ Q, const float *__restrict__ Z,
                     const TK *__restrict__ K, TK *__restrict__ Y) {
     constexpr int kMaxDPerLane = per_lane<DC>(), kTileElems = tile_elems<DC>();
@@ -400,13 +452,13 @@ dec_fwd_simt_kernel(Problem pr, const TQ *__restrict__ Q, const float *__restric
         float kv[kTileElems];
 #pragma unroll
         for (int k = 0; k < kTileElems; ++k) {
-            const int e = tid + k * kThreads, t = e / D, d = e - t * D;
+            const int e = tid + k * kFwdThreads, t = e / D, d = e - t * D;
             const int64_t n = t0 + t;
             kv[k] = (e < kSimtTile * D && n < N) ? pr.scale * to_f(K[(((int64_t)b * N + n) * H + h) * D + d]) : 0.f;
         }
 #pragma unroll
         for (int k = 0; k < kTileElems; ++k) {
-            const int e = tid + k * kThreads, t = e / D, d = e - t * D;
+            const int e = tid + k * kFwdThreads, t = e / D, d = e - t * D;
             if (e < kSimtTile * D) Rs[t * ld + d] = kv[k];
         }
     }
@@ -424,7 +476,7 @@ dec_fwd_simt_kernel(Problem pr, const TQ *__restrict__ Q, const float *__restric
         float qv[kTileElems], zv[kTileElems];
 #pragma unroll
         for (int k = 0; k < kTileElems; ++k) {
-            const int e = tid + k * kThreads, j = e / D, d = e - j * D;
+            const int e = tid + k * kFwdThreads, j = e / D, d = e - j * D;
             const bool ok = e < kSimtRows * D && l0 + j < M;
             qv[k] = ok ? to_f(Qb[(int64_t)(l0 + j) * D + d]) : 0.f;
             zv[k] = ok ? Zb[(int64_t)(l0 + j) * D + d] : 0.f;
@@ -432,7 +484,7 @@ dec_fwd_simt_kernel(Problem pr, const TQ *__restrict__ Q, const float *__restric
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < kTileElems; ++k) {
-            const int e = tid + k * kThreads, j = e / D, d = e - j * D;
+            const int e = tid + k * kFwdThreads, j = e / D, d = e - j * D;
             if (e < kSimtRows * D) {
                 Ls[j * ld + d] = qv[k];
                 Zs[j * D + d] = zv[k];
@@ -686,17 +738,17 @@ cudaError_t launch_encoder_simt_dc(const Problem &pr, const ShardPlan &plan, con
     if (!pr.bf16) {
         auto k = enc_fwd_simt_kernel<float, float, DC>;
         if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-        k<<<grid, kThreads, smem, st>>>(pr, plan, (const float *)Q, (const float *)K,
+        k<<<grid, kFwdThreads, smem, st>>>(pr, plan, (const float *)Q, (const float *)K,
                                         (const float *)V, mask, ws, out, mtiles);
     } else if (q_is_f32) {
         auto k = enc_fwd_simt_kernel<float, __nv_bfloat16, DC>;
         if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-        k<<<grid, kThreads, smem, st>>>(pr, plan, (const float *)Q, (const __nv_bfloat16 *)K,
+        k<<<grid, kFwdThreads, smem, st>>>(pr, plan, (const float *)Q, (const __nv_bfloat16 *)K,
                                         (const __nv_bfloat16 *)V, mask, ws, out, mtiles);
     } else {
         auto k = enc_fwd_simt_kernel<__nv_bfloat16, __nv_bfloat16, DC>;
         if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-        k<<<grid, kThreads, smem, st>>>(pr, plan, (const __nv_bfloat16 *)Q,
+        k<<<grid, kFwdThreads, smem, st>>>(pr, plan, (const __nv_bfloat16 *)Q,
                                         (const __nv_bfloat16 *)K, (const __nv_bfloat16 *)V, mask,
                                         ws, out, mtiles);
     }
@@ -714,16 +766,16 @@ cudaError_t launch_decode_simt_dc(const Problem &pr, const void *Q, bool q_is_f3
     if (!pr.bf16) {
         auto k = dec_fwd_simt_kernel<float, float, DC>;
         if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-        k<<<grid, kThreads, smem, st>>>(pr, (const float *)Q, Z, (const float *)K, (float *)Y);
+        k<<<grid, kFwdThreads, smem, st>>>(pr, (const float *)Q, Z, (const float *)K, (float *)Y);
     } else if (q_is_f32) {
         auto k = dec_fwd_simt_kernel<float, __nv_bfloat16, DC>;
         if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-        k<<<grid, kThreads, smem, st>>>(pr, (const float *)Q, Z, (const __nv_bfloat16 *)K,
+        k<<<grid, kFwdThreads, smem, st>>>(pr, (const float *)Q, Z, (const __nv_bfloat16 *)K,
                                         (__nv_bfloat16 *)Y);
     } else {
         auto k = dec_fwd_simt_kernel<__nv_bfloat16, __nv_bfloat16, DC>;
         if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-        k<<<grid, kThreads, smem, st>>>(pr, (const __nv_bfloat16 *)Q, Z,
+        k<<<grid, kFwdThreads, smem, st>>>(pr, (const __nv_bfloat16 *)Q, Z,
                                         (const __nv_bfloat16 *)K, (__nv_bfloat16 *)Y);
     }
     note_launch();

@@ -447,6 +447,12 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
             return __all_sync(0xffffffffu, wt.wait(bar, par));
         };
+        // M > 128: the waits on the softmax warps' arrivals spin (test_wait)
+        // instead of suspending in try_wait: a suspended issuer woke ~1000
+        // cycles after the last arrival, and each tile's P Z waited on it
+        auto wspin = [&](uint32_t bar, uint32_t par) -> bool {
+            return __all_sync(0xffffffffu, wt.spin(bar, par));
+        };
         constexpr uint32_t idS = idesc_bf16_m128(M, 0);
         // P Z: bf16, or fp16 with the row-sum block (N = D + 16)
         constexpr uint32_t idPV = C::F16P ? idesc_f16(128, C::YN, 0, 1) : idesc_bf16_m128(D, 1);
@@ -503,9 +509,9 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             for (int c = 0; c < NCH && ok; ++c) {
                 // P arrives whole, published by every softmax warp at once
                 if (c == 0) {
-                    ok = wwait(p_chunk(g, 0), (uint32_t)kP & 1);
+                    ok = NG == 1 ? wspin(p_chunk(g, 0), (uint32_t)kP & 1) : wwait(p_chunk(g, 0), (uint32_t)kP & 1);
                     // M > 128: Y of the previous tile has been read by its epilogue
-                    if (ok && NG == 1 && jP >= 1) ok = wwait(epi_done(0), (uint32_t)(jP - 1) & 1);
+                    if (ok && NG == 1 && jP >= 1) ok = wspin(epi_done(0), (uint32_t)(jP - 1) & 1);
                     if (!ok) break;
                     tc_fence_after();
                 }
@@ -633,6 +639,10 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
             return __all_sync(0xffffffffu, wt.wait(bar, par));
         };
+        // the wait for the softmax warps' reads spins (see the P Z issuer)
+        auto wspin = [&](uint32_t bar, uint32_t par) -> bool {
+            return __all_sync(0xffffffffu, wt.spin(bar, par));
+        };
         constexpr uint32_t idS = idesc_bf16_m128(M, 0);
         const uint64_t dK0 = desc_sw128(sStage, 16, 1024);
         constexpr uint64_t kStageDesc = C::STAGE_BYTES >> 4;
@@ -645,7 +655,7 @@ dec_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 if (!wwait(qz_full((int)(u % QZB)), (uint32_t)(u / QZB) & 1)) break;
             }
             if (!wwait(full(s), (uint32_t)(jj / STAGES) & 1)) break;
-            if (jj >= 1 && !wwait(s_free, (uint32_t)(jj - 1) & 1)) break;
+            if (jj >= 1 && !wspin(s_free, (uint32_t)(jj - 1) & 1)) break;
             tc_fence_after();
             const uint64_t dK = dK0 + kStageDesc * s;
             const uint64_t dQ0 = desc_sw128(sbase + (uint32_t)(u % QZB) * C::QZ_BYTES, 16, 1024);
