@@ -53,6 +53,10 @@ namespace tc {
 
 struct BwdArgs {
     int B, H, M, N;
+    // latent rows [m0, m0 + M) of M_all: M = 256 runs as two passes of 128
+    // latent rows (row statistics, Q, dZ and the dQ partials are indexed
+    // with M_all rows per (b, h))
+    int m0, M_all;
     float sl2;                  // s * log2(e)
     float s;                    // score scale
     int q_per_batch;            // Q has a batch dimension
@@ -60,6 +64,7 @@ struct BwdArgs {
     const float *lc;            // [B*H][2][M]: -L log2(e) (or -inf), then -s c
     float *part;                // [B*H][P_max][M][64] dQ partials
     const __nv_bfloat16 *dk_acc;  // with ACC: dK = dk_acc + this share (dk_acc may be dK)
+    const __nv_bfloat16 *dv_acc;  // with ACCV: dV = dv_acc + this share (dv_acc may be dV)
     int P_max;
     int64_t T_bh, T_total;      // 128-token tiles per (b, h), and overall
     int grid;
@@ -71,7 +76,7 @@ __host__ __device__ __forceinline__ int bwd_cta_of(int64_t t, int64_t T_total, i
     return (int)((t * grid) / T_total);
 }
 
-template <int M_, int STAGES_>
+template <int M_, int STAGES_, bool ACCV_ = false>
 struct BwdCfg {
     static constexpr int M = M_, D = 64, TILE = 128, STAGES = STAGES_;
     static constexpr int THREADS = 320;
@@ -90,8 +95,11 @@ struct BwdCfg {
     // of the dK half, 16-byte chunks XOR-swizzled by the row)
     static constexpr uint32_t DKIN_OFF = OUT_OFF + OUT_BYTES;
     static constexpr uint32_t DKIN_BYTES = TILE_BYTES;
+    // the same for the old dV rows (ACCV: the second latent pass of M = 256)
+    static constexpr uint32_t DVIN_OFF = DKIN_OFF + DKIN_BYTES;
+    static constexpr uint32_t DVIN_BYTES = ACCV_ ? TILE_BYTES : 0;
     // row statistics of two (b, h) generations: [2][-L2 (128), -s c (128)]
-    static constexpr uint32_t LC_OFF = DKIN_OFF + DKIN_BYTES;
+    static constexpr uint32_t LC_OFF = DVIN_OFF + DVIN_BYTES;
     static constexpr uint32_t LC_BYTES = 2 * 2 * 128 * 4;
     static constexpr uint32_t BAR_OFF = LC_OFF + LC_BYTES;
     // full[S], empty[S], qd_full, qd_free, lc_full[2], s_full, p_full,
@@ -159,13 +167,13 @@ __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const float *__restr
 }
 
 // ---- the tile kernel -------------------------------------------------------------
-template <int M, int STAGES, bool ACC>
-__global__ void __launch_bounds__(BwdCfg<M, STAGES>::THREADS, 1)
+template <int M, int STAGES, bool ACC, bool ACCV = false>
+__global__ void __launch_bounds__(BwdCfg<M, STAGES, ACCV>::THREADS, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdZ,
               const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
               const BwdArgs a) {
-    using C = BwdCfg<M, STAGES>;
+    using C = BwdCfg<M, STAGES, ACCV>;
     constexpr uint32_t TB = C::TILE_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -252,15 +260,15 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 // Q, dZ and the statistics of the previous (b, h) are no longer read
                 if (u > 0 && !__all_sync(0xffffffffu, wt.wait_inline(qd_free, (uint32_t)(u - 1) & 1))) break;
                 float *dst = lcs + (u & 1) * 256;
-                const float *src = a.lc + bh * 2 * M;
-                for (int i = lane; i < 2 * M; i += 32) dst[(i / M) * 128 + (i % M)] = src[i];
+                const float *src = a.lc + bh * 2 * a.M_all + a.m0;
+                for (int i = lane; i < 2 * M; i += 32) dst[(i / M) * 128 + (i % M)] = src[(i / M) * a.M_all + (i % M)];
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(lc_full(u & 1));
                     mbar_arrive_expect_tx(qd_full, 2 * C::QZ_BYTES);
                     if (dcheck(h >= 0 && h < a.H && b >= 0 && b < a.B, kChkBwdQ, a.status)) {
-                        tma_load_4d(sQ, &tmQ, 0, 0, h, a.q_per_batch ? b : 0, qd_full);
-                        tma_load_4d(sdZ, &tmdZ, 0, 0, h, b, qd_full);
+                        tma_load_4d(sQ, &tmQ, 0, a.m0, h, a.q_per_batch ? b : 0, qd_full);
+                        tma_load_4d(sdZ, &tmdZ, 0, a.m0, h, b, qd_full);
                     }
                 }
                 __syncwarp();
@@ -441,13 +449,18 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             if (a.mask != nullptr && n < a.N) v = __ldg(a.mask + (int64_t)t.b * a.N + n);
             return v;
         };
-        // the old dK rows of tile t (this thread's row; read by this thread only,
-        // in the tile's epilogue)
+        // Accumulation into this half's output (dK for half 1 with ACC, dV for
+        // half 0 with ACCV): the old rows of tile t (this thread's row; read by
+        // this thread only, in the tile's epilogue)
+        constexpr bool kAccAny = ACC || ACCV;
+        const bool acc_mine = hf == 1 ? ACC : ACCV;
+        const __nv_bfloat16 *acc_src = hf == 1 ? a.dk_acc : a.dv_acc;
+        const uint32_t acc_buf = hf == 1 ? C::DKIN_OFF : C::DVIN_OFF;
         auto prefetch_dk = [&](const Cursor &t) {
             const int64_t n = t.kt * 128 + rig;
-            if (ACC && hf == 1 && n < a.N) {
-                const __nv_bfloat16 *src = a.dk_acc + (((int64_t)t.b * a.N + n) * a.H + t.h) * 64;
-                const uint32_t dst = sbase + C::DKIN_OFF + (uint32_t)rig * 128;
+            if (acc_mine && n < a.N) {
+                const __nv_bfloat16 *src = acc_src + (((int64_t)t.b * a.N + n) * a.H + t.h) * 64;
+                const uint32_t dst = sbase + acc_buf + (uint32_t)rig * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) cp_async16(dst + ((c ^ (rig & 7)) << 4), src + 8 * c);
                 cp_async_commit();
@@ -474,7 +487,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                     for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(g[8 * q + k]);
                     if (old) {
                         // bf16 pairs, the even column in the low half
-                        const uint4 o = *reinterpret_cast<const uint4 *>(smem + C::DKIN_OFF + rig * 128 +
+                        const uint4 o = *reinterpret_cast<const uint4 *>(smem + acc_buf + rig * 128 +
                                                                           ((chunk ^ (rig & 7)) << 4));
                         const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
@@ -493,7 +506,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 if (lane == 0) bulk_wait_group_read0();
                 __syncwarp();
             }
-            if constexpr (!ACC) {
+            if constexpr (!kAccAny) {
                 uint32_t rg[2][32];
                 tmem_ld32(out_tm, rg[0]);
                 tmem_ld32(out_tm + 32, rg[1]);
@@ -506,7 +519,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             } else {
                 // one 32-column half at a time (fewer live registers); TMEM is
                 // released after the second half
-                const bool acc_row = hf == 1 && t.kt * 128 + rig < a.N;
+                const bool acc_row = acc_mine && t.kt * 128 + rig < a.N;
                 if (acc_row) cp_async_wait0();
 #pragma unroll 1
                 for (int h2 = 0; h2 < 2; ++h2) {
@@ -544,7 +557,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 if (lane == 0) mbar_arrive(dq_free);
                 if (rig < M) {
                     const int piece = cta - bwd_cta_of(t.bh * a.T_bh, a.T_total, a.grid);
-                    float4 *dst = reinterpret_cast<float4 *>(a.part + ((t.bh * a.P_max + piece) * M + rig) * 64 + 32 * hf);
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        a.part + ((t.bh * a.P_max + piece) * a.M_all + a.m0 + rig) * 64 + 32 * hf);
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
                         dst[q] = make_float4(__uint_as_float(rq[4 * q]), __uint_as_float(rq[4 * q + 1]),

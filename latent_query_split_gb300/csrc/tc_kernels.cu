@@ -277,7 +277,7 @@ cudaError_t launch_decode_tc(const Problem &pr, const void *Q, bool q_is_f32, co
     return cudaErrorNotSupported;
 }
 
-bool tc_bwd_supported(bool bf16, int M, int D) { return bf16 && D == 64 && (M == 64 || M == 128); }
+bool tc_bwd_supported(bool bf16, int M, int D) { return bf16 && D == 64 && (M == 64 || M == 128 || M == 256); }
 
 namespace {
 // Backward workspace: dZ in bf16 [B*H*M*64], the row constants [B*H][2][M]
@@ -307,10 +307,13 @@ void bwd_layout(const Problem &pr, int sms, BwdLayout &l) {
     l.bytes = o;
 }
 
-template <int M, bool ACC>
+template <int M, bool ACC, bool ACCV = false>
 cudaError_t launch_bwd(const CUtensorMap *maps, const tc::BwdArgs &a, cudaStream_t st) {
-    using C = tc::BwdCfg<M, 3>;
-    auto k = tc::bwd_tc_kernel<M, 3, ACC>;
+    // the dV-accumulating pass keeps two K/V stages (its old-dV buffer takes
+    // the third stage's shared memory)
+    constexpr int STAGES = ACCV ? 2 : 3;
+    using C = tc::BwdCfg<M, STAGES, ACCV>;
+    auto k = tc::bwd_tc_kernel<M, STAGES, ACC, ACCV>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
     if (e != cudaSuccess) return e;
     k<<<a.grid, C::THREADS, C::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
@@ -349,19 +352,25 @@ cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t qb = pr.q_bstride == 0 ? 1 : pr.B;
+    // M = 256 runs as two passes over the tokens, one per half of the latent
+    // rows (128 each, the TMEM columns of one pass); the second adds its
+    // shares of dK and dV to the first's
+    const int Mp = pr.M > 128 ? 128 : pr.M;
     CUtensorMap maps[6];
     if (!make_map(&maps[0], K, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
         !make_map(&maps[1], V, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
-        !make_map(&maps[2], Q, pr.D, pr.M, pr.H, qb, (uint32_t)pr.M, 1) ||
-        !make_map(&maps[3], dzb, pr.D, pr.M, pr.H, pr.B, (uint32_t)pr.M, 1) ||
+        !make_map(&maps[2], Q, pr.D, pr.M, pr.H, qb, (uint32_t)Mp, 1) ||
+        !make_map(&maps[3], dzb, pr.D, pr.M, pr.H, pr.B, (uint32_t)Mp, 1) ||
         !make_map(&maps[4], dK, pr.D, pr.H, pr.N, pr.B, 1, 32) ||
         !make_map(&maps[5], dV, pr.D, pr.H, pr.N, pr.B, 1, 32))
         return cudaErrorInvalidValue;
     tc::BwdArgs a;
     a.B = pr.B;
     a.H = pr.H;
-    a.M = pr.M;
+    a.M = Mp;
     a.N = pr.N;
+    a.m0 = 0;
+    a.M_all = pr.M;
     a.s = pr.scale;
     a.sl2 = pr.scale * 1.4426950408889634f;
     a.q_per_batch = pr.q_bstride != 0;
@@ -369,12 +378,22 @@ cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *
     a.lc = lc;
     a.part = part;
     a.dk_acc = accumulate ? (const __nv_bfloat16 *)dK : nullptr;
+    a.dv_acc = nullptr;
     a.P_max = l.P_max;
     a.T_bh = l.T_bh;
     a.T_total = l.T_total;
     a.grid = l.grid;
     a.status = status;
-    if (accumulate)
+    if (pr.M == 256) {
+        // latent rows [0, 128): dK (+)= and dV = their shares
+        e = accumulate ? launch_bwd<128, true>(maps, a, st) : launch_bwd<128, false>(maps, a, st);
+        if (e != cudaSuccess) return e;
+        // latent rows [128, 256): dK += and dV += their shares
+        a.m0 = 128;
+        a.dk_acc = (const __nv_bfloat16 *)dK;
+        a.dv_acc = (const __nv_bfloat16 *)dV;
+        e = launch_bwd<128, true, true>(maps, a, st);
+    } else if (accumulate)
         e = pr.M == 128 ? launch_bwd<128, true>(maps, a, st) : launch_bwd<64, true>(maps, a, st);
     else
         e = pr.M == 128 ? launch_bwd<128, false>(maps, a, st) : launch_bwd<64, false>(maps, a, st);

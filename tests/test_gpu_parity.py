@@ -139,12 +139,13 @@ def test_encoder_bwd(cuda_device, kernel, dt, M, D, N):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-@pytest.mark.parametrize("M,replicated", [(128, True), (64, True), (128, False)])
+@pytest.mark.parametrize("M,replicated", [(128, True), (64, True), (128, False), (256, True), (256, False)])
 def test_encoder_bwd_multi_tile_spans(cuda_device, kernel, M, replicated):
     """Enough 128-token tiles that each persistent CTA walks several tiles and
     crosses (b, h) boundaries, so dQ is assembled from several partial pieces;
     rows with a global L of -inf contribute nothing; repeated runs agree bit
-    for bit (the pieces are summed in a fixed order)."""
+    for bit (the pieces are summed in a fixed order). M = 256 runs as two
+    passes of 128 latent rows, the second adding its dK and dV shares."""
     B, H, N, D = 2, 3, 20000, 64
     off = [0, 5000, 5000, N]
     Q, K, V, mask = _problem(16, B, H, M, N, D, "bf16", off, q_std=1.0, replicated=replicated)
@@ -222,7 +223,8 @@ def test_flare_bwd(cuda_device, kernel, dt, M, D, N, replicated):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-@pytest.mark.parametrize("dt,M,D,N", [("f32", 16, 32, 700), ("bf16", 128, 64, 2500), ("bf16", 64, 64, 5000)])
+@pytest.mark.parametrize("dt,M,D,N", [("f32", 16, 32, 700), ("bf16", 128, 64, 2500), ("bf16", 64, 64, 5000),
+                                      ("bf16", 256, 64, 2500)])
 def test_flare_pp_bwd(cuda_device, kernel, dt, M, D, N):
     """FLARE++ mixer backward from the oracle's forward statistics: the seeds'
     gradient, the four token gradients and the summed gradient of Q(X)."""
