@@ -139,31 +139,16 @@ __device__ void merge_rows(const MergeArgs &a, int m0, int rows, float *s_lmax, 
     const int tid = threadIdx.x, nth = blockDim.x;
     for (int i = tid; i < rows; i += nth) {
         const int m = m0 + i;
+        // every chunk of the row in batches (a batch may cross shard ends):
+        // the running (maximum, rescaled sum) of the current shard, closed
+        // into L_r at the shard's end and folded into the row's (L_max, a)
+        const int total = a.chunk_start[a.R];
         float lmax = -INFINITY, asum = 0.f;
-        for (int r = 0; r < a.R; ++r) {
-            const int c0 = a.chunk_start[r], c1 = a.chunk_start[r + 1];
-            // one pass: running maximum and the sum rescaled to it
-            float cmax = -INFINITY, sum = 0.f;
-            for (int cb = c0; cb < c1; cb += kMergeBatch) {
-                float lc[kMergeBatch];
-#pragma unroll
-                for (int u = 0; u < kMergeBatch; ++u)
-                    lc[u] = (cb + u < c1) ? __ldcg(a.part_L + (int64_t)(cb + u) * a.M + m) : -INFINITY;
-                float bm = cmax;
-#pragma unroll
-                for (int u = 0; u < kMergeBatch; ++u) bm = fmaxf(bm, lc[u]);
-                if (bm == -INFINITY) continue;
-                if (bm > cmax) {
-                    sum = (cmax == -INFINITY) ? 0.f : sum * expf(cmax - bm);
-                    cmax = bm;
-                }
-#pragma unroll
-                for (int u = 0; u < kMergeBatch; ++u)
-                    if (lc[u] != -INFINITY) sum += expf(lc[u] - cmax);
-            }
+        float cmax = -INFINITY, sum = 0.f;
+        int r = 0;
+        auto close_shard = [&]() {
             const float Lr = (cmax == -INFINITY) ? -INFINITY : cmax + logf(sum);
             a.Lr_out[r * a.Lr_shard_stride + m] = Lr;
-            // the row's (L_max, a) folded in shard order as each shard is done
             if (Lr != -INFINITY) {
                 if (Lr > lmax) {
                     asum = (lmax == -INFINITY) ? 0.f : asum * expf(lmax - Lr);
@@ -171,7 +156,30 @@ __device__ void merge_rows(const MergeArgs &a, int m0, int rows, float *s_lmax, 
                 }
                 asum += expf(Lr - lmax);
             }
+            cmax = -INFINITY;
+            sum = 0.f;
+            ++r;
+        };
+        for (int cb = 0; cb < total; cb += kMergeBatch) {
+            float lc[kMergeBatch];
+#pragma unroll
+            for (int u = 0; u < kMergeBatch; ++u)
+                lc[u] = (cb + u < total) ? __ldcg(a.part_L + (int64_t)(cb + u) * a.M + m) : -INFINITY;
+#pragma unroll
+            for (int u = 0; u < kMergeBatch; ++u) {
+                const int c = cb + u;
+                if (c >= total) break;
+                while (c >= a.chunk_start[r + 1]) close_shard();
+                if (lc[u] != -INFINITY) {
+                    if (lc[u] > cmax) {
+                        sum = (cmax == -INFINITY) ? 0.f : sum * expf(cmax - lc[u]);
+                        cmax = lc[u];
+                    }
+                    sum += expf(lc[u] - cmax);
+                }
+            }
         }
+        while (r < a.R) close_shard();
         s_lmax[i] = lmax;
         s_a[i] = asum;
         if (a.L) a.L[m] = (lmax == -INFINITY) ? -INFINITY : lmax + logf(asum);
@@ -283,19 +291,13 @@ enc_fwd_simt_kernel(Problem pr, ShardPlan plan, const TQ *__restrict__ Q,
     chunk_range(plan, c, n0, n1);
 
     const TQ *Qb = Q + (int64_t)b * pr.q_bstride + (int64_t)h * M * D;
-    {
-        // all of this thread's loads first, then the stores (one round trip)
-        float qv[kTileElems];
+    // all of this thread's query loads first; the first tile's loads follow
+    // before any store (one round trip to memory for both)
+    float qv[kTileElems];
 #pragma unroll
-        for (int k = 0; k < kTileElems; ++k) {
-            const int e = tid + k * kFwdThreads, i = e / D, d = e - i * D;
-            qv[k] = (e < kSimtRows * D && m0 + i < M) ? pr.scale * to_f(Qb[(int64_t)(m0 + i) * D + d]) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < kTileElems; ++k) {
-            const int e = tid + k * kFwdThreads, i = e / D, d = e - i * D;
-            if (e < kSimtRows * D) Qs[i * ld + d] = qv[k];
-        }
+    for (int k = 0; k < kTileElems; ++k) {
+        const int e = tid + k * kFwdThreads, i = e / D, d = e - i * D;
+        qv[k] = (e < kSimtRows * D && m0 + i < M) ? to_f(Qb[(int64_t)(m0 + i) * D + d]) : 0.f;
     }
     float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][kMaxDPerLane];
 #pragma unroll
@@ -325,6 +327,11 @@ enc_fwd_simt_kernel(Problem pr, ShardPlan plan, const TQ *__restrict__ Q,
         okr = tid < kSimtTile && n < n1 && (!mask || mask[(int64_t)b * N + n]);
     };
     if (n0 < n1) fetch(n0);
+#pragma unroll
+    for (int k = 0; k < kTileElems; ++k) {
+        const int e = tid + k * kFwdThreads, i = e / D, d = e - i * D;
+        if (e < kSimtRows * D) Qs[i * ld + d] = pr.scale * qv[k];
+    }
     for (int64_t t0 = n0; t0 < n1; t0 += kSimtTile) {
         __syncthreads();
 #pragma unroll
@@ -448,20 +455,14 @@ dec_fwd_simt_kernel(Problem pr, const TQ *__restrict__ Q, const float *__restric
     const int64_t t0 = (int64_t)blockIdx.x * kSimtTile;
     const int h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    {
-        float kv[kTileElems];
+    float kv[kTileElems];
 #pragma unroll
-        for (int k = 0; k < kTileElems; ++k) {
-            const int e = tid + k * kFwdThreads, t = e / D, d = e - t * D;
-            const int64_t n = t0 + t;
-            kv[k] = (e < kSimtTile * D && n < N) ? pr.scale * to_f(K[(((int64_t)b * N + n) * H + h) * D + d]) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < kTileElems; ++k) {
-            const int e = tid + k * kFwdThreads, t = e / D, d = e - t * D;
-            if (e < kSimtTile * D) Rs[t * ld + d] = kv[k];
-        }
+    for (int k = 0; k < kTileElems; ++k) {
+        const int e = tid + k * kFwdThreads, t = e / D, d = e - t * D;
+        const int64_t n = t0 + t;
+        kv[k] = (e < kSimtTile * D && n < N) ? pr.scale * to_f(K[(((int64_t)b * N + n) * H + h) * D + d]) : 0.f;
     }
+    bool k_stored = false;   // the K tile goes to shared memory with the first latent tile's loads in flight
     float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][kMaxDPerLane];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
@@ -480,6 +481,14 @@ dec_fwd_simt_kernel(Problem pr, const TQ *__restrict__ Q, const float *__restric
             const bool ok = e < kSimtRows * D && l0 + j < M;
             qv[k] = ok ? to_f(Qb[(int64_t)(l0 + j) * D + d]) : 0.f;
             zv[k] = ok ? Zb[(int64_t)(l0 + j) * D + d] : 0.f;
+        }
+        if (!k_stored) {
+#pragma unroll
+            for (int k = 0; k < kTileElems; ++k) {
+                const int e = tid + k * kFwdThreads, t = e / D, d = e - t * D;
+                if (e < kSimtTile * D) Rs[t * ld + d] = kv[k];
+            }
+            k_stored = true;
         }
         __syncthreads();
 #pragma unroll
