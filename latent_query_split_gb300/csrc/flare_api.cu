@@ -326,7 +326,7 @@ flare_status_t decode_run(const flare_dims_t *d, const void *Q, bool q_is_f32, c
         if (s != FLARE_OK) return s;
         e = launch_decode_tc(pr, Q, q_is_f32, Z, K, Y, di.sms, di.status, after_merge, st);
     } else {
-        e = launch_decode_simt(pr, Q, q_is_f32, Z, K, Y, st);
+        e = launch_decode_simt(pr, Q, q_is_f32, Z, K, Y, after_merge, st);
     }
     return e == cudaSuccess ? FLARE_OK : cuda_fail(e, "decode launch");
 }

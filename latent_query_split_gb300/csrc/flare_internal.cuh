@@ -79,8 +79,10 @@ cudaError_t launch_encoder_simt(const Problem &pr, const ShardPlan &plan, const 
                                 cudaStream_t st);
 cudaError_t launch_lse_merge(const float *O_r, const float *L_r, int R, int B, int H, int M,
                              int D, float *Z, float *L, cudaStream_t st);
+// after_encoder: the previous kernel in the stream is this library's encoder
+// that writes Z (the decode is launched as its programmatic dependent).
 cudaError_t launch_decode_simt(const Problem &pr, const void *Q, bool q_is_f32, const float *Z,
-                               const void *K, void *Y, cudaStream_t st);
+                               const void *K, void *Y, bool after_encoder, cudaStream_t st);
 cudaError_t launch_encoder_bwd_simt(const Problem &pr, const void *Q, const void *K,
                                     const void *V, const uint8_t *mask, const float *Z,
                                     const float *L, const float *dZ, float *dQ, void *dK,

@@ -283,6 +283,9 @@ enc_fwd_simt_kernel(Problem pr, ShardPlan plan, const TQ *__restrict__ Q,
     __shared__ int s_last;
     __shared__ float s_lmax[kSimtRows], s_a[kSimtRows];
 
+    // a programmatic dependent (the decode) may be scheduled once every CTA
+    // of this grid has started; it waits for this grid's results itself
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int c = blockIdx.x, h = blockIdx.y;
     const int b = blockIdx.z / mtiles, mt = blockIdx.z % mtiles;
     const int m0 = mt * kSimtRows;
@@ -463,6 +466,11 @@ dec_fwd_simt_kernel(Problem pr, const TQ *__restrict__ Q, const float *__restric
         kv[k] = (e < kSimtTile * D && n < N) ? pr.scale * to_f(K[(((int64_t)b * N + n) * H + h) * D + d]) : 0.f;
     }
     bool k_stored = false;   // the K tile goes to shared memory with the first latent tile's loads in flight
+    // Launched as a programmatic dependent of the encoder that writes Z (in
+    // flare_fwd / flare_pp_fwd), this CTA may start while that grid runs:
+    // the K loads above go ahead, Q and Z are read only once it has completed
+    // (a no-op for a launch without the attribute).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][kMaxDPerLane];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
@@ -765,9 +773,25 @@ cudaError_t launch_encoder_simt_dc(const Problem &pr, const ShardPlan &plan, con
     return cudaGetLastError();
 }
 
+// Launch with the programmatic-stream-serialization attribute when `pdl`.
+template <typename Kernel, typename... Args>
+cudaError_t launch_fwd(Kernel k, dim3 grid, size_t smem, cudaStream_t st, bool pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kFwdThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 template <int DC>
 cudaError_t launch_decode_simt_dc(const Problem &pr, const void *Q, bool q_is_f32, const float *Z,
-                                  const void *K, void *Y, cudaStream_t st) {
+                                  const void *K, void *Y, bool pdl, cudaStream_t st) {
     dim3 grid((pr.N + kSimtTile - 1) / kSimtTile, pr.H, pr.B);
     const size_t smem = sizeof(float) * ((size_t)kSimtTile * (pr.D + 1) +
                                          (size_t)kSimtRows * (pr.D + 1) + (size_t)kSimtRows * pr.D);
@@ -775,20 +799,20 @@ cudaError_t launch_decode_simt_dc(const Problem &pr, const void *Q, bool q_is_f3
     if (!pr.bf16) {
         auto k = dec_fwd_simt_kernel<float, float, DC>;
         if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-        k<<<grid, kFwdThreads, smem, st>>>(pr, (const float *)Q, Z, (const float *)K, (float *)Y);
+        e = launch_fwd(k, grid, smem, st, pdl, pr, (const float *)Q, Z, (const float *)K, (float *)Y);
     } else if (q_is_f32) {
         auto k = dec_fwd_simt_kernel<float, __nv_bfloat16, DC>;
         if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-        k<<<grid, kFwdThreads, smem, st>>>(pr, (const float *)Q, Z, (const __nv_bfloat16 *)K,
-                                        (__nv_bfloat16 *)Y);
+        e = launch_fwd(k, grid, smem, st, pdl, pr, (const float *)Q, Z, (const __nv_bfloat16 *)K,
+                       (__nv_bfloat16 *)Y);
     } else {
         auto k = dec_fwd_simt_kernel<__nv_bfloat16, __nv_bfloat16, DC>;
         if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-        k<<<grid, kFwdThreads, smem, st>>>(pr, (const __nv_bfloat16 *)Q, Z,
-                                        (const __nv_bfloat16 *)K, (__nv_bfloat16 *)Y);
+        e = launch_fwd(k, grid, smem, st, pdl, pr, (const __nv_bfloat16 *)Q, Z,
+                       (const __nv_bfloat16 *)K, (__nv_bfloat16 *)Y);
     }
     note_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 }  // namespace
 
@@ -817,11 +841,11 @@ cudaError_t launch_lse_merge(const float *O_r, const float *L_r, int R, int B, i
 }
 
 cudaError_t launch_decode_simt(const Problem &pr, const void *Q, bool q_is_f32, const float *Z,
-                               const void *K, void *Y, cudaStream_t st) {
+                               const void *K, void *Y, bool after_encoder, cudaStream_t st) {
     if (pr.B == 0 || pr.N == 0) return cudaSuccess;
-    if (pr.D <= 32) return launch_decode_simt_dc<32>(pr, Q, q_is_f32, Z, K, Y, st);
-    if (pr.D <= 64) return launch_decode_simt_dc<64>(pr, Q, q_is_f32, Z, K, Y, st);
-    return launch_decode_simt_dc<128>(pr, Q, q_is_f32, Z, K, Y, st);
+    if (pr.D <= 32) return launch_decode_simt_dc<32>(pr, Q, q_is_f32, Z, K, Y, after_encoder, st);
+    if (pr.D <= 64) return launch_decode_simt_dc<64>(pr, Q, q_is_f32, Z, K, Y, after_encoder, st);
+    return launch_decode_simt_dc<128>(pr, Q, q_is_f32, Z, K, Y, after_encoder, st);
 }
 
 namespace {
