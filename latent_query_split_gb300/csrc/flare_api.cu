@@ -529,6 +529,7 @@ flare_status_t flare_encoder_fwd(const flare_dims_t *dims, const void *Q, const 
                                  const int64_t *shard_offsets, int R, float *O_r, float *L_r,
                                  float *Z, float *L, void *workspace, size_t workspace_bytes,
                                  void *stream) {
+    FLARE_TRACE();
     flare_status_t s = check_dims(dims);
     if (s != FLARE_OK) return s;
     if ((s = check_offsets(shard_offsets, R, dims->N)) != FLARE_OK) return s;
@@ -538,6 +539,7 @@ flare_status_t flare_encoder_fwd(const flare_dims_t *dims, const void *Q, const 
 
 flare_status_t flare_lse_merge(const float *O_r, const float *L_r, int R, int B, int H, int M,
                                int D, float *Z, float *L, void *stream) {
+    FLARE_TRACE();
     if (R < 1 || B < 0 || H < 1 || M < 1 || D < 1)
         return fail(FLARE_ERR_INVALID_ARG, "bad sizes R=%d B=%d H=%d M=%d D=%d", R, B, H, M, D);
     if (B == 0) return FLARE_OK;
@@ -550,6 +552,7 @@ flare_status_t flare_lse_merge(const float *O_r, const float *L_r, int R, int B,
 
 flare_status_t flare_decode_fwd(const flare_dims_t *dims, const void *Q, const float *Z,
                                 const void *K, void *Y, void *stream) {
+    FLARE_TRACE();
     flare_status_t s = check_dims(dims);
     if (s != FLARE_OK) return s;
     return decode_run(dims, Q, false, Z, K, Y, false, (cudaStream_t)stream);
@@ -559,6 +562,7 @@ flare_status_t flare_fwd(const flare_dims_t *dims, const void *Q, const void *K,
                          const uint8_t *mask, const int64_t *shard_offsets, int R, void *Y,
                          float *Z, float *L, void *workspace, size_t workspace_bytes,
                          void *stream) {
+    FLARE_TRACE();
     flare_status_t s = check_dims(dims);
     if (s != FLARE_OK) return s;
     if ((s = check_offsets(shard_offsets, R, dims->N)) != FLARE_OK) return s;
@@ -579,6 +583,7 @@ flare_status_t flare_pp_fwd(const flare_dims_t *dims, const void *Qseed, const v
                             const int64_t *shard_offsets, int R, void *Y, float *Qdyn,
                             float *L1, float *Z, float *L2, void *workspace,
                             size_t workspace_bytes, void *stream) {
+    FLARE_TRACE();
     flare_status_t s = check_dims(dims);
     if (s != FLARE_OK) return s;
     if ((s = check_offsets(shard_offsets, R, dims->N)) != FLARE_OK) return s;
@@ -604,6 +609,7 @@ flare_status_t flare_encoder_bwd(const flare_dims_t *dims, const void *Q, const 
                                  const int64_t *shard_offsets, int R, const float *Z,
                                  const float *L, const float *dZ, float *dQ, void *dK, void *dV,
                                  void *workspace, size_t workspace_bytes, void *stream) {
+    FLARE_TRACE();
     flare_status_t s = check_dims(dims);
     if (s != FLARE_OK) return s;
     if ((s = check_offsets(shard_offsets, R, dims->N)) != FLARE_OK) return s;
@@ -617,6 +623,7 @@ flare_status_t flare_encoder_bwd_accumulate(const flare_dims_t *dims, const void
                                             const float *L, const float *dZ, float *dQ, void *dK,
                                             void *dV, void *workspace, size_t workspace_bytes,
                                             void *stream) {
+    FLARE_TRACE();
     flare_status_t s = check_dims(dims);
     if (s != FLARE_OK) return s;
     if ((s = check_offsets(shard_offsets, R, dims->N)) != FLARE_OK) return s;
@@ -627,6 +634,7 @@ flare_status_t flare_encoder_bwd_accumulate(const flare_dims_t *dims, const void
 flare_status_t flare_decode_bwd(const flare_dims_t *dims, const void *Q, const float *Z,
                                 const void *K, const void *dY, float *dQ, float *dZ, void *dK,
                                 void *workspace, size_t workspace_bytes, void *stream) {
+    FLARE_TRACE();
     flare_status_t s = check_dims(dims);
     if (s != FLARE_OK) return s;
     return decode_bwd_run(dims, Q, Z, K, dY, dQ, dZ, dK, workspace, workspace_bytes,
@@ -637,6 +645,7 @@ flare_status_t flare_bwd(const flare_dims_t *dims, const void *Q, const void *K,
                          const uint8_t *mask, const int64_t *shard_offsets, int R, const float *Z,
                          const float *L, const void *dY, float *dQ, void *dK, void *dV,
                          void *workspace, size_t workspace_bytes, void *stream) {
+    FLARE_TRACE();
     flare_status_t s = check_dims(dims);
     if (s != FLARE_OK) return s;
     if ((s = check_offsets(shard_offsets, R, dims->N)) != FLARE_OK) return s;
@@ -670,6 +679,7 @@ flare_status_t flare_pp_bwd(const flare_dims_t *dims, const void *Qseed, const v
                             const float *L1, const float *Z, const float *L2, const void *dY,
                             float *dQseed, void *dKt, void *dVt, void *dK, void *dV, float *dQdyn,
                             void *workspace, size_t workspace_bytes, void *stream) {
+    FLARE_TRACE();
     flare_status_t s = check_dims(dims);
     if (s != FLARE_OK) return s;
     if ((s = check_offsets(shard_offsets, R, dims->N)) != FLARE_OK) return s;
@@ -718,6 +728,7 @@ flare_status_t flare_pp_bwd(const flare_dims_t *dims, const void *Qseed, const v
 }
 
 flare_status_t flare_check_bounded_wait(unsigned limit_us, void *stream) {
+    FLARE_TRACE();
     if (limit_us < 1 || limit_us > 1000000)
         return fail(FLARE_ERR_INVALID_ARG, "limit_us=%u outside [1, 1000000]", limit_us);
     DeviceInfo di;
@@ -728,6 +739,7 @@ flare_status_t flare_check_bounded_wait(unsigned limit_us, void *stream) {
 }
 
 flare_status_t flare_device_status(void *stream) {
+    FLARE_TRACE();
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     unsigned v = 0;

@@ -14,9 +14,23 @@
 
 #include "../../include/flare.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace flare {
 
 constexpr int kMaxShards = FLARE_MAX_SHARDS;
+
+// An NVTX range over one entry point, named after it: Nsight tools show each
+// library call with the kernels it launched (`ncu --nvtx --nvtx-include
+// "flare_fwd/"` profiles only the launches of flare_fwd). Without an attached
+// tool a push or pop costs one pointer test.
+struct TraceRange {
+    explicit TraceRange(const char *name) { nvtxRangePushA(name); }
+    ~TraceRange() { nvtxRangePop(); }
+    TraceRange(const TraceRange &) = delete;
+    TraceRange &operator=(const TraceRange &) = delete;
+};
+#define FLARE_TRACE() ::flare::TraceRange flare_trace_range_(__func__)
 
 // Shard offsets and their chunking, passed to kernels by value (about 3 KB of
 // kernel parameters at the maximum shard count).

@@ -48,6 +48,7 @@ flare_status_t scratch_on_current_device(void **out) {
 extern "C" FLARE_API flare_status_t flare_encoder_fwd_noalloc(
     const flare_dims_t *dims, const void *Q, const void *K, const void *V, const uint8_t *mask,
     const int64_t *shard_offsets, int R, float *O_r, float *L_r, float *Z, float *L, void *stream) {
+    FLARE_TRACE();
     const size_t need = flare::encoder_workspace_size(dims, shard_offsets, R);
     if (need == (size_t)-1)
         return flare::encoder_fwd_with_workspace(dims, Q, K, V, mask, shard_offsets, R, O_r, L_r, Z,
