@@ -28,6 +28,15 @@
 //  * dbw_reduce_kernel: dQ and dZ = the sums of the pieces in piece order.
 // Warp roles: warp 0 TMA producer (K, dY ring; Q, Z on every (b, h) change),
 // warp 1 TMEM allocator and MMA issuer (lane 0), warps 2-9 the two halves.
+//
+// M = 256: S^T and G^T of one tile would fill all 512 TMEM columns, so the
+// row statistics come first from dbs_stats_kernel (for every token, over all
+// 256 latents: lse2_n = log2 sum_m 2^(s log2e <K_n, Q_m>) and r_n =
+// sum_m A_nm g_nm), and dbw_tc_kernel<128, 3, true> then runs once per half
+// of the latent rows with those statistics instead of its own (A_nm =
+// 2^(s log2e <K_n, Q_m> - lse2_n), no exchange between the halves); the
+// second pass's dK share goes to a scratch tensor that is added to the
+// first's.
 #pragma once
 
 #include "tc_backward.cuh"
@@ -39,6 +48,10 @@ namespace tc {
 
 struct DbwArgs {
     int B, H, M, N;
+    // latent rows [m0, m0 + M) of M_all (Q and Z tiles, dQ and dZ pieces);
+    // with precomputed statistics (M = 256), one (lse2, r) per token
+    int m0, M_all;
+    const float2 *stats;        // [B*H][N]
     float sl2;                  // s * log2(e)
     float s;                    // score scale
     int q_per_batch;            // Q has a batch dimension
@@ -116,7 +129,263 @@ __global__ void __launch_bounds__(256) dbw_reduce_kernel(const float *__restrict
     reinterpret_cast<float4 *>(which ? dZ : dQ)[bh * per + rem] = acc;
 }
 
-template <int M, int STAGES>
+// dK += dK2, both bf16 (the two latent halves' shares of the M = 256 dK).
+__global__ void __launch_bounds__(256) dbw_add_kernel(uint4 *__restrict__ dK, const uint4 *__restrict__ dK2,
+                                                      int64_t n8) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n8) return;
+    uint4 x = dK[i];
+    const uint4 y = __ldcs(dK2 + i);
+    uint32_t *xp = &x.x;
+    const uint32_t *yp = &y.x;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 u = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(xp + q));
+        const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(yp + q));
+        xp[q] = pack_bf16(u.x + v.x, u.y + v.y);
+    }
+    dK[i] = x;
+}
+
+// ---- the row statistics of the M = 256 decode backward ----------------------
+struct DbsArgs {
+    int B, H, N;
+    float sl2;                  // s * log2(e)
+    int q_per_batch;
+    float2 *stats;              // [B*H][N]: (lse2, r)
+    int64_t T_bh, T_total;
+    int grid;
+    unsigned *status;
+};
+
+struct DbsCfg {
+    static constexpr int M = 256, TILE = 128, STAGES = 3;
+    static constexpr int THREADS = 192;                     // producer, MMA issuer, four row warps
+    static constexpr uint32_t TILE_BYTES = TILE * 128;      // 128 rows x 64 bf16 (swizzled)
+    static constexpr uint32_t QZ_BYTES = M * 128;           // [256][64] bf16 (swizzled)
+    static constexpr uint32_t Q_OFF = 0;
+    static constexpr uint32_t ZB_OFF = Q_OFF + QZ_BYTES;
+    static constexpr uint32_t STAGE_OFF = ZB_OFF + QZ_BYTES;
+    static constexpr uint32_t STAGE_BYTES = 2 * TILE_BYTES;   // K tile, then dY tile
+    static constexpr uint32_t BAR_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
+    // full[S], empty[S], qz_full, qz_free, s_full, s_free, drain
+    static constexpr int NBAR = 2 * STAGES + 5;
+    static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr uint32_t BYTES = MISC_OFF + 64;
+    static constexpr uint32_t ALLOC = BYTES + 1024;
+    static_assert(ALLOC <= 232448, "shared memory budget of one CTA exceeded");
+    static constexpr uint32_t S_COL = 0, G_COL = 256, TMEM_COLS = 512;
+};
+
+// One persistent CTA per SM over a contiguous span of 128-token tiles in
+// (b, h, tile) order. Per tile: S^T = K Q^T and G^T = dY Z^T (256 latents
+// each, all of TMEM); each of four warps takes the 32 token rows of its lane
+// quadrant and folds the 256 latents in chunks of 32 with a running maximum:
+// l = sum 2^(t - m), rg = sum 2^(t - m) g, then lse2 = m + log2 l and r = rg / l.
+__global__ void __launch_bounds__(DbsCfg::THREADS, 1)
+dbs_stats_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmdY,
+                 const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmZ,
+                 const DbsArgs a) {
+    using C = DbsCfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + C::Q_OFF, sZ = sbase + C::ZB_OFF, sStage = sbase + C::STAGE_OFF;
+    const uint32_t bar0 = sbase + C::BAR_OFF;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    const uint32_t qz_full = bar0 + 8u * (2 * C::STAGES), qz_free = qz_full + 8;
+    const uint32_t s_full = qz_full + 16, s_free = qz_full + 24, drain = qz_full + 32;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const int64_t tb = ((int64_t)cta * a.T_total + a.grid - 1) / a.grid;
+    const int64_t te = ((int64_t)(cta + 1) * a.T_total + a.grid - 1) / a.grid;
+    const int64_t ntiles = te - tb;
+    const int64_t bh0 = tb / a.T_bh, k0 = tb - bh0 * a.T_bh;
+    Waiter wt{abort_flag, a.status};
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(qz_full, 1);
+        mbar_init(qz_free, 1);
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 4);          // one arrival per row warp
+        mbar_init(drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmdY);
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmZ);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        const uint64_t pol = policy_evict_first();
+        int64_t bh = bh0, kt = k0, cur = -1;
+        int b = (int)(bh0 / a.H), h = (int)(bh0 - (int64_t)b * a.H);
+        int u = -1;
+        int64_t j = 0;
+        for (; j < ntiles && !wt.aborted(); ++j) {
+            if (bh != cur) {
+                ++u;
+                cur = bh;
+                // Q and Z of the previous (b, h) are no longer read
+                if (u > 0 && !__all_sync(0xffffffffu, wt.wait_inline(qz_free, (uint32_t)(u - 1) & 1))) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(qz_full, 2 * C::QZ_BYTES);
+                    if (dcheck(h >= 0 && h < a.H && b >= 0 && b < a.B, kChkDbwQ, a.status)) {
+                        tma_load_4d(sQ, &tmQ, 0, 0, h, a.q_per_batch ? b : 0, qz_full);
+                        tma_load_4d(sZ, &tmZ, 0, 0, h, b, qz_full);
+                    }
+                }
+                __syncwarp();
+            }
+            const int s = (int)(j % C::STAGES);
+            if (!__all_sync(0xffffffffu, wt.wait_inline(empty(s), ((uint32_t)(j / C::STAGES) & 1) ^ 1))) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full(s), C::STAGE_BYTES);
+                const uint32_t dst = sStage + s * C::STAGE_BYTES;
+                if (dcheck(tile_in_tensor(0, h, kt * 128, b, a.H, a.N, a.B) && kt < a.T_bh, kChkDbwKV, a.status)) {
+                    tma_load_4d_hint(dst, &tmK, 0, h, (int)(kt * 128), b, full(s), pol);
+                    tma_load_4d_hint(dst + C::TILE_BYTES, &tmdY, 0, h, (int)(kt * 128), b, full(s), pol);
+                }
+            }
+            __syncwarp();
+            if (++kt == a.T_bh) {
+                kt = 0;
+                ++bh;
+                if (++h == a.H) {
+                    h = 0;
+                    ++b;
+                }
+            }
+        }
+        if (wt.aborted() && lane == 0) {
+            const uint64_t t0 = globaltimer();
+            for (int64_t jj = (j > C::STAGES ? j - C::STAGES : 0); jj < j; ++jj)
+                while (!mbar_try_wait(full((int)(jj % C::STAGES)), (uint32_t)(jj / C::STAGES) & 1) &&
+                       globaltimer() - t0 < 500000000ull) {
+                }
+            if (u >= 0)
+                while (!mbar_try_wait(qz_full, (uint32_t)u & 1) && globaltimer() - t0 < 500000000ull) {
+                }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (lane 0) ----------------
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16(128, 256, 0, 0);
+            const uint64_t dQk = desc_sw128(sQ, 16, 1024);
+            const uint64_t dZk = desc_sw128(sZ, 16, 1024);
+            int64_t bh = bh0, kt = k0, cur = -1;
+            int u = -1;
+            bool ok = true;
+            for (int64_t j = 0; j < ntiles && ok; ++j) {
+                if (bh != cur) {
+                    ++u;
+                    cur = bh;
+                    if (!(ok = wt.wait_inline(qz_full, (uint32_t)u & 1))) break;
+                }
+                const int s = (int)(j % C::STAGES);
+                if (!(ok = wt.wait_inline(full(s), (uint32_t)(j / C::STAGES) & 1))) break;
+                // the row warps have read the previous tile's S and G
+                if (j > 0 && !(ok = wt.wait_inline(s_free, (uint32_t)(j - 1) & 1))) break;
+                tc_fence_after();
+                const uint64_t dK = desc_sw128(sStage + s * C::STAGE_BYTES, 16, 1024);
+                const uint64_t dY = desc_sw128(sStage + s * C::STAGE_BYTES + C::TILE_BYTES, 16, 1024);
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb)
+                    umma_bf16_ss(tmem + C::S_COL, dK + 2 * kb, dQk + 2 * kb, idS, kb > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb)
+                    umma_bf16_ss(tmem + C::G_COL, dY + 2 * kb, dZk + 2 * kb, idS, kb > 0 ? 1u : 0u);
+                umma_commit(s_full);
+                umma_commit(empty(s));
+                if (++kt == a.T_bh) {
+                    kt = 0;
+                    ++bh;
+                    umma_commit(qz_free);   // the (b, h)'s last S and G read Q and Z
+                }
+            }
+            if (wt.aborted()) {
+                umma_commit(drain);
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < 500000000ull) {
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- row warps (warps 2-5, one per lane quadrant) ----------------
+        const int quad = warp & 3;
+        const int rig = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const float sl2 = a.sl2;
+        int64_t bh = bh0, kt = k0;
+        for (int64_t j = 0; j < ntiles; ++j) {
+            if (!__all_sync(0xffffffffu, wt.wait_inline(s_full, (uint32_t)j & 1))) break;
+            tc_fence_after();
+            float m = -INFINITY, l = 0.f, rg = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+                uint32_t sv[32], gv[32];
+                tmem_ld32(tmem + C::S_COL + 32 * c + lane_off, sv);
+                tmem_ld32(tmem + C::G_COL + 32 * c + lane_off, gv);
+                tmem_wait_ld();
+                if (c == 7) {
+                    // S and G are in registers: the next tile's may be computed
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(s_free);
+                }
+                float cm = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) cm = fmaxf(cm, __uint_as_float(sv[i]) * sl2);
+                if (cm > m) {
+                    const float f = (m == -INFINITY) ? 0.f : ex2(m - cm);
+                    l *= f;
+                    rg *= f;
+                    m = cm;
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p = ex2(fmaf(__uint_as_float(sv[i]), sl2, -m));
+                    l += p;
+                    rg = fmaf(p, __uint_as_float(gv[i]), rg);
+                }
+            }
+            const int64_t n = kt * 128 + rig;
+            if (n < a.N) a.stats[bh * a.N + n] = make_float2(m + __log2f(l), rg / l);
+            if (++kt == a.T_bh) {
+                kt = 0;
+                ++bh;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template <int M, int STAGES, bool ST = false>
 __global__ void __launch_bounds__(DbwCfg<M, STAGES>::THREADS, 1)
 dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmdY,
               const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmZ,
@@ -208,8 +477,8 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 if (lane == 0) {
                     mbar_arrive_expect_tx(qz_full, 2 * C::QZ_BYTES);
                     if (dcheck(h >= 0 && h < a.H && b >= 0 && b < a.B, kChkDbwQ, a.status)) {
-                        tma_load_4d(sQ, &tmQ, 0, 0, h, a.q_per_batch ? b : 0, qz_full);
-                        tma_load_4d(sZ, &tmZ, 0, 0, h, b, qz_full);
+                        tma_load_4d(sQ, &tmQ, 0, a.m0, h, a.q_per_batch ? b : 0, qz_full);
+                        tma_load_4d(sZ, &tmZ, 0, a.m0, h, b, qz_full);
                     }
                 }
                 __syncwarp();
@@ -415,7 +684,7 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 if (rig < M) {
                     const int piece = cta - bwd_cta_of(bhp * a.T_bh, a.T_total, a.grid);
                     float4 *dst = reinterpret_cast<float4 *>(
-                        a.part + (((bhp * a.P_max + piece) * 2 + hf) * M + rig) * 64);
+                        a.part + (((bhp * a.P_max + piece) * 2 + hf) * a.M_all + a.m0 + rig) * 64);
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
@@ -449,23 +718,33 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             const bool last = (j + 1 == ntiles) || bhN != bh;
             const int64_t n = kt * 128 + rig;
             const bool valid = n < a.N;
+            // ST: the token's (lse2, r) over all latents, computed beforehand
+            float2 stv = make_float2(0.f, 0.f);
+            if constexpr (ST) {
+                if (valid) stv = __ldg(a.stats + bh * a.N + n);
+            }
             if (!(ok = wwait(s_full, (uint32_t)j & 1))) break;
             tc_fence_after();
-            // this half's scores: the maximum, exchanged with the other half
             uint32_t sv[W / 32][32];
 #pragma unroll
             for (int c = 0; c < W / 32; ++c) tmem_ld32(s_tm + 32 * c, sv[c]);
             tmem_wait_ld();
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < W / 32; ++c)
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    mx = max3(mx, __uint_as_float(sv[c][2 * i]), __uint_as_float(sv[c][2 * i + 1]));
             const int par = (int)(j & 1);
-            xm[(par * 2 + hf) * 128 + rig] = mx;
-            named_bar_sync(pair_bar, 64);
-            const float m2 = fmaxf(mx, xm[(par * 2 + (hf ^ 1)) * 128 + rig]) * sl2;
+            float m2;
+            if constexpr (ST) {
+                m2 = stv.x;                               // p = 2^(s log2e t - lse2) = A
+            } else {
+                // this half's scores: the maximum, exchanged with the other half
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < W / 32; ++c)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        mx = max3(mx, __uint_as_float(sv[c][2 * i]), __uint_as_float(sv[c][2 * i + 1]));
+                xm[(par * 2 + hf) * 128 + rig] = mx;
+                named_bar_sync(pair_bar, 64);
+                m2 = fmaxf(mx, xm[(par * 2 + (hf ^ 1)) * 128 + rig]) * sl2;
+            }
             // p = 2^(s t log2 e - max), the half's partial sum and <p, g>
             uint32_t gv[W / 32][32];
 #pragma unroll
@@ -495,19 +774,25 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                     lr2[i & 1] = fma2(p2, f2pack(__uint_as_float(gv[c][2 * i]), __uint_as_float(gv[c][2 * i + 1])),
                                       lr2[i & 1]);
                 }
-            float ls, lr;
-            {
-                float x0, x1, x2, x3;
-                f2unpack(add2(ls2[0], ls2[1]), x0, x1);
-                f2unpack(add2(lr2[0], lr2[1]), x2, x3);
-                ls = x0 + x1;
-                lr = x2 + x3;
+            float inv, r;
+            if constexpr (ST) {
+                inv = valid ? 1.f : 0.f;                  // p is A already; tokens past N: A = 0
+                r = stv.y;
+            } else {
+                float ls, lr;
+                {
+                    float x0, x1, x2, x3;
+                    f2unpack(add2(ls2[0], ls2[1]), x0, x1);
+                    f2unpack(add2(lr2[0], lr2[1]), x2, x3);
+                    ls = x0 + x1;
+                    lr = x2 + x3;
+                }
+                xl[(par * 2 + hf) * 128 + rig] = make_float2(ls, lr);
+                named_bar_sync(pair_bar, 64);
+                const float2 o = xl[(par * 2 + (hf ^ 1)) * 128 + rig];
+                inv = valid ? 1.f / (ls + o.x) : 0.f;      // tokens past N: A = 0
+                r = (lr + o.y) / (ls + o.x);
             }
-            xl[(par * 2 + hf) * 128 + rig] = make_float2(ls, lr);
-            named_bar_sync(pair_bar, 64);
-            const float2 o = xl[(par * 2 + (hf ^ 1)) * 128 + rig];
-            const float inv = valid ? 1.f / (ls + o.x) : 0.f;      // tokens past N: A = 0
-            const float r = (lr + o.y) / (ls + o.x);
             // s dT into DT_COL once dK of the previous tile (which read it) is
             // done; A^T and s dT^T into the MN-major operands of dZ and dQ once
             // the previous tile's products have read them

@@ -406,15 +406,19 @@ cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *
     return cudaGetLastError();
 }
 
-bool tc_decode_bwd_supported(bool bf16, int M, int D) { return bf16 && D == 64 && (M == 64 || M == 128); }
+bool tc_decode_bwd_supported(bool bf16, int M, int D) {
+    return bf16 && D == 64 && (M == 64 || M == 128 || M == 256);
+}
 
 namespace {
 // Decode-backward workspace: Z in bf16 [B*H*M*64] and the dQ/dZ pieces
-// [B*H][P_max][2][M][64]; tiles and spans as for the encoder backward.
+// [B*H][P_max][2][M][64]; tiles and spans as for the encoder backward. M = 256
+// adds the per-token statistics [B*H][N] (lse2, r) and the second half's dK
+// share [B][N][H][64] bf16.
 struct DbwLayout {
     int64_t T_bh, T_total;
     int grid, P_max;
-    size_t zb, part, bytes;
+    size_t zb, part, stats, dk2, bytes;
 };
 
 void dbw_layout(const Problem &pr, int sms, DbwLayout &l) {
@@ -430,16 +434,33 @@ void dbw_layout(const Problem &pr, int sms, DbwLayout &l) {
     o += align256(2 * bhm * 64);
     l.part = o;
     o += align256(4 * bhm * (size_t)l.P_max * 2 * 64);
+    l.stats = l.dk2 = o;
+    if (pr.M > 128) {
+        const size_t bhn = (size_t)pr.B * pr.H * (size_t)pr.N;
+        o += align256(8 * bhn);
+        l.dk2 = o;
+        o += align256(2 * bhn * 64);
+    }
     l.bytes = o;
 }
 
-template <int M>
+template <int M, bool ST = false>
 cudaError_t launch_dbw(const CUtensorMap *maps, const tc::DbwArgs &a, cudaStream_t st) {
     using C = tc::DbwCfg<M, 3>;
-    auto k = tc::dbw_tc_kernel<M, 3>;
+    auto k = tc::dbw_tc_kernel<M, 3, ST>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
     if (e != cudaSuccess) return e;
     k<<<a.grid, C::THREADS, C::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dbs(const CUtensorMap *maps, const tc::DbsArgs &a, cudaStream_t st) {
+    using C = tc::DbsCfg;
+    cudaError_t e = cudaFuncSetAttribute(tc::dbs_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::ALLOC);
+    if (e != cudaSuccess) return e;
+    tc::dbs_stats_kernel<<<a.grid, C::THREADS, C::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], a);
     note_launch();
     return cudaGetLastError();
 }
@@ -474,17 +495,22 @@ cudaError_t launch_decode_bwd_tc(const Problem &pr, const void *Q, const float *
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t qb = pr.q_bstride == 0 ? 1 : pr.B;
+    // the tile kernel's latent rows per launch: all of them, or one half of 256
+    const uint32_t Mp = pr.M > 128 ? 128 : (uint32_t)pr.M;
     CUtensorMap maps[5];
     if (!make_map(&maps[0], K, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
         !make_map(&maps[1], dY, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
-        !make_map(&maps[2], Q, pr.D, pr.M, pr.H, qb, (uint32_t)pr.M, 1) ||
-        !make_map(&maps[3], zb, pr.D, pr.M, pr.H, pr.B, (uint32_t)pr.M, 1) ||
+        !make_map(&maps[2], Q, pr.D, pr.M, pr.H, qb, Mp, 1) ||
+        !make_map(&maps[3], zb, pr.D, pr.M, pr.H, pr.B, Mp, 1) ||
         !make_map(&maps[4], dK, pr.D, pr.H, pr.N, pr.B, 1, 32))
         return cudaErrorInvalidValue;
     tc::DbwArgs a;
     a.B = pr.B;
     a.H = pr.H;
-    a.M = pr.M;
+    a.M = (int)Mp;
+    a.m0 = 0;
+    a.M_all = pr.M;
+    a.stats = nullptr;
     a.N = pr.N;
     a.s = pr.scale;
     a.sl2 = pr.scale * 1.4426950408889634f;
@@ -495,8 +521,44 @@ cudaError_t launch_decode_bwd_tc(const Problem &pr, const void *Q, const float *
     a.T_total = l.T_total;
     a.grid = l.grid;
     a.status = status;
-    e = pr.M == 128 ? launch_dbw<128>(maps, a, st) : launch_dbw<64>(maps, a, st);
-    if (e != cudaSuccess) return e;
+    if (pr.M <= 128) {
+        e = pr.M == 128 ? launch_dbw<128>(maps, a, st) : launch_dbw<64>(maps, a, st);
+        if (e != cudaSuccess) return e;
+    } else {
+        // M = 256: the token statistics over all latents, then one pass per
+        // half of the latents; the second half's dK share is added after
+        float2 *stats = (float2 *)(w + l.stats);
+        __nv_bfloat16 *dk2 = (__nv_bfloat16 *)(w + l.dk2);
+        CUtensorMap smaps[4], dk2map;
+        if (!make_map(&smaps[0], K, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
+            !make_map(&smaps[1], dY, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
+            !make_map(&smaps[2], Q, pr.D, pr.M, pr.H, qb, (uint32_t)pr.M, 1) ||
+            !make_map(&smaps[3], zb, pr.D, pr.M, pr.H, pr.B, (uint32_t)pr.M, 1) ||
+            !make_map(&dk2map, dk2, pr.D, pr.H, pr.N, pr.B, 1, 32))
+            return cudaErrorInvalidValue;
+        tc::DbsArgs sa;
+        sa.B = pr.B;
+        sa.H = pr.H;
+        sa.N = pr.N;
+        sa.sl2 = a.sl2;
+        sa.q_per_batch = a.q_per_batch;
+        sa.stats = stats;
+        sa.T_bh = l.T_bh;
+        sa.T_total = l.T_total;
+        sa.grid = l.grid;
+        sa.status = status;
+        if ((e = launch_dbs(smaps, sa, st)) != cudaSuccess) return e;
+        a.stats = stats;
+        if ((e = launch_dbw<128, true>(maps, a, st)) != cudaSuccess) return e;
+        a.m0 = 128;
+        maps[4] = dk2map;
+        if ((e = launch_dbw<128, true>(maps, a, st)) != cudaSuccess) return e;
+        const int64_t n8 = (int64_t)pr.B * pr.N * pr.H * 8;     // uint4s of dK
+        tc::dbw_add_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(
+            (uint4 *)dK, (const uint4 *)dk2, n8);
+        note_launch();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     const int64_t n4 = 2 * BH * pr.M * 16;
     tc::dbw_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(part, dQ, dZ, BH, pr.M, l.P_max,
                                                                        l.T_bh, l.T_total, l.grid);

@@ -172,7 +172,8 @@ def test_encoder_bwd_multi_tile_spans(cuda_device, kernel, M, replicated):
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dt,M,D,N,replicated", [("f32", 16, 32, 700, True), ("bf16", 128, 64, 3000, True),
                                                  ("bf16", 64, 64, 2100, False), ("bf16", 64, 128, 1100, True),
-                                                 ("bf16", 256, 64, 900, True), ("f32", 37, 40, 333, False)])
+                                                 ("bf16", 256, 64, 900, True), ("bf16", 256, 64, 9000, False),
+                                                 ("f32", 37, 40, 333, False)])
 def test_decode_bwd(cuda_device, kernel, dt, M, D, N, replicated):
     B, H = 2, 2
     Q, K, _, _ = _problem(18, B, H, M, N, D, dt, [0, N], pad=0, q_std=1.0, replicated=replicated)
