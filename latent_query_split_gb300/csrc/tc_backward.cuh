@@ -35,6 +35,14 @@
 // dQ = dQ + the encoder's share: the dK epilogue prefetches the tile's rows of
 // the old dK with cp.async at the start of the tile and adds them in fp32
 // before rounding once.
+// D = 128 (M = 64) runs as two passes over the tokens, one per 64-column half
+// of the outputs: each pass contracts S and dP over all 128 columns (K, V,
+// Q and dZ tiles of two 64-column atoms each) and computes dV, dK and dQ for
+// its half (the TMEM columns of D = 64); the dQ partials of each pass have
+// their own piece array. The shared memory of two 64 KB K/V stages leaves
+// no room for the old-dK rows beside the output staging, so at M = 64 those
+// rows sit in the upper atom of the s dS^T buffer: that atom feeds latent
+// rows 64..127 of the dQ MMA, whose output lanes are never read.
 // Warp roles of bwd_tc_kernel: warp 0 TMA producer (K, V ring; Q, dZ and the
 // row statistics on every (b, h) change), warp 1 TMEM allocator and MMA
 // issuer (lane 0), warps 2-9 two halves of four warps, each half owning M/2
@@ -62,7 +70,8 @@ struct BwdArgs {
     int q_per_batch;            // Q has a batch dimension
     const uint8_t *mask;        // [B, N] or null
     const float *lc;            // [B*H][2][M]: -L log2(e) (or -inf), then -s c
-    float *part;                // [B*H][P_max][M][64] dQ partials
+    float *part;                // [B*H][P_max][M][64] dQ partials (of this pass's column half)
+    int dh;                     // D = 128: the output column half [64 dh, 64 dh + 64)
     const __nv_bfloat16 *dk_acc;  // with ACC: dK = dk_acc + this share (dk_acc may be dK)
     const __nv_bfloat16 *dv_acc;  // with ACCV: dV = dv_acc + this share (dv_acc may be dV)
     int P_max;
@@ -76,16 +85,18 @@ __host__ __device__ __forceinline__ int bwd_cta_of(int64_t t, int64_t T_total, i
     return (int)((t * grid) / T_total);
 }
 
-template <int M_, int STAGES_, bool ACCV_ = false>
+template <int M_, int STAGES_, bool ACCV_ = false, int D_ = 64>
 struct BwdCfg {
-    static constexpr int M = M_, D = 64, TILE = 128, STAGES = STAGES_;
+    static constexpr int M = M_, D = D_, TILE = 128, STAGES = STAGES_;
+    static constexpr int DA = D / 64;                      // 64-column atoms of a row
     static constexpr int THREADS = 320;
     static constexpr uint32_t TILE_BYTES = TILE * 128;     // 128 rows x 64 bf16 (swizzled)
-    static constexpr uint32_t QZ_BYTES = M * 128;          // [M][64] bf16 (swizzled)
+    static constexpr uint32_t QZA = M * 128;               // one [M][64] bf16 atom (swizzled)
+    static constexpr uint32_t QZ_BYTES = DA * QZA;         // Q (or dZ): its atoms in column order
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t DZ_OFF = Q_OFF + QZ_BYTES;
     static constexpr uint32_t STAGE_OFF = DZ_OFF + QZ_BYTES;
-    static constexpr uint32_t STAGE_BYTES = 2 * TILE_BYTES; // K tile, then V tile
+    static constexpr uint32_t STAGE_BYTES = 2 * DA * TILE_BYTES; // K atoms, then V atoms
     // s dS^T in bf16: token rows of 64-latent atoms (atom a at a * TILE_BYTES)
     static constexpr uint32_t DS_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
     static constexpr uint32_t DS_BYTES = 2 * TILE_BYTES;
@@ -93,14 +104,16 @@ struct BwdCfg {
     static constexpr uint32_t OUT_BYTES = 2 * TILE_BYTES;
     // rows of the old dK being accumulated into (one 128-byte row per thread
     // of the dK half, 16-byte chunks XOR-swizzled by the row)
-    static constexpr uint32_t DKIN_OFF = OUT_OFF + OUT_BYTES;
-    static constexpr uint32_t DKIN_BYTES = TILE_BYTES;
+    // (D = 128 at M = 64: the upper atom of the s dS^T buffer)
+    static constexpr bool DKIN_IN_DS = DA == 2 && M <= 64;
+    static constexpr uint32_t DKIN_OFF = DKIN_IN_DS ? DS_OFF + TILE_BYTES : OUT_OFF + OUT_BYTES;
+    static constexpr uint32_t DKIN_BYTES = DKIN_IN_DS ? 0 : TILE_BYTES;
     // the same for the old dV rows (ACCV: the second latent pass of M = 256)
-    static constexpr uint32_t DVIN_OFF = DKIN_OFF + DKIN_BYTES;
+    static constexpr uint32_t DVIN_OFF = OUT_OFF + OUT_BYTES + DKIN_BYTES;
     static constexpr uint32_t DVIN_BYTES = ACCV_ ? TILE_BYTES : 0;
-    // row statistics of two (b, h) generations: [2][-L2 (128), -s c (128)]
+    // row statistics of two (b, h) generations: [2][-L2 (M), -s c (M)]
     static constexpr uint32_t LC_OFF = DVIN_OFF + DVIN_BYTES;
-    static constexpr uint32_t LC_BYTES = 2 * 2 * 128 * 4;
+    static constexpr uint32_t LC_BYTES = 2 * 2 * M * 4;
     static constexpr uint32_t BAR_OFF = LC_OFF + LC_BYTES;
     // full[S], empty[S], qd_full, qd_free, lc_full[2], s_full, p_full,
     // ds_free, dvdk_full, dvdk_free, dq_full, dq_free, drain, sdp_free
@@ -118,22 +131,26 @@ struct BwdCfg {
 };
 
 // ---- prologue: dZ in bf16 and the per-row constants -----------------------------
-// One warp per latent row (D = 64: two elements per lane).
+// One warp per latent row of D (64 or 128) columns, two per lane at a time.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const float *__restrict__ Z,
                                                        const float *__restrict__ L,
                                                        const float *__restrict__ dZ,
                                                        __nv_bfloat16 *__restrict__ dZb,
                                                        float *__restrict__ lc, int64_t rows, int M,
-                                                       float s) {
+                                                       float s, int D) {
     const int lane = threadIdx.x & 31;
     const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (r >= rows) return;
-    const float2 z = reinterpret_cast<const float2 *>(Z + r * 64)[lane];
-    const float2 g = reinterpret_cast<const float2 *>(dZ + r * 64)[lane];
-    float c = z.x * g.x + z.y * g.y;
+    float c = 0.f;
+    for (int k = lane; k < D / 2; k += 32) {
+        const float2 z = reinterpret_cast<const float2 *>(Z + r * D)[k];
+        const float2 g = reinterpret_cast<const float2 *>(dZ + r * D)[k];
+        c = fmaf(z.x, g.x, c);
+        c = fmaf(z.y, g.y, c);
+        reinterpret_cast<uint32_t *>(dZb + r * D)[k] = pack_bf16(g.x, g.y);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-    reinterpret_cast<uint32_t *>(dZb + r * 64)[lane] = pack_bf16(g.x, g.y);
     if (lane == 0) {
         const int64_t bh = r / M;
         const int m = (int)(r - bh * M);
@@ -144,20 +161,26 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const float *__restrict__
 }
 
 // ---- dQ = sum over the pieces of each (b, h) ------------------------------------
+// The pieces of column half dh (D = 128: one piece array per pass) start at
+// part + dh * half_stride floats; each holds [B*H][P_max][M][64].
 __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const float *__restrict__ part,
                                                             float *__restrict__ dQ, int64_t BH, int M,
                                                             int P_max, int64_t T_bh, int64_t T_total,
-                                                            int grid, int accumulate) {
-    const int64_t per_bh = (int64_t)M * 16;                 // float4s of one (b, h)
+                                                            int grid, int accumulate, int D,
+                                                            int64_t half_stride) {
+    const int64_t per_bh = (int64_t)M * (D / 4);            // float4s of one (b, h)
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= BH * per_bh) return;
     const int64_t bh = i / per_bh, rem = i - bh * per_bh;
+    const int64_t m = rem / (D / 4);
+    const int c4 = (int)(rem - m * (D / 4));
     const int c0 = bwd_cta_of(bh * T_bh, T_total, grid);
     const int np = bwd_cta_of(bh * T_bh + T_bh - 1, T_total, grid) - c0 + 1;
-    const float4 *src = reinterpret_cast<const float4 *>(part) + bh * P_max * per_bh + rem;
+    const float4 *src = reinterpret_cast<const float4 *>(part + (c4 >> 4) * half_stride) +
+                        (bh * P_max * M + m) * 16 + (c4 & 15);
     float4 acc = accumulate ? reinterpret_cast<const float4 *>(dQ)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int p = 0; p < np; ++p) {
-        const float4 v = __ldcg(src + p * per_bh);
+        const float4 v = __ldcg(src + (int64_t)p * M * 16);
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
@@ -167,14 +190,15 @@ __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const float *__restr
 }
 
 // ---- the tile kernel -------------------------------------------------------------
-template <int M, int STAGES, bool ACC, bool ACCV = false>
-__global__ void __launch_bounds__(BwdCfg<M, STAGES, ACCV>::THREADS, 1)
+template <int M, int STAGES, bool ACC, bool ACCV = false, int D = 64>
+__global__ void __launch_bounds__(BwdCfg<M, STAGES, ACCV, D>::THREADS, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdZ,
               const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
               const BwdArgs a) {
-    using C = BwdCfg<M, STAGES, ACCV>;
+    using C = BwdCfg<M, STAGES, ACCV, D>;
     constexpr uint32_t TB = C::TILE_BYTES;
+    constexpr int DA = C::DA;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -259,16 +283,19 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 cur = bh;
                 // Q, dZ and the statistics of the previous (b, h) are no longer read
                 if (u > 0 && !__all_sync(0xffffffffu, wt.wait_inline(qd_free, (uint32_t)(u - 1) & 1))) break;
-                float *dst = lcs + (u & 1) * 256;
+                float *dst = lcs + (u & 1) * 2 * M;
                 const float *src = a.lc + bh * 2 * a.M_all + a.m0;
-                for (int i = lane; i < 2 * M; i += 32) dst[(i / M) * 128 + (i % M)] = src[(i / M) * a.M_all + (i % M)];
+                for (int i = lane; i < 2 * M; i += 32) dst[i] = src[(i / M) * a.M_all + (i % M)];
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(lc_full(u & 1));
                     mbar_arrive_expect_tx(qd_full, 2 * C::QZ_BYTES);
                     if (dcheck(h >= 0 && h < a.H && b >= 0 && b < a.B, kChkBwdQ, a.status)) {
-                        tma_load_4d(sQ, &tmQ, 0, a.m0, h, a.q_per_batch ? b : 0, qd_full);
-                        tma_load_4d(sdZ, &tmdZ, 0, a.m0, h, b, qd_full);
+#pragma unroll
+                        for (int at = 0; at < DA; ++at) {
+                            tma_load_4d(sQ + at * C::QZA, &tmQ, 64 * at, a.m0, h, a.q_per_batch ? b : 0, qd_full);
+                            tma_load_4d(sdZ + at * C::QZA, &tmdZ, 64 * at, a.m0, h, b, qd_full);
+                        }
                     }
                 }
                 __syncwarp();
@@ -279,8 +306,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 mbar_arrive_expect_tx(full(s), C::STAGE_BYTES);
                 const uint32_t dst = sStage + s * C::STAGE_BYTES;
                 if (dcheck(tile_in_tensor(0, h, kt * 128, b, a.H, a.N, a.B) && kt < a.T_bh, kChkBwdKV, a.status)) {
-                    tma_load_4d_hint(dst, &tmK, 0, h, (int)(kt * 128), b, full(s), pol);
-                    tma_load_4d_hint(dst + TB, &tmV, 0, h, (int)(kt * 128), b, full(s), pol);
+#pragma unroll
+                    for (int at = 0; at < DA; ++at) {
+                        tma_load_4d_hint(dst + at * TB, &tmK, 64 * at, h, (int)(kt * 128), b, full(s), pol);
+                        tma_load_4d_hint(dst + (DA + at) * TB, &tmV, 64 * at, h, (int)(kt * 128), b, full(s), pol);
+                    }
                 }
             }
             __syncwarp();
@@ -312,8 +342,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             constexpr uint32_t idQ = idesc_bf16(128, 64, 1, 1);    // dQ: A, B MN-major
             const uint64_t dQk = desc_sw128(sQ, 16, 1024);          // Q, K-major (B of S^T)
             const uint64_t dZk = desc_sw128(sdZ, 16, 1024);         // dZ, K-major (B of dP^T)
-            const uint64_t dQm = desc_sw128(sQ, TB, 1024);          // Q, MN-major (B of dK)
-            const uint64_t dZm = desc_sw128(sdZ, TB, 1024);         // dZ, MN-major (B of dV)
+            // the output column half's atoms of Q and dZ
+            const uint64_t dQm = desc_sw128(sQ + a.dh * C::QZA, TB, 1024);   // Q, MN-major (B of dK)
+            const uint64_t dZm = desc_sw128(sdZ + a.dh * C::QZA, TB, 1024);  // dZ, MN-major (B of dV)
             const uint64_t dDS = desc_sw128(sDS, TB, 1024);         // s dS^T, MN-major (A of dQ)
             const uint64_t dDSk = desc_sw128(sDS, 16, 1024);        // s dS^T, K-major (A of dK)
             int64_t bhS = bh0, ktS = k0, curS = -1;                  // cursor of the S tiles
@@ -329,13 +360,16 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 if (!wt.wait_inline(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
                 tc_fence_after();
                 const uint64_t dK = desc_sw128(sStage + s * C::STAGE_BYTES, 16, 1024);
-                const uint64_t dV = desc_sw128(sStage + s * C::STAGE_BYTES + TB, 16, 1024);
+                const uint64_t dV = desc_sw128(sStage + s * C::STAGE_BYTES + DA * TB, 16, 1024);
+                // over all D columns: 16 per MMA, four per atom
 #pragma unroll
-                for (int kb = 0; kb < 4; ++kb)
-                    umma_bf16_ss(tmem + C::S_COL, dK + 2 * kb, dQk + 2 * kb, idS, kb > 0 ? 1u : 0u);
+                for (int kb = 0; kb < 4 * DA; ++kb)
+                    umma_bf16_ss(tmem + C::S_COL, dK + (((kb >> 2) * TB) >> 4) + 2 * (kb & 3),
+                                 dQk + (((kb >> 2) * C::QZA) >> 4) + 2 * (kb & 3), idS, kb > 0 ? 1u : 0u);
 #pragma unroll
-                for (int kb = 0; kb < 4; ++kb)
-                    umma_bf16_ss(tmem + C::DP_COL, dV + 2 * kb, dZk + 2 * kb, idS, kb > 0 ? 1u : 0u);
+                for (int kb = 0; kb < 4 * DA; ++kb)
+                    umma_bf16_ss(tmem + C::DP_COL, dV + (((kb >> 2) * TB) >> 4) + 2 * (kb & 3),
+                                 dZk + (((kb >> 2) * C::QZA) >> 4) + 2 * (kb & 3), idS, kb > 0 ? 1u : 0u);
                 umma_commit(s_full);
                 if (++ktS == a.T_bh) {
                     ktS = 0;
@@ -382,7 +416,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 if (first && uP > 0 && !(ok = wt.wait_inline(dq_free, (uint32_t)(uP - 1) & 1))) break;
                 tc_fence_after();
                 const int s = (int)(j % STAGES);
-                const uint64_t dKm = desc_sw128(sStage + s * C::STAGE_BYTES, TB, 1024);
+                const uint64_t dKm = desc_sw128(sStage + s * C::STAGE_BYTES + a.dh * TB, TB, 1024);
 #pragma unroll
                 for (int kb = 0; kb < 8; ++kb)
                     umma_bf16_ss(tmem + C::DQ_COL, dDS + kb * (2048 >> 4), dKm + kb * (2048 >> 4), idQ,
@@ -459,7 +493,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         auto prefetch_dk = [&](const Cursor &t) {
             const int64_t n = t.kt * 128 + rig;
             if (acc_mine && n < a.N) {
-                const __nv_bfloat16 *src = acc_src + (((int64_t)t.b * a.N + n) * a.H + t.h) * 64;
+                const __nv_bfloat16 *src = acc_src + (((int64_t)t.b * a.N + n) * a.H + t.h) * D + 64 * a.dh;
                 const uint32_t dst = sbase + acc_buf + (uint32_t)rig * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) cp_async16(dst + ((c ^ (rig & 7)) << 4), src + 8 * c);
@@ -538,9 +572,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             __syncwarp();
             const int n0 = (int)(t.kt * 128) + quad * 32;
             if (lane == 0 && n0 < a.N &&
-                dcheck(tile_in_tensor(0, t.h, n0, t.b, a.H, a.N, a.B), kChkBwdOut, a.status)) {
+                dcheck(tile_in_tensor(64 * a.dh, t.h, n0, t.b, a.H, a.N, a.B), kChkBwdOut, a.status)) {
                 // rows past N are clipped by the tensor map
-                tma_store_4d(tmOut, smem_u32(slab), 0, t.h, n0, t.b);
+                tma_store_4d(tmOut, smem_u32(slab), 64 * a.dh, t.h, n0, t.b);
                 bulk_commit_group();
             }
             if (nxt != nullptr) prefetch_dk(*nxt);
@@ -593,7 +627,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             Cursor cn = cu;
             advance(cn);
             const bool last = (j + 1 == ntiles) || cn.bh != bh;
-            const float *nl2 = lcs + (u & 1) * 256, *ncs = nl2 + 128;
+            const float *nl2 = lcs + (u & 1) * 2 * M, *ncs = nl2 + M;
             const bool valid = mb0 != 0;
             mb0 = mb1;
             mb1 = j + 2 < ntiles ? mask_byte(ca) : 0u;

@@ -37,6 +37,15 @@
 // 2^(s log2e <K_n, Q_m> - lse2_n), no exchange between the halves); the
 // second pass's dK share goes to a scratch tensor that is added to the
 // first's.
+//
+// D = 128 (M = 64) runs as two passes over the tokens, one per 64-column half
+// of dK, dQ and dZ: each pass contracts S and G over all 128 columns (K, dY,
+// Q and Z tiles of two 64-column atoms) and computes its half's gradients in
+// the TMEM columns of D = 64; each pass has its own dQ/dZ piece array. Two
+// 64 KB K/dY stages leave no room for the dK staging slabs and the halves'
+// exchange buffers, so at M = 64 these sit in the upper atoms of the A^T and
+// s dT^T buffers: those atoms feed latent rows 64..127 of the dZ and dQ MMAs,
+// whose output lanes are never read.
 #pragma once
 
 #include "tc_backward.cuh"
@@ -55,31 +64,37 @@ struct DbwArgs {
     float sl2;                  // s * log2(e)
     float s;                    // score scale
     int q_per_batch;            // Q has a batch dimension
-    float *part;                // [B*H][P_max][2][M][64]: dQ, then dZ pieces
+    float *part;                // [B*H][P_max][2][M][64]: dQ, then dZ pieces (of this pass's half)
+    int dh;                     // D = 128: the output column half [64 dh, 64 dh + 64)
     int P_max;
     int64_t T_bh, T_total;      // 128-token tiles per (b, h), and overall
     int grid;
     unsigned *status;
 };
 
-template <int M_, int STAGES_>
+template <int M_, int STAGES_, int D_ = 64>
 struct DbwCfg {
-    static constexpr int M = M_, D = 64, TILE = 128, STAGES = STAGES_;
+    static constexpr int M = M_, D = D_, TILE = 128, STAGES = STAGES_;
+    static constexpr int DA = D / 64;                      // 64-column atoms of a row
     static constexpr int THREADS = 320;
     static constexpr uint32_t TILE_BYTES = TILE * 128;     // 128 rows x 64 bf16 (swizzled)
-    static constexpr uint32_t QZ_BYTES = M * 128;          // [M][64] bf16 (swizzled)
+    static constexpr uint32_t QZA = M * 128;               // one [M][64] bf16 atom (swizzled)
+    static constexpr uint32_t QZ_BYTES = DA * QZA;         // Q (or Z): its atoms in column order
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t ZB_OFF = Q_OFF + QZ_BYTES;
     static constexpr uint32_t STAGE_OFF = ZB_OFF + QZ_BYTES;
-    static constexpr uint32_t STAGE_BYTES = 2 * TILE_BYTES; // K tile, then dY tile
+    static constexpr uint32_t STAGE_BYTES = 2 * DA * TILE_BYTES; // K atoms, then dY atoms
     // A^T and s dT^T in bf16: token rows of 64-latent atoms (atom a at a * TILE_BYTES)
     static constexpr uint32_t A_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
     static constexpr uint32_t DT_OFF = A_OFF + 2 * TILE_BYTES;
-    static constexpr uint32_t OUT_OFF = DT_OFF + 2 * TILE_BYTES;   // dK staging (4 slabs)
+    // D = 128 at M = 64: staging and exchange buffers in the upper atoms
+    static constexpr bool IN_UPPER = DA == 2 && M <= 64;
+    static constexpr uint32_t OUT_OFF = IN_UPPER ? A_OFF + TILE_BYTES : DT_OFF + 2 * TILE_BYTES;  // dK staging (4 slabs)
     // row statistics exchanged between the halves: [2 parity][2 half][128]
-    static constexpr uint32_t XM_OFF = OUT_OFF + TILE_BYTES;        // float: maxima
+    static constexpr uint32_t XM_OFF = IN_UPPER ? DT_OFF + TILE_BYTES : OUT_OFF + TILE_BYTES;  // float: maxima
     static constexpr uint32_t XL_OFF = XM_OFF + 2 * 2 * 128 * 4;    // float2: (sum, <p, g>)
-    static constexpr uint32_t BAR_OFF = XL_OFF + 2 * 2 * 128 * 8;
+    static constexpr uint32_t BAR_OFF = IN_UPPER ? DT_OFF + 2 * TILE_BYTES : XL_OFF + 2 * 2 * 128 * 8;
+    static_assert(!IN_UPPER || XL_OFF + 2 * 2 * 128 * 8 <= DT_OFF + 2 * TILE_BYTES, "exchange buffers overflow");
     // full[S], empty[S], qz_full, qz_free, s_full, p_full, at_free, dk_full,
     // dk_free, pz_full, pz_free, drain, sg_free
     static constexpr int NBAR = 2 * STAGES + 11;
@@ -105,22 +120,29 @@ __global__ void __launch_bounds__(256) dbw_prep_kernel(const float *__restrict__
 }
 
 // dQ (which = 0) and dZ (which = 1) = the sums of the pieces of each (b, h).
+// The pieces of column half dh (D = 128: one piece array per pass) start at
+// part + dh * half_stride floats; each holds [B*H][P_max][2][M][64].
 __global__ void __launch_bounds__(256) dbw_reduce_kernel(const float *__restrict__ part,
                                                          float *__restrict__ dQ, float *__restrict__ dZ,
                                                          int64_t BH, int M, int P_max, int64_t T_bh,
-                                                         int64_t T_total, int grid) {
-    const int64_t per = (int64_t)M * 16;                    // float4s of one (b, h) tensor
+                                                         int64_t T_total, int grid, int D,
+                                                         int64_t half_stride) {
+    const int64_t per = (int64_t)M * (D / 4);               // float4s of one (b, h) tensor
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= 2 * BH * per) return;
     const int which = (int)(i / (BH * per));
     const int64_t rest = i - which * BH * per;
     const int64_t bh = rest / per, rem = rest - bh * per;
+    const int64_t m = rem / (D / 4);
+    const int c4 = (int)(rem - m * (D / 4));
     const int c0 = bwd_cta_of(bh * T_bh, T_total, grid);
     const int np = bwd_cta_of(bh * T_bh + T_bh - 1, T_total, grid) - c0 + 1;
-    const float4 *src = reinterpret_cast<const float4 *>(part) + (bh * P_max * 2 + which) * per + rem;
+    const int64_t piece = (int64_t)M * 16;                  // float4s of one piece tensor
+    const float4 *src = reinterpret_cast<const float4 *>(part + (c4 >> 4) * half_stride) +
+                        (bh * P_max * 2 + which) * piece + m * 16 + (c4 & 15);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int p = 0; p < np; ++p) {
-        const float4 v = __ldcg(src + p * 2 * per);
+        const float4 v = __ldcg(src + p * 2 * piece);
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
@@ -385,13 +407,14 @@ dbs_stats_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int M, int STAGES, bool ST = false>
-__global__ void __launch_bounds__(DbwCfg<M, STAGES>::THREADS, 1)
+template <int M, int STAGES, bool ST = false, int D = 64>
+__global__ void __launch_bounds__(DbwCfg<M, STAGES, D>::THREADS, 1)
 dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmdY,
               const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmZ,
               const __grid_constant__ CUtensorMap tmdK, const DbwArgs a) {
-    using C = DbwCfg<M, STAGES>;
+    using C = DbwCfg<M, STAGES, D>;
     constexpr uint32_t TB = C::TILE_BYTES;
+    constexpr int DA = C::DA;
     constexpr int W = M / 2;                                   // latents of each half
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -477,8 +500,11 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 if (lane == 0) {
                     mbar_arrive_expect_tx(qz_full, 2 * C::QZ_BYTES);
                     if (dcheck(h >= 0 && h < a.H && b >= 0 && b < a.B, kChkDbwQ, a.status)) {
-                        tma_load_4d(sQ, &tmQ, 0, a.m0, h, a.q_per_batch ? b : 0, qz_full);
-                        tma_load_4d(sZ, &tmZ, 0, a.m0, h, b, qz_full);
+#pragma unroll
+                        for (int at = 0; at < DA; ++at) {
+                            tma_load_4d(sQ + at * C::QZA, &tmQ, 64 * at, a.m0, h, a.q_per_batch ? b : 0, qz_full);
+                            tma_load_4d(sZ + at * C::QZA, &tmZ, 64 * at, a.m0, h, b, qz_full);
+                        }
                     }
                 }
                 __syncwarp();
@@ -489,8 +515,11 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 mbar_arrive_expect_tx(full(s), C::STAGE_BYTES);
                 const uint32_t dst = sStage + s * C::STAGE_BYTES;
                 if (dcheck(tile_in_tensor(0, h, kt * 128, b, a.H, a.N, a.B) && kt < a.T_bh, kChkDbwKV, a.status)) {
-                    tma_load_4d_hint(dst, &tmK, 0, h, (int)(kt * 128), b, full(s), pol);
-                    tma_load_4d_hint(dst + TB, &tmdY, 0, h, (int)(kt * 128), b, full(s), pol);
+#pragma unroll
+                    for (int at = 0; at < DA; ++at) {
+                        tma_load_4d_hint(dst + at * TB, &tmK, 64 * at, h, (int)(kt * 128), b, full(s), pol);
+                        tma_load_4d_hint(dst + (DA + at) * TB, &tmdY, 64 * at, h, (int)(kt * 128), b, full(s), pol);
+                    }
                 }
             }
             __syncwarp();
@@ -522,7 +551,7 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             constexpr uint32_t idR = idesc_bf16(128, 64, 1, 1);    // dQ, dZ: A, B MN-major
             const uint64_t dQk = desc_sw128(sQ, 16, 1024);          // Q, K-major (B of S^T)
             const uint64_t dZk = desc_sw128(sZ, 16, 1024);          // Z, K-major (B of G^T)
-            const uint64_t dQm = desc_sw128(sQ, TB, 1024);          // Q, MN-major (B of dK)
+            const uint64_t dQm = desc_sw128(sQ + a.dh * C::QZA, TB, 1024);   // Q, MN-major (B of dK)
             const uint64_t dAm = desc_sw128(sA, TB, 1024);          // A^T, MN-major (A of dZ)
             const uint64_t dDTm = desc_sw128(sDT, TB, 1024);        // s dT^T, MN-major (A of dQ)
             int64_t bhS = bh0, ktS = k0, curS = -1;
@@ -538,13 +567,16 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 if (!wt.wait_inline(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
                 tc_fence_after();
                 const uint64_t dK = desc_sw128(sStage + s * C::STAGE_BYTES, 16, 1024);
-                const uint64_t dY = desc_sw128(sStage + s * C::STAGE_BYTES + TB, 16, 1024);
+                const uint64_t dY = desc_sw128(sStage + s * C::STAGE_BYTES + DA * TB, 16, 1024);
+                // over all D columns: 16 per MMA, four per atom
 #pragma unroll
-                for (int kb = 0; kb < 4; ++kb)
-                    umma_bf16_ss(tmem + C::S_COL, dK + 2 * kb, dQk + 2 * kb, idS, kb > 0 ? 1u : 0u);
+                for (int kb = 0; kb < 4 * DA; ++kb)
+                    umma_bf16_ss(tmem + C::S_COL, dK + (((kb >> 2) * TB) >> 4) + 2 * (kb & 3),
+                                 dQk + (((kb >> 2) * C::QZA) >> 4) + 2 * (kb & 3), idS, kb > 0 ? 1u : 0u);
 #pragma unroll
-                for (int kb = 0; kb < 4; ++kb)
-                    umma_bf16_ss(tmem + C::G_COL, dY + 2 * kb, dZk + 2 * kb, idS, kb > 0 ? 1u : 0u);
+                for (int kb = 0; kb < 4 * DA; ++kb)
+                    umma_bf16_ss(tmem + C::G_COL, dY + (((kb >> 2) * TB) >> 4) + 2 * (kb & 3),
+                                 dZk + (((kb >> 2) * C::QZA) >> 4) + 2 * (kb & 3), idS, kb > 0 ? 1u : 0u);
                 umma_commit(s_full);
                 if (++ktS == a.T_bh) {
                     ktS = 0;
@@ -586,8 +618,9 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 if (first && uP > 0 && !(ok = wt.wait_inline(pz_free, (uint32_t)(uP - 1) & 1))) break;
                 tc_fence_after();
                 const int s = (int)(j % STAGES);
-                const uint64_t dKm = desc_sw128(sStage + s * C::STAGE_BYTES, TB, 1024);
-                const uint64_t dYm = desc_sw128(sStage + s * C::STAGE_BYTES + TB, TB, 1024);
+                // the output column half's atoms of the K and dY tiles
+                const uint64_t dKm = desc_sw128(sStage + s * C::STAGE_BYTES + a.dh * TB, TB, 1024);
+                const uint64_t dYm = desc_sw128(sStage + s * C::STAGE_BYTES + (DA + a.dh) * TB, TB, 1024);
 #pragma unroll
                 for (int kb = 0; kb < 8; ++kb)
                     umma_bf16_ss(tmem + C::DQ_COL, dDTm + kb * (2048 >> 4), dKm + kb * (2048 >> 4), idR,
@@ -665,9 +698,9 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             fence_proxy_async_smem();
             named_bar_sync(pair_bar, 64);
             const int n0 = (int)(ktp * 128) + quad * 32;
-            if (storer && n0 < a.N && dcheck(tile_in_tensor(0, hp, n0, bp, a.H, a.N, a.B), kChkDbwOut, a.status)) {
+            if (storer && n0 < a.N && dcheck(tile_in_tensor(64 * a.dh, hp, n0, bp, a.H, a.N, a.B), kChkDbwOut, a.status)) {
                 // rows past N are clipped by the tensor map
-                tma_store_4d(&tmdK, smem_u32(slab), 0, hp, n0, bp);
+                tma_store_4d(&tmdK, smem_u32(slab), 64 * a.dh, hp, n0, bp);
                 bulk_commit_group();
             }
             ++stores;

@@ -277,15 +277,17 @@ cudaError_t launch_decode_tc(const Problem &pr, const void *Q, bool q_is_f32, co
     return cudaErrorNotSupported;
 }
 
-bool tc_bwd_supported(bool bf16, int M, int D) { return bf16 && D == 64 && (M == 64 || M == 128 || M == 256); }
+bool tc_bwd_supported(bool bf16, int M, int D) {
+    return bf16 && ((D == 64 && (M == 64 || M == 128 || M == 256)) || (D == 128 && M == 64));
+}
 
 namespace {
-// Backward workspace: dZ in bf16 [B*H*M*64], the row constants [B*H][2][M]
-// and the dQ partials [B*H][P_max][M][64].
+// Backward workspace: dZ in bf16 [B*H*M*D], the row constants [B*H][2][M]
+// and the dQ partials [B*H][P_max][M][64] of each 64-column half of D.
 struct BwdLayout {
     int64_t T_bh, T_total;
     int grid, P_max;
-    size_t dzb, lc, part, bytes;
+    size_t dzb, lc, part, part_half, bytes;
 };
 
 void bwd_layout(const Problem &pr, int sms, BwdLayout &l) {
@@ -299,21 +301,22 @@ void bwd_layout(const Problem &pr, int sms, BwdLayout &l) {
     const size_t bhm = (size_t)pr.B * pr.H * pr.M;
     size_t o = 0;
     l.dzb = o;
-    o += align256(2 * bhm * 64);
+    o += align256(2 * bhm * (size_t)pr.D);
     l.lc = o;
     o += align256(4 * bhm * 2);
     l.part = o;
-    o += align256(4 * bhm * (size_t)l.P_max * 64);
+    l.part_half = align256(4 * bhm * (size_t)l.P_max * 64);
+    o += l.part_half * (size_t)(pr.D / 64);
     l.bytes = o;
 }
 
-template <int M, bool ACC, bool ACCV = false>
+template <int M, bool ACC, bool ACCV = false, int D = 64>
 cudaError_t launch_bwd(const CUtensorMap *maps, const tc::BwdArgs &a, cudaStream_t st) {
     // the dV-accumulating pass keeps two K/V stages (its old-dV buffer takes
-    // the third stage's shared memory)
-    constexpr int STAGES = ACCV ? 2 : 3;
-    using C = tc::BwdCfg<M, STAGES, ACCV>;
-    auto k = tc::bwd_tc_kernel<M, STAGES, ACC, ACCV>;
+    // the third stage's shared memory), and so does D = 128 (stages of 64 KB)
+    constexpr int STAGES = (ACCV || D == 128) ? 2 : 3;
+    using C = tc::BwdCfg<M, STAGES, ACCV, D>;
+    auto k = tc::bwd_tc_kernel<M, STAGES, ACC, ACCV, D>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
     if (e != cudaSuccess) return e;
     k<<<a.grid, C::THREADS, C::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
@@ -347,7 +350,7 @@ cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *
     float *lc = (float *)(w + l.lc), *part = (float *)(w + l.part);
     const int64_t rows = BH * pr.M;
     tc::bwd_prep_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(Z, L, dZ, dzb, lc, rows, pr.M,
-                                                                            pr.scale);
+                                                                            pr.scale, pr.D);
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -377,6 +380,7 @@ cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *
     a.mask = mask;
     a.lc = lc;
     a.part = part;
+    a.dh = 0;
     a.dk_acc = accumulate ? (const __nv_bfloat16 *)dK : nullptr;
     a.dv_acc = nullptr;
     a.P_max = l.P_max;
@@ -384,7 +388,15 @@ cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *
     a.T_total = l.T_total;
     a.grid = l.grid;
     a.status = status;
-    if (pr.M == 256) {
+    if (pr.D == 128) {
+        // one pass per 64-column half of dK, dV and dQ (M = 64)
+        for (int dh = 0; dh < 2 && e == cudaSuccess; ++dh) {
+            a.dh = dh;
+            a.part = (float *)(w + l.part + dh * l.part_half);
+            e = accumulate ? launch_bwd<64, true, false, 128>(maps, a, st)
+                           : launch_bwd<64, false, false, 128>(maps, a, st);
+        }
+    } else if (pr.M == 256) {
         // latent rows [0, 128): dK (+)= and dV = their shares
         e = accumulate ? launch_bwd<128, true>(maps, a, st) : launch_bwd<128, false>(maps, a, st);
         if (e != cudaSuccess) return e;
@@ -398,27 +410,27 @@ cudaError_t launch_encoder_bwd_tc(const Problem &pr, const void *Q, const void *
     else
         e = pr.M == 128 ? launch_bwd<128, false>(maps, a, st) : launch_bwd<64, false>(maps, a, st);
     if (e != cudaSuccess) return e;
-    const int64_t n4 = BH * pr.M * 16;
-    tc::bwd_dq_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(part, dQ, BH, pr.M, l.P_max,
-                                                                          l.T_bh, l.T_total, l.grid,
-                                                                          accumulate ? 1 : 0);
+    const int64_t n4 = BH * pr.M * (pr.D / 4);
+    tc::bwd_dq_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(
+        part, dQ, BH, pr.M, l.P_max, l.T_bh, l.T_total, l.grid, accumulate ? 1 : 0, pr.D,
+        (int64_t)(l.part_half / sizeof(float)));
     note_launch();
     return cudaGetLastError();
 }
 
 bool tc_decode_bwd_supported(bool bf16, int M, int D) {
-    return bf16 && D == 64 && (M == 64 || M == 128 || M == 256);
+    return bf16 && ((D == 64 && (M == 64 || M == 128 || M == 256)) || (D == 128 && M == 64));
 }
 
 namespace {
-// Decode-backward workspace: Z in bf16 [B*H*M*64] and the dQ/dZ pieces
-// [B*H][P_max][2][M][64]; tiles and spans as for the encoder backward. M = 256
-// adds the per-token statistics [B*H][N] (lse2, r) and the second half's dK
-// share [B][N][H][64] bf16.
+// Decode-backward workspace: Z in bf16 [B*H*M*D] and the dQ/dZ pieces
+// [B*H][P_max][2][M][64] of each 64-column half of D; tiles and spans as for
+// the encoder backward. M = 256 adds the per-token statistics [B*H][N]
+// (lse2, r) and the second latent half's dK share [B][N][H][64] bf16.
 struct DbwLayout {
     int64_t T_bh, T_total;
     int grid, P_max;
-    size_t zb, part, stats, dk2, bytes;
+    size_t zb, part, part_half, stats, dk2, bytes;
 };
 
 void dbw_layout(const Problem &pr, int sms, DbwLayout &l) {
@@ -431,9 +443,10 @@ void dbw_layout(const Problem &pr, int sms, DbwLayout &l) {
     const size_t bhm = (size_t)pr.B * pr.H * pr.M;
     size_t o = 0;
     l.zb = o;
-    o += align256(2 * bhm * 64);
+    o += align256(2 * bhm * (size_t)pr.D);
     l.part = o;
-    o += align256(4 * bhm * (size_t)l.P_max * 2 * 64);
+    l.part_half = align256(4 * bhm * (size_t)l.P_max * 2 * 64);
+    o += l.part_half * (size_t)(pr.D / 64);
     l.stats = l.dk2 = o;
     if (pr.M > 128) {
         const size_t bhn = (size_t)pr.B * pr.H * (size_t)pr.N;
@@ -444,10 +457,11 @@ void dbw_layout(const Problem &pr, int sms, DbwLayout &l) {
     l.bytes = o;
 }
 
-template <int M, bool ST = false>
+template <int M, bool ST = false, int D = 64>
 cudaError_t launch_dbw(const CUtensorMap *maps, const tc::DbwArgs &a, cudaStream_t st) {
-    using C = tc::DbwCfg<M, 3>;
-    auto k = tc::dbw_tc_kernel<M, 3, ST>;
+    constexpr int STAGES = D == 128 ? 2 : 3;     // K/dY stages of 64 KB at D = 128
+    using C = tc::DbwCfg<M, STAGES, D>;
+    auto k = tc::dbw_tc_kernel<M, STAGES, ST, D>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
     if (e != cudaSuccess) return e;
     k<<<a.grid, C::THREADS, C::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a);
@@ -489,7 +503,7 @@ cudaError_t launch_decode_bwd_tc(const Problem &pr, const void *Q, const float *
     char *w = (char *)ws;
     __nv_bfloat16 *zb = (__nv_bfloat16 *)(w + l.zb);
     float *part = (float *)(w + l.part);
-    const int64_t n2 = BH * pr.M * 32;
+    const int64_t n2 = BH * pr.M * (pr.D / 2);
     tc::dbw_prep_kernel<<<(unsigned)((n2 + 255) / 256), 256, 0, st>>>(Z, zb, n2);
     note_launch();
     cudaError_t e = cudaGetLastError();
@@ -511,6 +525,7 @@ cudaError_t launch_decode_bwd_tc(const Problem &pr, const void *Q, const float *
     a.m0 = 0;
     a.M_all = pr.M;
     a.stats = nullptr;
+    a.dh = 0;
     a.N = pr.N;
     a.s = pr.scale;
     a.sl2 = pr.scale * 1.4426950408889634f;
@@ -521,7 +536,14 @@ cudaError_t launch_decode_bwd_tc(const Problem &pr, const void *Q, const float *
     a.T_total = l.T_total;
     a.grid = l.grid;
     a.status = status;
-    if (pr.M <= 128) {
+    if (pr.D == 128) {
+        // one pass per 64-column half of dK, dQ and dZ (M = 64)
+        for (int dh = 0; dh < 2; ++dh) {
+            a.dh = dh;
+            a.part = (float *)(w + l.part + dh * l.part_half);
+            if ((e = launch_dbw<64, false, 128>(maps, a, st)) != cudaSuccess) return e;
+        }
+    } else if (pr.M <= 128) {
         e = pr.M == 128 ? launch_dbw<128>(maps, a, st) : launch_dbw<64>(maps, a, st);
         if (e != cudaSuccess) return e;
     } else {
@@ -559,9 +581,9 @@ cudaError_t launch_decode_bwd_tc(const Problem &pr, const void *Q, const float *
         note_launch();
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    const int64_t n4 = 2 * BH * pr.M * 16;
-    tc::dbw_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(part, dQ, dZ, BH, pr.M, l.P_max,
-                                                                       l.T_bh, l.T_total, l.grid);
+    const int64_t n4 = 2 * BH * pr.M * (pr.D / 4);
+    tc::dbw_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(
+        part, dQ, dZ, BH, pr.M, l.P_max, l.T_bh, l.T_total, l.grid, pr.D, (int64_t)(l.part_half / sizeof(float)));
     note_launch();
     return cudaGetLastError();
 }

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from latent_query_split_gb300 import flare
-from parity import assert_close, assert_L_close
+from parity import assert_close, assert_L_close, max_err
 
 pytestmark = pytest.mark.gpu
 
@@ -119,7 +119,8 @@ def test_flare_pp_fwd(cuda_device, kernel, dt, M, D):
 
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dt,M,D,N", [("f32", 16, 32, 700), ("bf16", 128, 64, 3000),
-                                      ("bf16", 64, 128, 1100), ("bf16", 256, 64, 900)])
+                                      ("bf16", 64, 128, 1100), ("bf16", 64, 128, 9000),
+                                      ("bf16", 256, 64, 900)])
 def test_encoder_bwd(cuda_device, kernel, dt, M, D, N):
     B, H = 2, 2
     off = [0, 200, 200, N]
@@ -173,7 +174,7 @@ def test_encoder_bwd_multi_tile_spans(cuda_device, kernel, M, replicated):
 @pytest.mark.parametrize("dt,M,D,N,replicated", [("f32", 16, 32, 700, True), ("bf16", 128, 64, 3000, True),
                                                  ("bf16", 64, 64, 2100, False), ("bf16", 64, 128, 1100, True),
                                                  ("bf16", 256, 64, 900, True), ("bf16", 256, 64, 9000, False),
-                                                 ("f32", 37, 40, 333, False)])
+                                                 ("bf16", 64, 128, 9000, False), ("f32", 37, 40, 333, False)])
 def test_decode_bwd(cuda_device, kernel, dt, M, D, N, replicated):
     B, H = 2, 2
     Q, K, _, _ = _problem(18, B, H, M, N, D, dt, [0, N], pad=0, q_std=1.0, replicated=replicated)
@@ -184,8 +185,14 @@ def test_decode_bwd(cuda_device, kernel, dt, M, D, N, replicated):
     dQ, dZ, dK = _call(flare.flare_decode_bwd, Q, Z, K, dY, kernel=kernel)
     flare.flare_device_status()
     dQo, dZo, dKo = oracle.decode_bwd(Q, Z, K, dY)
-    assert_close("dQ", dQ, dQo, dt)
-    assert_close("dZ", dZ, dZo, dt)
+    # dQ and dZ add one bf16-rounded product per token, so their rounding
+    # error grows like sqrt(N): past a few thousand tokens they are held to
+    # the full-size bound, 2e-2 of max(1, largest reference magnitude)
+    many = dt == "bf16" and N > 4096
+    for name, dev, ref in (("dQ", dQ, dQo), ("dZ", dZ, dZo)):
+        err, scale = max_err(dev, ref)
+        print(f"{name}: max abs err {err:.3e}, max |ref| {scale:.3e}")
+        assert_close(name, dev, ref, dt, atol=2e-2 * max(1.0, scale) if many else None)
     assert_close("dK", dK, dKo, dt)
     # two runs agree bit for bit (fixed-order sums)
     dQ2, dZ2, dK2 = _call(flare.flare_decode_bwd, Q, Z, K, dY, kernel=kernel)
@@ -195,7 +202,7 @@ def test_decode_bwd(cuda_device, kernel, dt, M, D, N, replicated):
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dt,M,D,N,replicated", [("f32", 16, 32, 700, True), ("bf16", 128, 64, 3000, True),
                                                  ("bf16", 64, 64, 2100, False), ("bf16", 256, 64, 900, True),
-                                                 ("bf16", 128, 64, 20000, True)])
+                                                 ("bf16", 128, 64, 20000, True), ("bf16", 64, 128, 4000, False)])
 def test_flare_bwd(cuda_device, kernel, dt, M, D, N, replicated):
     """FLARE mixer backward: the decode's shares of dQ and dK are written
     first and the encoder's are added in place (dK read back and summed in
@@ -225,7 +232,7 @@ def test_flare_bwd(cuda_device, kernel, dt, M, D, N, replicated):
 
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dt,M,D,N", [("f32", 16, 32, 700), ("bf16", 128, 64, 2500), ("bf16", 64, 64, 5000),
-                                      ("bf16", 256, 64, 2500)])
+                                      ("bf16", 256, 64, 2500), ("bf16", 64, 128, 3000)])
 def test_flare_pp_bwd(cuda_device, kernel, dt, M, D, N):
     """FLARE++ mixer backward from the oracle's forward statistics: the seeds'
     gradient, the four token gradients and the summed gradient of Q(X)."""
