@@ -182,16 +182,18 @@ struct DbsArgs {
 
 struct DbsCfg {
     static constexpr int M = 256, TILE = 128, STAGES = 3;
-    static constexpr int THREADS = 192;                     // producer, MMA issuer, four row warps
+    static constexpr int THREADS = 320;                     // producer, MMA issuer, eight row warps
     static constexpr uint32_t TILE_BYTES = TILE * 128;      // 128 rows x 64 bf16 (swizzled)
     static constexpr uint32_t QZ_BYTES = M * 128;           // [256][64] bf16 (swizzled)
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t ZB_OFF = Q_OFF + QZ_BYTES;
     static constexpr uint32_t STAGE_OFF = ZB_OFF + QZ_BYTES;
     static constexpr uint32_t STAGE_BYTES = 2 * TILE_BYTES;   // K tile, then dY tile
-    static constexpr uint32_t BAR_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
-    // full[S], empty[S], qz_full, qz_free, s_full, s_free, drain
-    static constexpr int NBAR = 2 * STAGES + 5;
+    // the second latent half's (m, l, rg) per token row: [2][3][128] by tile parity
+    static constexpr uint32_t XS_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
+    static constexpr uint32_t BAR_OFF = XS_OFF + 2 * 3 * 128 * 4;
+    // full[S], empty[S], qz_full, qz_free, s_full, s_free, drain, x_full[4], x_free[4]
+    static constexpr int NBAR = 2 * STAGES + 13;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t BYTES = MISC_OFF + 64;
     static constexpr uint32_t ALLOC = BYTES + 1024;
@@ -201,9 +203,11 @@ struct DbsCfg {
 
 // One persistent CTA per SM over a contiguous span of 128-token tiles in
 // (b, h, tile) order. Per tile: S^T = K Q^T and G^T = dY Z^T (256 latents
-// each, all of TMEM); each of four warps takes the 32 token rows of its lane
-// quadrant and folds the 256 latents in chunks of 32 with a running maximum:
-// l = sum 2^(t - m), rg = sum 2^(t - m) g, then lse2 = m + log2 l and r = rg / l.
+// each, all of TMEM); two warps per lane quadrant take its 32 token rows,
+// each folding 128 of the latents, 64 at a time, with a running maximum:
+// l = sum 2^(t - m), rg = sum 2^(t - m) g. The second half's (m, l, rg) goes
+// through shared memory (mbarrier hand-off per quadrant) to the first, which
+// combines the two and writes lse2 = m + log2 l and r = rg / l.
 __global__ void __launch_bounds__(DbsCfg::THREADS, 1)
 dbs_stats_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmdY,
                  const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmZ,
@@ -219,6 +223,8 @@ dbs_stats_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     auto empty = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
     const uint32_t qz_full = bar0 + 8u * (2 * C::STAGES), qz_free = qz_full + 8;
     const uint32_t s_full = qz_full + 16, s_free = qz_full + 24, drain = qz_full + 32;
+    auto x_full = [&](int q) { return qz_full + 40 + 8u * q; };
+    auto x_free = [&](int q) { return qz_full + 72 + 8u * q; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
 
@@ -239,8 +245,12 @@ dbs_stats_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         mbar_init(qz_full, 1);
         mbar_init(qz_free, 1);
         mbar_init(s_full, 1);
-        mbar_init(s_free, 4);          // one arrival per row warp
+        mbar_init(s_free, 8);          // one arrival per row warp
         mbar_init(drain, 1);
+        for (int q = 0; q < 4; ++q) {
+            mbar_init(x_full(q), 1);   // the quadrant's second-half warp has published
+            mbar_init(x_free(q), 1);   // the quadrant's first-half warp has read
+        }
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -355,46 +365,84 @@ dbs_stats_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         }
         __syncwarp();
     } else {
-        // ---------------- row warps (warps 2-5, one per lane quadrant) ----------------
+        // ---------------- row warps (warps 2-9, two per lane quadrant) ----------------
         const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;                 // latents [128 half, 128 half + 128)
         const int rig = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const float sl2 = a.sl2;
+        float *xs = reinterpret_cast<float *>(smem + C::XS_OFF);
+        auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
+            return __all_sync(0xffffffffu, wt.wait_inline(bar, par));
+        };
         int64_t bh = bh0, kt = k0;
         for (int64_t j = 0; j < ntiles; ++j) {
-            if (!__all_sync(0xffffffffu, wt.wait_inline(s_full, (uint32_t)j & 1))) break;
+            if (!wwait(s_full, (uint32_t)j & 1)) break;
             tc_fence_after();
-            float m = -INFINITY, l = 0.f, rg = 0.f;
+            float m = -INFINITY, l0 = 0.f, l1 = 0.f, r0 = 0.f, r1 = 0.f;
 #pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-                uint32_t sv[32], gv[32];
-                tmem_ld32(tmem + C::S_COL + 32 * c + lane_off, sv);
-                tmem_ld32(tmem + C::G_COL + 32 * c + lane_off, gv);
+            for (int c = 0; c < 2; ++c) {
+                const uint32_t col = 128 * half + 64 * c;
+                uint32_t sv[2][32], gv[2][32];
+                tmem_ld32(tmem + C::S_COL + col + lane_off, sv[0]);
+                tmem_ld32(tmem + C::S_COL + col + 32 + lane_off, sv[1]);
+                tmem_ld32(tmem + C::G_COL + col + lane_off, gv[0]);
+                tmem_ld32(tmem + C::G_COL + col + 32 + lane_off, gv[1]);
                 tmem_wait_ld();
-                if (c == 7) {
+                if (c == 1) {
                     // S and G are in registers: the next tile's may be computed
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(s_free);
                 }
-                float cm = -INFINITY;
+                float c0 = -INFINITY, c1 = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) cm = fmaxf(cm, __uint_as_float(sv[i]) * sl2);
+                for (int i = 0; i < 16; ++i) {
+                    c0 = max3(c0, __uint_as_float(sv[0][2 * i]), __uint_as_float(sv[0][2 * i + 1]));
+                    c1 = max3(c1, __uint_as_float(sv[1][2 * i]), __uint_as_float(sv[1][2 * i + 1]));
+                }
+                const float cm = fmaxf(c0, c1) * sl2;
                 if (cm > m) {
                     const float f = (m == -INFINITY) ? 0.f : ex2(m - cm);
-                    l *= f;
-                    rg *= f;
+                    l0 *= f;
+                    l1 *= f;
+                    r0 *= f;
+                    r1 *= f;
                     m = cm;
                 }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float p = ex2(fmaf(__uint_as_float(sv[i]), sl2, -m));
-                    l += p;
-                    rg = fmaf(p, __uint_as_float(gv[i]), rg);
+                    const float p0 = ex2(fmaf(__uint_as_float(sv[0][i]), sl2, -m));
+                    const float p1 = ex2(fmaf(__uint_as_float(sv[1][i]), sl2, -m));
+                    l0 += p0;
+                    l1 += p1;
+                    r0 = fmaf(p0, __uint_as_float(gv[0][i]), r0);
+                    r1 = fmaf(p1, __uint_as_float(gv[1][i]), r1);
                 }
             }
-            const int64_t n = kt * 128 + rig;
-            if (n < a.N) a.stats[bh * a.N + n] = make_float2(m + __log2f(l), rg / l);
+            const float l = l0 + l1, rg = r0 + r1;
+            float *x = xs + (j & 1) * 384;
+            if (half == 1) {
+                // publish (m, l, rg) once the first half has read the previous
+                // tile's: x_full then never runs two phases ahead of its
+                // reader (a parity wait cannot tell phase j from phase j + 2)
+                if (j >= 1 && !wwait(x_free(quad), (uint32_t)(j - 1) & 1)) break;
+                x[rig] = m;
+                x[128 + rig] = l;
+                x[256 + rig] = rg;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(x_full(quad));
+            } else {
+                if (!wwait(x_full(quad), (uint32_t)j & 1)) break;
+                const float m1 = x[rig], l1v = x[128 + rig], r1v = x[256 + rig];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(x_free(quad));
+                const float mm = fmaxf(m, m1);
+                const float f0 = ex2(m - mm), f1 = ex2(m1 - mm);   // maxima are finite
+                const float lt = l * f0 + l1v * f1, rt = rg * f0 + r1v * f1;
+                const int64_t n = kt * 128 + rig;
+                if (n < a.N) a.stats[bh * a.N + n] = make_float2(mm + __log2f(lt), rt / lt);
+            }
             if (++kt == a.T_bh) {
                 kt = 0;
                 ++bh;

@@ -200,6 +200,33 @@ def test_decode_bwd(cuda_device, kernel, dt, M, D, N, replicated):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("M,D,replicated", [(128, 64, True), (256, 64, False), (256, 64, True),
+                                            (64, 128, False)])
+def test_decode_bwd_multi_tile_spans(cuda_device, kernel, M, D, replicated):
+    """Enough 128-token tiles that each persistent CTA walks several tiles
+    and crosses (b, h) boundaries: the pipelines' barriers go through many
+    phases (the M = 256 statistics kernel hands each tile's partial row
+    statistics from one warp to another), and dQ, dZ are assembled from
+    several pieces; repeated runs agree bit for bit."""
+    B, H, N = 2, 3, 20000
+    Q, K, _, _ = _problem(20, B, H, M, N, D, "bf16", [0, N], pad=0, q_std=1.0, replicated=replicated)
+    g = torch.Generator().manual_seed(21)
+    Z = torch.randn((B, H, M, D), generator=g).cuda()
+    dY = torch.randn((B, N, H, D), generator=g).to(torch.bfloat16).cuda()
+    dQ, dZ, dK = _call(flare.flare_decode_bwd, Q, Z, K, dY, kernel=kernel)
+    flare.flare_device_status()
+    dQo, dZo, dKo = oracle.decode_bwd(Q, Z, K, dY)
+    for name, dev, ref in (("dQ", dQ, dQo), ("dZ", dZ, dZo)):
+        err, scale = max_err(dev, ref)
+        print(f"{name}: max abs err {err:.3e}, max |ref| {scale:.3e}")
+        # one bf16-rounded product per token: the full-size bound (see test_decode_bwd)
+        assert_close(name, dev, ref, "bf16", atol=2e-2 * max(1.0, scale))
+    assert_close("dK", dK, dKo, "bf16")
+    dQ2, dZ2, dK2 = _call(flare.flare_decode_bwd, Q, Z, K, dY, kernel=kernel)
+    assert torch.equal(dQ, dQ2) and torch.equal(dZ, dZ2) and torch.equal(dK, dK2)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dt,M,D,N,replicated", [("f32", 16, 32, 700, True), ("bf16", 128, 64, 3000, True),
                                                  ("bf16", 64, 64, 2100, False), ("bf16", 256, 64, 900, True),
                                                  ("bf16", 128, 64, 20000, True), ("bf16", 64, 128, 4000, False)])
