@@ -71,7 +71,13 @@ typedef enum { FLARE_F32 = 0, FLARE_BF16 = 1 } flare_dtype_t;
 
 /* Kernel family selection. AUTO picks the tensor-core (tcgen05/TMEM, TMA)
  * kernels for bf16 shapes they support and the CUDA-core kernels otherwise;
- * TENSOR returns FLARE_ERR_UNSUPPORTED where no tensor-core kernel applies. */
+ * TENSOR returns FLARE_ERR_UNSUPPORTED where no tensor-core kernel applies.
+ * Tensor-core shapes (bf16 only; fp32 always runs on CUDA cores):
+ *   encoder, merge, decode:        D = 64 with M in {64, 128, 256},
+ *                                  D = 128 with M in {64, 128};
+ *   encoder and decode backward:   D = 64 with M in {64, 128, 256},
+ *                                  D = 128 with M = 64.
+ * The mixer entry points take, per step, the kernel family of that step. */
 typedef enum { FLARE_KERNEL_AUTO = 0, FLARE_KERNEL_SIMT = 1, FLARE_KERNEL_TENSOR = 2 } flare_kernel_t;
 
 typedef struct {
