@@ -53,15 +53,17 @@ UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "c4_long_bf16"
 # library sources whose content a committed ncu traffic figure belongs to
 KERNEL_SOURCES = {
-    "encoder": ["tc_encoder.cuh", "tc_ptx.cuh", "tc_kernels.cu"],
-    "decode": ["tc_decode.cuh", "tc_ptx.cuh", "tc_kernels.cu"],
-    "encoder_bwd": ["tc_backward.cuh", "tc_ptx.cuh", "tc_kernels.cu", "simt_kernels.cu"],
-    "flare_pp_fwd": ["tc_encoder.cuh", "tc_decode.cuh", "tc_ptx.cuh", "tc_kernels.cu"],
-    "decode_bwd": ["tc_decode_bwd.cuh", "tc_ptx.cuh", "tc_kernels.cu", "simt_decode_bwd.cu"],
-    "flare_bwd": ["tc_decode_bwd.cuh", "tc_backward.cuh", "tc_ptx.cuh", "tc_kernels.cu",
-                  "simt_decode_bwd.cu", "simt_kernels.cu", "flare_api.cu"],
-    "flare_pp_bwd": ["tc_decode_bwd.cuh", "tc_backward.cuh", "tc_ptx.cuh", "tc_kernels.cu",
-                     "simt_decode_bwd.cu", "simt_kernels.cu", "flare_api.cu"],
+    "encoder": ["tc_encoder.cuh", "tc_ptx.cuh", "tc_host.cuh", "tc_kernels.cu"],
+    "decode": ["tc_decode.cuh", "tc_ptx.cuh", "tc_host.cuh", "tc_kernels.cu"],
+    "encoder_bwd": ["tc_backward.cuh", "tc_ptx.cuh", "tc_host.cuh", "tc_bwd_launch.cu",
+                    "simt_kernels.cu"],
+    "flare_pp_fwd": ["tc_encoder.cuh", "tc_decode.cuh", "tc_ptx.cuh", "tc_host.cuh", "tc_kernels.cu"],
+    "decode_bwd": ["tc_decode_bwd.cuh", "tc_backward.cuh", "tc_ptx.cuh", "tc_host.cuh",
+                   "tc_bwd_launch.cu", "simt_decode_bwd.cu"],
+    "flare_bwd": ["tc_decode_bwd.cuh", "tc_backward.cuh", "tc_ptx.cuh", "tc_host.cuh",
+                  "tc_bwd_launch.cu", "simt_decode_bwd.cu", "simt_kernels.cu", "flare_api.cu"],
+    "flare_pp_bwd": ["tc_decode_bwd.cuh", "tc_backward.cuh", "tc_ptx.cuh", "tc_host.cuh",
+                     "tc_bwd_launch.cu", "simt_decode_bwd.cu", "simt_kernels.cu", "flare_api.cu"],
 }
 
 

@@ -76,7 +76,7 @@ typedef enum { FLARE_F32 = 0, FLARE_BF16 = 1 } flare_dtype_t;
  *   encoder, merge, decode:        D = 64 with M in {64, 128, 256},
  *                                  D = 128 with M in {64, 128};
  *   encoder and decode backward:   D = 64 with M in {64, 128, 256},
- *                                  D = 128 with M = 64.
+ *                                  D = 128 with M in {64, 128}.
  * The mixer entry points take, per step, the kernel family of that step. */
 typedef enum { FLARE_KERNEL_AUTO = 0, FLARE_KERNEL_SIMT = 1, FLARE_KERNEL_TENSOR = 2 } flare_kernel_t;
 

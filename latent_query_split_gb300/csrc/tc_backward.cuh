@@ -35,14 +35,16 @@
 // dQ = dQ + the encoder's share: the dK epilogue prefetches the tile's rows of
 // the old dK with cp.async at the start of the tile and adds them in fp32
 // before rounding once.
-// D = 128 (M = 64) runs as two passes over the tokens, one per 64-column half
+// D = 128 (M = 64 or 128) runs as two passes over the tokens, one per 64-column half
 // of the outputs: each pass contracts S and dP over all 128 columns (K, V,
 // Q and dZ tiles of two 64-column atoms each) and computes dV, dK and dQ for
 // its half (the TMEM columns of D = 64); the dQ partials of each pass have
 // their own piece array. The shared memory of two 64 KB K/V stages leaves
 // no room for the old-dK rows beside the output staging, so at M = 64 those
 // rows sit in the upper atom of the s dS^T buffer: that atom feeds latent
-// rows 64..127 of the dQ MMA, whose output lanes are never read.
+// rows 64..127 of the dQ MMA, whose output lanes are never read. At M = 128
+// there is room for one 64 KB stage only: S/dP of the next tile is then
+// issued after this tile's dQ has released the stage (no early issue).
 // Warp roles of bwd_tc_kernel: warp 0 TMA producer (K, V ring; Q, dZ and the
 // row statistics on every (b, h) change), warp 1 TMEM allocator and MMA
 // issuer (lane 0), warps 2-9 two halves of four warps, each half owning M/2
@@ -389,7 +391,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 }
                 const bool last = (j + 1 == ntiles) || bhN != bhP;
                 // tile j + 1 of the same (b, h): its S/dP as soon as S/dP of tile j is read
-                const bool early = j + 1 < ntiles && !last;
+                // (one K/V stage: the next tile's load waits for this tile's dQ)
+                const bool early = STAGES > 1 && j + 1 < ntiles && !last;
                 if (early) {
                     if (!(ok = wt.wait_inline(sdp_free, (uint32_t)j & 1))) break;
                     if (!(ok = issue_sdp(j + 1))) break;
@@ -411,7 +414,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 umma_commit(dvdk_full);
                 if (last) umma_commit(qd_free);
                 // a tile of the next (b, h): its Q and dZ arrive once qd_free fired
-                if (j + 1 < ntiles && !early && !(ok = issue_sdp(j + 1))) break;
+                if (STAGES > 1 && j + 1 < ntiles && !early && !(ok = issue_sdp(j + 1))) break;
                 // dQ += (s dS) K over the tile's 128 tokens, 16 per MMA
                 if (first && uP > 0 && !(ok = wt.wait_inline(dq_free, (uint32_t)(uP - 1) & 1))) break;
                 tc_fence_after();
@@ -427,6 +430,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                     umma_commit(dq_full);
                     ++uP;
                 }
+                // one stage: S/dP of the next tile once this tile's dQ has released it
+                if (STAGES == 1 && j + 1 < ntiles && !(ok = issue_sdp(j + 1))) break;
                 bhP = bhN;
                 ktP = ktN;
             }

@@ -38,14 +38,16 @@
 // second pass's dK share goes to a scratch tensor that is added to the
 // first's.
 //
-// D = 128 (M = 64) runs as two passes over the tokens, one per 64-column half
+// D = 128 (M = 64 or 128) runs as two passes over the tokens, one per 64-column half
 // of dK, dQ and dZ: each pass contracts S and G over all 128 columns (K, dY,
 // Q and Z tiles of two 64-column atoms) and computes its half's gradients in
 // the TMEM columns of D = 64; each pass has its own dQ/dZ piece array. Two
 // 64 KB K/dY stages leave no room for the dK staging slabs and the halves'
 // exchange buffers, so at M = 64 these sit in the upper atoms of the A^T and
 // s dT^T buffers: those atoms feed latent rows 64..127 of the dZ and dQ MMAs,
-// whose output lanes are never read.
+// whose output lanes are never read. At M = 128 there is room for one 64 KB
+// stage only: S/G of the next tile is then issued after this tile's dQ and dZ
+// have released the stage (no early issue).
 #pragma once
 
 #include "tc_backward.cuh"
@@ -644,7 +646,8 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 }
                 const bool last = (j + 1 == ntiles) || bhN != bhP;
                 // tile j + 1 of the same (b, h): its S/G as soon as S/G of tile j is read
-                const bool early = j + 1 < ntiles && !last;
+                // (one K/dY stage: the next tile's load waits for this tile's dQ, dZ)
+                const bool early = STAGES > 1 && j + 1 < ntiles && !last;
                 if (early) {
                     if (!(ok = wt.wait_inline(sg_free, (uint32_t)j & 1))) break;
                     if (!(ok = issue_sg(j + 1))) break;
@@ -661,7 +664,7 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 umma_commit(dk_full);
                 if (last) umma_commit(qz_free);
                 // a tile of the next (b, h): its Q and Z arrive once qz_free fired
-                if (j + 1 < ntiles && !early && !(ok = issue_sg(j + 1))) break;
+                if (STAGES > 1 && j + 1 < ntiles && !early && !(ok = issue_sg(j + 1))) break;
                 // dQ += (s dT)^T K, dZ += A^T dY over the tile's 128 tokens
                 if (first && uP > 0 && !(ok = wt.wait_inline(pz_free, (uint32_t)(uP - 1) & 1))) break;
                 tc_fence_after();
@@ -683,6 +686,8 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                     umma_commit(pz_full);
                     ++uP;
                 }
+                // one stage: S/G of the next tile once this tile's dQ, dZ have released it
+                if (STAGES == 1 && j + 1 < ntiles && !(ok = issue_sg(j + 1))) break;
                 bhP = bhN;
                 ktP = ktN;
             }

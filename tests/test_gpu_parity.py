@@ -120,7 +120,7 @@ def test_flare_pp_fwd(cuda_device, kernel, dt, M, D):
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dt,M,D,N", [("f32", 16, 32, 700), ("bf16", 128, 64, 3000),
                                       ("bf16", 64, 128, 1100), ("bf16", 64, 128, 9000),
-                                      ("bf16", 256, 64, 900)])
+                                      ("bf16", 128, 128, 3000), ("bf16", 256, 64, 900)])
 def test_encoder_bwd(cuda_device, kernel, dt, M, D, N):
     B, H = 2, 2
     off = [0, 200, 200, N]
@@ -174,7 +174,8 @@ def test_encoder_bwd_multi_tile_spans(cuda_device, kernel, M, replicated):
 @pytest.mark.parametrize("dt,M,D,N,replicated", [("f32", 16, 32, 700, True), ("bf16", 128, 64, 3000, True),
                                                  ("bf16", 64, 64, 2100, False), ("bf16", 64, 128, 1100, True),
                                                  ("bf16", 256, 64, 900, True), ("bf16", 256, 64, 9000, False),
-                                                 ("bf16", 64, 128, 9000, False), ("f32", 37, 40, 333, False)])
+                                                 ("bf16", 64, 128, 9000, False), ("bf16", 128, 128, 3000, True),
+                                                 ("f32", 37, 40, 333, False)])
 def test_decode_bwd(cuda_device, kernel, dt, M, D, N, replicated):
     B, H = 2, 2
     Q, K, _, _ = _problem(18, B, H, M, N, D, dt, [0, N], pad=0, q_std=1.0, replicated=replicated)
@@ -201,7 +202,7 @@ def test_decode_bwd(cuda_device, kernel, dt, M, D, N, replicated):
 
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("M,D,replicated", [(128, 64, True), (256, 64, False), (256, 64, True),
-                                            (64, 128, False)])
+                                            (64, 128, False), (128, 128, False)])
 def test_decode_bwd_multi_tile_spans(cuda_device, kernel, M, D, replicated):
     """Enough 128-token tiles that each persistent CTA walks several tiles
     and crosses (b, h) boundaries: the pipelines' barriers go through many
@@ -229,7 +230,8 @@ def test_decode_bwd_multi_tile_spans(cuda_device, kernel, M, D, replicated):
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dt,M,D,N,replicated", [("f32", 16, 32, 700, True), ("bf16", 128, 64, 3000, True),
                                                  ("bf16", 64, 64, 2100, False), ("bf16", 256, 64, 900, True),
-                                                 ("bf16", 128, 64, 20000, True), ("bf16", 64, 128, 4000, False)])
+                                                 ("bf16", 128, 64, 20000, True), ("bf16", 64, 128, 4000, False),
+                                                 ("bf16", 128, 128, 2500, True)])
 def test_flare_bwd(cuda_device, kernel, dt, M, D, N, replicated):
     """FLARE mixer backward: the decode's shares of dQ and dK are written
     first and the encoder's are added in place (dK read back and summed in
@@ -259,7 +261,7 @@ def test_flare_bwd(cuda_device, kernel, dt, M, D, N, replicated):
 
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dt,M,D,N", [("f32", 16, 32, 700), ("bf16", 128, 64, 2500), ("bf16", 64, 64, 5000),
-                                      ("bf16", 256, 64, 2500), ("bf16", 64, 128, 3000)])
+                                      ("bf16", 256, 64, 2500), ("bf16", 64, 128, 3000), ("bf16", 128, 128, 2000)])
 def test_flare_pp_bwd(cuda_device, kernel, dt, M, D, N):
     """FLARE++ mixer backward from the oracle's forward statistics: the seeds'
     gradient, the four token gradients and the summed gradient of Q(X)."""
