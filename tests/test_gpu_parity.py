@@ -332,10 +332,13 @@ def test_no_tokens(cuda_device):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("M,D", [(128, 64), (256, 64), (64, 128), (128, 128)])
 @pytest.mark.parametrize("N", [1, 127, 129])
-def test_mixer_bwd_tiny_token_counts(cuda_device, kernel, N):
+def test_mixer_bwd_tiny_token_counts(cuda_device, kernel, N, M, D):
     """FLARE and FLARE++ backward with a single tile that is partly or almost
-    entirely past N (tokens past N are neither read nor written). With one
+    entirely past N (tokens past N are neither read nor written), for every
+    tensor-core backward shape family (two latent passes at M = 256, two
+    column passes at D = 128). With one
     token every latent output equals that token's value, so Y does not depend
     on the queries or keys and no gradient reaches the query-synthesis
     encoder: dQ, dK, dQseed, dK~, dV~ are exactly zero. A bound relative to a
@@ -349,7 +352,7 @@ def test_mixer_bwd_tiny_token_counts(cuda_device, kernel, N):
         else:
             assert_close(name, dev, r, "bf16")
 
-    Q, K, V, _ = _problem(11, 1, 2, 128, N, 64, "bf16", [0, N], pad=0, q_std=1.0)
+    Q, K, V, _ = _problem(11, 1, 2, M, N, D, "bf16", [0, N], pad=0, q_std=1.0)
     g = torch.Generator().manual_seed(12)
     dY = torch.randn(K.shape, generator=g).to(K.dtype).cuda()
     Zo, Lo = oracle.encode(Q, K, V, None)
