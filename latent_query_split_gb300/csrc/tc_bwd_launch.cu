@@ -162,11 +162,11 @@ namespace {
 // Decode-backward workspace: Z in bf16 [B*H*M*D] and the dQ/dZ pieces
 // [B*H][P_max][2][M][64] of each 64-column half of D; tiles and spans as for
 // the encoder backward. M = 256 adds the per-token statistics [B*H][N]
-// (lse2, r) and the second latent half's dK share [B][N][H][64] bf16.
+// (lse2, r).
 struct DbwLayout {
     int64_t T_bh, T_total;
     int grid, P_max;
-    size_t zb, part, part_half, stats, dk2, bytes;
+    size_t zb, part, part_half, stats, bytes;
 };
 
 void dbw_layout(const Problem &pr, int sms, DbwLayout &l) {
@@ -183,22 +183,17 @@ void dbw_layout(const Problem &pr, int sms, DbwLayout &l) {
     l.part = o;
     l.part_half = align256(4 * bhm * (size_t)l.P_max * 2 * 64);
     o += l.part_half * (size_t)(pr.D / 64);
-    l.stats = l.dk2 = o;
-    if (pr.M > 128) {
-        const size_t bhn = (size_t)pr.B * pr.H * (size_t)pr.N;
-        o += align256(8 * bhn);
-        l.dk2 = o;
-        o += align256(2 * bhn * 64);
-    }
+    l.stats = o;
+    if (pr.M > 128) o += align256(8 * (size_t)pr.B * pr.H * (size_t)pr.N);
     l.bytes = o;
 }
 
-template <int M, bool ST = false, int D = 64>
+template <int M, bool ST = false, int D = 64, bool ACCK = false>
 cudaError_t launch_dbw(const CUtensorMap *maps, const tc::DbwArgs &a, cudaStream_t st) {
     // K/dY stages of 64 KB at D = 128: two at M = 64, one beside M = 128's Q and Z
     constexpr int STAGES = D == 128 ? (M == 128 ? 1 : 2) : 3;
     using C = tc::DbwCfg<M, STAGES, D>;
-    auto k = tc::dbw_tc_kernel<M, STAGES, ST, D>;
+    auto k = tc::dbw_tc_kernel<M, STAGES, ST, D, ACCK>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
     if (e != cudaSuccess) return e;
     k<<<a.grid, C::THREADS, C::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a);
@@ -286,15 +281,13 @@ cudaError_t launch_decode_bwd_tc(const Problem &pr, const void *Q, const float *
         if (e != cudaSuccess) return e;
     } else {
         // M = 256: the token statistics over all latents, then one pass per
-        // half of the latents; the second half's dK share is added after
+        // half of the latents; the second adds its dK share to the first's
         float2 *stats = (float2 *)(w + l.stats);
-        __nv_bfloat16 *dk2 = (__nv_bfloat16 *)(w + l.dk2);
-        CUtensorMap smaps[4], dk2map;
+        CUtensorMap smaps[4];
         if (!make_map(&smaps[0], K, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
             !make_map(&smaps[1], dY, pr.D, pr.H, pr.N, pr.B, 1, 128) ||
             !make_map(&smaps[2], Q, pr.D, pr.M, pr.H, qb, (uint32_t)pr.M, 1) ||
-            !make_map(&smaps[3], zb, pr.D, pr.M, pr.H, pr.B, (uint32_t)pr.M, 1) ||
-            !make_map(&dk2map, dk2, pr.D, pr.H, pr.N, pr.B, 1, 32))
+            !make_map(&smaps[3], zb, pr.D, pr.M, pr.H, pr.B, (uint32_t)pr.M, 1))
             return cudaErrorInvalidValue;
         tc::DbsArgs sa;
         sa.B = pr.B;
@@ -311,13 +304,7 @@ cudaError_t launch_decode_bwd_tc(const Problem &pr, const void *Q, const float *
         a.stats = stats;
         if ((e = launch_dbw<128, true>(maps, a, st)) != cudaSuccess) return e;
         a.m0 = 128;
-        maps[4] = dk2map;
-        if ((e = launch_dbw<128, true>(maps, a, st)) != cudaSuccess) return e;
-        const int64_t n8 = (int64_t)pr.B * pr.N * pr.H * 8;     // uint4s of dK
-        tc::dbw_add_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(
-            (uint4 *)dK, (const uint4 *)dk2, n8);
-        note_launch();
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_dbw<128, true, 64, true>(maps, a, st)) != cudaSuccess) return e;
     }
     const int64_t n4 = 2 * BH * pr.M * (pr.D / 4);
     tc::dbw_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(

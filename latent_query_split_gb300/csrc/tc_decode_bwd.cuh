@@ -35,8 +35,10 @@
 // sum_m A_nm g_nm), and dbw_tc_kernel<128, 3, true> then runs once per half
 // of the latent rows with those statistics instead of its own (A_nm =
 // 2^(s log2e <K_n, Q_m> - lse2_n), no exchange between the halves); the
-// second pass's dK share goes to a scratch tensor that is added to the
-// first's.
+// second pass (ACCK) adds its dK share to the first's: each quadrant's
+// storing thread loads the tile's old dK rows by TMA into the quadrant's
+// staging slab during the tile after it, and the epilogue adds them in
+// fp32 before rounding once more.
 //
 // D = 128 (M = 64 or 128) runs as two passes over the tokens, one per 64-column half
 // of dK, dQ and dZ: each pass contracts S and G over all 128 columns (K, dY,
@@ -98,8 +100,8 @@ struct DbwCfg {
     static constexpr uint32_t BAR_OFF = IN_UPPER ? DT_OFF + 2 * TILE_BYTES : XL_OFF + 2 * 2 * 128 * 8;
     static_assert(!IN_UPPER || XL_OFF + 2 * 2 * 128 * 8 <= DT_OFF + 2 * TILE_BYTES, "exchange buffers overflow");
     // full[S], empty[S], qz_full, qz_free, s_full, p_full, at_free, dk_full,
-    // dk_free, pz_full, pz_free, drain, sg_free
-    static constexpr int NBAR = 2 * STAGES + 11;
+    // dk_free, pz_full, pz_free, drain, sg_free, dkin[4] (ACCK: old dK rows)
+    static constexpr int NBAR = 2 * STAGES + 15;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t BYTES = MISC_OFF + 64;
     static constexpr uint32_t ALLOC = BYTES + 1024;
@@ -151,24 +153,6 @@ __global__ void __launch_bounds__(256) dbw_reduce_kernel(const float *__restrict
         acc.w += v.w;
     }
     reinterpret_cast<float4 *>(which ? dZ : dQ)[bh * per + rem] = acc;
-}
-
-// dK += dK2, both bf16 (the two latent halves' shares of the M = 256 dK).
-__global__ void __launch_bounds__(256) dbw_add_kernel(uint4 *__restrict__ dK, const uint4 *__restrict__ dK2,
-                                                      int64_t n8) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n8) return;
-    uint4 x = dK[i];
-    const uint4 y = __ldcs(dK2 + i);
-    uint32_t *xp = &x.x;
-    const uint32_t *yp = &y.x;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float2 u = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(xp + q));
-        const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(yp + q));
-        xp[q] = pack_bf16(u.x + v.x, u.y + v.y);
-    }
-    dK[i] = x;
 }
 
 // ---- the row statistics of the M = 256 decode backward ----------------------
@@ -457,7 +441,7 @@ dbs_stats_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int M, int STAGES, bool ST = false, int D = 64>
+template <int M, int STAGES, bool ST = false, int D = 64, bool ACCK = false>
 __global__ void __launch_bounds__(DbwCfg<M, STAGES, D>::THREADS, 1)
 dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmdY,
               const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmZ,
@@ -480,6 +464,7 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     const uint32_t dk_full = qz_full + 40, dk_free = qz_full + 48;
     const uint32_t pz_full = qz_full + 56, pz_free = qz_full + 64, drain = qz_full + 72;
     const uint32_t sg_free = qz_full + 80;
+    auto dkin = [&](int q) { return qz_full + 88 + 8u * q; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
 
@@ -508,6 +493,7 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         mbar_init(pz_free, 8);
         mbar_init(drain, 1);
         mbar_init(sg_free, 8);         // every softmax warp has read S and G of the tile
+        for (int q = 0; q < 4; ++q) mbar_init(dkin(q), 1);   // a quadrant's old dK rows are in
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -724,6 +710,20 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         };
         int pieces = 0;
         uint32_t stores = 0;
+        uint32_t dk_loads = 0, dk_issued = 0;            // ACCK: old-dK loads waited for, issued
+        // ACCK: the storing thread loads the old dK rows of tile (ktp, bp, hp)
+        // into the quadrant's slab once the slab's last store has read it
+        auto load_old = [&](int64_t ktp_, int bp_, int hp_) {
+            const int n0 = (int)(ktp_ * 128) + quad * 32;
+            if (n0 >= a.N) return;
+            if (storer) {
+                if (stores > 0) bulk_wait_group_read0();
+                mbar_arrive_expect_tx(dkin(quad), 32 * 128);
+                if (dcheck(tile_in_tensor(64 * a.dh, hp_, n0, bp_, a.H, a.N, a.B), kChkDbwOut, a.status))
+                    tma_load_4d(smem_u32(slab), &tmdK, 64 * a.dh, hp_, n0, bp_, dkin(quad));
+            }
+            ++dk_issued;
+        };
         // Epilogue of tile jp at (bhp, ktp, bp, hp): dK of the quadrant's 32
         // rows (half hf converts columns [32 hf, 32 hf + 32)); at the end of a
         // (b, h) piece, the span's dQ (half 0) and dZ (half 1) pieces.
@@ -736,17 +736,34 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(dk_free);
-            if (stores > 0 && storer) bulk_wait_group_read0();    // the slab's last store has read it
+            if (ACCK && (int)(ktp * 128) + quad * 32 < a.N) {
+                // the old rows were loaded into the slab (after its last store read it)
+                if (!wwait(dkin(quad), (uint32_t)dk_loads & 1)) return false;
+                ++dk_loads;
+            } else if (stores > 0 && storer) {
+                bulk_wait_group_read0();    // the slab's last store has read it
+            }
             named_bar_sync(pair_bar, 64);
             uint8_t *srow = slab + lane * 128;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const uint32_t *k8 = rk + 8 * q;
-                *reinterpret_cast<uint4 *>(srow + (((4 * hf + q) ^ (lane & 7)) << 4)) = make_uint4(
-                    pack_bf16(__uint_as_float(k8[0]), __uint_as_float(k8[1])),
-                    pack_bf16(__uint_as_float(k8[2]), __uint_as_float(k8[3])),
-                    pack_bf16(__uint_as_float(k8[4]), __uint_as_float(k8[5])),
-                    pack_bf16(__uint_as_float(k8[6]), __uint_as_float(k8[7])));
+                uint32_t *k8 = rk + 8 * q;
+                uint4 *dst = reinterpret_cast<uint4 *>(srow + (((4 * hf + q) ^ (lane & 7)) << 4));
+                if constexpr (ACCK) {
+                    // bf16 pairs of the old row, the even column in the low half
+                    const uint4 o = *dst;
+                    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        k8[2 * k] = __float_as_uint(__uint_as_float(k8[2 * k]) + __uint_as_float(ow[k] << 16));
+                        k8[2 * k + 1] =
+                            __float_as_uint(__uint_as_float(k8[2 * k + 1]) + __uint_as_float(ow[k] & 0xffff0000u));
+                    }
+                }
+                *dst = make_uint4(pack_bf16(__uint_as_float(k8[0]), __uint_as_float(k8[1])),
+                                  pack_bf16(__uint_as_float(k8[2]), __uint_as_float(k8[3])),
+                                  pack_bf16(__uint_as_float(k8[4]), __uint_as_float(k8[5])),
+                                  pack_bf16(__uint_as_float(k8[6]), __uint_as_float(k8[7])));
             }
             fence_proxy_async_smem();
             named_bar_sync(pair_bar, 64);
@@ -840,6 +857,9 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(sg_free);
+            if constexpr (ACCK) {
+                if (j > 0) load_old(ktp, bp, hp);        // for the previous tile's epilogue
+            }
             // two latents per packed instruction; two partial sums of each kind
             const uint64_t sl2x2 = f2pack(sl2, sl2), nm2x2 = f2pack(-m2, -m2);
             uint64_t ls2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
@@ -929,7 +949,18 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             b = bN;
             h = hN;
         }
-        if (ok && ntiles > 0) epilogue(ntiles - 1, bhp, ktp, bp, hp, lastp);
+        if (ok && ntiles > 0) {
+            if constexpr (ACCK) load_old(ktp, bp, hp);
+            epilogue(ntiles - 1, bhp, ktp, bp, hp, lastp);
+        }
+        if constexpr (ACCK) {
+            // an old-dK load still in flight (a wait given up) lands before the CTA exits
+            if (storer && dk_issued > dk_loads) {
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(dkin(quad), (uint32_t)dk_loads & 1) && globaltimer() - t0 < 500000000ull) {
+                }
+            }
+        }
         if (storer) bulk_wait_group0();
     }
     tc_fence_before();
