@@ -27,7 +27,8 @@
 //    as one fp32 piece per (b, h) of the span.
 //  * dbw_reduce_kernel: dQ and dZ = the sums of the pieces in piece order.
 // Warp roles: warp 0 TMA producer (K, dY ring; Q, Z on every (b, h) change),
-// warp 1 TMEM allocator and MMA issuer (lane 0), warps 2-9 the two halves.
+// warp 1 TMEM allocator and MMA issuer (the converged warp; elect.sync picks
+// the issuing lane), warps 2-9 the two halves.
 //
 // M = 256: S^T and G^T of one tile would fill all 512 TMEM columns, so the
 // row statistics come first from dbs_stats_kernel (for every token, over all
@@ -307,8 +308,8 @@ dbs_stats_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
                 }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer (lane 0) ----------------
-        if (lane == 0) {
+        // ---------------- MMA issuer (converged warp, elect.sync issues) ----------------
+        {
             constexpr uint32_t idS = idesc_bf16(128, 256, 0, 0);
             const uint64_t dQk = desc_sw128(sQ, 16, 1024);
             const uint64_t dZk = desc_sw128(sZ, 16, 1024);
@@ -319,31 +320,31 @@ dbs_stats_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
                 if (bh != cur) {
                     ++u;
                     cur = bh;
-                    if (!(ok = wt.wait_inline(qz_full, (uint32_t)u & 1))) break;
+                    if (!(ok = __all_sync(0xffffffffu, wt.wait_inline(qz_full, (uint32_t)u & 1)))) break;
                 }
                 const int s = (int)(j % C::STAGES);
-                if (!(ok = wt.wait_inline(full(s), (uint32_t)(j / C::STAGES) & 1))) break;
+                if (!(ok = __all_sync(0xffffffffu, wt.wait_inline(full(s), (uint32_t)(j / C::STAGES) & 1)))) break;
                 // the row warps have read the previous tile's S and G
-                if (j > 0 && !(ok = wt.wait_inline(s_free, (uint32_t)(j - 1) & 1))) break;
+                if (j > 0 && !(ok = __all_sync(0xffffffffu, wt.wait_inline(s_free, (uint32_t)(j - 1) & 1)))) break;
                 tc_fence_after();
                 const uint64_t dK = desc_sw128(sStage + s * C::STAGE_BYTES, 16, 1024);
                 const uint64_t dY = desc_sw128(sStage + s * C::STAGE_BYTES + C::TILE_BYTES, 16, 1024);
 #pragma unroll
                 for (int kb = 0; kb < 4; ++kb)
-                    umma_bf16_ss(tmem + C::S_COL, dK + 2 * kb, dQk + 2 * kb, idS, kb > 0 ? 1u : 0u);
+                    umma_ss_elect(tmem + C::S_COL, dK + 2 * kb, dQk + 2 * kb, idS, kb > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kb = 0; kb < 4; ++kb)
-                    umma_bf16_ss(tmem + C::G_COL, dY + 2 * kb, dZk + 2 * kb, idS, kb > 0 ? 1u : 0u);
-                umma_commit(s_full);
-                umma_commit(empty(s));
+                    umma_ss_elect(tmem + C::G_COL, dY + 2 * kb, dZk + 2 * kb, idS, kb > 0 ? 1u : 0u);
+                umma_commit_elect(s_full);
+                umma_commit_elect(empty(s));
                 if (++kt == a.T_bh) {
                     kt = 0;
                     ++bh;
-                    umma_commit(qz_free);   // the (b, h)'s last S and G read Q and Z
+                    umma_commit_elect(qz_free);   // the (b, h)'s last S and G read Q and Z
                 }
             }
             if (wt.aborted()) {
-                umma_commit(drain);
+                umma_commit_elect(drain);
                 const uint64_t t0 = globaltimer();
                 while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < 500000000ull) {
                 }
@@ -580,8 +581,8 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer (lane 0) ----------------
-        if (lane == 0) {
+        // ---------------- MMA issuer (converged warp, elect.sync issues) ----------------
+        {
             constexpr uint32_t idS = idesc_bf16(128, M, 0, 0);
             constexpr uint32_t idG = idesc_bf16(128, 64, 0, 1);    // dK: A in TMEM, B MN-major
             constexpr uint32_t idR = idesc_bf16(128, 64, 1, 1);    // dQ, dZ: A, B MN-major
@@ -597,23 +598,23 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 if (bhS != curS) {
                     ++uS;
                     curS = bhS;
-                    if (!wt.wait_inline(qz_full, (uint32_t)uS & 1)) return false;
+                    if (!__all_sync(0xffffffffu, wt.wait_inline(qz_full, (uint32_t)uS & 1))) return false;
                 }
                 const int s = (int)(jj % STAGES);
-                if (!wt.wait_inline(full(s), (uint32_t)(jj / STAGES) & 1)) return false;
+                if (!__all_sync(0xffffffffu, wt.wait_inline(full(s), (uint32_t)(jj / STAGES) & 1))) return false;
                 tc_fence_after();
                 const uint64_t dK = desc_sw128(sStage + s * C::STAGE_BYTES, 16, 1024);
                 const uint64_t dY = desc_sw128(sStage + s * C::STAGE_BYTES + DA * TB, 16, 1024);
                 // over all D columns: 16 per MMA, four per atom
 #pragma unroll
                 for (int kb = 0; kb < 4 * DA; ++kb)
-                    umma_bf16_ss(tmem + C::S_COL, dK + (((kb >> 2) * TB) >> 4) + 2 * (kb & 3),
+                    umma_ss_elect(tmem + C::S_COL, dK + (((kb >> 2) * TB) >> 4) + 2 * (kb & 3),
                                  dQk + (((kb >> 2) * C::QZA) >> 4) + 2 * (kb & 3), idS, kb > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kb = 0; kb < 4 * DA; ++kb)
-                    umma_bf16_ss(tmem + C::G_COL, dY + (((kb >> 2) * TB) >> 4) + 2 * (kb & 3),
+                    umma_ss_elect(tmem + C::G_COL, dY + (((kb >> 2) * TB) >> 4) + 2 * (kb & 3),
                                  dZk + (((kb >> 2) * C::QZA) >> 4) + 2 * (kb & 3), idS, kb > 0 ? 1u : 0u);
-                umma_commit(s_full);
+                umma_commit_elect(s_full);
                 if (++ktS == a.T_bh) {
                     ktS = 0;
                     ++bhS;
@@ -635,24 +636,24 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 // (one K/dY stage: the next tile's load waits for this tile's dQ, dZ)
                 const bool early = STAGES > 1 && j + 1 < ntiles && !last;
                 if (early) {
-                    if (!(ok = wt.wait_inline(sg_free, (uint32_t)j & 1))) break;
+                    if (!(ok = __all_sync(0xffffffffu, wt.wait_inline(sg_free, (uint32_t)j & 1)))) break;
                     if (!(ok = issue_sg(j + 1))) break;
                 }
-                if (!(ok = wt.wait_inline(p_full, (uint32_t)j & 1))) break;
+                if (!(ok = __all_sync(0xffffffffu, wt.wait_inline(p_full, (uint32_t)j & 1)))) break;
                 tc_fence_after();
-                if (j > 0 && !(ok = wt.wait_inline(dk_free, (uint32_t)(j - 1) & 1))) break;
+                if (j > 0 && !(ok = __all_sync(0xffffffffu, wt.wait_inline(dk_free, (uint32_t)(j - 1) & 1)))) break;
                 tc_fence_after();
                 // dK = (s dT) Q: K = M latents, 16 per MMA (A = s dT from its TMEM columns)
 #pragma unroll
                 for (int kb = 0; kb < M / 16; ++kb)
-                    umma_bf16_ts(tmem + C::DK_COL, tmem + C::DT_COL + 8 * kb, dQm + kb * (2048 >> 4), idG,
+                    umma_ts_elect(tmem + C::DK_COL, tmem + C::DT_COL + 8 * kb, dQm + kb * (2048 >> 4), idG,
                                  kb > 0 ? 1u : 0u);
-                umma_commit(dk_full);
-                if (last) umma_commit(qz_free);
+                umma_commit_elect(dk_full);
+                if (last) umma_commit_elect(qz_free);
                 // a tile of the next (b, h): its Q and Z arrive once qz_free fired
                 if (STAGES > 1 && j + 1 < ntiles && !early && !(ok = issue_sg(j + 1))) break;
                 // dQ += (s dT)^T K, dZ += A^T dY over the tile's 128 tokens
-                if (first && uP > 0 && !(ok = wt.wait_inline(pz_free, (uint32_t)(uP - 1) & 1))) break;
+                if (first && uP > 0 && !(ok = __all_sync(0xffffffffu, wt.wait_inline(pz_free, (uint32_t)(uP - 1) & 1)))) break;
                 tc_fence_after();
                 const int s = (int)(j % STAGES);
                 // the output column half's atoms of the K and dY tiles
@@ -660,16 +661,16 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 const uint64_t dYm = desc_sw128(sStage + s * C::STAGE_BYTES + (DA + a.dh) * TB, TB, 1024);
 #pragma unroll
                 for (int kb = 0; kb < 8; ++kb)
-                    umma_bf16_ss(tmem + C::DQ_COL, dDTm + kb * (2048 >> 4), dKm + kb * (2048 >> 4), idR,
+                    umma_ss_elect(tmem + C::DQ_COL, dDTm + kb * (2048 >> 4), dKm + kb * (2048 >> 4), idR,
                                  (kb > 0 || !first) ? 1u : 0u);
 #pragma unroll
                 for (int kb = 0; kb < 8; ++kb)
-                    umma_bf16_ss(tmem + C::DZ_COL, dAm + kb * (2048 >> 4), dYm + kb * (2048 >> 4), idR,
+                    umma_ss_elect(tmem + C::DZ_COL, dAm + kb * (2048 >> 4), dYm + kb * (2048 >> 4), idR,
                                  (kb > 0 || !first) ? 1u : 0u);
-                umma_commit(at_free);
-                umma_commit(empty(s));
+                umma_commit_elect(at_free);
+                umma_commit_elect(empty(s));
                 if (last) {
-                    umma_commit(pz_full);
+                    umma_commit_elect(pz_full);
                     ++uP;
                 }
                 // one stage: S/G of the next tile once this tile's dQ, dZ have released it
@@ -678,7 +679,7 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 ktP = ktN;
             }
             if (wt.aborted()) {
-                umma_commit(drain);
+                umma_commit_elect(drain);
                 const uint64_t t0 = globaltimer();
                 while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < 500000000ull) {
                 }
