@@ -621,6 +621,9 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 }
                 return true;
             };
+            // the waits on the halves' arrivals (sg_free, p_full, dk_free, pz_free)
+            // spin with test_wait rather than suspend: this tile's products
+            // start as soon as the slowest quadrant is done
             int64_t bhP = bh0, ktP = k0;
             int uP = 0;
             if (ntiles > 0) ok = issue_sg(0);
@@ -636,12 +639,12 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 // (one K/dY stage: the next tile's load waits for this tile's dQ, dZ)
                 const bool early = STAGES > 1 && j + 1 < ntiles && !last;
                 if (early) {
-                    if (!(ok = __all_sync(0xffffffffu, wt.wait_inline(sg_free, (uint32_t)j & 1)))) break;
+                    if (!(ok = __all_sync(0xffffffffu, wt.spin(sg_free, (uint32_t)j & 1)))) break;
                     if (!(ok = issue_sg(j + 1))) break;
                 }
-                if (!(ok = __all_sync(0xffffffffu, wt.wait_inline(p_full, (uint32_t)j & 1)))) break;
+                if (!(ok = __all_sync(0xffffffffu, wt.spin(p_full, (uint32_t)j & 1)))) break;
                 tc_fence_after();
-                if (j > 0 && !(ok = __all_sync(0xffffffffu, wt.wait_inline(dk_free, (uint32_t)(j - 1) & 1)))) break;
+                if (j > 0 && !(ok = __all_sync(0xffffffffu, wt.spin(dk_free, (uint32_t)(j - 1) & 1)))) break;
                 tc_fence_after();
                 // dK = (s dT) Q: K = M latents, 16 per MMA (A = s dT from its TMEM columns)
 #pragma unroll
@@ -653,7 +656,7 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 // a tile of the next (b, h): its Q and Z arrive once qz_free fired
                 if (STAGES > 1 && j + 1 < ntiles && !early && !(ok = issue_sg(j + 1))) break;
                 // dQ += (s dT)^T K, dZ += A^T dY over the tile's 128 tokens
-                if (first && uP > 0 && !(ok = __all_sync(0xffffffffu, wt.wait_inline(pz_free, (uint32_t)(uP - 1) & 1)))) break;
+                if (first && uP > 0 && !(ok = __all_sync(0xffffffffu, wt.spin(pz_free, (uint32_t)(uP - 1) & 1)))) break;
                 tc_fence_after();
                 const int s = (int)(j % STAGES);
                 // the output column half's atoms of the K and dY tiles
