@@ -367,13 +367,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 const uint64_t dV = desc_sw128(sStage + s * C::STAGE_BYTES + DA * TB, 16, 1024);
                 // over all D columns: 16 per MMA, four per atom
 #pragma unroll
-                for (int kb = 0; kb < 4 * DA; ++kb)
+                for (int kb = 0; kb < 4 * DA; ++kb) {
                     umma_ss_elect(tmem + C::S_COL, dK + (((kb >> 2) * TB) >> 4) + 2 * (kb & 3),
                                  dQk + (((kb >> 2) * C::QZA) >> 4) + 2 * (kb & 3), idS, kb > 0 ? 1u : 0u);
-#pragma unroll
-                for (int kb = 0; kb < 4 * DA; ++kb)
                     umma_ss_elect(tmem + C::DP_COL, dV + (((kb >> 2) * TB) >> 4) + 2 * (kb & 3),
                                  dZk + (((kb >> 2) * C::QZA) >> 4) + 2 * (kb & 3), idS, kb > 0 ? 1u : 0u);
+                }
                 umma_commit_elect(s_full);
                 if (++ktS == a.T_bh) {
                     ktS = 0;
@@ -406,13 +405,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 // dV = P^T dZ (A = P^T from tensor memory), dK = (s dS)^T Q (A = dS^T
                 // from shared memory): K = M latents, 16 per MMA
 #pragma unroll
-                for (int kb = 0; kb < M / 16; ++kb)
+                for (int kb = 0; kb < M / 16; ++kb) {
                     umma_ts_elect(tmem + C::DV_COL, tmem + C::P_COL + 8 * kb, dZm + kb * (2048 >> 4), idG,
                                  kb > 0 ? 1u : 0u);
-#pragma unroll
-                for (int kb = 0; kb < M / 16; ++kb)
                     umma_ss_elect(tmem + C::DK_COL, dDSk + (uint64_t)(((kb >> 2) * TB + (kb & 3) * 32) >> 4),
                                  dQm + kb * (2048 >> 4), idG, kb > 0 ? 1u : 0u);
+                }
                 umma_commit_elect(dvdk_full);
                 if (last) umma_commit_elect(qd_free);
                 // a tile of the next (b, h): its Q and dZ arrive once qd_free fired
