@@ -26,9 +26,12 @@
 //    accumulate in TMEM over the (b, h)'s tiles of the span and are written
 //    as one fp32 piece per (b, h) of the span.
 //  * dbw_reduce_kernel: dQ and dZ = the sums of the pieces in piece order.
-// Warp roles: warp 0 TMA producer (K, dY ring; Q, Z on every (b, h) change),
-// warp 1 TMEM allocator and MMA issuer (the converged warp; elect.sync picks
-// the issuing lane), warps 2-9 the two halves.
+// Warp roles (four warpgroups, each with its own register budget): warp 0
+// TMA producer (K, dY ring; Q, Z on every (b, h) change), warp 1 TMEM
+// allocator and MMA issuer (the converged warp; elect.sync picks the issuing
+// lane), warps 4-11 the two latent halves, warps 12-15 the epilogue (dK of a
+// lane quadrant's 32 token rows per tile, dQ and dZ pieces at a piece's end),
+// so the halves never wait for a store.
 //
 // M = 256: S^T and G^T of one tile would fill all 512 TMEM columns, so the
 // row statistics come first from dbs_stats_kernel (for every token, over all
@@ -81,7 +84,13 @@ template <int M_, int STAGES_, int D_ = 64>
 struct DbwCfg {
     static constexpr int M = M_, D = D_, TILE = 128, STAGES = STAGES_;
     static constexpr int DA = D / 64;                      // 64-column atoms of a row
-    static constexpr int THREADS = 320;
+    // four warpgroups: producer and MMA issuer (warps 0, 1; 2 and 3 idle),
+    // the two latent halves (warps 4-11), the dK/dQ/dZ epilogue (warps 12-15)
+    static constexpr int THREADS = 512;
+    static constexpr int SOFT0 = 4, EPI0 = 12;
+    // registers per thread of each warpgroup (setmaxnreg): 128 at launch,
+    // 112 + 144 + 144 + 112 = 4 x 128
+    static constexpr uint32_t REG_CTL = 112, REG_SOFT = 144, REG_EPI = 112;
     static constexpr uint32_t TILE_BYTES = TILE * 128;     // 128 rows x 64 bf16 (swizzled)
     static constexpr uint32_t QZA = M * 128;               // one [M][64] bf16 atom (swizzled)
     static constexpr uint32_t QZ_BYTES = DA * QZA;         // Q (or Z): its atoms in column order
@@ -442,6 +451,33 @@ dbs_stats_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
+// Per-warpgroup register budgets (every warp of a warpgroup executes the same one).
+template <uint32_t R>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <uint32_t R>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+
+// Spin with test_wait and the bounded loop inline (no call: the warpgroups'
+// register budgets differ).
+__device__ __forceinline__ bool spin_inline(const Waiter &wt, uint32_t bar, uint32_t parity) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_test(bar, parity)) return true;
+        if (*wt.abort) return false;
+        if (globaltimer() - t0 > kWaitNs) {
+            *wt.abort = 1;
+            atomicCAS(wt.status, 0u, 1u);
+            return false;
+        }
+    }
+}
+
 template <int M, int STAGES, bool ST = false, int D = 64, bool ACCK = false>
 __global__ void __launch_bounds__(DbwCfg<M, STAGES, D>::THREADS, 1)
 dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmdY,
@@ -489,9 +525,9 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         mbar_init(p_full, 8);          // one arrival per softmax warp
         mbar_init(at_free, 1);
         mbar_init(dk_full, 1);
-        mbar_init(dk_free, 8);
+        mbar_init(dk_free, 4);         // one arrival per epilogue warp
         mbar_init(pz_full, 1);
-        mbar_init(pz_free, 8);
+        mbar_init(pz_free, 4);
         mbar_init(drain, 1);
         mbar_init(sg_free, 8);         // every softmax warp has read S and G of the tile
         for (int q = 0; q < 4; ++q) mbar_init(dkin(q), 1);   // a quadrant's old dK rows are in
@@ -508,9 +544,9 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
-    if (M < 128 && warp >= 2) {
+    if (M < 128 && warp >= C::SOFT0 && warp < C::EPI0) {
         // latents M..127 of A^T and dT^T stay zero: the dQ and dZ MMAs span 128 rows
-        for (int q = threadIdx.x - 64; q < (int)TB / 16; q += 256) {
+        for (int q = threadIdx.x - 32 * C::SOFT0; q < (int)TB / 16; q += 256) {
             reinterpret_cast<uint4 *>(smem + C::A_OFF + TB)[q] = make_uint4(0, 0, 0, 0);
             reinterpret_cast<uint4 *>(smem + C::DT_OFF + TB)[q] = make_uint4(0, 0, 0, 0);
         }
@@ -521,6 +557,8 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    if (warp < C::SOFT0) {
+    regs_dec<C::REG_CTL>();
     if (warp == 0) {
         // ---------------- producer ----------------
         const uint64_t pol = policy_evict_first();
@@ -639,12 +677,12 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 // (one K/dY stage: the next tile's load waits for this tile's dQ, dZ)
                 const bool early = STAGES > 1 && j + 1 < ntiles && !last;
                 if (early) {
-                    if (!(ok = __all_sync(0xffffffffu, wt.spin(sg_free, (uint32_t)j & 1)))) break;
+                    if (!(ok = __all_sync(0xffffffffu, spin_inline(wt, sg_free, (uint32_t)j & 1)))) break;
                     if (!(ok = issue_sg(j + 1))) break;
                 }
-                if (!(ok = __all_sync(0xffffffffu, wt.spin(p_full, (uint32_t)j & 1)))) break;
+                if (!(ok = __all_sync(0xffffffffu, spin_inline(wt, p_full, (uint32_t)j & 1)))) break;
                 tc_fence_after();
-                if (j > 0 && !(ok = __all_sync(0xffffffffu, wt.spin(dk_free, (uint32_t)(j - 1) & 1)))) break;
+                if (j > 0 && !(ok = __all_sync(0xffffffffu, spin_inline(wt, dk_free, (uint32_t)(j - 1) & 1)))) break;
                 tc_fence_after();
                 // dK = (s dT) Q: K = M latents, 16 per MMA (A = s dT from its TMEM columns)
 #pragma unroll
@@ -656,7 +694,7 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 // a tile of the next (b, h): its Q and Z arrive once qz_free fired
                 if (STAGES > 1 && j + 1 < ntiles && !early && !(ok = issue_sg(j + 1))) break;
                 // dQ += (s dT)^T K, dZ += A^T dY over the tile's 128 tokens
-                if (first && uP > 0 && !(ok = __all_sync(0xffffffffu, wt.spin(pz_free, (uint32_t)(uP - 1) & 1)))) break;
+                if (first && uP > 0 && !(ok = __all_sync(0xffffffffu, spin_inline(wt, pz_free, (uint32_t)(uP - 1) & 1)))) break;
                 tc_fence_after();
                 const int s = (int)(j % STAGES);
                 // the output column half's atoms of the K and dY tiles
@@ -689,14 +727,15 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             }
         }
         __syncwarp();
-    } else {
-        // ---------------- the two latent halves (warps 2-9) ----------------
+    }
+    } else if (warp < C::EPI0) {
+        regs_inc<C::REG_SOFT>();
+        // ---------------- the two latent halves (warps 4-11) ----------------
         // Per tile j: S and G loaded (then sg_free, so S/G of tile j + 1 can be
         // computed), A and s dT formed, s dT into DT_COL once dK of tile j - 1
         // is done, A^T and s dT^T into shared memory once dQ, dZ of tile j - 1
-        // are done, p_full; then the epilogue of tile j - 1, whose dK was
-        // computed meanwhile.
-        const int hf = (warp - 2) >> 2;                       // latent half
+        // are done, p_full.
+        const int hf = (warp - C::SOFT0) >> 2;                // latent half
         const int quad = warp & 3;
         const int rig = quad * 32 + lane;                     // token row within the tile
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
@@ -706,123 +745,13 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         const float sl2 = a.sl2, sc = a.s;
         float *xm = reinterpret_cast<float *>(smem + C::XM_OFF);
         float2 *xl = reinterpret_cast<float2 *>(smem + C::XL_OFF);
-        uint8_t *slab = smem + C::OUT_OFF + quad * (32 * 128);   // the quadrant's 32 dK rows
-        const bool storer = hf == 0 && lane == 0;
         const int pair_bar = 1 + quad;                         // named barrier of the quadrant
         auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
             return __all_sync(0xffffffffu, wt.wait_inline(bar, par));
         };
-        int pieces = 0;
-        uint32_t stores = 0;
-        uint32_t dk_loads = 0, dk_issued = 0;            // ACCK: old-dK loads waited for, issued
-        // ACCK: the storing thread loads the old dK rows of tile (ktp, bp, hp)
-        // into the quadrant's slab once the slab's last store has read it
-        auto load_old = [&](int64_t ktp_, int bp_, int hp_) {
-            const int n0 = (int)(ktp_ * 128) + quad * 32;
-            if (n0 >= a.N) return;
-            if (storer) {
-                if (stores > 0) bulk_wait_group_read0();
-                mbar_arrive_expect_tx(dkin(quad), 32 * 128);
-                if (dcheck(tile_in_tensor(64 * a.dh, hp_, n0, bp_, a.H, a.N, a.B), kChkDbwOut, a.status))
-                    tma_load_4d(smem_u32(slab), &tmdK, 64 * a.dh, hp_, n0, bp_, dkin(quad));
-            }
-            ++dk_issued;
-        };
-        // Epilogue of tile jp at (bhp, ktp, bp, hp): dK of the quadrant's 32
-        // rows (half hf converts columns [32 hf, 32 hf + 32)); at the end of a
-        // (b, h) piece, the span's dQ (half 0) and dZ (half 1) pieces.
-        auto epilogue = [&](int64_t jp, int64_t bhp, int64_t ktp, int bp, int hp, bool lastp) -> bool {
-            if (!wwait(dk_full, (uint32_t)jp & 1)) return false;
-            tc_fence_after();
-            uint32_t rk[32];
-            tmem_ld32(tmem + C::DK_COL + 32 * hf + lane_off, rk);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(dk_free);
-            if (ACCK && (int)(ktp * 128) + quad * 32 < a.N) {
-                // the old rows were loaded into the slab (after its last store read it)
-                if (!wwait(dkin(quad), (uint32_t)dk_loads & 1)) return false;
-                ++dk_loads;
-            } else if (stores > 0 && storer) {
-                bulk_wait_group_read0();    // the slab's last store has read it
-            }
-            named_bar_sync(pair_bar, 64);
-            uint8_t *srow = slab + lane * 128;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t *k8 = rk + 8 * q;
-                uint4 *dst = reinterpret_cast<uint4 *>(srow + (((4 * hf + q) ^ (lane & 7)) << 4));
-                if constexpr (ACCK) {
-                    // bf16 pairs of the old row, the even column in the low half
-                    const uint4 o = *dst;
-                    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        k8[2 * k] = __float_as_uint(__uint_as_float(k8[2 * k]) + __uint_as_float(ow[k] << 16));
-                        k8[2 * k + 1] =
-                            __float_as_uint(__uint_as_float(k8[2 * k + 1]) + __uint_as_float(ow[k] & 0xffff0000u));
-                    }
-                }
-                *dst = make_uint4(pack_bf16(__uint_as_float(k8[0]), __uint_as_float(k8[1])),
-                                  pack_bf16(__uint_as_float(k8[2]), __uint_as_float(k8[3])),
-                                  pack_bf16(__uint_as_float(k8[4]), __uint_as_float(k8[5])),
-                                  pack_bf16(__uint_as_float(k8[6]), __uint_as_float(k8[7])));
-            }
-            fence_proxy_async_smem();
-            named_bar_sync(pair_bar, 64);
-            const int n0 = (int)(ktp * 128) + quad * 32;
-            if (storer && n0 < a.N && dcheck(tile_in_tensor(64 * a.dh, hp, n0, bp, a.H, a.N, a.B), kChkDbwOut, a.status)) {
-                // rows past N are clipped by the tensor map
-                tma_store_4d(&tmdK, smem_u32(slab), 64 * a.dh, hp, n0, bp);
-                bulk_commit_group();
-            }
-            ++stores;
-            if (lastp) {
-                if (!wwait(pz_full, (uint32_t)pieces & 1)) return false;
-                tc_fence_after();
-                uint32_t rq[2][32];
-                tmem_ld32(tmem + (hf ? C::DZ_COL : C::DQ_COL) + lane_off, rq[0]);
-                tmem_ld32(tmem + (hf ? C::DZ_COL : C::DQ_COL) + 32 + lane_off, rq[1]);
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(pz_free);
-                if (rig < M) {
-                    const int piece = cta - bwd_cta_of(bhp * a.T_bh, a.T_total, a.grid);
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        a.part + (((bhp * a.P_max + piece) * 2 + hf) * a.M_all + a.m0 + rig) * 64);
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[8 * h2 + q] = make_float4(
-                                __uint_as_float(rq[h2][4 * q]), __uint_as_float(rq[h2][4 * q + 1]),
-                                __uint_as_float(rq[h2][4 * q + 2]), __uint_as_float(rq[h2][4 * q + 3]));
-                }
-                ++pieces;
-            }
-            return true;
-        };
         int64_t bh = bh0, kt = k0;
-        int b = (int)(bh0 / a.H), h = (int)(bh0 - (int64_t)b * a.H);
-        // the previous tile, whose epilogue runs after this tile's operands are out
-        int64_t bhp = bh, ktp = kt;
-        int bp = b, hp = h;
-        bool lastp = false;
         bool ok = true;
         for (int64_t j = 0; j < ntiles; ++j) {
-            int64_t bhN = bh, ktN = kt + 1;
-            int bN = b, hN = h;
-            if (ktN == a.T_bh) {
-                ktN = 0;
-                ++bhN;
-                if (++hN == a.H) {
-                    hN = 0;
-                    ++bN;
-                }
-            }
-            const bool last = (j + 1 == ntiles) || bhN != bh;
             const int64_t n = kt * 128 + rig;
             const bool valid = n < a.N;
             // ST: the token's (lse2, r) over all latents, computed beforehand
@@ -861,9 +790,6 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(sg_free);
-            if constexpr (ACCK) {
-                if (j > 0) load_old(ktp, bp, hp);        // for the previous tile's epilogue
-            }
             // two latents per packed instruction; two partial sums of each kind
             const uint64_t sl2x2 = f2pack(sl2, sl2), nm2x2 = f2pack(-m2, -m2);
             uint64_t ls2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
@@ -941,31 +867,139 @@ dbw_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
-            // the previous tile's epilogue (its dK was computed meanwhile)
-            if (j > 0 && !(ok = epilogue(j - 1, bhp, ktp, bp, hp, lastp))) break;
-            bhp = bh;
-            ktp = kt;
-            bp = b;
-            hp = h;
-            lastp = last;
+            if (++kt == a.T_bh) {
+                kt = 0;
+                ++bh;
+            }
+        }
+        (void)ok;
+    } else {
+        regs_dec<C::REG_EPI>();
+        // ---------------- epilogue (warps 12-15, one per lane quadrant) ----------------
+        // Per tile j: dK of the quadrant's 32 token rows (all 64 columns) out
+        // of TMEM once computed, through the quadrant's shared-memory slab by
+        // one TMA store (ACCK: the old rows, loaded into the slab first, added
+        // in fp32); at the end of a (b, h) piece, the span's dQ and dZ pieces
+        // of the quadrant's 32 latent rows.
+        const int quad = warp & 3;
+        const int rig = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        uint8_t *slab = smem + C::OUT_OFF + quad * (32 * 128);
+        auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
+            return __all_sync(0xffffffffu, wt.wait_inline(bar, par));
+        };
+        int64_t bh = bh0, kt = k0;
+        int b = (int)(bh0 / a.H), h = (int)(bh0 - (int64_t)b * a.H);
+        int pieces = 0;
+        uint32_t stores = 0, dk_loads = 0, dk_issued = 0;
+        for (int64_t j = 0; j < ntiles; ++j) {
+            int64_t bhN = bh, ktN = kt + 1;
+            int bN = b, hN = h;
+            if (ktN == a.T_bh) {
+                ktN = 0;
+                ++bhN;
+                if (++hN == a.H) {
+                    hN = 0;
+                    ++bN;
+                }
+            }
+            const bool last = (j + 1 == ntiles) || bhN != bh;
+            const int n0 = (int)(kt * 128) + quad * 32;
+            const bool rows = n0 < a.N;
+            // the slab is free once its last store has read it
+            if (stores > 0 && lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+            if (ACCK && rows) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(dkin(quad), 32 * 128);
+                    if (dcheck(tile_in_tensor(64 * a.dh, h, n0, b, a.H, a.N, a.B), kChkDbwOut, a.status))
+                        tma_load_4d(smem_u32(slab), &tmdK, 64 * a.dh, h, n0, b, dkin(quad));
+                }
+                ++dk_issued;
+            }
+            if (!wwait(dk_full, (uint32_t)j & 1)) break;
+            tc_fence_after();
+            uint32_t rk[2][32];
+            tmem_ld32(tmem + C::DK_COL + lane_off, rk[0]);
+            tmem_ld32(tmem + C::DK_COL + 32 + lane_off, rk[1]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dk_free);
+            if (ACCK && rows) {
+                if (!wwait(dkin(quad), (uint32_t)dk_loads & 1)) break;
+                ++dk_loads;
+            }
+            uint8_t *srow = slab + lane * 128;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                uint32_t *k8 = rk[q >> 2] + 8 * (q & 3);
+                uint4 *dst = reinterpret_cast<uint4 *>(srow + ((q ^ (lane & 7)) << 4));
+                if constexpr (ACCK) {
+                    // bf16 pairs of the old row, the even column in the low half
+                    const uint4 o = *dst;
+                    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        k8[2 * k] = __float_as_uint(__uint_as_float(k8[2 * k]) + __uint_as_float(ow[k] << 16));
+                        k8[2 * k + 1] =
+                            __float_as_uint(__uint_as_float(k8[2 * k + 1]) + __uint_as_float(ow[k] & 0xffff0000u));
+                    }
+                }
+                *dst = make_uint4(pack_bf16(__uint_as_float(k8[0]), __uint_as_float(k8[1])),
+                                  pack_bf16(__uint_as_float(k8[2]), __uint_as_float(k8[3])),
+                                  pack_bf16(__uint_as_float(k8[4]), __uint_as_float(k8[5])),
+                                  pack_bf16(__uint_as_float(k8[6]), __uint_as_float(k8[7])));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && rows && dcheck(tile_in_tensor(64 * a.dh, h, n0, b, a.H, a.N, a.B), kChkDbwOut, a.status)) {
+                // rows past N are clipped by the tensor map
+                tma_store_4d(&tmdK, smem_u32(slab), 64 * a.dh, h, n0, b);
+                bulk_commit_group();
+            }
+            ++stores;
+            if (last) {
+                if (!wwait(pz_full, (uint32_t)pieces & 1)) break;
+                tc_fence_after();
+                const int piece = cta - bwd_cta_of(bh * a.T_bh, a.T_total, a.grid);
+#pragma unroll 1
+                for (int which = 0; which < 2; ++which) {     // dQ, then dZ
+                    uint32_t rq[2][32];
+                    tmem_ld32(tmem + (which ? C::DZ_COL : C::DQ_COL) + lane_off, rq[0]);
+                    tmem_ld32(tmem + (which ? C::DZ_COL : C::DQ_COL) + 32 + lane_off, rq[1]);
+                    tmem_wait_ld();
+                    if (rig < M) {
+                        float4 *dst = reinterpret_cast<float4 *>(
+                            a.part + (((bh * a.P_max + piece) * 2 + which) * a.M_all + a.m0 + rig) * 64);
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                dst[8 * h2 + q] = make_float4(
+                                    __uint_as_float(rq[h2][4 * q]), __uint_as_float(rq[h2][4 * q + 1]),
+                                    __uint_as_float(rq[h2][4 * q + 2]), __uint_as_float(rq[h2][4 * q + 3]));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pz_free);
+                ++pieces;
+            }
             bh = bhN;
             kt = ktN;
             b = bN;
             h = hN;
         }
-        if (ok && ntiles > 0) {
-            if constexpr (ACCK) load_old(ktp, bp, hp);
-            epilogue(ntiles - 1, bhp, ktp, bp, hp, lastp);
-        }
         if constexpr (ACCK) {
             // an old-dK load still in flight (a wait given up) lands before the CTA exits
-            if (storer && dk_issued > dk_loads) {
+            if (lane == 0 && dk_issued > dk_loads) {
                 const uint64_t t0 = globaltimer();
                 while (!mbar_try_wait(dkin(quad), (uint32_t)dk_loads & 1) && globaltimer() - t0 < 500000000ull) {
                 }
             }
         }
-        if (storer) bulk_wait_group0();
+        if (lane == 0) bulk_wait_group0();
     }
     tc_fence_before();
     __syncthreads();
