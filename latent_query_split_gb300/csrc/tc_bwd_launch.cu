@@ -196,6 +196,13 @@ cudaError_t launch_dbw(const CUtensorMap *maps, const tc::DbwArgs &a, cudaStream
     auto k = tc::dbw_tc_kernel<M, STAGES, ST, D, ACCK>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::ALLOC);
     if (e != cudaSuccess) return e;
+    // the warpgroups' register budgets (setmaxnreg) must add up to no more
+    // than the block's registers at launch, or an increase would wait forever
+    static_assert((C::REG_CTL + 2 * C::REG_SOFT + C::REG_EPI) * 128 <= 65536, "register budgets exceed the SM");
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, k)) != cudaSuccess) return e;
+    // (four warpgroups: numRegs per thread at launch against their four budgets)
+    if ((uint32_t)fa.numRegs * 4 < C::REG_CTL + 2 * C::REG_SOFT + C::REG_EPI) return cudaErrorInvalidConfiguration;
     k<<<a.grid, C::THREADS, C::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a);
     note_launch();
     return cudaGetLastError();
