@@ -198,3 +198,29 @@ def test_accumulating_encoder_bwd_validates_before_launch(lib):
     assert lib.flare_encoder_bwd_accumulate(ctypes.byref(dims), None, None, None, None, bad, 2,
                                             None, None, None, None, None, None, None, 0,
                                             None) == flare.FLARE_ERR_INVALID_ARG
+
+
+def test_backward_workspaces_cover_the_tensor_core_layouts(lib):
+    """The tensor-core backward workspaces hold what their passes use: the
+    bf16 copy of Z (or dZ) with all D columns, one dQ (and dZ) piece array per
+    64-column half of D, and at M = 256 the decode backward's per-token
+    statistics, 8 bytes per (b, h, token)."""
+    B, H, N = 2, 4, 5000
+
+    def ws(op, M, D, kernel=2):
+        d = _dims(B=B, H=H, M=M, N=N, D=D, dtype=flare.FLARE_BF16, kernel=kernel)
+        offs = (ctypes.c_int64 * 2)(0, N)     # the encoder backward takes the shard split
+        return lib.flare_workspace_bytes(op, ctypes.byref(d), offs, 1)
+
+    dec, enc = flare.FLARE_OP_DECODE_BWD, flare.FLARE_OP_ENCODER_BWD
+    for op in (dec, enc):
+        for M, D in ((64, 64), (128, 64), (256, 64), (64, 128), (128, 128)):
+            assert 0 < ws(op, M, D) != BAD, (op, M, D)
+        # two column halves: twice the pieces and twice Z's (dZ's) bf16 copy
+        # (the encoder's per-row constants, 8 bytes per latent row, do not
+        # grow with D)
+        slack = 8 * B * H * 128 + 4096
+        assert ws(op, 64, 128) >= 2 * ws(op, 64, 64) - slack
+        assert ws(op, 128, 128) >= 2 * ws(op, 128, 64) - slack
+    assert ws(dec, 256, 64) >= 2 * ws(dec, 128, 64) + 8 * B * H * N - 4096
+    assert ws(enc, 256, 64) >= 2 * ws(enc, 128, 64) - 4096
