@@ -7,24 +7,23 @@
 //   dT_nm = A_nm (g_nm - r_n),
 //   dK_n = s sum_m dT_nm Q_m,  dQ_m = s sum_n dT_nm K_n,  dZ_m = sum_n A_nm dY_n.
 //
-// Kernels (D = 64, M in {64, 128}):
+// Kernels (D = 64, M in {64, 128}; the other shapes below):
 //  * dbw_prep_kernel: Z rounded to bf16 (an MMA operand).
 //  * dbw_tc_kernel: one persistent CTA per SM over a contiguous span of
 //    128-token tiles in (b, h, tile) order. Per tile, token rows in the TMEM
 //    lanes:
 //        S^T = K Q^T,  G^T = dY Z^T                 (A, B from shared memory)
-//        A, s dT from the row softmax (warps 2-9)   (fp32, bf16 operands out)
+//        A, s dT from the row softmax (warps 4-11)  (fp32, bf16 operands out)
 //        dK = (s dT) Q                              (A = s dT in its own TMEM columns)
 //        dQ += (s dT)^T K,  dZ += A^T dY           (A from shared memory, MN-major)
 //    Eight warps form two latent halves of every token row; the halves
 //    exchange the row maximum, then their partial row sums and <A, g>.
 //    Because s dT leaves S's columns, S/G of the next tile (same (b, h)) is
 //    issued as soon as the halves have read this tile's, ahead of this tile's
-//    gradient MMAs; a tile's dK is stored (its epilogue) after the next tile's
-//    operands are out. dK leaves through shared memory (one TMA store per 32
-//    rows); dQ and dZ
-//    accumulate in TMEM over the (b, h)'s tiles of the span and are written
-//    as one fp32 piece per (b, h) of the span.
+//    gradient MMAs. dK leaves through shared memory (one TMA store per 32
+//    rows, by the epilogue warps); dQ and dZ accumulate in TMEM over the
+//    (b, h)'s tiles of the span and are written as one fp32 piece per (b, h)
+//    of the span.
 //  * dbw_reduce_kernel: dQ and dZ = the sums of the pieces in piece order.
 // Warp roles (four warpgroups, each with its own register budget): warp 0
 // TMA producer (K, dY ring; Q, Z on every (b, h) change), warp 1 TMEM
@@ -39,13 +38,13 @@
 // sum_m A_nm g_nm), and dbw_tc_kernel<128, 3, true> then runs once per half
 // of the latent rows with those statistics instead of its own (A_nm =
 // 2^(s log2e <K_n, Q_m> - lse2_n), no exchange between the halves); the
-// second pass (ACCK) adds its dK share to the first's: each quadrant's
-// storing thread loads the tile's old dK rows by TMA into the quadrant's
-// staging slab during the tile after it, and the epilogue adds them in
-// fp32 before rounding once more.
+// second pass (ACCK) adds its dK share to the first's: each epilogue warp
+// loads the tile's old dK rows by TMA into its quadrant's staging slab
+// before the tile's dK is ready, and adds them in fp32 before rounding once
+// more.
 //
-// D = 128 (M = 64 or 128) runs as two passes over the tokens, one per 64-column half
-// of dK, dQ and dZ: each pass contracts S and G over all 128 columns (K, dY,
+// D = 128 (M = 64 or 128) runs as two passes over the tokens, one per
+// 64-column half of dK, dQ and dZ: each pass contracts S and G over all 128 columns (K, dY,
 // Q and Z tiles of two 64-column atoms) and computes its half's gradients in
 // the TMEM columns of D = 64; each pass has its own dQ/dZ piece array. Two
 // 64 KB K/dY stages leave no room for the dK staging slabs and the halves'
